@@ -1,0 +1,25 @@
+"""Shared pytest set-up.
+
+``-m "not gpu"`` runs the CPU suite: the oracle against its pins, the input
+generator, host-side logic and the C-ABI library's exported symbols.
+``-m gpu`` runs the parity tests proper, which call the CUDA library through
+its C ABI and compare with the oracle.
+"""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+
+
+@pytest.fixture(scope="session")
+def orc():
+    import oracle
+    return oracle.load()
