@@ -1,0 +1,277 @@
+/*
+ * ns_paged.h -- C ABI of the GB300 (sm_103a) paged-KV attention library.
+ *
+ * The library is the data-parallel hot path of a nanoserve-style LLM server:
+ * every query head of every running sequence walks its block table over a
+ * paged K/V pool with online softmax (nanoserve project page, "What I built":
+ * paged KV cache with block tables; fused paged-attention decode kernel with
+ * online softmax over the block table), after the step's new tokens have been
+ * written into their slots ("updates the KV cache with the new key and value
+ * vectors": Inference Engineering Day 11 short, "How does vLLM work").  Long
+ * contexts are split across CTAs and merged by log-sum-exp, the flash-decoding
+ * split arm of the nanoserve author's build log (Day 74 post).  A chunked
+ * prefill variant takes a span of query tokens per sequence (nanoserve project
+ * page, "What I built", continuous batching bullet: chunked prefill;
+ * Inference Engineering Day 12 short, "What is chunked prefill within vLLM").
+ *
+ * ---------------------------------------------------------------------------
+ * Conventions shared by every entry point
+ * ---------------------------------------------------------------------------
+ *  Pointers     Every tensor argument is a DEVICE pointer on the current CUDA
+ *               device, 16-byte aligned, dense (row-major, no padding) unless
+ *               a stride argument says otherwise.  The caller owns and
+ *               allocates every buffer; the library allocates nothing and
+ *               frees nothing.
+ *  Streams      Work is enqueued on `stream` (NULL = the legacy default
+ *               stream) and the call returns without synchronising.  Inputs
+ *               must stay valid until the work completes.
+ *  Elements     K, V, q and out are fp16 or bf16 (`ns_dtype`), all of one type.
+ *  Shapes       head_dim must be 64.  num_q_heads must be a multiple of
+ *               num_kv_heads with at most 8 query heads per KV head; query
+ *               head j reads KV head j / (num_q_heads / num_kv_heads).
+ *               block_size must be 4, 8, 16 or 32.
+ *  Pool layout  k_pool and v_pool are [num_blocks][num_kv_heads][block_size]
+ *               [head_dim]: one (block, kv head) is block_size*head_dim
+ *               contiguous elements.  Token slot s lives in block
+ *               s / block_size at offset s % block_size.
+ *  Tables       block_tables is int32 [num_seqs][max_blocks_per_seq]; entry
+ *               [s][i] is the pool block holding tokens i*block_size ..
+ *               (i+1)*block_size-1 of sequence s.  Only the first
+ *               ceil(context_lens[s] / block_size) entries of a row are read.
+ *               context_lens is int32 [num_seqs] and counts the tokens in the
+ *               pool INCLUDING this step's new ones.
+ *  Errors       Argument checks run on the host before anything is enqueued
+ *               and return a negative ns_status; nothing is launched then.  A
+ *               failed launch returns NS_ERR_CUDA.  Checks that need device
+ *               data (block ids inside the pool, lengths that fit the table,
+ *               slots inside the pool) run inside the kernels on every call:
+ *               a bad unit is skipped (never read or written out of bounds)
+ *               and a bit is OR-ed into the device status word, which
+ *               ns_get_device_status() returns.  No kernel traps or aborts.
+ *  Waits        Every wait inside a kernel is bounded (about one second);
+ *               on expiry the kernel sets NS_DEV_WAIT_TIMEOUT and returns.
+ */
+#ifndef NS_PAGED_H
+#define NS_PAGED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *ns_stream_t;
+
+typedef enum ns_status {
+    NS_OK = 0,
+    NS_ERR_INVALID_ARG = -1,   /* null pointer, misalignment, negative size, too-small buffer */
+    NS_ERR_UNSUPPORTED = -2,   /* a shape or type outside the supported set above */
+    NS_ERR_CUDA = -3,          /* a CUDA runtime call or a launch failed */
+    NS_ERR_DEVICE = -4         /* ns_get_device_status found a device-side status bit */
+} ns_status;
+
+typedef enum ns_dtype { NS_F16 = 0, NS_BF16 = 1 } ns_dtype;
+
+/* Device status bits (ns_get_device_status). */
+#define NS_DEV_BAD_BLOCK_ID 0x1u     /* a block table entry outside [0, num_blocks) */
+#define NS_DEV_BAD_CONTEXT_LEN 0x2u  /* context_len < 0 or > max_blocks_per_seq*block_size */
+#define NS_DEV_BAD_SLOT 0x4u         /* a slot_mapping entry >= num_blocks*block_size */
+#define NS_DEV_WAIT_TIMEOUT 0x8u     /* a bounded wait inside a kernel expired */
+#define NS_DEV_FUSED_SLOT 0x10u      /* fused append: slot is not the slot of position L-1 */
+#define NS_DEV_BAD_QUERY_SPAN 0x20u  /* prefill: query span longer than the context, or negative */
+
+/* Human-readable name of a status code (static string). */
+const char *ns_status_string(ns_status status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int ns_version(void);
+
+/*
+ * ns_kv_append -- write the step's new tokens into their pool slots.
+ *
+ * Definition (Inference Engineering Day 11 short, "How does vLLM work": the
+ * engine updates the KV cache with the new key and value vectors; paged
+ * layout from the nanoserve project page, "What I built"):
+ *   for every token t with slot_mapping[t] >= 0 and every kv head h:
+ *     k_pool[slot/bs][h][slot%bs][:] = k[t][h][:]   (same for v)
+ * A bit-exact copy.  A negative slot marks a padding token and is skipped.
+ *
+ *   k, v          [num_tokens][num_kv_heads][head_dim] elements (read)
+ *   slot_mapping  int64 [num_tokens] (read)
+ *   k_pool/v_pool [num_blocks][num_kv_heads][block_size][head_dim] (written)
+ * Slots >= num_blocks*block_size are skipped and set NS_DEV_BAD_SLOT.  Two
+ * tokens with the same slot race (one of them wins).  num_tokens == 0 is a
+ * no-op.
+ */
+ns_status ns_kv_append(const void *k, const void *v, const int64_t *slot_mapping,
+                       void *k_pool, void *v_pool, int num_tokens, int num_kv_heads,
+                       int head_dim, int block_size, int64_t num_blocks, ns_dtype dtype,
+                       ns_stream_t stream);
+
+/*
+ * Workspace for the attention entry points: split-KV partial results
+ * (fp32 running max, running sum and unnormalised output of each piece of a
+ * sequence that was cut across CTAs), one arrival counter per (sequence, kv
+ * head) and a small plan record.  Size it with ns_paged_attn_workspace_bytes
+ * for the largest num_seqs you will pass.  It must be zero-filled once before
+ * first use (ns_paged_attn_workspace_init or cudaMemsetAsync); every call
+ * that completes without a device status bit leaves it ready for the next
+ * call.  Two calls that share a workspace must not run concurrently.
+ */
+size_t ns_paged_attn_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                     int head_dim);
+
+/* cudaMemsetAsync(workspace, 0, workspace_bytes, stream). */
+ns_status ns_paged_attn_workspace_init(void *workspace, size_t workspace_bytes,
+                                       ns_stream_t stream);
+
+/*
+ * ns_paged_attn_decode -- one decode step of paged attention.
+ *
+ * Definition (nanoserve project page, "What I built": fused paged-attention
+ * decode with online softmax over the block table).  For every sequence s,
+ * query head j, with h = j / (num_q_heads/num_kv_heads) and L = context_lens[s]:
+ *   z_p   = scale * sum_d q[s][j][d] * K_s[p][d],    p = 0 .. L-1
+ *   out[s][j][:] = sum_p softmax(z)_p * V_s[p][:]
+ * where K_s[p] = k_pool[block_tables[s][p/bs]][h][p%bs].  A sequence with
+ * L == 0 gets out = 0.  Arithmetic is fp32 with the output rounded to the
+ * element type; the result matches the exact value within the tolerance of
+ * the test suite, not bit for bit.
+ *
+ *   q            [num_seqs][num_q_heads][head_dim] (read)
+ *   out          [num_seqs][num_q_heads][head_dim] (written)
+ *   max_blocks_per_seq  row stride of block_tables (entries)
+ *   num_blocks   pool size in blocks (block ids are checked against it)
+ *   scale        softmax scale, usually 1/sqrt(head_dim)
+ *   workspace    see ns_paged_attn_workspace_bytes (read and written)
+ *
+ * The work is spread evenly over a persistent grid: the KV blocks of all
+ * (sequence, kv head) pairs are laid end to end and each CTA takes an equal
+ * run of them, so a long context is split across CTAs (flash-decoding style)
+ * and its partial results are merged by log-sum-exp.  How many CTAs run is
+ * decided on the device from the actual context lengths and batch size.
+ */
+ns_status ns_paged_attn_decode(const void *q, const void *k_pool, const void *v_pool,
+                               const int32_t *block_tables, const int32_t *context_lens,
+                               int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                               int block_size, float scale, void *out, ns_stream_t stream,
+                               int max_blocks_per_seq, int64_t num_blocks, ns_dtype dtype,
+                               void *workspace, size_t workspace_bytes);
+
+/*
+ * Policy overrides for the split-KV decode (tests and measurements).
+ *   num_ctas            0 = auto (resident CTAs on this GPU); else the grid size
+ *                       (1 .. NS_MAX_CTAS)
+ *   min_blocks_per_cta  0 = auto; fewer CTAs are used when the total work
+ *                       would give each less than this many KV blocks
+ *   whole_sequences     nonzero = never split a (sequence, kv head): CTA c
+ *                       takes pairs c, c+G, c+2G, ... (no merge step)
+ */
+#define NS_MAX_CTAS 1024
+typedef struct ns_decode_config {
+    int num_ctas;
+    int min_blocks_per_cta;
+    int whole_sequences;
+    int reserved[5];
+} ns_decode_config;
+
+/* ns_paged_attn_decode with policy overrides (cfg may be NULL = auto). */
+ns_status ns_paged_attn_decode_ex(const void *q, const void *k_pool, const void *v_pool,
+                                  const int32_t *block_tables, const int32_t *context_lens,
+                                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int block_size, float scale, void *out, ns_stream_t stream,
+                                  int max_blocks_per_seq, int64_t num_blocks, ns_dtype dtype,
+                                  void *workspace, size_t workspace_bytes,
+                                  const ns_decode_config *cfg);
+
+/*
+ * ns_kv_append_paged_attn_decode -- ns_kv_append of one new token per
+ * sequence followed by ns_paged_attn_decode, in one kernel.
+ *
+ *   k_new, v_new  [num_seqs][num_kv_heads][head_dim] (read): token s is the
+ *                 new token of sequence s, at position context_lens[s]-1
+ *   slot_mapping  int64 [num_seqs]: must be the slot of that position,
+ *                 block_tables[s][(L-1)/bs]*bs + (L-1)%bs
+ * The result equals the two calls in order: the pool slot is written and the
+ * attention includes the new token.  The CTA that owns a sequence's last
+ * block takes the new K/V from k_new/v_new (never from the pool slot it is
+ * writing), so nothing reads the slot while it is written.  A slot that is
+ * not the slot of position L-1 sets NS_DEV_FUSED_SLOT (the slot is still
+ * written; the attention still uses the new token at position L-1).
+ */
+ns_status ns_kv_append_paged_attn_decode(const void *q, const void *k_new, const void *v_new,
+                                         const int64_t *slot_mapping, void *k_pool,
+                                         void *v_pool, const int32_t *block_tables,
+                                         const int32_t *context_lens, int num_seqs,
+                                         int num_q_heads, int num_kv_heads, int head_dim,
+                                         int block_size, float scale, void *out,
+                                         ns_stream_t stream, int max_blocks_per_seq,
+                                         int64_t num_blocks, ns_dtype dtype, void *workspace,
+                                         size_t workspace_bytes);
+
+/*
+ * Plan record the decode kernels leave at the start of the workspace (CTA 0
+ * writes it during every call).  It shows which split the device chose:
+ *   ctas_launched   grid size
+ *   ctas_active     CTAs that received work
+ *   total_blocks    KV blocks over all (sequence, kv head) pairs
+ *   split_pairs     (sequence, kv head) pairs cut across two or more CTAs
+ *   max_pieces      most CTAs sharing one pair
+ *   whole_sequences 1 when the no-split policy ran
+ */
+typedef struct ns_decode_plan {
+    int32_t ctas_launched;
+    int32_t ctas_active;
+    int64_t total_blocks;
+    int32_t split_pairs;
+    int32_t max_pieces;
+    int32_t whole_sequences;
+    int32_t reserved[9];
+} ns_decode_plan;
+
+/* Copy the plan record out of `workspace` (synchronises `stream`). */
+ns_status ns_read_decode_plan(const void *workspace, ns_decode_plan *plan, ns_stream_t stream);
+
+/*
+ * ns_paged_attn_prefill -- chunked-prefill attention over query spans.
+ *
+ * Definition (Inference Engineering Day 12 short, "What is chunked prefill
+ * within vLLM": a chunk's K/V are written into blocks and the chunk attends
+ * to everything already cached; nanoserve project page, "What I built").
+ * Sequence s owns query rows query_start_loc[s] .. query_start_loc[s+1]-1;
+ * with n = query_start_loc[s+1]-query_start_loc[s] and L = context_lens[s],
+ * row i sits at position L-n+i and sees keys p <= L-n+i (cached prefix plus
+ * causal within the span).  The span's own K/V must already be in the pool
+ * (ns_kv_append first).  A span of one row is a decode step.
+ *
+ *   q               [total_q_tokens][num_q_heads][head_dim] (read)
+ *   query_start_loc int32 [num_seqs+1], nondecreasing, [0] == 0,
+ *                   [num_seqs] == total_q_tokens (read)
+ *   out             [total_q_tokens][num_q_heads][head_dim] (written)
+ * Query-key products and probability-value products of spans longer than
+ * one row run on the tensor cores (fp16/bf16 operands, fp32 accumulation).
+ */
+ns_status ns_paged_attn_prefill(const void *q, const int32_t *query_start_loc,
+                                const void *k_pool, const void *v_pool,
+                                const int32_t *block_tables, const int32_t *context_lens,
+                                int num_seqs, int total_q_tokens, int num_q_heads,
+                                int num_kv_heads, int head_dim, int block_size, float scale,
+                                void *out, ns_stream_t stream, int max_blocks_per_seq,
+                                int64_t num_blocks, ns_dtype dtype, void *workspace,
+                                size_t workspace_bytes);
+
+/*
+ * Device status word of the current device: OR of NS_DEV_* bits raised by
+ * kernels since the last clear.  Synchronises `stream`, copies the word to
+ * *bits, and zeroes it when `clear` is nonzero.  Returns NS_OK (whatever the
+ * bits) or NS_ERR_CUDA.
+ */
+ns_status ns_get_device_status(ns_stream_t stream, uint32_t *bits, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NS_PAGED_H */

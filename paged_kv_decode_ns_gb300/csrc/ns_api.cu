@@ -1,0 +1,434 @@
+// ns_api.cu -- the C ABI (include/ns_paged.h): argument checks, workspace
+// layout, kernel dispatch and the device status word.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "ns_internal.h"
+#include "paged_decode.cuh"
+
+namespace {
+
+// OR of NS_DEV_* bits raised by the kernels (one word per device).
+__device__ unsigned int g_device_status;
+
+constexpr int kMaxDevices = 64;
+std::atomic<unsigned *> g_status_ptr[kMaxDevices];
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_ctas_per_sm[kMaxDevices][2][4];
+
+// Split-KV policy default: a CTA gets at least this many KV blocks.
+constexpr int kDefaultMinBlocksPerCta = 8;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int bs_index(int bs)
+{
+    switch (bs) {
+    case 4: return 0;
+    case 8: return 1;
+    case 16: return 2;
+    case 32: return 3;
+    default: return -1;
+    }
+}
+
+cudaError_t current_device(int *dev)
+{
+    cudaError_t e = cudaGetDevice(dev);
+    if (e == cudaSuccess && (*dev < 0 || *dev >= kMaxDevices))
+        e = cudaErrorInvalidDevice;
+    return e;
+}
+
+unsigned *status_word(int dev)
+{
+    unsigned *p = g_status_ptr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        void *a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_device_status) != cudaSuccess)
+            return nullptr;
+        p = static_cast<unsigned *>(a);
+        g_status_ptr[dev].store(p, std::memory_order_release);
+    }
+    return p;
+}
+
+int sm_count(int dev)
+{
+    int n = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (n <= 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 1;
+        g_sm_count[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
+template <typename T>
+cudaError_t dispatch_decode(int bs, const ns::DecodeParams &P, int ctas, cudaStream_t s)
+{
+    switch (bs) {
+    case 4: return ns::launch_paged_decode<T, 4>(P, ctas, s);
+    case 8: return ns::launch_paged_decode<T, 8>(P, ctas, s);
+    case 16: return ns::launch_paged_decode<T, 16>(P, ctas, s);
+    default: return ns::launch_paged_decode<T, 32>(P, ctas, s);
+    }
+}
+
+template <typename T>
+int dispatch_ctas_per_sm(int bs)
+{
+    switch (bs) {
+    case 4: return ns::decode_ctas_per_sm<T, 4>();
+    case 8: return ns::decode_ctas_per_sm<T, 8>();
+    case 16: return ns::decode_ctas_per_sm<T, 16>();
+    default: return ns::decode_ctas_per_sm<T, 32>();
+    }
+}
+
+int resident_ctas(int dev, ns_dtype dt, int bs)
+{
+    std::atomic<int> &slot = g_ctas_per_sm[dev][dt == NS_BF16 ? 1 : 0][bs_index(bs)];
+    int n = slot.load(std::memory_order_relaxed);
+    if (n <= 0) {
+        n = dt == NS_BF16 ? dispatch_ctas_per_sm<ns::BF16>(bs) : dispatch_ctas_per_sm<ns::F16>(bs);
+        slot.store(n, std::memory_order_relaxed);
+    }
+    long long total = (long long)n * sm_count(dev);
+    return (int)(total > NS_MAX_CTAS ? NS_MAX_CTAS : total);
+}
+
+// Workspace layout (byte offsets), for up to `rows` query rows.
+struct WsLayout {
+    size_t plan, counters, partials, row_seq, row_len, total;
+};
+
+WsLayout ws_layout(long long rows, int num_kv_heads)
+{
+    WsLayout L;
+    L.plan = 0;
+    L.counters = 256;
+    L.partials = L.counters + align256((size_t)rows * num_kv_heads * sizeof(int32_t));
+    L.row_seq = L.partials + align256((size_t)NS_MAX_CTAS * 2 * ns::kSlotFloats * sizeof(float));
+    L.row_len = L.row_seq + align256((size_t)rows * sizeof(int32_t));
+    L.total = L.row_len + align256((size_t)rows * sizeof(int32_t));
+    return L;
+}
+
+ns_status check_shapes(int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                       ns_dtype dtype)
+{
+    if (num_q_heads <= 0 || num_kv_heads <= 0)
+        return NS_ERR_INVALID_ARG;
+    if (dtype != NS_F16 && dtype != NS_BF16)
+        return NS_ERR_UNSUPPORTED;
+    if (head_dim != ns::kHeadDim || bs_index(block_size) < 0)
+        return NS_ERR_UNSUPPORTED;
+    if (num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > ns::kMaxGroup)
+        return NS_ERR_UNSUPPORTED;
+    return NS_OK;
+}
+
+struct DecodeCall {
+    const void *q;
+    const void *k_pool;
+    const void *v_pool;
+    const int32_t *block_tables;
+    const int32_t *lens;       // per row
+    const int32_t *table_row;  // nullptr: identity
+    int rows;
+    int num_q_heads, num_kv_heads, block_size;
+    float scale;
+    void *out;
+    cudaStream_t stream;
+    int max_blocks_per_seq;
+    long long num_blocks;
+    ns_dtype dtype;
+    void *workspace;
+    const ns_decode_config *cfg;
+    const void *k_new, *v_new;
+    const int64_t *slot_mapping;
+};
+
+ns_status run_decode(const DecodeCall &c, int dev)
+{
+    unsigned *status = status_word(dev);
+    if (status == nullptr)
+        return NS_ERR_CUDA;
+    const WsLayout L = ws_layout(c.rows, c.num_kv_heads);
+    char *ws = static_cast<char *>(c.workspace);
+
+    ns::DecodeParams P;
+    std::memset(&P, 0, sizeof(P));
+    P.q = static_cast<const uint16_t *>(c.q);
+    P.k_pool = static_cast<const uint16_t *>(c.k_pool);
+    P.v_pool = static_cast<const uint16_t *>(c.v_pool);
+    P.block_tables = c.block_tables;
+    P.context_lens = c.lens;
+    P.table_row = c.table_row;
+    P.out = static_cast<uint16_t *>(c.out);
+    P.k_new = static_cast<const uint16_t *>(c.k_new);
+    P.v_new = static_cast<const uint16_t *>(c.v_new);
+    P.slot_mapping = c.slot_mapping;
+    P.k_pool_w = const_cast<uint16_t *>(static_cast<const uint16_t *>(c.k_pool));
+    P.v_pool_w = const_cast<uint16_t *>(static_cast<const uint16_t *>(c.v_pool));
+    P.num_seqs = c.rows;
+    P.num_q_heads = c.num_q_heads;
+    P.num_kv_heads = c.num_kv_heads;
+    P.group = c.num_q_heads / c.num_kv_heads;
+    P.max_blocks_per_seq = c.max_blocks_per_seq;
+    P.num_blocks = c.num_blocks;
+    P.scale_log2 = c.scale * 1.4426950408889634f;
+    P.counters = reinterpret_cast<int *>(ws + L.counters);
+    P.partials = reinterpret_cast<float *>(ws + L.partials);
+    P.plan = reinterpret_cast<ns_decode_plan *>(ws + L.plan);
+    P.status = status;
+    P.min_blocks_per_cta = (c.cfg && c.cfg->min_blocks_per_cta > 0) ? c.cfg->min_blocks_per_cta
+                                                                     : kDefaultMinBlocksPerCta;
+    P.whole_sequences = (c.cfg && c.cfg->whole_sequences) ? 1 : 0;
+
+    int ctas = (c.cfg && c.cfg->num_ctas > 0) ? c.cfg->num_ctas : resident_ctas(dev, c.dtype, c.block_size);
+    if (ctas > NS_MAX_CTAS)
+        ctas = NS_MAX_CTAS;
+    const cudaError_t e = c.dtype == NS_BF16
+                              ? dispatch_decode<ns::BF16>(c.block_size, P, ctas, c.stream)
+                              : dispatch_decode<ns::F16>(c.block_size, P, ctas, c.stream);
+    return e == cudaSuccess ? NS_OK : NS_ERR_CUDA;
+}
+
+ns_status check_decode_args(const void *q, const void *k_pool, const void *v_pool,
+                            const int32_t *block_tables, const int32_t *context_lens, int rows,
+                            int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                            float scale, void *out, int max_blocks_per_seq, int64_t num_blocks,
+                            ns_dtype dtype, void *workspace, size_t workspace_bytes,
+                            const ns_decode_config *cfg)
+{
+    if (rows < 0)
+        return NS_ERR_INVALID_ARG;
+    const ns_status s = check_shapes(num_q_heads, num_kv_heads, head_dim, block_size, dtype);
+    if (s != NS_OK)
+        return s;
+    if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out || !workspace)
+        return NS_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out) ||
+        !aligned16(workspace))
+        return NS_ERR_INVALID_ARG;
+    if (max_blocks_per_seq < 1 || num_blocks < 1 || !std::isfinite(scale))
+        return NS_ERR_INVALID_ARG;
+    if (workspace_bytes < ns_paged_attn_workspace_bytes(rows, num_q_heads, num_kv_heads, head_dim))
+        return NS_ERR_INVALID_ARG;
+    if (cfg && (cfg->num_ctas < 0 || cfg->num_ctas > NS_MAX_CTAS || cfg->min_blocks_per_cta < 0))
+        return NS_ERR_INVALID_ARG;
+    return NS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ns_status_string(ns_status status)
+{
+    switch (status) {
+    case NS_OK: return "NS_OK";
+    case NS_ERR_INVALID_ARG: return "NS_ERR_INVALID_ARG: invalid argument";
+    case NS_ERR_UNSUPPORTED: return "NS_ERR_UNSUPPORTED: shape or type not supported";
+    case NS_ERR_CUDA: return "NS_ERR_CUDA: CUDA call or launch failed";
+    case NS_ERR_DEVICE: return "NS_ERR_DEVICE: a kernel raised a device status bit";
+    default: return "unknown ns_status";
+    }
+}
+
+int ns_version(void) { return 100; }
+
+ns_status ns_kv_append(const void *k, const void *v, const int64_t *slot_mapping, void *k_pool,
+                       void *v_pool, int num_tokens, int num_kv_heads, int head_dim,
+                       int block_size, int64_t num_blocks, ns_dtype dtype, ns_stream_t stream)
+{
+    if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks < 1)
+        return NS_ERR_INVALID_ARG;
+    if (dtype != NS_F16 && dtype != NS_BF16)
+        return NS_ERR_UNSUPPORTED;
+    if (head_dim != ns::kHeadDim || bs_index(block_size) < 0)
+        return NS_ERR_UNSUPPORTED;
+    if (num_tokens == 0)
+        return NS_OK;
+    if (!k || !v || !slot_mapping || !k_pool || !v_pool)
+        return NS_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_pool) || !aligned16(v_pool))
+        return NS_ERR_INVALID_ARG;
+    int dev = 0;
+    if (current_device(&dev) != cudaSuccess)
+        return NS_ERR_CUDA;
+    unsigned *status = status_word(dev);
+    if (status == nullptr)
+        return NS_ERR_CUDA;
+    const cudaError_t e = ns::launch_kv_append(k, v, slot_mapping, k_pool, v_pool, num_tokens,
+                                               num_kv_heads, block_size, num_blocks, status,
+                                               reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? NS_OK : NS_ERR_CUDA;
+}
+
+size_t ns_paged_attn_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim)
+{
+    (void)num_q_heads;
+    (void)head_dim;
+    if (num_seqs < 0 || num_kv_heads <= 0)
+        return 0;
+    return ws_layout(num_seqs, num_kv_heads).total;
+}
+
+ns_status ns_paged_attn_workspace_init(void *workspace, size_t workspace_bytes, ns_stream_t stream)
+{
+    if (!workspace)
+        return NS_ERR_INVALID_ARG;
+    return cudaMemsetAsync(workspace, 0, workspace_bytes, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? NS_OK
+               : NS_ERR_CUDA;
+}
+
+ns_status ns_paged_attn_decode_ex(const void *q, const void *k_pool, const void *v_pool,
+                                  const int32_t *block_tables, const int32_t *context_lens,
+                                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int block_size, float scale, void *out, ns_stream_t stream,
+                                  int max_blocks_per_seq, int64_t num_blocks, ns_dtype dtype,
+                                  void *workspace, size_t workspace_bytes,
+                                  const ns_decode_config *cfg)
+{
+    const ns_status s = check_decode_args(q, k_pool, v_pool, block_tables, context_lens, num_seqs,
+                                          num_q_heads, num_kv_heads, head_dim, block_size, scale,
+                                          out, max_blocks_per_seq, num_blocks, dtype, workspace,
+                                          workspace_bytes, cfg);
+    if (s != NS_OK)
+        return s;
+    if (num_seqs == 0)
+        return NS_OK;
+    int dev = 0;
+    if (current_device(&dev) != cudaSuccess)
+        return NS_ERR_CUDA;
+    DecodeCall c{q, k_pool, v_pool, block_tables, context_lens, nullptr, num_seqs, num_q_heads,
+                 num_kv_heads, block_size, scale, out, reinterpret_cast<cudaStream_t>(stream),
+                 max_blocks_per_seq, num_blocks, dtype, workspace, cfg, nullptr, nullptr, nullptr};
+    return run_decode(c, dev);
+}
+
+ns_status ns_paged_attn_decode(const void *q, const void *k_pool, const void *v_pool,
+                               const int32_t *block_tables, const int32_t *context_lens,
+                               int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                               int block_size, float scale, void *out, ns_stream_t stream,
+                               int max_blocks_per_seq, int64_t num_blocks, ns_dtype dtype,
+                               void *workspace, size_t workspace_bytes)
+{
+    return ns_paged_attn_decode_ex(q, k_pool, v_pool, block_tables, context_lens, num_seqs,
+                                   num_q_heads, num_kv_heads, head_dim, block_size, scale, out,
+                                   stream, max_blocks_per_seq, num_blocks, dtype, workspace,
+                                   workspace_bytes, nullptr);
+}
+
+ns_status ns_kv_append_paged_attn_decode(const void *q, const void *k_new, const void *v_new,
+                                         const int64_t *slot_mapping, void *k_pool,
+                                         void *v_pool, const int32_t *block_tables,
+                                         const int32_t *context_lens, int num_seqs,
+                                         int num_q_heads, int num_kv_heads, int head_dim,
+                                         int block_size, float scale, void *out,
+                                         ns_stream_t stream, int max_blocks_per_seq,
+                                         int64_t num_blocks, ns_dtype dtype, void *workspace,
+                                         size_t workspace_bytes)
+{
+    const ns_status s = check_decode_args(q, k_pool, v_pool, block_tables, context_lens, num_seqs,
+                                          num_q_heads, num_kv_heads, head_dim, block_size, scale,
+                                          out, max_blocks_per_seq, num_blocks, dtype, workspace,
+                                          workspace_bytes, nullptr);
+    if (s != NS_OK)
+        return s;
+    if (num_seqs == 0)
+        return NS_OK;
+    if (!k_new || !v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new))
+        return NS_ERR_INVALID_ARG;
+    int dev = 0;
+    if (current_device(&dev) != cudaSuccess)
+        return NS_ERR_CUDA;
+    DecodeCall c{q, k_pool, v_pool, block_tables, context_lens, nullptr, num_seqs, num_q_heads,
+                 num_kv_heads, block_size, scale, out, reinterpret_cast<cudaStream_t>(stream),
+                 max_blocks_per_seq, num_blocks, dtype, workspace, nullptr, k_new, v_new,
+                 slot_mapping};
+    return run_decode(c, dev);
+}
+
+ns_status ns_read_decode_plan(const void *workspace, ns_decode_plan *plan, ns_stream_t stream)
+{
+    if (!workspace || !plan)
+        return NS_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(plan, workspace, sizeof(ns_decode_plan), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return NS_ERR_CUDA;
+    return NS_OK;
+}
+
+ns_status ns_paged_attn_prefill(const void *q, const int32_t *query_start_loc, const void *k_pool,
+                                const void *v_pool, const int32_t *block_tables,
+                                const int32_t *context_lens, int num_seqs, int total_q_tokens,
+                                int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                float scale, void *out, ns_stream_t stream, int max_blocks_per_seq,
+                                int64_t num_blocks, ns_dtype dtype, void *workspace,
+                                size_t workspace_bytes)
+{
+    if (num_seqs < 0 || total_q_tokens < 0 || !query_start_loc)
+        return NS_ERR_INVALID_ARG;
+    const ns_status s = check_decode_args(q, k_pool, v_pool, block_tables, context_lens,
+                                          total_q_tokens, num_q_heads, num_kv_heads, head_dim,
+                                          block_size, scale, out, max_blocks_per_seq, num_blocks,
+                                          dtype, workspace, workspace_bytes, nullptr);
+    if (s != NS_OK)
+        return s;
+    if (total_q_tokens == 0 || num_seqs == 0)
+        return NS_OK;
+    int dev = 0;
+    if (current_device(&dev) != cudaSuccess)
+        return NS_ERR_CUDA;
+    unsigned *status = status_word(dev);
+    if (status == nullptr)
+        return NS_ERR_CUDA;
+    const WsLayout L = ws_layout(total_q_tokens, num_kv_heads);
+    char *ws = static_cast<char *>(workspace);
+    int32_t *row_seq = reinterpret_cast<int32_t *>(ws + L.row_seq);
+    int32_t *row_len = reinterpret_cast<int32_t *>(ws + L.row_len);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (ns::launch_span_rows(query_start_loc, context_lens, num_seqs, total_q_tokens, row_seq,
+                             row_len, status, st) != cudaSuccess)
+        return NS_ERR_CUDA;
+    DecodeCall c{q, k_pool, v_pool, block_tables, row_len, row_seq, total_q_tokens, num_q_heads,
+                 num_kv_heads, block_size, scale, out, st, max_blocks_per_seq, num_blocks, dtype,
+                 workspace, nullptr, nullptr, nullptr, nullptr};
+    return run_decode(c, dev);
+}
+
+ns_status ns_get_device_status(ns_stream_t stream, uint32_t *bits, int clear)
+{
+    if (!bits)
+        return NS_ERR_INVALID_ARG;
+    int dev = 0;
+    if (current_device(&dev) != cudaSuccess)
+        return NS_ERR_CUDA;
+    unsigned *p = status_word(dev);
+    if (p == nullptr)
+        return NS_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned v = 0;
+    if (cudaMemcpyAsync(&v, p, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return NS_ERR_CUDA;
+    if (clear && cudaMemsetAsync(p, 0, sizeof(unsigned), s) != cudaSuccess)
+        return NS_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return NS_ERR_CUDA;
+    *bits = v;
+    return NS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,93 @@
+"""GPU parity of chunked-prefill attention over query spans."""
+import numpy as np
+import pytest
+import torch
+
+import _gpu
+from _gpu import DevStep, compare
+from paged_kv_decode_ns_gb300 import binding as nb
+from paged_kv_decode_ns_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def test_mixed_chunked_prefill_step(orc):
+    """16 decode rows + two 512-token chunks over 1500 / 3000 cached tokens."""
+    st = wl.mixed_chunked_prefill()
+    ref, kp, vp = orc.step(st, num_threads=max(1, orc.max_threads()))
+    d = DevStep(st)
+    d.append()
+    out = d.prefill()
+    torch.cuda.synchronize()
+    assert np.array_equal(_gpu.to_bits(d.k_pool), kp)
+    compare(out, ref, st.dtype, "mixed step")
+    _gpu.assert_no_device_status()
+
+
+@pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
+@pytest.mark.parametrize("bs", [4, 16])
+def test_spans_with_ragged_prefixes(dtype, bs, orc):
+    rng = np.random.default_rng(bs)
+    lens = np.array([1, 9, 40, 130, 77, 300], np.int32)
+    qlens = np.array([1, 9, 13, 1, 64, 33], np.int32)
+    st = wl.make_step(rng, lens, qlens, dtype=dtype, block_size=bs)
+    ref, kp, vp = orc.step(st)
+    d = DevStep(st)
+    d.append()
+    out = d.prefill()
+    torch.cuda.synchronize()
+    compare(out, ref, dtype, f"spans bs={bs}")
+    _gpu.assert_no_device_status()
+
+
+def test_chunked_writes_equal_whole_prompt(orc):
+    """The chunked-prefill worked example (8-token chunks, 4-token blocks):
+    appending the prompt chunk by chunk leaves the same pool as appending it
+    whole, and each chunk's attention matches the oracle."""
+    rng = np.random.default_rng(21)
+    whole, chunks, *_ = wl.chunked_prompt_steps(rng, 64, 8, dtype=wl.F16, block_size=4,
+                                                num_q_heads=14, num_kv_heads=2)
+    dw = DevStep(whole)
+    dw.append()
+    ow = dw.prefill().clone()
+    dc = DevStep(chunks[0])
+    outs = []
+    for st in chunks:
+        dc.st = st
+        dc.q = _gpu.to_dev(st.q, st.dtype)
+        dc.k_new = _gpu.to_dev(st.k_new, st.dtype)
+        dc.v_new = _gpu.to_dev(st.v_new, st.dtype)
+        dc.slot_mapping = _gpu.dev_ints(st.slot_mapping, np.int64)
+        dc.context_lens = _gpu.dev_ints(st.context_lens, np.int32)
+        dc.query_start_loc = _gpu.dev_ints(st.query_start_loc, np.int32)
+        dc.out = torch.empty_like(dc.q)
+        dc.append()
+        outs.append(dc.prefill().clone())
+    torch.cuda.synchronize()
+    assert torch.equal(dc.k_pool, dw.k_pool) and torch.equal(dc.v_pool, dw.v_pool)
+    ref, *_ = orc.step(whole)
+    compare(torch.cat(outs), ref, wl.F16, "chunked")
+    compare(ow, ref, wl.F16, "whole")
+    _gpu.assert_no_device_status()
+
+
+def test_single_row_spans_equal_decode(orc):
+    st = wl.decode_batch32()
+    ref, kp, vp = orc.step(st)
+    d = DevStep(st, k_pool=kp, v_pool=vp)
+    a = d.decode().clone()
+    b = d.prefill()
+    torch.cuda.synchronize()
+    compare(a, ref, st.dtype)
+    compare(b, ref, st.dtype)
+
+
+def test_bad_span_is_flagged():
+    rng = np.random.default_rng(5)
+    st = wl.make_step(rng, np.array([10, 10], np.int32), np.array([3, 2], np.int32),
+                      dtype=wl.F16)
+    d = DevStep(st)
+    d.context_lens = _gpu.dev_ints(np.array([2, 10], np.int32), np.int32)  # span longer than context
+    d.prefill()
+    torch.cuda.synchronize()
+    assert nb.ns_get_device_status(clear=True) & 0x20
