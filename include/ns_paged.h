@@ -250,8 +250,12 @@ ns_status ns_read_decode_plan(const void *workspace, ns_decode_plan *plan, ns_st
  *   query_start_loc int32 [num_seqs+1], nondecreasing, [0] == 0,
  *                   [num_seqs] == total_q_tokens (read)
  *   out             [total_q_tokens][num_q_heads][head_dim] (written)
- * Query-key products and probability-value products of spans longer than
- * one row run on the tensor cores (fp16/bf16 operands, fp32 accumulation).
+ * Spans of two or more rows run on the tcgen05 tensor cores when block_size
+ * is 16 or 32: query-key and probability-value products take fp16/bf16
+ * operands with fp32 accumulation (the probabilities are rounded to the
+ * element type before the second product).  Single-row spans, and every span
+ * for other block sizes, take the split-KV decode walk.  The workspace is
+ * sized with ns_paged_attn_workspace_bytes(total_q_tokens, ...).
  */
 ns_status ns_paged_attn_prefill(const void *q, const int32_t *query_start_loc,
                                 const void *k_pool, const void *v_pool,
@@ -261,6 +265,28 @@ ns_status ns_paged_attn_prefill(const void *q, const int32_t *query_start_loc,
                                 void *out, ns_stream_t stream, int max_blocks_per_seq,
                                 int64_t num_blocks, ns_dtype dtype, void *workspace,
                                 size_t workspace_bytes);
+
+/*
+ * Policy overrides for the chunked prefill (tests and measurements).
+ *   tensor_core_min_span  0 = auto: spans of 2 or more query tokens run on the
+ *                         tensor cores when block_size is 16 or 32; a positive
+ *                         value raises that threshold; -1 = never (every row
+ *                         takes the split-KV decode walk)
+ */
+typedef struct ns_prefill_config {
+    int tensor_core_min_span;
+    int reserved[7];
+} ns_prefill_config;
+
+/* ns_paged_attn_prefill with policy overrides (cfg may be NULL = auto). */
+ns_status ns_paged_attn_prefill_ex(const void *q, const int32_t *query_start_loc,
+                                   const void *k_pool, const void *v_pool,
+                                   const int32_t *block_tables, const int32_t *context_lens,
+                                   int num_seqs, int total_q_tokens, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int block_size, float scale,
+                                   void *out, ns_stream_t stream, int max_blocks_per_seq,
+                                   int64_t num_blocks, ns_dtype dtype, void *workspace,
+                                   size_t workspace_bytes, const ns_prefill_config *cfg);
 
 /*
  * Device status word of the current device: OR of NS_DEV_* bits raised by

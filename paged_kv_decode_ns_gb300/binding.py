@@ -41,6 +41,10 @@ class DecodeConfig(ctypes.Structure):
                 ("whole_sequences", ctypes.c_int), ("reserved", ctypes.c_int * 5)]
 
 
+class PrefillConfig(ctypes.Structure):
+    _fields_ = [("tensor_core_min_span", ctypes.c_int), ("reserved", ctypes.c_int * 7)]
+
+
 class DecodePlan(ctypes.Structure):
     _fields_ = [("ctas_launched", ctypes.c_int32), ("ctas_active", ctypes.c_int32),
                 ("total_blocks", ctypes.c_int64), ("split_pairs", ctypes.c_int32),
@@ -64,6 +68,8 @@ _SIGNATURES = {
                                            I64, I, P, SZ]),
     "ns_read_decode_plan": (I, [P, ctypes.POINTER(DecodePlan), P]),
     "ns_paged_attn_prefill": (I, [P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, I, I64, I, P, SZ]),
+    "ns_paged_attn_prefill_ex": (I, [P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, I, I64, I, P, SZ,
+                                     ctypes.POINTER(PrefillConfig)]),
     "ns_get_device_status": (I, [P, ctypes.POINTER(ctypes.c_uint32), I]),
 }
 
@@ -202,18 +208,21 @@ def ns_kv_append_paged_attn_decode(q, k_new, v_new, slot_mapping, k_pool, v_pool
 
 
 def ns_paged_attn_prefill(q, query_start_loc, k_pool, v_pool, block_tables, context_lens, scale,
-                          out, workspace, stream=None):
+                          out, workspace, config: PrefillConfig | None = None, stream=None):
     """Chunked-prefill attention of the query spans ``query_start_loc`` over the paged pool."""
     T, hq, hkv, d, bs, nb, dt, p = _attn_common(q, k_pool, v_pool, block_tables, context_lens,
                                                 out, workspace)
     S = context_lens.shape[0]
     if query_start_loc.shape != (S + 1,) or block_tables.shape[0] != S:
         raise ValueError("query_start_loc must be [num_seqs + 1]")
-    st = lib().ns_paged_attn_prefill(
-        p["q"], _dev(query_start_loc, "query_start_loc", torch.int32), p["k"], p["v"], p["bt"],
-        p["cl"], S, T, hq, hkv, d, bs, float(scale), p["out"], _stream(stream),
-        block_tables.shape[1], nb, dt, p["ws"], workspace.numel())
-    _check(st, "ns_paged_attn_prefill")
+    args = (p["q"], _dev(query_start_loc, "query_start_loc", torch.int32), p["k"], p["v"], p["bt"],
+            p["cl"], S, T, hq, hkv, d, bs, float(scale), p["out"], _stream(stream),
+            block_tables.shape[1], nb, dt, p["ws"], workspace.numel())
+    if config is None:
+        _check(lib().ns_paged_attn_prefill(*args), "ns_paged_attn_prefill")
+    else:
+        _check(lib().ns_paged_attn_prefill_ex(*args, ctypes.byref(config)),
+               "ns_paged_attn_prefill_ex")
 
 
 def ns_read_decode_plan(workspace, stream=None) -> dict:

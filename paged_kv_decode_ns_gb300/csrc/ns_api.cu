@@ -371,13 +371,14 @@ ns_status ns_read_decode_plan(const void *workspace, ns_decode_plan *plan, ns_st
     return NS_OK;
 }
 
-ns_status ns_paged_attn_prefill(const void *q, const int32_t *query_start_loc, const void *k_pool,
-                                const void *v_pool, const int32_t *block_tables,
-                                const int32_t *context_lens, int num_seqs, int total_q_tokens,
-                                int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                                float scale, void *out, ns_stream_t stream, int max_blocks_per_seq,
-                                int64_t num_blocks, ns_dtype dtype, void *workspace,
-                                size_t workspace_bytes)
+ns_status ns_paged_attn_prefill_ex(const void *q, const int32_t *query_start_loc,
+                                   const void *k_pool, const void *v_pool,
+                                   const int32_t *block_tables, const int32_t *context_lens,
+                                   int num_seqs, int total_q_tokens, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int block_size, float scale,
+                                   void *out, ns_stream_t stream, int max_blocks_per_seq,
+                                   int64_t num_blocks, ns_dtype dtype, void *workspace,
+                                   size_t workspace_bytes, const ns_prefill_config *cfg)
 {
     if (num_seqs < 0 || total_q_tokens < 0 || !query_start_loc)
         return NS_ERR_INVALID_ARG;
@@ -400,13 +401,39 @@ ns_status ns_paged_attn_prefill(const void *q, const int32_t *query_start_loc, c
     int32_t *row_seq = reinterpret_cast<int32_t *>(ws + L.row_seq);
     int32_t *row_len = reinterpret_cast<int32_t *>(ws + L.row_len);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (ns::launch_span_rows(query_start_loc, context_lens, num_seqs, total_q_tokens, row_seq,
-                             row_len, status, st) != cudaSuccess)
+    int tc_min = cfg && cfg->tensor_core_min_span != 0 ? cfg->tensor_core_min_span : 2;
+    if (tc_min < 0 || !ns::tc_prefill_supported(block_size, num_q_heads / num_kv_heads) ||
+        (long long)num_blocks * num_kv_heads * block_size > 0x7fffffffLL)
+        tc_min = 0;
+    if (ns::launch_span_rows(query_start_loc, context_lens, num_seqs, total_q_tokens, tc_min,
+                             row_seq, row_len, status, st) != cudaSuccess)
         return NS_ERR_CUDA;
     DecodeCall c{q, k_pool, v_pool, block_tables, row_len, row_seq, total_q_tokens, num_q_heads,
                  num_kv_heads, block_size, scale, out, st, max_blocks_per_seq, num_blocks, dtype,
                  workspace, nullptr, nullptr, nullptr, nullptr};
-    return run_decode(c, dev);
+    const ns_status r = run_decode(c, dev);
+    if (r != NS_OK || tc_min == 0)
+        return r;
+    return ns::launch_tc_prefill(q, query_start_loc, k_pool, v_pool, block_tables, context_lens,
+                                 num_seqs, total_q_tokens, num_q_heads, num_kv_heads, block_size,
+                                 scale, out, max_blocks_per_seq, num_blocks, dtype, status,
+                                 st) == cudaSuccess
+               ? NS_OK
+               : NS_ERR_CUDA;
+}
+
+ns_status ns_paged_attn_prefill(const void *q, const int32_t *query_start_loc, const void *k_pool,
+                                const void *v_pool, const int32_t *block_tables,
+                                const int32_t *context_lens, int num_seqs, int total_q_tokens,
+                                int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                float scale, void *out, ns_stream_t stream, int max_blocks_per_seq,
+                                int64_t num_blocks, ns_dtype dtype, void *workspace,
+                                size_t workspace_bytes)
+{
+    return ns_paged_attn_prefill_ex(q, query_start_loc, k_pool, v_pool, block_tables, context_lens,
+                                    num_seqs, total_q_tokens, num_q_heads, num_kv_heads, head_dim,
+                                    block_size, scale, out, stream, max_blocks_per_seq, num_blocks,
+                                    dtype, workspace, workspace_bytes, nullptr);
 }
 
 ns_status ns_get_device_status(ns_stream_t stream, uint32_t *bits, int clear)

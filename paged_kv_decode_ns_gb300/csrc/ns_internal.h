@@ -12,9 +12,20 @@ cudaError_t launch_kv_append(const void *k, const void *v, const int64_t *slot_m
                              void *v_pool, int num_tokens, int num_kv_heads, int block_size,
                              long long num_blocks, unsigned *status, cudaStream_t stream);
 
-// Query spans -> per-row table row and key count (prefill through the decode walk).
+// Query spans -> per-row table row and key count (prefill through the decode
+// walk).  Rows of spans with at least `tc_min_span` tokens (tc_min_span > 0)
+// are marked for the tensor-core kernel: table row -1, key count 0.
 cudaError_t launch_span_rows(const int32_t *query_start_loc, const int32_t *context_lens,
-                             int num_seqs, int total_rows, int32_t *row_seq, int32_t *row_len,
-                             unsigned *status, cudaStream_t stream);
+                             int num_seqs, int total_rows, int tc_min_span, int32_t *row_seq,
+                             int32_t *row_len, unsigned *status, cudaStream_t stream);
+
+// Chunked prefill of every span of two or more tokens on the tcgen05 tensor cores.
+bool tc_prefill_supported(int block_size, int group);
+cudaError_t launch_tc_prefill(const void *q, const int32_t *query_start_loc, const void *k_pool,
+                              const void *v_pool, const int32_t *block_tables,
+                              const int32_t *context_lens, int num_seqs, int total_q_tokens,
+                              int num_q_heads, int num_kv_heads, int block_size, float scale,
+                              void *out, int max_blocks_per_seq, long long num_blocks, ns_dtype dtype,
+                              unsigned *status, cudaStream_t stream);
 
 }  // namespace ns

@@ -692,7 +692,8 @@ __device__ bool decode_prologue(const DecodeParams &P, DecodeSmem<BS, NW, STAGES
     for (int s = s_lo; s < s_hi; ++s) {
         const int L = clamped_len(P, s, BS, report);
         mine += (long long)Hkv * nblocks_of(L, BS);
-        if (L == 0 && (s % (int)gridDim.x) == (int)blockIdx.x) {
+        if (L == 0 && (s % (int)gridDim.x) == (int)blockIdx.x &&
+            (P.table_row == nullptr || __ldg(P.table_row + s) >= 0)) {
             uint16_t *o = P.out + (long long)s * P.num_q_heads * kHeadDim;
             for (int i = 0; i < P.num_q_heads * kHeadDim; ++i)
                 o[i] = 0;

@@ -5,15 +5,17 @@
 // causal within the chunk (Inference Engineering Day 12 short, "What is
 // chunked prefill within vLLM").  This kernel writes, per query row, the
 // sequence whose block table it walks and its key count L - n + i + 1, so the
-// split-KV decode walk can serve the rows.
+// split-KV decode walk can serve the rows.  Rows of spans long enough for the
+// tensor-core kernel get table row -1 and are left to that kernel.
 #include "ns_common.cuh"
 #include "ns_internal.h"
 
 namespace ns {
 
 __global__ void span_rows_kernel(const int32_t *__restrict__ qsl, const int32_t *__restrict__ lens,
-                                 int num_seqs, int total_rows, int32_t *__restrict__ row_seq,
-                                 int32_t *__restrict__ row_len, unsigned *status)
+                                 int num_seqs, int total_rows, int tc_min_span,
+                                 int32_t *__restrict__ row_seq, int32_t *__restrict__ row_len,
+                                 unsigned *status)
 {
     const int v = blockIdx.x * blockDim.x + threadIdx.x;
     if (v >= total_rows)
@@ -36,19 +38,20 @@ __global__ void span_rows_kernel(const int32_t *__restrict__ qsl, const int32_t 
         raise_status(status, NS_DEV_BAD_QUERY_SPAN);
         keys = 0;
     }
-    row_seq[v] = s;
-    row_len[v] = keys;
+    const bool tensor_core = tc_min_span > 0 && n >= tc_min_span;
+    row_seq[v] = tensor_core ? -1 : s;
+    row_len[v] = tensor_core ? 0 : keys;
 }
 
 cudaError_t launch_span_rows(const int32_t *query_start_loc, const int32_t *context_lens,
-                             int num_seqs, int total_rows, int32_t *row_seq, int32_t *row_len,
-                             unsigned *status, cudaStream_t stream)
+                             int num_seqs, int total_rows, int tc_min_span, int32_t *row_seq,
+                             int32_t *row_len, unsigned *status, cudaStream_t stream)
 {
     if (total_rows <= 0)
         return cudaSuccess;
     const int threads = 256;
     span_rows_kernel<<<(total_rows + threads - 1) / threads, threads, 0, stream>>>(
-        query_start_loc, context_lens, num_seqs, total_rows, row_seq, row_len, status);
+        query_start_loc, context_lens, num_seqs, total_rows, tc_min_span, row_seq, row_len, status);
     return cudaGetLastError();
 }
 

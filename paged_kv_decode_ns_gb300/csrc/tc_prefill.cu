@@ -1,0 +1,551 @@
+// tc_prefill.cu -- chunked-prefill attention on the tcgen05 tensor cores.
+//
+// What it computes (Inference Engineering Day 12 short, "What is chunked
+// prefill within vLLM"; nanoserve project page, "What I built"): query token i
+// of a span of n tokens in a sequence of L tokens sits at position L-n+i and
+// attends to keys 0..L-n+i -- the cached prefix plus causally within the
+// chunk -- through the sequence's block table.
+//
+// Work unit: (span, kv head, query tile).  A query tile is QT tokens x G query
+// heads of one GQA group packed into M = QT*G <= 128 rows (row r = token r/G,
+// head r%G), so every K/V tile is loaded once for all heads of the group.
+//
+//   warp 5   producer: TMA 3D load of the Q tile; per 128-key tile, one TMA 2D
+//            load per pool block for K and for V (128-byte swizzle), into a
+//            2-stage ring;
+//   warp 4   allocates 256 TMEM columns; lane 0 issues tcgen05.mma:
+//              S[128x128] = Q K^T   (4 steps of K=16, A and B K-major)
+//              O[128x64] += P V     (8 steps of K=16, P K-major from shared
+//                                    memory, V MN-major)
+//            and commits each group to an mbarrier;
+//   warps 0-3 softmax: thread t owns row t (TMEM lane t).  It reads its S row
+//            from TMEM, masks keys past its position, keeps a running max and
+//            sum (max moves lazily, by more than 8 in log2 units), writes P as
+//            fp16/bf16 into a 128-byte-swizzled K-major panel, rescales its O
+//            row in TMEM when the max moved, and finally writes O / sum.
+// Values of keys past the context are zeroed in shared memory before the PV
+// product, so undefined (even NaN) pool slots never reach the accumulator.
+#include <cudaTypedefs.h>
+
+#include "ns_internal.h"
+#include "tcgen05.cuh"
+
+namespace ns {
+
+namespace {
+
+constexpr int kKT = 128;         // keys per K/V tile
+constexpr int kRows = 128;       // MMA M
+constexpr int kTmemCols = 256;   // S: columns [0,128), O: [128,192)
+constexpr int kTmemO = 128;
+constexpr int kStages = 2;
+constexpr int kThreads = 192;    // warps 0-3 softmax, 4 MMA, 5 producer
+constexpr float kSlack = 8.0f;   // lazy rescale: the max moves by more than this (log2 units)
+
+struct PrefillParams {
+    const int32_t *qsl;
+    const int32_t *context_lens;
+    const int32_t *block_tables;
+    uint16_t *out;
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;
+    int qt;  // tokens per query tile
+    int max_blocks_per_seq;
+    long long num_blocks;
+    float scale_log2;
+    unsigned *status;
+};
+
+struct alignas(1024) PrefillSmem {
+    uint8_t q[kRows * 128];
+    uint8_t k[kStages][kKT * 128];
+    uint8_t v[kStages][kKT * 128];
+    uint8_t p[2][kRows * 128];  // keys 0..63 and 64..127
+    uint64_t q_full;
+    uint64_t kv_full[kStages];
+    uint64_t kv_empty[kStages];
+    uint64_t s_full;
+    uint64_t s_free;
+    uint64_t p_full;
+    uint64_t o_done;
+    uint32_t tmem_base;
+    uint32_t loaded[kStages];  // bit i: block i of the tile was loaded
+    int u_s, u_h, u_i0, u_n, u_L, u_tiles, u_ok;
+};
+
+constexpr size_t kSmemBytes = sizeof(PrefillSmem) + 1024;  // + alignment slack
+
+__device__ __forceinline__ PrefillSmem &smem_of(unsigned char *raw)
+{
+    const uintptr_t a = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023);
+    return *reinterpret_cast<PrefillSmem *>(a);
+}
+
+// Find this CTA's unit.  Units are enumerated spans last-to-first (later
+// chunks sit on longer prefixes), query tiles last-to-first, then kv heads.
+__device__ void find_unit(const PrefillParams &P, PrefillSmem &sm, int lane)
+{
+    const long long u = blockIdx.x;
+    long long base = 0;
+    int found = 0;
+    for (int s0 = P.num_seqs - 1; s0 >= 0 && !found; s0 -= 32) {
+        const int s = s0 - lane;
+        int tiles = 0;
+        if (s >= 0) {
+            const int n = __ldg(P.qsl + s + 1) - __ldg(P.qsl + s);
+            tiles = n >= 2 ? (n + P.qt - 1) / P.qt : 0;
+        }
+        long long w = (long long)tiles * P.num_kv_heads;
+        long long incl = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+        const long long excl = base + incl - w;
+        const bool mine = w > 0 && u >= excl && u < excl + w;
+        const unsigned who = __ballot_sync(0xffffffffu, mine);
+        if (who) {
+            found = 1;
+            if (mine) {
+                const long long r = u - excl;
+                const int tile_rev = (int)(r / P.num_kv_heads);
+                const int h = (int)(r % P.num_kv_heads);
+                const int n = __ldg(P.qsl + s + 1) - __ldg(P.qsl + s);
+                const int ntiles = (n + P.qt - 1) / P.qt;
+                const int tile = ntiles - 1 - tile_rev;
+                sm.u_s = s;
+                sm.u_h = h;
+                sm.u_i0 = tile * P.qt;
+                sm.u_n = n;
+                sm.u_L = __ldg(P.context_lens + s);
+                sm.u_ok = 1;
+            }
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0 && !found)
+        sm.u_ok = -1;  // no unit for this CTA
+}
+
+template <typename T, int BS>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const PrefillParams P)
+{
+    extern __shared__ unsigned char smem_raw[];
+    PrefillSmem &sm = smem_of(smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = P.group;
+
+    if (warp == 5) {
+        find_unit(P, sm, lane);
+        __syncwarp();
+        if (lane == 0 && sm.u_ok == 1) {
+            const int n = sm.u_n;
+            int L = sm.u_L;
+            const long long cap = (long long)P.max_blocks_per_seq * BS;
+            if (L < n || n < 1 || L < 0) {
+                raise_status(P.status, NS_DEV_BAD_QUERY_SPAN);
+                sm.u_ok = 0;
+            } else if (L > cap) {
+                raise_status(P.status, NS_DEV_BAD_CONTEXT_LEN);
+                sm.u_ok = 0;
+            } else {
+                const int last_tok = min(sm.u_i0 + P.qt, n) - 1;
+                const long long keys = (long long)(L - n) + last_tok + 1;
+                sm.u_tiles = (int)((keys + kKT - 1) / kKT);
+            }
+        }
+    }
+    if (threadIdx.x == 0) {
+        mbar_init(&sm.q_full, 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&sm.kv_full[i], 1);
+            mbar_init(&sm.kv_empty[i], 1);
+        }
+        mbar_init(&sm.s_full, 1);
+        mbar_init(&sm.s_free, 128);
+        mbar_init(&sm.p_full, 128);
+        mbar_init(&sm.o_done, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (sm.u_ok != 1)
+        return;
+    // Rows of the Q tile the TMA box does not cover are zeroed once.
+    if (warp < 4 && (int)threadIdx.x >= P.qt * G) {
+#pragma unroll
+        for (int b = 0; b < kRowBytes; b += 16)
+            *reinterpret_cast<uint4 *>(sm.q + threadIdx.x * kRowBytes + b) = make_uint4(0, 0, 0, 0);
+        tc::fence_async_smem();
+    }
+    if (warp == 4) {
+        tc::tmem_alloc(&sm.tmem_base, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+
+    const int s = sm.u_s, h = sm.u_h, i0 = sm.u_i0, n = sm.u_n, L = sm.u_L;
+    const int tiles = sm.u_tiles;
+    const int prefix = L - n;
+    const uint32_t tmem = sm.tmem_base;
+    const int ab_fmt = T::code == NS_BF16 ? 1 : 0;
+
+    if (warp == 5) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tc::prefetch_tensormap(&tm_q);
+            tc::prefetch_tensormap(&tm_k);
+            tc::prefetch_tensormap(&tm_v);
+            mbar_arrive_expect_tx(&sm.q_full, (uint32_t)(P.qt * G * kRowBytes));
+            tc::tma_load_3d(sm.q, &tm_q, 0, h * G, __ldg(P.qsl + s) + i0, &sm.q_full);
+        }
+        constexpr int kBlocksPerTile = kKT / BS;
+        const int nb_seq = (L + BS - 1) / BS;
+        bool ok = true;
+        int issued = 0;
+        for (int j = 0; ok && j < tiles; ++j) {
+            const int stage = j % kStages;
+            const uint32_t par = ((uint32_t)(j / kStages) & 1u) ^ 1u;
+            int phys = -1;
+            const int blk = j * kBlocksPerTile + lane;
+            if (lane < kBlocksPerTile && blk < nb_seq) {
+                phys = __ldg(P.block_tables + (long long)s * P.max_blocks_per_seq + blk);
+                if (phys < 0 || (long long)phys >= P.num_blocks) {
+                    raise_status(P.status, NS_DEV_BAD_BLOCK_ID);
+                    phys = -1;
+                }
+            }
+            const unsigned mask = __ballot_sync(0xffffffffu, phys >= 0);
+            if (lane == 0) {
+                if (!mbar_wait(&sm.kv_empty[stage], par)) {
+                    raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
+                    ok = false;
+                } else {
+                    sm.loaded[stage] = mask;
+                    mbar_arrive_expect_tx(&sm.kv_full[stage],
+                                          (uint32_t)__popc(mask) * 2u * BS * kRowBytes);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (ok && phys >= 0) {
+                const int row = (int)(((long long)phys * P.num_kv_heads + h) * BS);
+                tc::tma_load_2d(sm.k[stage] + lane * BS * kRowBytes, &tm_k, 0, row, &sm.kv_full[stage]);
+                tc::tma_load_2d(sm.v[stage] + lane * BS * kRowBytes, &tm_v, 0, row, &sm.kv_full[stage]);
+            }
+            if (ok)
+                issued = j + 1;
+        }
+        // Never leave while copies may still land in this CTA's shared memory.
+        if (lane == 0) {
+            bool drained = mbar_wait(&sm.q_full, 0);
+            for (int k = 1; drained && k <= kStages && k <= issued; ++k) {
+                const int j = issued - k;
+                drained = mbar_wait(&sm.kv_full[j % kStages], (uint32_t)(j / kStages) & 1u);
+            }
+            if (!drained)
+                raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
+        }
+        __syncwarp();
+    } else if (warp == 4) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            const uint32_t idesc_s = tc::idesc_f16(kRows, kKT, ab_fmt, false);
+            const uint32_t idesc_o = tc::idesc_f16(kRows, kHeadDim, ab_fmt, true);
+            const uint32_t q_addr = smem_addr(sm.q);
+            bool ok = mbar_wait(&sm.q_full, 0);
+            for (int j = 0; ok && j < tiles; ++j) {
+                const int stage = j % kStages;
+                ok = mbar_wait(&sm.kv_full[stage], (uint32_t)(j / kStages) & 1u);
+                if (ok && j > 0)
+                    ok = mbar_wait(&sm.s_free, (uint32_t)(j - 1) & 1u);
+                if (!ok)
+                    break;
+                tc::fence_after_sync();
+                const uint32_t k_addr = smem_addr(sm.k[stage]);
+#pragma unroll
+                for (int kk = 0; kk < kHeadDim / 16; ++kk)
+                    tc::mma_ss(tmem, tc::desc_sw128(q_addr + kk * 32), tc::desc_sw128(k_addr + kk * 32),
+                               idesc_s, kk > 0 ? 1u : 0u);
+                tc::mma_commit(&sm.s_full);
+                ok = mbar_wait(&sm.p_full, (uint32_t)j & 1u);
+                if (!ok)
+                    break;
+                tc::fence_after_sync();
+                const uint32_t v_addr = smem_addr(sm.v[stage]);
+#pragma unroll
+                for (int kk = 0; kk < kKT / 16; ++kk) {
+                    const uint32_t p_addr = smem_addr(sm.p[kk >> 2]) + (kk & 3) * 32;
+                    tc::mma_ss(tmem + kTmemO, tc::desc_sw128(p_addr),
+                               tc::desc_sw128(v_addr + kk * 16 * kRowBytes), idesc_o,
+                               (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc::mma_commit(&sm.o_done);
+                tc::mma_commit(&sm.kv_empty[stage]);
+            }
+            if (!ok)
+                raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int r = threadIdx.x;  // row == TMEM lane
+        const int tok = r / G;
+        const bool row_ok = r < P.qt * G && i0 + tok < n;
+        const int pos = row_ok ? prefix + i0 + tok : -1;
+        const int pos_lo = prefix + i0;  // smallest position in the tile
+        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < tiles; ++j) {
+            const int stage = j % kStages;
+            if (!mbar_wait(&sm.s_full, (uint32_t)j & 1u)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            float sv[kKT];
+#pragma unroll
+            for (int c = 0; c < kKT / 32; ++c)
+                tc::tmem_ld32(lane_addr + c * 32, *reinterpret_cast<float(*)[32]>(&sv[c * 32]));
+            tc::tmem_ld_wait();
+            tc::fence_before_sync();
+            mbar_arrive(&sm.s_free);
+
+            const int kbase = j * kKT;
+            const bool masked = kbase + kKT - 1 > pos_lo;
+            float tmax = -INFINITY;
+            if (masked) {
+#pragma unroll
+                for (int c = 0; c < kKT; ++c) {
+                    sv[c] = (kbase + c <= pos) ? sv[c] : -INFINITY;
+                    tmax = fmaxf(tmax, sv[c]);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kKT; ++c)
+                    tmax = fmaxf(tmax, sv[c]);
+            }
+            tmax *= P.scale_log2;  // scale > 0 keeps the order
+            float m_new = m;
+            if (tmax > m + kSlack)
+                m_new = tmax;
+            const float alpha = fast_exp2(m - m_new);
+            const bool rescale = (m_new != m) && j > 0;
+            l *= (m_new != m) ? alpha : 1.f;
+            m = m_new;
+
+            uint32_t pk[kKT / 2];
+            float lsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < kKT; c += 2) {
+                float p0 = fast_exp2(fmaf(sv[c], P.scale_log2, -m));
+                float p1 = fast_exp2(fmaf(sv[c + 1], P.scale_log2, -m));
+                if (masked) {
+                    p0 = sv[c] > -INFINITY ? p0 : 0.f;
+                    p1 = sv[c + 1] > -INFINITY ? p1 : 0.f;
+                }
+                lsum += p0 + p1;
+                pk[c >> 1] = pack2<T>(p0, p1);
+            }
+            l += lsum;
+
+            // PV of the previous tile must be done before P and O are touched.
+            if (j > 0 && !mbar_wait(&sm.o_done, (uint32_t)(j - 1) & 1u)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            if (__any_sync(0xffffffffu, rescale)) {
+                const float a = rescale ? alpha : 1.f;
+#pragma unroll
+                for (int c = 0; c < kHeadDim / 32; ++c) {
+                    float ov[32];
+                    tc::tmem_ld32(lane_addr + kTmemO + c * 32, ov);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        ov[e] *= a;
+                    tc::tmem_st32(lane_addr + kTmemO + c * 32, ov);
+                }
+                tc::tmem_st_wait();
+            }
+            // P row r: 16-byte chunk q (keys 8q..8q+7) of panel q/8 at chunk (q%8) ^ (r%8)
+#pragma unroll
+            for (int q = 0; q < kKT / 8; ++q) {
+                uint8_t *dst = sm.p[q >> 3] + r * 128 + (((q & 7) ^ (r & 7)) << 4);
+                *reinterpret_cast<uint4 *>(dst) =
+                    make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            }
+            // Values of keys past the context, or of blocks that were not
+            // loaded, must be zero: P is zero there but 0 * NaN is not.
+            if (masked || sm.loaded[stage] != (1u << (kKT / BS)) - 1u) {
+                if (!mbar_wait(&sm.kv_full[stage], (uint32_t)(j / kStages) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                const int key = kbase + r;
+                const bool blk_loaded = (sm.loaded[stage] >> (r / BS)) & 1u;
+                if (key >= L || !blk_loaded) {
+#pragma unroll
+                    for (int b = 0; b < kRowBytes; b += 16)
+                        *reinterpret_cast<uint4 *>(sm.v[stage] + r * kRowBytes + b) = make_uint4(0, 0, 0, 0);
+                }
+            }
+            tc::fence_async_smem();
+            tc::fence_before_sync();
+            mbar_arrive(&sm.p_full);
+        }
+        // ---- epilogue: O / l
+        if (ok && mbar_wait(&sm.o_done, (uint32_t)(tiles - 1) & 1u)) {
+            tc::fence_after_sync();
+            float ov[kHeadDim];
+#pragma unroll
+            for (int c = 0; c < kHeadDim / 32; ++c)
+                tc::tmem_ld32(lane_addr + kTmemO + c * 32, *reinterpret_cast<float(*)[32]>(&ov[c * 32]));
+            tc::tmem_ld_wait();
+            if (row_ok) {
+                const float inv = 1.f / l;
+                const long long tok_g = __ldg(P.qsl + s) + i0 + tok;
+                uint16_t *o = P.out + (tok_g * P.num_q_heads + (long long)h * G + (r % G)) * kHeadDim;
+#pragma unroll
+                for (int c = 0; c < kHeadDim; c += 8) {
+                    uint4 w;
+                    w.x = pack2<T>(ov[c] * inv, ov[c + 1] * inv);
+                    w.y = pack2<T>(ov[c + 2] * inv, ov[c + 3] * inv);
+                    w.z = pack2<T>(ov[c + 4] * inv, ov[c + 5] * inv);
+                    w.w = pack2<T>(ov[c + 6] * inv, ov[c + 7] * inv);
+                    *reinterpret_cast<uint4 *>(o + c) = w;
+                }
+            }
+        } else {
+            raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 4) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Host side: tensor maps and launch.
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+static bool encode(CUtensorMap *map, ns_dtype dt, int rank, const void *base, const cuuint64_t *dims,
+                   const cuuint64_t *strides, const cuuint32_t *box)
+{
+    auto fn = encode_fn();
+    if (fn == nullptr)
+        return false;
+    cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, dt == NS_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          (cuuint32_t)rank, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool tc_prefill_supported(int block_size, int group)
+{
+    return (block_size == 16 || block_size == 32) && group >= 1 && group <= kMaxGroup;
+}
+
+template <typename T, int BS>
+static cudaError_t launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                             const PrefillParams &P, int grid, cudaStream_t stream)
+{
+    static int done_mask = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (!(dev < 31 && ((done_mask >> dev) & 1))) {
+        e = cudaFuncSetAttribute(tc_prefill_kernel<T, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBytes);
+        if (e != cudaSuccess)
+            return e;
+        if (dev < 31)
+            __atomic_fetch_or(&done_mask, 1 << dev, __ATOMIC_RELAXED);
+    }
+    tc_prefill_kernel<T, BS><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, P);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tc_prefill(const void *q, const int32_t *query_start_loc, const void *k_pool,
+                              const void *v_pool, const int32_t *block_tables,
+                              const int32_t *context_lens, int num_seqs, int total_q_tokens,
+                              int num_q_heads, int num_kv_heads, int block_size, float scale,
+                              void *out, int max_blocks_per_seq, long long num_blocks, ns_dtype dtype,
+                              unsigned *status, cudaStream_t stream)
+{
+    const int G = num_q_heads / num_kv_heads;
+    const int qt = kRows / G;
+    CUtensorMap tq, tk, tv;
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)num_q_heads, (cuuint64_t)total_q_tokens};
+        const cuuint64_t strides[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)num_q_heads * kRowBytes};
+        const cuuint32_t box[3] = {(cuuint32_t)kHeadDim, (cuuint32_t)G, (cuuint32_t)qt};
+        if (!encode(&tq, dtype, 3, q, dims, strides, box))
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t rows = (cuuint64_t)num_blocks * num_kv_heads * block_size;
+        const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)kRowBytes};
+        const cuuint32_t box[2] = {(cuuint32_t)kHeadDim, (cuuint32_t)block_size};
+        if (!encode(&tk, dtype, 2, k_pool, dims, strides, box) ||
+            !encode(&tv, dtype, 2, v_pool, dims, strides, box))
+            return cudaErrorInvalidValue;
+    }
+    PrefillParams P;
+    P.qsl = query_start_loc;
+    P.context_lens = context_lens;
+    P.block_tables = block_tables;
+    P.out = static_cast<uint16_t *>(out);
+    P.num_seqs = num_seqs;
+    P.num_q_heads = num_q_heads;
+    P.num_kv_heads = num_kv_heads;
+    P.group = G;
+    P.qt = qt;
+    P.max_blocks_per_seq = max_blocks_per_seq;
+    P.num_blocks = num_blocks;
+    P.scale_log2 = scale * 1.4426950408889634f;
+    P.status = status;
+    // an upper bound on the units; CTAs without one exit at once
+    const long long units = (long long)num_kv_heads * ((total_q_tokens + qt - 1) / qt + num_seqs);
+    const int grid = (int)(units > 0x7fffffff ? 0x7fffffff : units);
+    if (grid == 0)
+        return cudaSuccess;
+    if (dtype == NS_BF16)
+        return block_size == 16 ? launch_tc<BF16, 16>(tq, tk, tv, P, grid, stream)
+                                : launch_tc<BF16, 32>(tq, tk, tv, P, grid, stream);
+    return block_size == 16 ? launch_tc<F16, 16>(tq, tk, tv, P, grid, stream)
+                            : launch_tc<F16, 32>(tq, tk, tv, P, grid, stream);
+}
+
+}  // namespace ns

@@ -91,3 +91,46 @@ def test_bad_span_is_flagged():
     d.prefill()
     torch.cuda.synchronize()
     assert nb.ns_get_device_status(clear=True) & 0x20
+
+
+def _prefill_cfg(min_span):
+    c = nb.PrefillConfig()
+    c.tensor_core_min_span = min_span
+    return c
+
+
+@pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
+@pytest.mark.parametrize("bs", [16, 32])
+@pytest.mark.parametrize("hq,hkv", [(14, 2), (8, 1), (4, 2), (2, 2), (16, 2)])
+def test_tensor_core_spans(dtype, bs, hq, hkv, orc):
+    """Spans of 2+ rows on the tcgen05 kernel: ragged prefixes, query tiles
+    cut mid-span, key tiles cut mid-block, both element types."""
+    rng = np.random.default_rng(100 + bs + hq)
+    lens = np.array([2, 30, 150, 129, 400, 700], np.int32)
+    qlens = np.array([2, 30, 19, 128, 37, 300], np.int32)
+    st = wl.make_step(rng, lens, qlens, dtype=dtype, block_size=bs, num_q_heads=hq,
+                      num_kv_heads=hkv, poison_unused=True)
+    ref, kp, vp = orc.step(st)
+    d = DevStep(st)
+    d.append()
+    out = d.prefill()
+    torch.cuda.synchronize()
+    compare(out, ref, dtype, f"tc bs={bs} Hq={hq} Hkv={hkv}")
+    _gpu.assert_no_device_status()
+
+
+def test_tensor_core_and_cuda_core_paths_agree(orc):
+    st = wl.mixed_chunked_prefill()
+    ref, kp, vp = orc.step(st, num_threads=max(1, orc.max_threads()))
+    d = DevStep(st, k_pool=kp, v_pool=vp)
+    nb.ns_paged_attn_prefill(d.q, d.query_start_loc, d.k_pool, d.v_pool, d.block_tables,
+                             d.context_lens, st.scale, d.out, d.ws, config=_prefill_cfg(-1))
+    cuda_core = d.out.clone()
+    nb.ns_paged_attn_prefill(d.q, d.query_start_loc, d.k_pool, d.v_pool, d.block_tables,
+                             d.context_lens, st.scale, d.out, d.ws, config=_prefill_cfg(2))
+    torch.cuda.synchronize()
+    compare(cuda_core, ref, st.dtype, "cuda-core path")
+    compare(d.out, ref, st.dtype, "tensor-core path")
+    # the 16 single-row decode spans take the same walk on both paths
+    assert torch.equal(cuda_core[:16], d.out[:16])
+    _gpu.assert_no_device_status()
