@@ -161,12 +161,14 @@ def make_workload(name: str):
 
 
 def workload_config(st, name, pools):
+    step = ("fused kv_append + split-KV paged decode" if st.is_decode
+            else "kv_append + chunked prefill (tensor-core spans, decode-walk rows)")
     return {"workload": f"{st.name}: {name}", "num_seqs": st.num_seqs,
             "context_tokens": int(st.context_lens.sum()),
             "max_context": int(st.context_lens.max()),
             "num_q_heads": st.num_q_heads, "num_kv_heads": st.num_kv_heads,
             "head_dim": st.head_dim, "block_size": st.block_size,
-            "num_blocks": st.num_blocks, "step": "fused kv_append + split-KV paged decode",
+            "num_blocks": st.num_blocks, "step": step, "query_tokens": st.num_tokens,
             "l2": (f"inputs larger than L2: {pools} rotating pool copies of "
                    f"{2 * st.k_pool.nbytes / 1e6:.0f} MB each (L2 129 MB)")}
 
@@ -197,6 +199,90 @@ def host_cores() -> int:
 # our arm
 # ---------------------------------------------------------------------------
 
+def prefill_flops(st) -> int:
+    """Tensor-core flops of the spans of 2+ rows: 4*D*Hq per (row, key it sees)."""
+    f = 0
+    for s in range(st.num_seqs):
+        n, L = int(st.query_lens[s]), int(st.context_lens[s])
+        if n >= 2:
+            keys = n * (L - n) + n * (n + 1) // 2
+            f += 4 * st.head_dim * st.num_q_heads * keys
+    return f
+
+
+class Step:
+    """Device-resident state of one workload and the public-API call of one step.
+
+    Decode workloads: one fused call (append the new token of every sequence
+    and run the split-KV decode).  The mixed workload: ns_kv_append of all new
+    tokens, then ns_paged_attn_prefill over every span.
+    """
+
+    def __init__(self, st, dev, npools):
+        import torch
+        from paged_kv_decode_ns_gb300 import binding as nb
+        self.nb, self.torch, self.st, self.dev = nb, torch, st, dev
+
+        def dt_of(bits):
+            t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev)
+            return t.view(torch.bfloat16 if st.dtype == "bf16" else torch.float16)
+
+        def ints(a, dt):
+            return torch.from_numpy(np.ascontiguousarray(a, dtype=dt)).to(dev)
+
+        k0, v0 = dt_of(st.k_pool), dt_of(st.v_pool)
+        self.pools = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(npools - 1)]
+        self.npools = npools
+        self.q = dt_of(st.q)
+        self.k_new, self.v_new = dt_of(st.k_new), dt_of(st.v_new)
+        self.slots = ints(st.slot_mapping, np.int64)
+        self.tables = ints(st.block_tables, np.int32)
+        self.lens = ints(st.context_lens, np.int32)
+        self.qsl = ints(st.query_start_loc, np.int32)
+        self.out = torch.empty_like(self.q)
+        self.ws = nb.alloc_workspace(st.num_tokens, st.num_q_heads, st.num_kv_heads,
+                                     st.head_dim, dev)
+        self.decode = st.is_decode
+        self.inputs = [self.q, self.k_new, self.v_new, self.slots, self.tables, self.lens]
+        if not self.decode:
+            self.inputs.append(self.qsl)
+        # kernels per step: fused decode = 1; append + span rows + walk + tensor-core = 4
+        self.launches = 1 if self.decode else 4
+
+    def run(self, i, stream=None):
+        kp, vp = self.pools[i % self.npools]
+        if self.decode:
+            self.nb.ns_kv_append_paged_attn_decode(self.q, self.k_new, self.v_new, self.slots, kp,
+                                                   vp, self.tables, self.lens, self.st.scale,
+                                                   self.out, self.ws, stream=stream)
+        else:
+            self.nb.ns_kv_append(self.k_new, self.v_new, self.slots, kp, vp, stream=stream)
+            self.nb.ns_paged_attn_prefill(self.q, self.qsl, kp, vp, self.tables, self.lens,
+                                          self.st.scale, self.out, self.ws, stream=stream)
+
+    def run_dominant(self, i, stream=None):
+        """The dominant kernel alone: the fused decode, or the tensor-core prefill."""
+        if self.decode:
+            return self.run(i, stream)
+        kp, vp = self.pools[i % self.npools]
+        cfg = self.nb.PrefillConfig()
+        cfg.phases = self.nb.NS_PREFILL_TENSOR_CORE
+        self.nb.ns_paged_attn_prefill(self.q, self.qsl, kp, vp, self.tables, self.lens,
+                                      self.st.scale, self.out, self.ws, config=cfg, stream=stream)
+
+
+def time_events(torch, stream, fn, n):
+    """Mean device time of fn(i) over n calls, each bracketed by events (ms)."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for i, (a, b) in enumerate(evs):
+        a.record(stream)
+        fn(i)
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
 def bench_ours(args):
     import torch
     from paged_kv_decode_ns_gb300 import binding as nb
@@ -206,39 +292,16 @@ def bench_ours(args):
     dist = init_dist(world, "nccl")
     dev = torch.device("cuda", local)
     st = make_workload(args.workload)
-
-    def dt_of(bits):
-        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev)
-        return t.view(torch.bfloat16 if st.dtype == "bf16" else torch.float16)
-
-    def ints(a, dt):
-        return torch.from_numpy(np.ascontiguousarray(a, dtype=dt)).to(dev)
-
-    # device-resident state: the pool (rotated copies so that no step finds
-    # its K/V in L2), the step's inputs, the output and the workspace
     pool_bytes = 2 * st.k_pool.nbytes
     npools = max(1, args.pools if args.pools else math.ceil(2 * L2_BYTES / max(pool_bytes, 1)))
-    k0, v0 = dt_of(st.k_pool), dt_of(st.v_pool)
-    pools = [(k0, v0)] + [(k0.clone(), v0.clone()) for _ in range(npools - 1)]
-    q = dt_of(st.q)
-    k_new, v_new = dt_of(st.k_new), dt_of(st.v_new)
-    slots = ints(st.slot_mapping, np.int64)
-    tables = ints(st.block_tables, np.int32)
-    lens = ints(st.context_lens, np.int32)
-    out = torch.empty_like(q)
-    ws = nb.alloc_workspace(st.num_seqs, st.num_q_heads, st.num_kv_heads, st.head_dim, dev)
+    step = Step(st, dev, npools)
     stream = torch.cuda.current_stream(dev)
-
-    def step(i):
-        kp, vp = pools[i % npools]
-        nb.ns_kv_append_paged_attn_decode(q, k_new, v_new, slots, kp, vp, tables, lens,
-                                          st.scale, out, ws, stream=stream)
 
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
     for i in range(args.warmup):
-        step(i)
+        step.run(i)
     torch.cuda.synchronize(dev)
     nb.raise_on_device_status()
 
@@ -248,29 +311,49 @@ def bench_ours(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
-        step(i)
+        step.run(i)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(dist)
     elapsed_ms = e0.elapsed_time(e1)
 
-    # ---- per-launch duration of the decode kernel (events on its stream)
-    n_lat = min(args.steps, 200)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(n_lat)]
-    for i, (a, b) in enumerate(evs):
-        a.record(stream)
-        step(i)
-        b.record(stream)
-    torch.cuda.synchronize(dev)
-    launch_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    # ---- the dominant kernel per launch (events on its stream)
+    n_lat = max(3, min(args.steps, 200))
+    launch_ms = time_events(torch, stream, step.run_dominant, n_lat)
+
+    # ---- CUDA-graph replay of the same steps (launch overhead removed)
+    graph_us = None
+    if args.graph:
+        per_graph = 2 * npools
+        g = torch.cuda.CUDAGraph()
+        s2 = torch.cuda.Stream(dev)
+        s2.wait_stream(stream)
+        with torch.cuda.stream(s2):
+            for i in range(per_graph):          # warm the capture stream's path
+                step.run(i)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(g):
+            for i in range(per_graph):
+                step.run(i)
+        reps = max(3, args.steps // per_graph)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        graph_us = 1e3 * g0.elapsed_time(g1) / (reps * per_graph)
+        del g
 
     # keep the GPU busy long enough for the clock sampler (untimed)
     t_end = time.time() + max(0.0, args.soak_s - elapsed_ms / 1e3)
     i = 0
     while time.time() < t_end:
         for _ in range(200):
-            step(i)
+            step.run(i)
             i += 1
         torch.cuda.synchronize(dev)
     clocks = sampler.stop() if sampler else None
@@ -279,26 +362,25 @@ def bench_ours(args):
     # ---- end to end through the public API with host buffers
     def pinned(t):
         return torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
-    h_in = [pinned(x) for x in (q, k_new, v_new, slots, tables, lens)]
-    d_in = [q, k_new, v_new, slots, tables, lens]
-    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h_in = [pinned(x) for x in step.inputs]
+    h_out = torch.empty(step.out.shape, dtype=step.out.dtype, pin_memory=True)
     h2d = sum(x.numel() * x.element_size() for x in h_in)
     d2h = h_out.numel() * h_out.element_size()
     n_e2e = max(1, min(args.steps, args.e2e_steps))
-    for i in range(3):
-        for h, d in zip(h_in, d_in):
+
+    def e2e_step(i):
+        for h, d in zip(h_in, step.inputs):
             d.copy_(h, non_blocking=True)
-        step(i)
-        h_out.copy_(out, non_blocking=True)
+        step.run(i)
+        h_out.copy_(step.out, non_blocking=True)
+    for i in range(3):
+        e2e_step(i)
     torch.cuda.synchronize(dev)
     barrier(dist)
     e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2.record(stream)
     for i in range(n_e2e):
-        for h, d in zip(h_in, d_in):
-            d.copy_(h, non_blocking=True)
-        step(i)
-        h_out.copy_(out, non_blocking=True)
+        e2e_step(i)
     e3.record(stream)
     torch.cuda.synchronize(dev)
     barrier(dist)
@@ -313,34 +395,48 @@ def bench_ours(args):
         return None
 
     peaks, peak_src = measured_peaks()
-    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    achieved = alg_bytes / (launch_ms * 1e-3) / 1e9
     value = units / (t_max * 1e-3) / 1e9
+    if step.decode:
+        peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+        achieved = alg_bytes / (launch_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                    "frac": achieved / peak, "traffic": args.traffic,
+                    "kernel": "paged_decode_kernel (fused kv_append + split-KV decode)",
+                    "bytes_per_launch": alg_bytes, "launch_us": launch_ms * 1e3,
+                    "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"}
+    else:
+        # fp16 and bf16 share the nominal dense tensor rate: bf16 peak x 1.0
+        peak = float(peaks.get("bf16_tflops", 1900.0))
+        flops = prefill_flops(st)
+        achieved = flops / (launch_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": args.traffic,
+                    "kernel": "tc_prefill_kernel (tcgen05, spans of 2+ rows)",
+                    "flops_per_launch": flops, "launch_us": launch_ms * 1e3,
+                    "peak_source": f"{peak_src} bf16_tflops (burst) x nominal fp16/bf16 ratio 1.0"}
     cpu = None
     if args.cpu_baseline:
         cores = host_cores()
-        secs, kvb, n, thr = run_cpu_oracle(st, cores)
+        max_seqs = None if step.decode else 16
+        secs, kvb, n, thr = run_cpu_oracle(st, cores, max_seqs=max_seqs)
         cpu = {"value": kvb / secs / 1e9, "unit": "GB/s", "cores": thr, "kind": "oracle",
-               "sample": f"all {n} sequences of the batch, attention only, one pass, "
-                         f"{secs:.2f} s (fp64 C oracle, OpenMP over (sequence, head))"}
+               "sample": f"{'all' if n == st.num_seqs else 'first'} {n} sequences of the "
+                         f"batch (decode rows), attention only, one pass, {secs:.2f} s "
+                         f"(fp64 C oracle, OpenMP over (row, head))"}
     return {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": t_max / args.steps, "us_per_step": 1e3 * t_max / args.steps,
-        "hbm_peak_frac": value / peak,
+        "graph_us_per_step": graph_us, "hbm_peak_frac": value / float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS)),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": st.dtype, "data": "synthetic (seeded; no dataset or weights involved)",
         "config": workload_config(st, args.workload, npools),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": args.traffic,
-                     "kernel": "paged_decode_kernel (fused kv_append)",
-                     "bytes_per_launch": alg_bytes, "launch_us": launch_ms * 1e3,
-                     "peak_source": f"{peak_src} hbm_gbs"},
+        "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": units_e2e / (te2e_max * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "us_per_step": 1e3 * te2e_max / n_e2e, "steps": n_e2e},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * step.launches,
         "clocks": clocks,
     }
 
@@ -396,6 +492,7 @@ def main(argv=None):
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch from an ncu capture of the current kernel")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-graph", dest="graph", action="store_false")
     ap.add_argument("--reference-budget-s", type=float, default=120.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -272,10 +272,17 @@ ns_status ns_paged_attn_prefill(const void *q, const int32_t *query_start_loc,
  *                         tensor cores when block_size is 16 or 32; a positive
  *                         value raises that threshold; -1 = never (every row
  *                         takes the split-KV decode walk)
+ *   phases                0 = everything; else a mask of the parts to run
+ *                         (NS_PREFILL_WALK: the split-KV walk over the rows it
+ *                         owns, NS_PREFILL_TENSOR_CORE: the tensor-core spans),
+ *                         so each part can be timed on its own
  */
+#define NS_PREFILL_WALK 1
+#define NS_PREFILL_TENSOR_CORE 2
 typedef struct ns_prefill_config {
     int tensor_core_min_span;
-    int reserved[7];
+    int phases;
+    int reserved[6];
 } ns_prefill_config;
 
 /* ns_paged_attn_prefill with policy overrides (cfg may be NULL = auto). */

@@ -19,6 +19,8 @@ NS_OK = 0
 NS_F16 = 0
 NS_BF16 = 1
 NS_MAX_CTAS = 1024
+NS_PREFILL_WALK = 1
+NS_PREFILL_TENSOR_CORE = 2
 DEV_BITS = {
     0x1: "NS_DEV_BAD_BLOCK_ID",
     0x2: "NS_DEV_BAD_CONTEXT_LEN",
@@ -42,7 +44,8 @@ class DecodeConfig(ctypes.Structure):
 
 
 class PrefillConfig(ctypes.Structure):
-    _fields_ = [("tensor_core_min_span", ctypes.c_int), ("reserved", ctypes.c_int * 7)]
+    _fields_ = [("tensor_core_min_span", ctypes.c_int), ("phases", ctypes.c_int),
+                ("reserved", ctypes.c_int * 6)]
 
 
 class DecodePlan(ctypes.Structure):

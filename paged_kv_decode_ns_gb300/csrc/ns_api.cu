@@ -405,15 +405,20 @@ ns_status ns_paged_attn_prefill_ex(const void *q, const int32_t *query_start_loc
     if (tc_min < 0 || !ns::tc_prefill_supported(block_size, num_q_heads / num_kv_heads) ||
         (long long)num_blocks * num_kv_heads * block_size > 0x7fffffffLL)
         tc_min = 0;
-    if (ns::launch_span_rows(query_start_loc, context_lens, num_seqs, total_q_tokens, tc_min,
-                             row_seq, row_len, status, st) != cudaSuccess)
-        return NS_ERR_CUDA;
-    DecodeCall c{q, k_pool, v_pool, block_tables, row_len, row_seq, total_q_tokens, num_q_heads,
-                 num_kv_heads, block_size, scale, out, st, max_blocks_per_seq, num_blocks, dtype,
-                 workspace, nullptr, nullptr, nullptr, nullptr};
-    const ns_status r = run_decode(c, dev);
-    if (r != NS_OK || tc_min == 0)
-        return r;
+    const int phases = cfg && cfg->phases != 0 ? cfg->phases : (NS_PREFILL_WALK | NS_PREFILL_TENSOR_CORE);
+    if (phases & NS_PREFILL_WALK) {
+        if (ns::launch_span_rows(query_start_loc, context_lens, num_seqs, total_q_tokens, tc_min,
+                                 row_seq, row_len, status, st) != cudaSuccess)
+            return NS_ERR_CUDA;
+        DecodeCall c{q, k_pool, v_pool, block_tables, row_len, row_seq, total_q_tokens, num_q_heads,
+                     num_kv_heads, block_size, scale, out, st, max_blocks_per_seq, num_blocks, dtype,
+                     workspace, nullptr, nullptr, nullptr, nullptr};
+        const ns_status r = run_decode(c, dev);
+        if (r != NS_OK)
+            return r;
+    }
+    if (tc_min == 0 || !(phases & NS_PREFILL_TENSOR_CORE))
+        return NS_OK;
     return ns::launch_tc_prefill(q, query_start_loc, k_pool, v_pool, block_tables, context_lens,
                                  num_seqs, total_q_tokens, num_q_heads, num_kv_heads, block_size,
                                  scale, out, max_blocks_per_seq, num_blocks, dtype, status,

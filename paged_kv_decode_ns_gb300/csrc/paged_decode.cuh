@@ -222,7 +222,8 @@ __device__ __forceinline__ void process_block(const uint16_t *__restrict__ kb,
         const bool grow = z > m_run + kRescaleSlack;
         if (__any_sync(0xffffffffu, grow)) {
             const float m_new = grow ? z : m_run;
-            const float alpha = fast_exp2(m_run - m_new);  // 1 if unchanged, 0 from -inf
+            // 1 for lanes whose max stays (also at -inf: -inf - -inf would be NaN); 0 from -inf
+            const float alpha = grow ? fast_exp2(m_run - z) : 1.f;
             l_run *= alpha;
             m_run = m_new;
 #pragma unroll
