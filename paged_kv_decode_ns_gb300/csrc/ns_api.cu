@@ -16,10 +16,7 @@ __device__ unsigned int g_device_status;
 constexpr int kMaxDevices = 64;
 std::atomic<unsigned *> g_status_ptr[kMaxDevices];
 std::atomic<int> g_sm_count[kMaxDevices];
-std::atomic<int> g_ctas_per_sm[kMaxDevices][2][4];
-
-// Split-KV policy default: a CTA gets at least this many KV blocks.
-constexpr int kDefaultMinBlocksPerCta = 8;
+std::atomic<int> g_ctas_per_sm[kMaxDevices][2][4][ns::kMaxGroup];
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -68,34 +65,64 @@ int sm_count(int dev)
     return n;
 }
 
-template <typename T>
-cudaError_t dispatch_decode(int bs, const ns::DecodeParams &P, int ctas, cudaStream_t s)
+template <typename T, int BS>
+cudaError_t dispatch_decode_g(int g, const ns::DecodeParams &P, int ctas, cudaStream_t s)
 {
-    switch (bs) {
-    case 4: return ns::launch_paged_decode<T, 4>(P, ctas, s);
-    case 8: return ns::launch_paged_decode<T, 8>(P, ctas, s);
-    case 16: return ns::launch_paged_decode<T, 16>(P, ctas, s);
-    default: return ns::launch_paged_decode<T, 32>(P, ctas, s);
+    switch (g) {
+    case 1: return ns::launch_paged_decode<T, BS, 1>(P, ctas, s);
+    case 2: return ns::launch_paged_decode<T, BS, 2>(P, ctas, s);
+    case 3: return ns::launch_paged_decode<T, BS, 3>(P, ctas, s);
+    case 4: return ns::launch_paged_decode<T, BS, 4>(P, ctas, s);
+    case 5: return ns::launch_paged_decode<T, BS, 5>(P, ctas, s);
+    case 6: return ns::launch_paged_decode<T, BS, 6>(P, ctas, s);
+    case 7: return ns::launch_paged_decode<T, BS, 7>(P, ctas, s);
+    default: return ns::launch_paged_decode<T, BS, 8>(P, ctas, s);
     }
 }
 
 template <typename T>
-int dispatch_ctas_per_sm(int bs)
+cudaError_t dispatch_decode(int bs, int g, const ns::DecodeParams &P, int ctas, cudaStream_t s)
 {
     switch (bs) {
-    case 4: return ns::decode_ctas_per_sm<T, 4>();
-    case 8: return ns::decode_ctas_per_sm<T, 8>();
-    case 16: return ns::decode_ctas_per_sm<T, 16>();
-    default: return ns::decode_ctas_per_sm<T, 32>();
+    case 4: return dispatch_decode_g<T, 4>(g, P, ctas, s);
+    case 8: return dispatch_decode_g<T, 8>(g, P, ctas, s);
+    case 16: return dispatch_decode_g<T, 16>(g, P, ctas, s);
+    default: return dispatch_decode_g<T, 32>(g, P, ctas, s);
     }
 }
 
-int resident_ctas(int dev, ns_dtype dt, int bs)
+template <typename T, int BS>
+int ctas_per_sm_g(int g)
 {
-    std::atomic<int> &slot = g_ctas_per_sm[dev][dt == NS_BF16 ? 1 : 0][bs_index(bs)];
+    switch (g) {
+    case 1: return ns::decode_ctas_per_sm<T, BS, 1>();
+    case 2: return ns::decode_ctas_per_sm<T, BS, 2>();
+    case 3: return ns::decode_ctas_per_sm<T, BS, 3>();
+    case 4: return ns::decode_ctas_per_sm<T, BS, 4>();
+    case 5: return ns::decode_ctas_per_sm<T, BS, 5>();
+    case 6: return ns::decode_ctas_per_sm<T, BS, 6>();
+    case 7: return ns::decode_ctas_per_sm<T, BS, 7>();
+    default: return ns::decode_ctas_per_sm<T, BS, 8>();
+    }
+}
+
+template <typename T>
+int dispatch_ctas_per_sm(int bs, int g)
+{
+    switch (bs) {
+    case 4: return ctas_per_sm_g<T, 4>(g);
+    case 8: return ctas_per_sm_g<T, 8>(g);
+    case 16: return ctas_per_sm_g<T, 16>(g);
+    default: return ctas_per_sm_g<T, 32>(g);
+    }
+}
+
+int resident_ctas(int dev, ns_dtype dt, int bs, int g)
+{
+    std::atomic<int> &slot = g_ctas_per_sm[dev][dt == NS_BF16 ? 1 : 0][bs_index(bs)][g - 1];
     int n = slot.load(std::memory_order_relaxed);
     if (n <= 0) {
-        n = dt == NS_BF16 ? dispatch_ctas_per_sm<ns::BF16>(bs) : dispatch_ctas_per_sm<ns::F16>(bs);
+        n = dt == NS_BF16 ? dispatch_ctas_per_sm<ns::BF16>(bs, g) : dispatch_ctas_per_sm<ns::F16>(bs, g);
         slot.store(n, std::memory_order_relaxed);
     }
     long long total = (long long)n * sm_count(dev);
@@ -188,15 +215,17 @@ ns_status run_decode(const DecodeCall &c, int dev)
     P.plan = reinterpret_cast<ns_decode_plan *>(ws + L.plan);
     P.status = status;
     P.min_blocks_per_cta = (c.cfg && c.cfg->min_blocks_per_cta > 0) ? c.cfg->min_blocks_per_cta
-                                                                     : kDefaultMinBlocksPerCta;
+                                                                     : ns::kDefaultMinBlocksPerCta;
     P.whole_sequences = (c.cfg && c.cfg->whole_sequences) ? 1 : 0;
 
-    int ctas = (c.cfg && c.cfg->num_ctas > 0) ? c.cfg->num_ctas : resident_ctas(dev, c.dtype, c.block_size);
+    const int g = P.group;
+    int ctas = (c.cfg && c.cfg->num_ctas > 0) ? c.cfg->num_ctas
+                                              : resident_ctas(dev, c.dtype, c.block_size, g);
     if (ctas > NS_MAX_CTAS)
         ctas = NS_MAX_CTAS;
     const cudaError_t e = c.dtype == NS_BF16
-                              ? dispatch_decode<ns::BF16>(c.block_size, P, ctas, c.stream)
-                              : dispatch_decode<ns::F16>(c.block_size, P, ctas, c.stream);
+                              ? dispatch_decode<ns::BF16>(c.block_size, g, P, ctas, c.stream)
+                              : dispatch_decode<ns::F16>(c.block_size, g, P, ctas, c.stream);
     return e == cudaSuccess ? NS_OK : NS_ERR_CUDA;
 }
 

@@ -59,6 +59,13 @@ __device__ __forceinline__ void mbar_init_fence()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Generic-proxy accesses to shared memory are ordered with later async-proxy
+// (TMA / tensor core) accesses to it.
+__device__ __forceinline__ void fence_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
@@ -104,10 +111,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
 // multiple of 16), completing on an mbarrier.  The L2 policy marks the
 // streamed K/V as evict-first so they do not push out reused data.
 // ---------------------------------------------------------------------------
+// Build-time knob: 0 gives the streamed K/V the default (evict-normal) policy.
+#ifndef NS_KV_EVICT_FIRST
+#define NS_KV_EVICT_FIRST 1
+#endif
+
 __device__ __forceinline__ uint64_t l2_evict_first_policy()
 {
     uint64_t pol;
+#if NS_KV_EVICT_FIRST
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+#else
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+#endif
     return pol;
 }
 

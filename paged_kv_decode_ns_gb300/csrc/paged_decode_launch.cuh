@@ -1,39 +1,27 @@
 // paged_decode_launch.cuh -- host launch of the decode kernel for one element
-// type and block size (included by the per-type instantiation files).
+// type, block size and group size (included by the instantiation files).
 #pragma once
 
 #include "paged_decode.cuh"
 
 namespace ns {
 
-constexpr int kDecodeWarps = 4;  // consumer warps per CTA (one block each per stage)
-
-// Shared-memory ring depth: about 64 KB of K/V staging per CTA.
-constexpr int decode_stages(int BS)
-{
-    return (65536 / (kDecodeWarps * 2 * BS * kRowBytes)) < 2 ? 2
-           : (65536 / (kDecodeWarps * 2 * BS * kRowBytes)) > 8
-               ? 8
-               : (65536 / (kDecodeWarps * 2 * BS * kRowBytes));
-}
-
-template <typename T, int BS>
+template <typename T, int BS, int G>
 struct DecodeKernel {
-    static constexpr int NW = kDecodeWarps;
-    static constexpr int STAGES = decode_stages(BS);
-    static constexpr int THREADS = (NW + 1) * 32;
-    static constexpr size_t SMEM = sizeof(DecodeSmem<BS, NW, STAGES>);
-    static void (*fn())(const DecodeParams) { return paged_decode_kernel<T, BS, NW, STAGES>; }
+    static constexpr int S = decode_stages(BS);
+    static constexpr int THREADS = kDecodeWarps * 32;
+    static constexpr size_t SMEM = sizeof(DecodeSmem<BS, G, S>);
+    static void (*fn())(const DecodeParams) { return paged_decode_kernel<T, BS, G, S>; }
 
     static cudaError_t prepare()
     {
-        // Opt in to more than 48 KB of dynamic shared memory (per device; cheap to repeat).
+        // Opt in to more than 48 KB of dynamic shared memory (per device).
         static int done_mask = 0;
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e != cudaSuccess)
             return e;
-        if (dev < 31 && (done_mask >> dev) & 1)
+        if (dev < 31 && ((__atomic_load_n(&done_mask, __ATOMIC_RELAXED) >> dev) & 1))
             return cudaSuccess;
         e = cudaFuncSetAttribute(fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
         if (e == cudaSuccess && dev < 31)
@@ -42,10 +30,10 @@ struct DecodeKernel {
     }
 };
 
-template <typename T, int BS>
+template <typename T, int BS, int G>
 cudaError_t launch_paged_decode(const DecodeParams &P, int num_ctas, cudaStream_t stream)
 {
-    using K = DecodeKernel<T, BS>;
+    using K = DecodeKernel<T, BS, G>;
     cudaError_t e = K::prepare();
     if (e != cudaSuccess)
         return e;
@@ -53,10 +41,10 @@ cudaError_t launch_paged_decode(const DecodeParams &P, int num_ctas, cudaStream_
     return cudaGetLastError();
 }
 
-template <typename T, int BS>
+template <typename T, int BS, int G>
 int decode_ctas_per_sm()
 {
-    using K = DecodeKernel<T, BS>;
+    using K = DecodeKernel<T, BS, G>;
     if (K::prepare() != cudaSuccess)
         return 1;
     int n = 0;
@@ -65,8 +53,18 @@ int decode_ctas_per_sm()
     return n;
 }
 
+#define NS_INSTANTIATE_DECODE_G(T, BS, G)                                                          \
+    template cudaError_t launch_paged_decode<T, BS, G>(const DecodeParams &, int, cudaStream_t);   \
+    template int decode_ctas_per_sm<T, BS, G>();
+
 #define NS_INSTANTIATE_DECODE(T, BS)                                                               \
-    template cudaError_t launch_paged_decode<T, BS>(const DecodeParams &, int, cudaStream_t);      \
-    template int decode_ctas_per_sm<T, BS>();
+    NS_INSTANTIATE_DECODE_G(T, BS, 1)                                                              \
+    NS_INSTANTIATE_DECODE_G(T, BS, 2)                                                              \
+    NS_INSTANTIATE_DECODE_G(T, BS, 3)                                                              \
+    NS_INSTANTIATE_DECODE_G(T, BS, 4)                                                              \
+    NS_INSTANTIATE_DECODE_G(T, BS, 5)                                                              \
+    NS_INSTANTIATE_DECODE_G(T, BS, 6)                                                              \
+    NS_INSTANTIATE_DECODE_G(T, BS, 7)                                                              \
+    NS_INSTANTIATE_DECODE_G(T, BS, 8)
 
 }  // namespace ns

@@ -58,11 +58,20 @@ struct PrefillParams {
     unsigned *status;
 };
 
+// P goes to the tensor core as fp16/bf16.  For bf16 one rounding (2^-9
+// relative) is too coarse, so P is split into P_hi + P_lo (both bf16, about
+// 16 bits together) and multiplied by V twice.
+template <typename T>
+struct PParts {
+    static constexpr int N = T::code == NS_BF16 ? 2 : 1;
+};
+
+template <int NP>
 struct alignas(1024) PrefillSmem {
     uint8_t q[kRows * 128];
     uint8_t k[kStages][kKT * 128];
     uint8_t v[kStages][kKT * 128];
-    uint8_t p[2][kRows * 128];  // keys 0..63 and 64..127
+    uint8_t p[NP][2][kRows * 128];  // [part][keys 0..63 | 64..127]
     uint64_t q_full;
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
@@ -75,17 +84,23 @@ struct alignas(1024) PrefillSmem {
     int u_s, u_h, u_i0, u_n, u_L, u_tiles, u_ok;
 };
 
-constexpr size_t kSmemBytes = sizeof(PrefillSmem) + 1024;  // + alignment slack
+template <int NP>
+constexpr size_t smem_bytes()
+{
+    return sizeof(PrefillSmem<NP>) + 1024;  // + alignment slack
+}
 
-__device__ __forceinline__ PrefillSmem &smem_of(unsigned char *raw)
+template <int NP>
+__device__ __forceinline__ PrefillSmem<NP> &smem_of(unsigned char *raw)
 {
     const uintptr_t a = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023);
-    return *reinterpret_cast<PrefillSmem *>(a);
+    return *reinterpret_cast<PrefillSmem<NP> *>(a);
 }
 
 // Find this CTA's unit.  Units are enumerated spans last-to-first (later
 // chunks sit on longer prefixes), query tiles last-to-first, then kv heads.
-__device__ void find_unit(const PrefillParams &P, PrefillSmem &sm, int lane)
+template <int NP>
+__device__ void find_unit(const PrefillParams &P, PrefillSmem<NP> &sm, int lane)
 {
     const long long u = blockIdx.x;
     long long base = 0;
@@ -136,8 +151,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const PrefillParams P)
 {
+    constexpr int NP = PParts<T>::N;
     extern __shared__ unsigned char smem_raw[];
-    PrefillSmem &sm = smem_of(smem_raw);
+    PrefillSmem<NP> &sm = smem_of<NP>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = P.group;
 
@@ -259,35 +275,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc_s = tc::idesc_f16(kRows, kKT, ab_fmt, false);
             const uint32_t idesc_o = tc::idesc_f16(kRows, kHeadDim, ab_fmt, true);
             const uint32_t q_addr = smem_addr(sm.q);
-            bool ok = mbar_wait(&sm.q_full, 0);
-            for (int j = 0; ok && j < tiles; ++j) {
-                const int stage = j % kStages;
-                ok = mbar_wait(&sm.kv_full[stage], (uint32_t)(j / kStages) & 1u);
-                if (ok && j > 0)
-                    ok = mbar_wait(&sm.s_free, (uint32_t)(j - 1) & 1u);
-                if (!ok)
-                    break;
-                tc::fence_after_sync();
-                const uint32_t k_addr = smem_addr(sm.k[stage]);
+            // S_j = Q K_j^T into TMEM columns [0, 128)
+            auto issue_s = [&](int j) {
+                const uint32_t k_addr = smem_addr(sm.k[j % kStages]);
 #pragma unroll
                 for (int kk = 0; kk < kHeadDim / 16; ++kk)
                     tc::mma_ss(tmem, tc::desc_sw128(q_addr + kk * 32), tc::desc_sw128(k_addr + kk * 32),
                                idesc_s, kk > 0 ? 1u : 0u);
                 tc::mma_commit(&sm.s_full);
+            };
+            // Order: S_0, then per tile j: S_{j+1} as soon as the softmax has
+            // read S_j, then PV_j once P_j is in shared memory -- the softmax
+            // of tile j overlaps S_{j+1} and PV_{j-1} on the tensor core.
+            bool ok = mbar_wait(&sm.q_full, 0) && mbar_wait(&sm.kv_full[0], 0);
+            if (ok) {
+                tc::fence_after_sync();
+                issue_s(0);
+            }
+            for (int j = 0; ok && j < tiles; ++j) {
+                if (j + 1 < tiles) {
+                    ok = mbar_wait(&sm.kv_full[(j + 1) % kStages], (uint32_t)((j + 1) / kStages) & 1u) &&
+                         mbar_wait(&sm.s_free, (uint32_t)j & 1u);
+                    if (!ok)
+                        break;
+                    tc::fence_after_sync();
+                    issue_s(j + 1);
+                }
                 ok = mbar_wait(&sm.p_full, (uint32_t)j & 1u);
                 if (!ok)
                     break;
                 tc::fence_after_sync();
-                const uint32_t v_addr = smem_addr(sm.v[stage]);
+                const uint32_t v_addr = smem_addr(sm.v[j % kStages]);
 #pragma unroll
-                for (int kk = 0; kk < kKT / 16; ++kk) {
-                    const uint32_t p_addr = smem_addr(sm.p[kk >> 2]) + (kk & 3) * 32;
-                    tc::mma_ss(tmem + kTmemO, tc::desc_sw128(p_addr),
-                               tc::desc_sw128(v_addr + kk * 16 * kRowBytes), idesc_o,
-                               (j > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int part = 0; part < NP; ++part)
+#pragma unroll
+                    for (int kk = 0; kk < kKT / 16; ++kk) {
+                        const uint32_t p_addr = smem_addr(sm.p[part][kk >> 2]) + (kk & 3) * 32;
+                        tc::mma_ss(tmem + kTmemO, tc::desc_sw128(p_addr),
+                                   tc::desc_sw128(v_addr + kk * 16 * kRowBytes), idesc_o,
+                                   (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                    }
                 tc::mma_commit(&sm.o_done);
-                tc::mma_commit(&sm.kv_empty[stage]);
+                tc::mma_commit(&sm.kv_empty[j % kStages]);
             }
             if (!ok)
                 raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
@@ -353,6 +382,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 lsum += p0 + p1;
                 pk[c >> 1] = pack2<T>(p0, p1);
+                if (NP == 2) {
+                    // keep the rounding residue of P for the second product
+                    const float2 hi = unpack2<T>(pk[c >> 1]);
+                    sv[c] = p0 - hi.x;
+                    sv[c + 1] = p1 - hi.y;
+                }
             }
             l += lsum;
 
@@ -379,9 +414,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             // P row r: 16-byte chunk q (keys 8q..8q+7) of panel q/8 at chunk (q%8) ^ (r%8)
 #pragma unroll
             for (int q = 0; q < kKT / 8; ++q) {
-                uint8_t *dst = sm.p[q >> 3] + r * 128 + (((q & 7) ^ (r & 7)) << 4);
+                uint8_t *dst = sm.p[0][q >> 3] + r * 128 + (((q & 7) ^ (r & 7)) << 4);
                 *reinterpret_cast<uint4 *>(dst) =
                     make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            }
+            if (NP == 2) {
+#pragma unroll
+                for (int q = 0; q < kKT / 8; ++q) {
+                    uint8_t *dst = sm.p[NP - 1][q >> 3] + r * 128 + (((q & 7) ^ (r & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(dst) =
+                        make_uint4(pack2<T>(sv[8 * q], sv[8 * q + 1]), pack2<T>(sv[8 * q + 2], sv[8 * q + 3]),
+                                   pack2<T>(sv[8 * q + 4], sv[8 * q + 5]), pack2<T>(sv[8 * q + 6], sv[8 * q + 7]));
+                }
             }
             // Values of keys past the context, or of blocks that were not
             // loaded, must be zero: P is zero there but 0 * NaN is not.
@@ -486,13 +530,13 @@ static cudaError_t launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const
         return e;
     if (!(dev < 31 && ((done_mask >> dev) & 1))) {
         e = cudaFuncSetAttribute(tc_prefill_kernel<T, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSmemBytes);
+                                 (int)smem_bytes<PParts<T>::N>());
         if (e != cudaSuccess)
             return e;
         if (dev < 31)
             __atomic_fetch_or(&done_mask, 1 << dev, __ATOMIC_RELAXED);
     }
-    tc_prefill_kernel<T, BS><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, P);
+    tc_prefill_kernel<T, BS><<<grid, kThreads, smem_bytes<PParts<T>::N>(), stream>>>(tq, tk, tv, P);
     return cudaGetLastError();
 }
 

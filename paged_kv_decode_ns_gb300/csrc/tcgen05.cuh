@@ -43,10 +43,7 @@ __device__ __forceinline__ void fence_after_sync()
 }
 
 // Generic-proxy writes to shared memory -> visible to the tensor core / TMA.
-__device__ __forceinline__ void fence_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
+__device__ __forceinline__ void fence_async_smem() { ns::fence_async_smem(); }
 
 // ---- matrix descriptors -----------------------------------------------------
 // Shared-memory matrix descriptor, 128-byte swizzle: start address, leading
