@@ -296,6 +296,37 @@ ns_status ns_paged_attn_prefill_ex(const void *q, const int32_t *query_start_loc
                                    size_t workspace_bytes, const ns_prefill_config *cfg);
 
 /*
+ * ns_paged_attn_decode_noalloc -- ns_paged_attn_decode for callers that
+ * cannot allocate device memory.
+ *
+ * The pages describe no such entry point; it serves callers that may not
+ * call cudaMalloc or a caching allocator at all: code that runs while a CUDA
+ * graph is being captured (an allocation cannot be captured), plugins inside
+ * a host runtime that owns every device allocation, and serving loops that
+ * must not allocate once they run.  It takes the same inputs and output as
+ * ns_paged_attn_decode (same checks, same result) but no workspace: the split
+ * partial records, arrival counters and plan record live in a scratch array
+ * compiled into the library (about 4.4 MB, held by every GPU that loads the
+ * library until the process exits).
+ *   - num_seqs * num_kv_heads must not exceed NS_NOALLOC_MAX_PAIRS; larger
+ *     calls return NS_ERR_UNSUPPORTED and launch nothing.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call clears the arrival counters it needs (cudaMemsetAsync on
+ *     `stream`) before its kernel; it allocates and frees nothing.
+ *   - All calls share the one array: calls that overlap on the GPU (two
+ *     streams, two threads) race and give wrong results.
+ */
+#define NS_NOALLOC_MAX_PAIRS 16384
+ns_status ns_paged_attn_decode_noalloc(const void *q, const void *k_pool, const void *v_pool,
+                                       const int32_t *block_tables, const int32_t *context_lens,
+                                       int num_seqs, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int block_size, float scale, void *out,
+                                       ns_stream_t stream, int max_blocks_per_seq,
+                                       int64_t num_blocks, ns_dtype dtype);
+
+/*
  * Device status word of the current device: OR of NS_DEV_* bits raised by
  * kernels since the last clear.  Synchronises `stream`, copies the word to
  * *bits, and zeroes it when `clear` is nonzero.  Returns NS_OK (whatever the

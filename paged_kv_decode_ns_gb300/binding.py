@@ -21,6 +21,7 @@ NS_BF16 = 1
 NS_MAX_CTAS = 1024
 NS_PREFILL_WALK = 1
 NS_PREFILL_TENSOR_CORE = 2
+NS_NOALLOC_MAX_PAIRS = 16384
 DEV_BITS = {
     0x1: "NS_DEV_BAD_BLOCK_ID",
     0x2: "NS_DEV_BAD_CONTEXT_LEN",
@@ -74,6 +75,7 @@ _SIGNATURES = {
     "ns_paged_attn_prefill_ex": (I, [P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, I, I64, I, P, SZ,
                                      ctypes.POINTER(PrefillConfig)]),
     "ns_get_device_status": (I, [P, ctypes.POINTER(ctypes.c_uint32), I]),
+    "ns_paged_attn_decode_noalloc": (I, [P, P, P, P, P, I, I, I, I, I, F, P, P, I, I64, I]),
 }
 
 
@@ -193,6 +195,29 @@ def ns_paged_attn_decode(q, k_pool, v_pool, block_tables, context_lens, scale, o
         _check(lib().ns_paged_attn_decode(*args), "ns_paged_attn_decode")
     else:
         _check(lib().ns_paged_attn_decode_ex(*args, ctypes.byref(config)), "ns_paged_attn_decode_ex")
+
+
+def ns_paged_attn_decode_noalloc(q, k_pool, v_pool, block_tables, context_lens, scale, out,
+                                 stream=None):
+    """ns_paged_attn_decode for callers that cannot allocate device memory.
+
+    Takes no workspace: the library's own scratch array holds the split
+    partials and counters (at most NS_NOALLOC_MAX_PAIRS sequence x kv-head
+    pairs).  The first call on a device must come before any stream capture;
+    calls that overlap on the GPU race.
+    """
+    S, hq, d = q.shape
+    nb_, hkv, bs, d2 = k_pool.shape
+    if v_pool.shape != k_pool.shape or d2 != d or out.shape != q.shape:
+        raise ValueError("shape mismatch")
+    if context_lens.shape != (S,) or block_tables.dim() != 2 or block_tables.shape[0] != S:
+        raise ValueError("one context length and one table row per sequence")
+    st = lib().ns_paged_attn_decode_noalloc(
+        _dev(q, "q"), _dev(k_pool, "k_pool", q.dtype), _dev(v_pool, "v_pool", q.dtype),
+        _dev(block_tables, "block_tables", torch.int32),
+        _dev(context_lens, "context_lens", torch.int32), S, hq, hkv, d, bs, float(scale),
+        _dev(out, "out", q.dtype), _stream(stream), block_tables.shape[1], nb_, _dtype_code(q))
+    _check(st, "ns_paged_attn_decode_noalloc")
 
 
 def ns_kv_append_paged_attn_decode(q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables,

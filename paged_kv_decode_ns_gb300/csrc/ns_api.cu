@@ -257,6 +257,11 @@ ns_status check_decode_args(const void *q, const void *k_pool, const void *v_poo
 
 }  // namespace
 
+unsigned *ns::device_status_word(int dev)
+{
+    return (dev >= 0 && dev < kMaxDevices) ? status_word(dev) : nullptr;
+}
+
 extern "C" {
 
 const char *ns_status_string(ns_status status)

@@ -19,6 +19,9 @@ cudaError_t launch_span_rows(const int32_t *query_start_loc, const int32_t *cont
                              int num_seqs, int total_rows, int tc_min_span, int32_t *row_seq,
                              int32_t *row_len, unsigned *status, cudaStream_t stream);
 
+// Address of the device status word on device `dev` (current), or nullptr.
+unsigned *device_status_word(int dev);
+
 // Chunked prefill of every span of two or more tokens on the tcgen05 tensor cores.
 bool tc_prefill_supported(int block_size, int group);
 cudaError_t launch_tc_prefill(const void *q, const int32_t *query_start_loc, const void *k_pool,

@@ -1,0 +1,185 @@
+// paged_decode_noalloc.cu -- the split-KV decode with library-owned scratch,
+// for callers that cannot allocate device memory.
+//
+// ns_paged_attn_decode needs a caller-provided workspace (split-KV partial
+// records, one arrival counter per (sequence, kv head) and a plan record).
+// Some callers cannot call cudaMalloc or a caching allocator: code that runs
+// while a CUDA graph is being captured (allocation is not capturable), plugins
+// embedded in a host runtime that owns every device allocation, and serving
+// loops that forbid allocation after start-up.  This file gives them
+// ns_paged_attn_decode_noalloc, which runs the same kernel over a fixed-size
+// scratch array that lives in the library image itself.
+//
+// The scratch is a file-scope __device__ array: every GPU that loads the
+// library holds it (about 4.4 MB) until the process exits.  Host code cannot
+// use the array's name as a device address, so the first call on each device
+// asks the runtime for that device's address (cudaGetSymbolAddress) with the
+// device current, checks the result and caches it; that first call should come
+// before any stream capture.  Every call shares the one array: calls that
+// overlap on the GPU (two streams, two threads) race and give wrong results.
+// The arrival counters must start at zero, so each call clears them with
+// cudaMemsetAsync on its own stream before the kernel; the partial records need
+// no clearing.
+#include <atomic>
+#include <cstring>
+
+#include "ns_internal.h"
+#include "paged_decode.cuh"
+
+namespace {
+
+constexpr size_t kPlanBytes = 256;
+constexpr size_t kCounterBytes = (size_t)NS_NOALLOC_MAX_PAIRS * sizeof(int32_t);
+constexpr size_t kPartialBytes = (size_t)NS_MAX_CTAS * 2 * ns::kSlotFloats * sizeof(float);
+constexpr size_t kScratchBytes = kPlanBytes + kCounterBytes + kPartialBytes;
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::atomic<unsigned char *> g_scratch_ptr[kMaxDevices];
+
+// Device address of the scratch array on device `dev` (which must be current).
+unsigned char *scratch_address(int dev)
+{
+    unsigned char *p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        void *a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_noalloc_scratch) != cudaSuccess || a == nullptr)
+            return nullptr;
+        p = static_cast<unsigned char *>(a);
+        g_scratch_ptr[dev].store(p, std::memory_order_release);
+    }
+    return p;
+}
+
+template <typename T, int BS>
+cudaError_t launch_g(int g, const ns::DecodeParams &P, int ctas, cudaStream_t s)
+{
+    switch (g) {
+    case 1: return ns::launch_paged_decode<T, BS, 1>(P, ctas, s);
+    case 2: return ns::launch_paged_decode<T, BS, 2>(P, ctas, s);
+    case 3: return ns::launch_paged_decode<T, BS, 3>(P, ctas, s);
+    case 4: return ns::launch_paged_decode<T, BS, 4>(P, ctas, s);
+    case 5: return ns::launch_paged_decode<T, BS, 5>(P, ctas, s);
+    case 6: return ns::launch_paged_decode<T, BS, 6>(P, ctas, s);
+    case 7: return ns::launch_paged_decode<T, BS, 7>(P, ctas, s);
+    default: return ns::launch_paged_decode<T, BS, 8>(P, ctas, s);
+    }
+}
+
+template <typename T>
+cudaError_t launch(int bs, int g, const ns::DecodeParams &P, int ctas, cudaStream_t s)
+{
+    switch (bs) {
+    case 4: return launch_g<T, 4>(g, P, ctas, s);
+    case 8: return launch_g<T, 8>(g, P, ctas, s);
+    case 16: return launch_g<T, 16>(g, P, ctas, s);
+    default: return launch_g<T, 32>(g, P, ctas, s);
+    }
+}
+
+template <typename T, int BS>
+int ctas_per_sm_g(int g)
+{
+    switch (g) {
+    case 1: return ns::decode_ctas_per_sm<T, BS, 1>();
+    case 2: return ns::decode_ctas_per_sm<T, BS, 2>();
+    case 3: return ns::decode_ctas_per_sm<T, BS, 3>();
+    case 4: return ns::decode_ctas_per_sm<T, BS, 4>();
+    case 5: return ns::decode_ctas_per_sm<T, BS, 5>();
+    case 6: return ns::decode_ctas_per_sm<T, BS, 6>();
+    case 7: return ns::decode_ctas_per_sm<T, BS, 7>();
+    default: return ns::decode_ctas_per_sm<T, BS, 8>();
+    }
+}
+
+template <typename T>
+int ctas_per_sm(int bs, int g)
+{
+    switch (bs) {
+    case 4: return ctas_per_sm_g<T, 4>(g);
+    case 8: return ctas_per_sm_g<T, 8>(g);
+    case 16: return ctas_per_sm_g<T, 16>(g);
+    default: return ctas_per_sm_g<T, 32>(g);
+    }
+}
+
+}  // namespace
+
+extern "C" ns_status ns_paged_attn_decode_noalloc(const void *q, const void *k_pool,
+                                                  const void *v_pool, const int32_t *block_tables,
+                                                  const int32_t *context_lens, int num_seqs,
+                                                  int num_q_heads, int num_kv_heads, int head_dim,
+                                                  int block_size, float scale, void *out,
+                                                  ns_stream_t stream, int max_blocks_per_seq,
+                                                  int64_t num_blocks, ns_dtype dtype)
+{
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0)
+        return NS_ERR_INVALID_ARG;
+    if (dtype != NS_F16 && dtype != NS_BF16)
+        return NS_ERR_UNSUPPORTED;
+    if (head_dim != ns::kHeadDim ||
+        (block_size != 4 && block_size != 8 && block_size != 16 && block_size != 32) ||
+        num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > ns::kMaxGroup)
+        return NS_ERR_UNSUPPORTED;
+    // the scratch array holds one arrival counter per (sequence, kv head)
+    if ((long long)num_seqs * num_kv_heads > NS_NOALLOC_MAX_PAIRS)
+        return NS_ERR_UNSUPPORTED;
+    if (num_seqs == 0)
+        return NS_OK;
+    const auto aligned = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out)
+        return NS_ERR_INVALID_ARG;
+    if (!aligned(q) || !aligned(k_pool) || !aligned(v_pool) || !aligned(out))
+        return NS_ERR_INVALID_ARG;
+    if (max_blocks_per_seq < 1 || num_blocks < 1 || !(scale == scale))
+        return NS_ERR_INVALID_ARG;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return NS_ERR_CUDA;
+    unsigned char *scratch = scratch_address(dev);
+    unsigned *status = ns::device_status_word(dev);
+    if (scratch == nullptr || status == nullptr)
+        return NS_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int *counters = reinterpret_cast<int *>(scratch + kPlanBytes);
+    if (cudaMemsetAsync(counters, 0, (size_t)num_seqs * num_kv_heads * sizeof(int32_t), st) !=
+        cudaSuccess)
+        return NS_ERR_CUDA;
+
+    ns::DecodeParams P;
+    std::memset(&P, 0, sizeof(P));
+    P.q = static_cast<const uint16_t *>(q);
+    P.k_pool = static_cast<const uint16_t *>(k_pool);
+    P.v_pool = static_cast<const uint16_t *>(v_pool);
+    P.block_tables = block_tables;
+    P.context_lens = context_lens;
+    P.out = static_cast<uint16_t *>(out);
+    P.num_seqs = num_seqs;
+    P.num_q_heads = num_q_heads;
+    P.num_kv_heads = num_kv_heads;
+    P.group = num_q_heads / num_kv_heads;
+    P.max_blocks_per_seq = max_blocks_per_seq;
+    P.num_blocks = num_blocks;
+    P.scale_log2 = scale * 1.4426950408889634f;
+    P.counters = counters;
+    P.partials = reinterpret_cast<float *>(scratch + kPlanBytes + kCounterBytes);
+    P.plan = reinterpret_cast<ns_decode_plan *>(scratch);
+    P.status = status;
+    P.min_blocks_per_cta = ns::kDefaultMinBlocksPerCta;
+    P.whole_sequences = 0;
+
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+        return NS_ERR_CUDA;
+    const int g = num_q_heads / num_kv_heads;
+    const int per_sm = dtype == NS_BF16 ? ctas_per_sm<ns::BF16>(block_size, g)
+                                        : ctas_per_sm<ns::F16>(block_size, g);
+    long long ctas = (long long)per_sm * sms;
+    if (ctas > NS_MAX_CTAS)
+        ctas = NS_MAX_CTAS;
+    const cudaError_t e = dtype == NS_BF16 ? launch<ns::BF16>(block_size, g, P, (int)ctas, st)
+                                           : launch<ns::F16>(block_size, g, P, (int)ctas, st);
+    return e == cudaSuccess ? NS_OK : NS_ERR_CUDA;
+}
