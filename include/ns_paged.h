@@ -152,6 +152,9 @@ ns_status ns_paged_attn_workspace_init(void *workspace, size_t workspace_bytes,
  * run of them, so a long context is split across CTAs (flash-decoding style)
  * and its partial results are merged by log-sum-exp.  How many CTAs run is
  * decided on the device from the actual context lengths and batch size.
+ * Block sizes 16 and 32 run on the tcgen05 tensor cores (S = Q K^T and
+ * P V per 128-key tile, one CTA per SM); block sizes 4 and 8 run on the
+ * CUDA cores.
  */
 ns_status ns_paged_attn_decode(const void *q, const void *k_pool, const void *v_pool,
                                const int32_t *block_tables, const int32_t *context_lens,
@@ -168,13 +171,24 @@ ns_status ns_paged_attn_decode(const void *q, const void *k_pool, const void *v_
  *                       would give each less than this many KV blocks
  *   whole_sequences     nonzero = never split a (sequence, kv head): CTA c
  *                       takes pairs c, c+G, c+2G, ... (no merge step)
+ *   kernel              NS_DECODE_KERNEL_AUTO (0): tensor cores for block
+ *                       sizes 16 and 32, CUDA cores otherwise;
+ *                       NS_DECODE_KERNEL_CUDA_CORE / _TENSOR_CORE force one
+ *                       (the tensor-core kernel with another block size
+ *                       returns NS_ERR_UNSUPPORTED).  Both compute the same
+ *                       result within the stated tolerance.
+ *   reserved            must be zero
  */
 #define NS_MAX_CTAS 1024
+#define NS_DECODE_KERNEL_AUTO 0
+#define NS_DECODE_KERNEL_CUDA_CORE 1
+#define NS_DECODE_KERNEL_TENSOR_CORE 2
 typedef struct ns_decode_config {
     int num_ctas;
     int min_blocks_per_cta;
     int whole_sequences;
-    int reserved[5];
+    int kernel;
+    int reserved[4];
 } ns_decode_config;
 
 /* ns_paged_attn_decode with policy overrides (cfg may be NULL = auto). */
@@ -195,11 +209,13 @@ ns_status ns_paged_attn_decode_ex(const void *q, const void *k_pool, const void 
  *   slot_mapping  int64 [num_seqs]: must be the slot of that position,
  *                 block_tables[s][(L-1)/bs]*bs + (L-1)%bs
  * The result equals the two calls in order: the pool slot is written and the
- * attention includes the new token.  The CTA that owns a sequence's last
- * block takes the new K/V from k_new/v_new (never from the pool slot it is
- * writing), so nothing reads the slot while it is written.  A slot that is
- * not the slot of position L-1 sets NS_DEV_FUSED_SLOT (the slot is still
- * written; the attention still uses the new token at position L-1).
+ * attention includes the new token.  Only the CTA that owns a sequence's
+ * last block touches the slot, and it never reads the slot while writing
+ * it (the CUDA-core kernel takes the new K/V from k_new/v_new; the
+ * tensor-core kernel writes the slot, fences, then loads the block).  A slot
+ * that is not the slot of position L-1 sets NS_DEV_FUSED_SLOT: the given
+ * slot is still written if it lies in the pool, and the attention result of
+ * the sequences involved is then unspecified.
  */
 ns_status ns_kv_append_paged_attn_decode(const void *q, const void *k_new, const void *v_new,
                                          const int64_t *slot_mapping, void *k_pool,

@@ -41,7 +41,11 @@ class NsError(RuntimeError):
 
 class DecodeConfig(ctypes.Structure):
     _fields_ = [("num_ctas", ctypes.c_int), ("min_blocks_per_cta", ctypes.c_int),
-                ("whole_sequences", ctypes.c_int), ("reserved", ctypes.c_int * 5)]
+                ("whole_sequences", ctypes.c_int), ("kernel", ctypes.c_int),
+                ("reserved", ctypes.c_int * 4)]
+
+
+DECODE_KERNEL_AUTO, DECODE_KERNEL_CUDA_CORE, DECODE_KERNEL_TENSOR_CORE = 0, 1, 2
 
 
 class PrefillConfig(ctypes.Structure):

@@ -17,6 +17,7 @@ constexpr int kMaxDevices = 64;
 std::atomic<unsigned *> g_status_ptr[kMaxDevices];
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_ctas_per_sm[kMaxDevices][2][4][ns::kMaxGroup];
+std::atomic<int> g_tc_ctas_per_sm[kMaxDevices][2][2];
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -129,6 +130,18 @@ int resident_ctas(int dev, ns_dtype dt, int bs, int g)
     return (int)(total > NS_MAX_CTAS ? NS_MAX_CTAS : total);
 }
 
+int resident_tc_ctas(int dev, ns_dtype dt, int bs)
+{
+    std::atomic<int> &slot = g_tc_ctas_per_sm[dev][dt == NS_BF16 ? 1 : 0][bs == 16 ? 0 : 1];
+    int n = slot.load(std::memory_order_relaxed);
+    if (n <= 0) {
+        n = ns::tc_decode_ctas_per_sm(dt, bs);
+        slot.store(n, std::memory_order_relaxed);
+    }
+    long long total = (long long)n * sm_count(dev);
+    return (int)(total > NS_MAX_CTAS ? NS_MAX_CTAS : total);
+}
+
 // Workspace layout (byte offsets), for up to `rows` query rows.
 struct WsLayout {
     size_t plan, counters, partials, row_seq, row_len, total;
@@ -217,16 +230,13 @@ ns_status run_decode(const DecodeCall &c, int dev)
     P.min_blocks_per_cta = (c.cfg && c.cfg->min_blocks_per_cta > 0) ? c.cfg->min_blocks_per_cta
                                                                      : ns::kDefaultMinBlocksPerCta;
     P.whole_sequences = (c.cfg && c.cfg->whole_sequences) ? 1 : 0;
+    P.auto_policy = (c.cfg == nullptr || (c.cfg->num_ctas == 0 && c.cfg->min_blocks_per_cta == 0 &&
+                                          c.cfg->whole_sequences == 0))
+                        ? 1
+                        : 0;
 
-    const int g = P.group;
-    int ctas = (c.cfg && c.cfg->num_ctas > 0) ? c.cfg->num_ctas
-                                              : resident_ctas(dev, c.dtype, c.block_size, g);
-    if (ctas > NS_MAX_CTAS)
-        ctas = NS_MAX_CTAS;
-    const cudaError_t e = c.dtype == NS_BF16
-                              ? dispatch_decode<ns::BF16>(c.block_size, g, P, ctas, c.stream)
-                              : dispatch_decode<ns::F16>(c.block_size, g, P, ctas, c.stream);
-    return e == cudaSuccess ? NS_OK : NS_ERR_CUDA;
+    return ns::launch_decode(P, c.dtype, c.block_size, c.cfg ? c.cfg->kernel : NS_DECODE_KERNEL_AUTO,
+                             c.cfg ? c.cfg->num_ctas : 0, c.stream, dev);
 }
 
 ns_status check_decode_args(const void *q, const void *k_pool, const void *v_pool,
@@ -250,12 +260,50 @@ ns_status check_decode_args(const void *q, const void *k_pool, const void *v_poo
         return NS_ERR_INVALID_ARG;
     if (workspace_bytes < ns_paged_attn_workspace_bytes(rows, num_q_heads, num_kv_heads, head_dim))
         return NS_ERR_INVALID_ARG;
-    if (cfg && (cfg->num_ctas < 0 || cfg->num_ctas > NS_MAX_CTAS || cfg->min_blocks_per_cta < 0))
+    if (cfg && (cfg->num_ctas < 0 || cfg->num_ctas > NS_MAX_CTAS || cfg->min_blocks_per_cta < 0 ||
+                cfg->kernel < NS_DECODE_KERNEL_AUTO || cfg->kernel > NS_DECODE_KERNEL_TENSOR_CORE))
         return NS_ERR_INVALID_ARG;
+    if (cfg && cfg->kernel == NS_DECODE_KERNEL_TENSOR_CORE &&
+        !ns::tc_decode_supported(block_size, num_q_heads / num_kv_heads))
+        return NS_ERR_UNSUPPORTED;
     return NS_OK;
 }
 
 }  // namespace
+
+namespace ns {
+
+ns_status launch_decode(const DecodeParams &P, ns_dtype dtype, int block_size, int kernel,
+                        int num_ctas, cudaStream_t stream, int dev)
+{
+    const int g = P.group;
+    bool tc;
+    if (kernel == NS_DECODE_KERNEL_TENSOR_CORE) {
+        if (!tc_decode_supported(block_size, g))
+            return NS_ERR_UNSUPPORTED;
+        tc = true;
+    } else if (kernel == NS_DECODE_KERNEL_AUTO) {
+        tc = tc_decode_supported(block_size, g);
+    } else if (kernel == NS_DECODE_KERNEL_CUDA_CORE) {
+        tc = false;
+    } else {
+        return NS_ERR_INVALID_ARG;
+    }
+    int ctas = num_ctas > 0 ? num_ctas
+                            : (tc ? resident_tc_ctas(dev, dtype, block_size)
+                                  : resident_ctas(dev, dtype, block_size, g));
+    if (ctas > NS_MAX_CTAS)
+        ctas = NS_MAX_CTAS;
+    cudaError_t e;
+    if (tc)
+        e = launch_tc_decode(P, dtype, block_size, ctas, stream);
+    else
+        e = dtype == NS_BF16 ? dispatch_decode<BF16>(block_size, g, P, ctas, stream)
+                             : dispatch_decode<F16>(block_size, g, P, ctas, stream);
+    return e == cudaSuccess ? NS_OK : NS_ERR_CUDA;
+}
+
+}  // namespace ns
 
 unsigned *ns::device_status_word(int dev)
 {

@@ -22,6 +22,19 @@ cudaError_t launch_span_rows(const int32_t *query_start_loc, const int32_t *cont
 // Address of the device status word on device `dev` (current), or nullptr.
 unsigned *device_status_word(int dev);
 
+struct DecodeParams;
+
+// Split-KV decode on the tcgen05 tensor cores (block sizes 16 and 32).
+bool tc_decode_supported(int block_size, int group);
+int tc_decode_ctas_per_sm(ns_dtype dtype, int block_size);
+cudaError_t launch_tc_decode(const DecodeParams &P, ns_dtype dtype, int block_size, int num_ctas,
+                             cudaStream_t stream);
+
+// Launch the decode kernel chosen by `kernel` (NS_DECODE_KERNEL_*) with
+// num_ctas CTAs, or the resident CTAs of device `dev` when num_ctas is 0.
+ns_status launch_decode(const DecodeParams &P, ns_dtype dtype, int block_size, int kernel,
+                        int num_ctas, cudaStream_t stream, int dev);
+
 // Chunked prefill of every span of two or more tokens on the tcgen05 tensor cores.
 bool tc_prefill_supported(int block_size, int group);
 cudaError_t launch_tc_prefill(const void *q, const int32_t *query_start_loc, const void *k_pool,

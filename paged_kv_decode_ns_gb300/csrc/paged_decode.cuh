@@ -50,7 +50,7 @@ namespace ns {
 constexpr int kSlotFloats = 2 * kMaxGroup + kMaxGroup * kHeadDim;
 constexpr float kRescaleSlack = 8.0f;
 constexpr int kDecodeWarps = 4;
-constexpr int kDefaultMinBlocksPerCta = 8;
+constexpr int kDefaultMinBlocksPerCta = 32;
 
 struct DecodeParams {
     const uint16_t *q;
@@ -79,6 +79,7 @@ struct DecodeParams {
     unsigned *status;
     int min_blocks_per_cta;
     int whole_sequences;
+    int auto_policy;  // no override given: the device may deal whole pairs instead of splitting
 };
 
 enum : int {
@@ -426,15 +427,25 @@ __device__ __forceinline__ void process_block(const uint16_t *__restrict__ kb,
             kw = lds128(knew + c * 8);
         const float2 k0 = unpack2<T>(kw.x), k1 = unpack2<T>(kw.y);
         const float2 k2 = unpack2<T>(kw.z), k3 = unpack2<T>(kw.w);
+        // breadth-first over the head slots: NS independent chains between
+        // each dependent step
+        float2 a[NS];
+#pragma unroll
+        for (int i = 0; i < NS; ++i)
+            a[i] = fmul2(q2[i][0], k0);
+#pragma unroll
+        for (int i = 0; i < NS; ++i)
+            a[i] = ffma2(q2[i][1], k1, a[i]);
+#pragma unroll
+        for (int i = 0; i < NS; ++i)
+            a[i] = ffma2(q2[i][2], k2, a[i]);
+#pragma unroll
+        for (int i = 0; i < NS; ++i)
+            a[i] = ffma2(q2[i][3], k3, a[i]);
         float part[NS];
 #pragma unroll
-        for (int i = 0; i < NS; ++i) {
-            float2 a = fmul2(q2[i][0], k0);
-            a = ffma2(q2[i][1], k1, a);
-            a = ffma2(q2[i][2], k2, a);
-            a = ffma2(q2[i][3], k3, a);
-            part[i] = a.x + a.y;
-        }
+        for (int i = 0; i < NS; ++i)
+            part[i] = a[i].x + a[i].y;
         // halving steps (lane masks 4, 2, 1 from the top), then the lanes that
         // share a head sum what is left
 #pragma unroll
@@ -480,12 +491,11 @@ __device__ __forceinline__ void process_block(const uint16_t *__restrict__ kb,
         l_run += p[st];
     }
 
-    // ---- share p of (token, head) with the row: one lane per head writes
-    if ((c & ((1 << SHIFT) - 1)) == 0 && (c >> SHIFT) < G) {
+    // ---- share p of (token, head) with the row (lanes that share a head
+    // write the same value; a padding head lands in an unused slot)
 #pragma unroll
-        for (int st = 0; st < STEPS; ++st)
-            pbuf[(st * 4 + r) * 8 + (c >> SHIFT)] = make_float2(p[st], p[st]);
-    }
+    for (int st = 0; st < STEPS; ++st)
+        pbuf[(st * 4 + r) * 8 + (c >> SHIFT)] = make_float2(p[st], p[st]);
     __syncwarp();
 
     // ---- values
@@ -515,6 +525,59 @@ __device__ __forceinline__ void process_block(const uint16_t *__restrict__ kb,
         }
     }
     __syncwarp();  // the next block rewrites pbuf
+}
+
+// ---------------------------------------------------------------------------
+// Log-sum-exp merge of the partial records of one (sequence, kv head) pair,
+// pieces c0..c1 (the first in its CTA's second slot when c0_second), written
+// to out[out_row + j*64 + d] for the G heads.  Threads tid = 0..NT-1 of the
+// calling CTA share the G*64 outputs.
+// ---------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ void merge_pieces(const DecodeParams &P, long long c0, long long c1,
+                                             bool c0_second, long long out_row, int G, int tid, int NT)
+{
+    const int npieces = (int)(c1 - c0 + 1);
+    constexpr int U = 8;  // records read per round, so their latencies overlap
+    for (int idx = tid; idx < G * kHeadDim; idx += NT) {
+        const int j = idx >> 6;
+        float M = -INFINITY;
+        for (int k0 = 0; k0 < npieces; k0 += U) {
+            float mk[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int k = k0 + u;
+                const long long cc = c0 + k;
+                const int wh = (k == 0 && c0_second) ? 1 : 0;
+                mk[u] = k < npieces ? __ldcg(P.partials + (cc * 2 + wh) * kSlotFloats + j) : -INFINITY;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                M = fmaxf(M, mk[u]);
+        }
+        float Ls = 0.f, o = 0.f;
+        for (int k0 = 0; k0 < npieces; k0 += U) {
+            float mk[U], lk[U], ak[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int k = k0 + u;
+                const long long cc = c0 + k;
+                const int wh = (k == 0 && c0_second) ? 1 : 0;
+                const float *sl = P.partials + (cc * 2 + wh) * kSlotFloats;
+                const bool in = k < npieces;
+                mk[u] = in ? __ldcg(sl + j) : -INFINITY;
+                lk[u] = in ? __ldcg(sl + kMaxGroup + j) : 0.f;
+                ak[u] = in ? __ldcg(sl + 2 * kMaxGroup + idx) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const float f = (mk[u] > -INFINITY) ? fast_exp2(mk[u] - M) : 0.f;
+                Ls += f * lk[u];
+                o += f * ak[u];
+            }
+        }
+        P.out[out_row + idx] = pack1<T>(o / Ls);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -623,26 +686,7 @@ __device__ bool piece_epilogue(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
         return false;
     if (sm.merge_prev == (int)(c1 - c0)) {
         __threadfence();
-        const bool c0_second = range_begin(c0, B, Gc) != pc.pstart;
-        for (int idx = tid; idx < G * kHeadDim; idx += NT) {
-            const int j = idx >> 6;
-            float M = -INFINITY;
-            for (long long cc = c0; cc <= c1; ++cc) {
-                const int wh = (cc == c0 && c0_second) ? 1 : 0;
-                const float *sl = P.partials + (cc * 2 + wh) * kSlotFloats;
-                M = fmaxf(M, __ldcg(sl + j));
-            }
-            float Ls = 0.f, o = 0.f;
-            for (long long cc = c0; cc <= c1; ++cc) {
-                const int wh = (cc == c0 && c0_second) ? 1 : 0;
-                const float *sl = P.partials + (cc * 2 + wh) * kSlotFloats;
-                const float m = __ldcg(sl + j);
-                const float f = (m > -INFINITY) ? fast_exp2(m - M) : 0.f;
-                Ls += f * __ldcg(sl + kMaxGroup + j);
-                o += f * __ldcg(sl + 2 * kMaxGroup + idx);
-            }
-            P.out[out_row + idx] = pack1<T>(o / Ls);
-        }
+        merge_pieces<T>(P, c0, c1, range_begin(c0, B, Gc) != pc.pstart, out_row, G, tid, NT);
         if (tid == 0)
             P.counters[pair] = 0;
     }
@@ -817,7 +861,7 @@ __device__ bool decode_prologue(const DecodeParams &P, Smem &sm)
         G = 1;
     const long long pairs = (long long)P.num_seqs * Hkv;
     const bool whole = P.whole_sequences ||
-                       (P.min_blocks_per_cta == 0 && total > 0 &&
+                       (P.auto_policy && total > 0 &&
                         (long long)maxnb <= 2 * ((total + G - 1) / G) && pairs <= (long long)gridDim.x);
     if (whole)
         G = gridDim.x;
@@ -882,8 +926,13 @@ __device__ bool decode_prologue(const DecodeParams &P, Smem &sm)
     return c < G && b0 < b1;
 }
 
+// CTAs per SM the register allocation is sized for; a build-time tuning knob.
+#ifndef NS_DECODE_MIN_CTAS
+#define NS_DECODE_MIN_CTAS 2
+#endif
+
 template <typename T, int BS, int G, int S>
-__global__ void __launch_bounds__(kDecodeWarps * 32, 2) paged_decode_kernel(const DecodeParams P)
+__global__ void __launch_bounds__(kDecodeWarps * 32, NS_DECODE_MIN_CTAS) paged_decode_kernel(const DecodeParams P)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     auto &sm = *reinterpret_cast<DecodeSmem<BS, G, S> *>(smem_raw);

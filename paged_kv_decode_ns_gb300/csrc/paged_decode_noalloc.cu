@@ -7,8 +7,9 @@
 // while a CUDA graph is being captured (allocation is not capturable), plugins
 // embedded in a host runtime that owns every device allocation, and serving
 // loops that forbid allocation after start-up.  This file gives them
-// ns_paged_attn_decode_noalloc, which runs the same kernel over a fixed-size
-// scratch array that lives in the library image itself.
+// ns_paged_attn_decode_noalloc, which runs the same kernels (same choice of
+// tensor-core or CUDA-core kernel, same grid) over a fixed-size scratch array
+// that lives in the library image itself.
 //
 // The scratch is a file-scope __device__ array: every GPU that loads the
 // library holds it (about 4.4 MB) until the process exits.  Host code cannot
@@ -50,58 +51,6 @@ unsigned char *scratch_address(int dev)
         g_scratch_ptr[dev].store(p, std::memory_order_release);
     }
     return p;
-}
-
-template <typename T, int BS>
-cudaError_t launch_g(int g, const ns::DecodeParams &P, int ctas, cudaStream_t s)
-{
-    switch (g) {
-    case 1: return ns::launch_paged_decode<T, BS, 1>(P, ctas, s);
-    case 2: return ns::launch_paged_decode<T, BS, 2>(P, ctas, s);
-    case 3: return ns::launch_paged_decode<T, BS, 3>(P, ctas, s);
-    case 4: return ns::launch_paged_decode<T, BS, 4>(P, ctas, s);
-    case 5: return ns::launch_paged_decode<T, BS, 5>(P, ctas, s);
-    case 6: return ns::launch_paged_decode<T, BS, 6>(P, ctas, s);
-    case 7: return ns::launch_paged_decode<T, BS, 7>(P, ctas, s);
-    default: return ns::launch_paged_decode<T, BS, 8>(P, ctas, s);
-    }
-}
-
-template <typename T>
-cudaError_t launch(int bs, int g, const ns::DecodeParams &P, int ctas, cudaStream_t s)
-{
-    switch (bs) {
-    case 4: return launch_g<T, 4>(g, P, ctas, s);
-    case 8: return launch_g<T, 8>(g, P, ctas, s);
-    case 16: return launch_g<T, 16>(g, P, ctas, s);
-    default: return launch_g<T, 32>(g, P, ctas, s);
-    }
-}
-
-template <typename T, int BS>
-int ctas_per_sm_g(int g)
-{
-    switch (g) {
-    case 1: return ns::decode_ctas_per_sm<T, BS, 1>();
-    case 2: return ns::decode_ctas_per_sm<T, BS, 2>();
-    case 3: return ns::decode_ctas_per_sm<T, BS, 3>();
-    case 4: return ns::decode_ctas_per_sm<T, BS, 4>();
-    case 5: return ns::decode_ctas_per_sm<T, BS, 5>();
-    case 6: return ns::decode_ctas_per_sm<T, BS, 6>();
-    case 7: return ns::decode_ctas_per_sm<T, BS, 7>();
-    default: return ns::decode_ctas_per_sm<T, BS, 8>();
-    }
-}
-
-template <typename T>
-int ctas_per_sm(int bs, int g)
-{
-    switch (bs) {
-    case 4: return ctas_per_sm_g<T, 4>(g);
-    case 8: return ctas_per_sm_g<T, 8>(g);
-    case 16: return ctas_per_sm_g<T, 16>(g);
-    default: return ctas_per_sm_g<T, 32>(g);
-    }
 }
 
 }  // namespace
@@ -169,17 +118,7 @@ extern "C" ns_status ns_paged_attn_decode_noalloc(const void *q, const void *k_p
     P.status = status;
     P.min_blocks_per_cta = ns::kDefaultMinBlocksPerCta;
     P.whole_sequences = 0;
+    P.auto_policy = 1;
 
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
-        return NS_ERR_CUDA;
-    const int g = num_q_heads / num_kv_heads;
-    const int per_sm = dtype == NS_BF16 ? ctas_per_sm<ns::BF16>(block_size, g)
-                                        : ctas_per_sm<ns::F16>(block_size, g);
-    long long ctas = (long long)per_sm * sms;
-    if (ctas > NS_MAX_CTAS)
-        ctas = NS_MAX_CTAS;
-    const cudaError_t e = dtype == NS_BF16 ? launch<ns::BF16>(block_size, g, P, (int)ctas, st)
-                                           : launch<ns::F16>(block_size, g, P, (int)ctas, st);
-    return e == cudaSuccess ? NS_OK : NS_ERR_CUDA;
+    return ns::launch_decode(P, dtype, block_size, NS_DECODE_KERNEL_AUTO, 0, st, dev);
 }

@@ -25,6 +25,7 @@
 //            row in TMEM when the max moved, and finally writes O / sum.
 // Values of keys past the context are zeroed in shared memory before the PV
 // product, so undefined (even NaN) pool slots never reach the accumulator.
+#include <cstddef>
 #include <cudaTypedefs.h>
 
 #include "ns_internal.h"
@@ -79,10 +80,22 @@ struct alignas(1024) PrefillSmem {
     uint64_t s_free;
     uint64_t p_full;
     uint64_t o_done;
+    // rank 1's unnormalised rows, written remotely into rank 0 with 16-byte stores
+    alignas(16) float rem_o[kRows][kHeadDim];
+    float rem_m[kRows];
+    float rem_l[kRows];
+    uint64_t rem_bar;
     uint32_t tmem_base;
     uint32_t loaded[kStages];  // bit i: block i of the tile was loaded
     int u_s, u_h, u_i0, u_n, u_L, u_tiles, u_ok;
+    int u_j0, u_nt;  // this CTA's key tiles: [u_j0, u_j0 + u_nt)
 };
+
+// Vector (16-byte) and mbarrier (8-byte) accesses need these alignments.
+static_assert(offsetof(PrefillSmem<1>, rem_o) % 16 == 0 && offsetof(PrefillSmem<2>, rem_o) % 16 == 0,
+              "remote 16-byte stores into rem_o");
+static_assert(offsetof(PrefillSmem<1>, q_full) % 8 == 0 && offsetof(PrefillSmem<2>, rem_bar) % 8 == 0,
+              "mbarriers are 8-byte aligned");
 
 template <int NP>
 constexpr size_t smem_bytes()
@@ -102,7 +115,7 @@ __device__ __forceinline__ PrefillSmem<NP> &smem_of(unsigned char *raw)
 template <int NP>
 __device__ void find_unit(const PrefillParams &P, PrefillSmem<NP> &sm, int lane)
 {
-    const long long u = blockIdx.x;
+    const long long u = blockIdx.x >> 1;  // one unit per 2-CTA cluster
     long long base = 0;
     int found = 0;
     for (int s0 = P.num_seqs - 1; s0 >= 0 && !found; s0 -= 32) {
@@ -147,7 +160,7 @@ __device__ void find_unit(const PrefillParams &P, PrefillSmem<NP> &sm, int lane)
 }
 
 template <typename T, int BS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const PrefillParams P)
 {
@@ -173,7 +186,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 const int last_tok = min(sm.u_i0 + P.qt, n) - 1;
                 const long long keys = (long long)(L - n) + last_tok + 1;
-                sm.u_tiles = (int)((keys + kKT - 1) / kKT);
+                const int tiles = (int)((keys + kKT - 1) / kKT);
+                // the two CTAs of the cluster take the first and second half of the key tiles
+                const int half = (tiles + 1) / 2;
+                const bool second = tc::cluster_rank() != 0;
+                sm.u_tiles = tiles;
+                sm.u_j0 = second ? half : 0;
+                sm.u_nt = second ? tiles - half : half;
             }
         }
     }
@@ -187,11 +206,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&sm.s_free, 128);
         mbar_init(&sm.p_full, 128);
         mbar_init(&sm.o_done, 1);
+        mbar_init(&sm.rem_bar, 128);
         mbar_init_fence();
     }
     __syncthreads();
     if (sm.u_ok != 1)
-        return;
+        return;  // both CTAs of the cluster see the same unit and leave together
+    tc::cluster_sync();  // rank 0's barriers are initialised before rank 1 can arrive on them
+    const uint32_t rank = tc::cluster_rank();
     // Rows of the Q tile the TMA box does not cover are zeroed once.
     if (warp < 4 && (int)threadIdx.x >= P.qt * G) {
 #pragma unroll
@@ -208,14 +230,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after_sync();
 
     const int s = sm.u_s, h = sm.u_h, i0 = sm.u_i0, n = sm.u_n, L = sm.u_L;
-    const int tiles = sm.u_tiles;
+    const int tiles = sm.u_nt;   // this CTA's key tiles ...
+    const int j0 = sm.u_j0;      // ... starting at key tile j0
     const int prefix = L - n;
     const uint32_t tmem = sm.tmem_base;
     const int ab_fmt = T::code == NS_BF16 ? 1 : 0;
 
     if (warp == 5) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
+        if (lane == 0 && tiles > 0) {
             tc::prefetch_tensormap(&tm_q);
             tc::prefetch_tensormap(&tm_k);
             tc::prefetch_tensormap(&tm_v);
@@ -230,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int stage = j % kStages;
             const uint32_t par = ((uint32_t)(j / kStages) & 1u) ^ 1u;
             int phys = -1;
-            const int blk = j * kBlocksPerTile + lane;
+            const int blk = (j0 + j) * kBlocksPerTile + lane;
             if (lane < kBlocksPerTile && blk < nb_seq) {
                 phys = __ldg(P.block_tables + (long long)s * P.max_blocks_per_seq + blk);
                 if (phys < 0 || (long long)phys >= P.num_blocks) {
@@ -259,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issued = j + 1;
         }
         // Never leave while copies may still land in this CTA's shared memory.
-        if (lane == 0) {
+        if (lane == 0 && tiles > 0) {
             bool drained = mbar_wait(&sm.q_full, 0);
             for (int k = 1; drained && k <= kStages && k <= issued; ++k) {
                 const int j = issued - k;
@@ -271,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 4) {
         // ------------------------------------------------------------ MMA issue
-        if (lane == 0) {
+        if (lane == 0 && tiles > 0) {
             const uint32_t idesc_s = tc::idesc_f16(kRows, kKT, ab_fmt, false);
             const uint32_t idesc_o = tc::idesc_f16(kRows, kHeadDim, ab_fmt, true);
             const uint32_t q_addr = smem_addr(sm.q);
@@ -347,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_before_sync();
             mbar_arrive(&sm.s_free);
 
-            const int kbase = j * kKT;
+            const int kbase = (j0 + j) * kKT;
             const bool masked = kbase + kKT - 1 > pos_lo;
             float tmax = -INFINITY;
             if (masked) {
@@ -374,8 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             float lsum = 0.f;
 #pragma unroll
             for (int c = 0; c < kKT; c += 2) {
+                // even columns on the MUFU pipe, odd columns on the FMA pipe
                 float p0 = fast_exp2(fmaf(sv[c], P.scale_log2, -m));
-                float p1 = fast_exp2(fmaf(sv[c + 1], P.scale_log2, -m));
+                float p1 = exp2_fma(fmaf(sv[c + 1], P.scale_log2, -m));
                 if (masked) {
                     p0 = sv[c] > -INFINITY ? p0 : 0.f;
                     p1 = sv[c + 1] > -INFINITY ? p1 : 0.f;
@@ -446,25 +470,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_before_sync();
             mbar_arrive(&sm.p_full);
         }
-        // ---- epilogue: O / l
-        if (ok && mbar_wait(&sm.o_done, (uint32_t)(tiles - 1) & 1u)) {
-            tc::fence_after_sync();
-            float ov[kHeadDim];
+        // ---- epilogue: this CTA's unnormalised rows (zero when it had no tile)
+        float ov[kHeadDim];
+        if (ok && tiles > 0) {
+            ok = mbar_wait(&sm.o_done, (uint32_t)(tiles - 1) & 1u);
+            if (ok) {
+                tc::fence_after_sync();
 #pragma unroll
-            for (int c = 0; c < kHeadDim / 32; ++c)
-                tc::tmem_ld32(lane_addr + kTmemO + c * 32, *reinterpret_cast<float(*)[32]>(&ov[c * 32]));
-            tc::tmem_ld_wait();
+                for (int c = 0; c < kHeadDim / 32; ++c)
+                    tc::tmem_ld32(lane_addr + kTmemO + c * 32, *reinterpret_cast<float(*)[32]>(&ov[c * 32]));
+                tc::tmem_ld_wait();
+            }
+        }
+        if (!ok || tiles == 0) {
+#pragma unroll
+            for (int c = 0; c < kHeadDim; ++c)
+                ov[c] = 0.f;
+        }
+        if (!ok)
+            raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
+        if (rank != 0) {
+            // rank 1: hand (max, sum, rows) to rank 0 through distributed shared memory
+            const uint32_t dst = tc::map_to_rank(&sm.rem_o[r][0], 0);
+#pragma unroll
+            for (int c = 0; c < kHeadDim; c += 4)
+                tc::st_cluster_v4(dst + c * 4, ov[c], ov[c + 1], ov[c + 2], ov[c + 3]);
+            tc::st_cluster_f32(tc::map_to_rank(&sm.rem_m[r], 0), m);
+            tc::st_cluster_f32(tc::map_to_rank(&sm.rem_l[r], 0), l);
+            tc::mbar_arrive_remote(tc::map_to_rank(&sm.rem_bar, 0));
+        } else if (tc::mbar_wait_cluster(&sm.rem_bar, 0)) {
+            // rank 0: log-sum-exp merge of the two halves, then O / l
+            const float m1 = sm.rem_m[r], l1 = sm.rem_l[r];
+            const float M = fmaxf(m, m1);
+            const float f0 = (m > -INFINITY) ? fast_exp2(m - M) : 0.f;
+            const float f1 = (m1 > -INFINITY) ? fast_exp2(m1 - M) : 0.f;
             if (row_ok) {
-                const float inv = 1.f / l;
+                const float inv = 1.f / (f0 * l + f1 * l1);
+                const float a0 = f0 * inv, a1 = f1 * inv;
                 const long long tok_g = __ldg(P.qsl + s) + i0 + tok;
                 uint16_t *o = P.out + (tok_g * P.num_q_heads + (long long)h * G + (r % G)) * kHeadDim;
+                const float *o1 = &sm.rem_o[r][0];
 #pragma unroll
                 for (int c = 0; c < kHeadDim; c += 8) {
                     uint4 w;
-                    w.x = pack2<T>(ov[c] * inv, ov[c + 1] * inv);
-                    w.y = pack2<T>(ov[c + 2] * inv, ov[c + 3] * inv);
-                    w.z = pack2<T>(ov[c + 4] * inv, ov[c + 5] * inv);
-                    w.w = pack2<T>(ov[c + 6] * inv, ov[c + 7] * inv);
+                    w.x = pack2<T>(fmaf(ov[c], a0, o1[c] * a1), fmaf(ov[c + 1], a0, o1[c + 1] * a1));
+                    w.y = pack2<T>(fmaf(ov[c + 2], a0, o1[c + 2] * a1), fmaf(ov[c + 3], a0, o1[c + 3] * a1));
+                    w.z = pack2<T>(fmaf(ov[c + 4], a0, o1[c + 4] * a1), fmaf(ov[c + 5], a0, o1[c + 5] * a1));
+                    w.w = pack2<T>(fmaf(ov[c + 6], a0, o1[c + 6] * a1), fmaf(ov[c + 7], a0, o1[c + 7] * a1));
                     *reinterpret_cast<uint4 *>(o + c) = w;
                 }
             }
@@ -478,6 +530,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
+    // Neither CTA leaves while the other may still touch its shared memory
+    // (rank 1's remote stores land before it reaches this barrier, also when
+    // rank 0 gave up waiting for them).
+    tc::cluster_sync();
 }
 
 }  // namespace
@@ -580,9 +636,9 @@ cudaError_t launch_tc_prefill(const void *q, const int32_t *query_start_loc, con
     P.num_blocks = num_blocks;
     P.scale_log2 = scale * 1.4426950408889634f;
     P.status = status;
-    // an upper bound on the units; CTAs without one exit at once
+    // an upper bound on the units (2 CTAs each); CTA pairs without one exit at once
     const long long units = (long long)num_kv_heads * ((total_q_tokens + qt - 1) / qt + num_seqs);
-    const int grid = (int)(units > 0x7fffffff ? 0x7fffffff : units);
+    const int grid = (int)(2 * units > 0x7ffffffe ? 0x7ffffffe : 2 * units);
     if (grid == 0)
         return cudaSuccess;
     if (dtype == NS_BF16)

@@ -8,14 +8,24 @@ import torch
 from paged_kv_decode_ns_gb300 import binding as nb
 from paged_kv_decode_ns_gb300 import workloads as wl
 
-# Tolerance on fp16 / bf16 attention outputs: max-abs 2e-3 and relative L2
-# 1e-3, measured against the fp64 oracle rounded (nearest-even) to the output
-# element type.  The rounding of the output itself is not charged to the
-# kernel: rounding exact values to bf16 alone gives a relative L2 error near
-# 1.6e-3, above the bound, so the bound can only apply to what the kernel
-# adds to that last rounding.
+# Tolerance on fp16 / bf16 attention outputs: max-abs error 2e-3 and relative
+# L2 error 1e-3.  The final rounding of the output to its 16-bit type is not
+# charged to the kernel:
+#   * max-abs: |out - exact| <= 2e-3 + half an ulp of the output type at the
+#     exact value (a value within the kernel's fp32 error of a rounding
+#     midpoint may round either way: one bf16 ulp is 7.8e-3 in [1, 2));
+#   * rel-L2: against the exact value rounded to the output type (rounding
+#     exact values to bf16 alone gives a relative L2 near 1.6e-3).
 MAX_ABS = 2e-3
 REL_L2 = 1e-3
+
+
+def ulp(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Spacing of the fp16 / bf16 numbers around |x| (normal range; the
+    subnormal quantum below it)."""
+    m, e = np.frexp(np.abs(np.asarray(x, dtype=np.float64)))
+    p = 10 if dtype == wl.F16 else 7
+    return np.maximum(np.ldexp(1.0, e - 1 - p), 2.0 ** -24 if dtype == wl.F16 else 2.0 ** -133)
 
 
 def torch_dtype(dtype: str):
@@ -52,18 +62,17 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
 
 
 def compare(got: torch.Tensor, ref64: np.ndarray, dtype: str, what: str = ""):
-    """Assert max-abs <= MAX_ABS and rel-L2 <= REL_L2 against the rounded oracle.
-    Returns (max_abs, rel_l2, raw_max_abs_vs_fp64)."""
+    """Assert the tolerance above.  Returns (kernel max-abs error beyond the
+    output rounding, rel-L2 against the rounded oracle, raw max-abs vs fp64)."""
     g = to_f64(got).reshape(ref64.shape)
     r = round_to_dtype(ref64, dtype)
     assert np.all(np.isfinite(g)), f"{what}: non-finite output"
-    err = np.abs(g - r)
-    max_abs = float(err.max(initial=0.0))
+    raw = np.abs(g - ref64)
+    excess = float(np.max(raw - 0.5 * ulp(ref64, dtype), initial=0.0))
     rel = float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30))
-    raw = float(np.abs(g - ref64).max(initial=0.0))
-    assert max_abs <= MAX_ABS, f"{what}: max-abs {max_abs:.3g} > {MAX_ABS}"
+    assert excess <= MAX_ABS, f"{what}: max-abs {excess:.3g} beyond the output rounding > {MAX_ABS}"
     assert rel <= REL_L2, f"{what}: rel-L2 {rel:.3g} > {REL_L2}"
-    return max_abs, rel, raw
+    return excess, rel, float(raw.max(initial=0.0))
 
 
 class DevStep:
@@ -110,9 +119,14 @@ def assert_no_device_status():
     assert bits == 0, f"device status 0x{bits:x}"
 
 
-def config(num_ctas=0, min_blocks_per_cta=0, whole_sequences=0):
+def config(num_ctas=0, min_blocks_per_cta=0, whole_sequences=0, kernel=nb.DECODE_KERNEL_AUTO):
     c = nb.DecodeConfig()
     c.num_ctas = num_ctas
     c.min_blocks_per_cta = min_blocks_per_cta
     c.whole_sequences = whole_sequences
+    c.kernel = kernel
     return c
+
+
+# The two decode kernels: tensor cores (block sizes 16, 32) and CUDA cores (all).
+KERNELS = {"tc": nb.DECODE_KERNEL_TENSOR_CORE, "cuda": nb.DECODE_KERNEL_CUDA_CORE}
