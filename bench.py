@@ -42,6 +42,37 @@ sys.path.insert(0, ROOT)
 METRIC = ("paged decode attention: KV-read GB/s (% of GB300 HBM peak), "
           "µs per decode step")
 FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes per launch of the dominant kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum) from one ncu capture, keyed by workload and kernel,
+# with a hash of the kernel's source files at capture time.  The bench reports
+# the figure only while those sources are unchanged (else null).
+KERNEL_SOURCES = {
+    "paged_decode_kernel": ["paged_kv_decode_ns_gb300/csrc/paged_decode.cuh",
+                            "paged_kv_decode_ns_gb300/csrc/paged_decode_launch.cuh",
+                            "paged_kv_decode_ns_gb300/csrc/ns_common.cuh", "include/ns_paged.h"],
+    "tc_prefill_kernel": ["paged_kv_decode_ns_gb300/csrc/tc_prefill.cu",
+                          "paged_kv_decode_ns_gb300/csrc/ns_common.cuh",
+                          "paged_kv_decode_ns_gb300/csrc/tcgen05.cuh", "include/ns_paged.h"],
+}
+PROFILED_TRAFFIC = {}
+
+
+def kernel_sources_sha(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(rel.encode())
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload: str, kernel: str):
+    rec = PROFILED_TRAFFIC.get((workload, kernel))
+    if rec is None or rec["sources_sha256"] != kernel_sources_sha(kernel):
+        return None
+    return rec["bytes"]
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -399,8 +430,10 @@ def bench_ours(args):
     if step.decode:
         peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
         achieved = alg_bytes / (launch_ms * 1e-3) / 1e9
+        traffic = args.traffic if args.traffic is not None else profiled_traffic(args.workload,
+                                                                                  "paged_decode_kernel")
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                    "frac": achieved / peak, "traffic": args.traffic,
+                    "frac": achieved / peak, "traffic": traffic,
                     "kernel": "paged_decode_kernel (fused kv_append + split-KV decode)",
                     "bytes_per_launch": alg_bytes, "launch_us": launch_ms * 1e3,
                     "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"}
@@ -409,8 +442,10 @@ def bench_ours(args):
         peak = float(peaks.get("bf16_tflops", 1900.0))
         flops = prefill_flops(st)
         achieved = flops / (launch_ms * 1e-3) / 1e12
+        traffic = args.traffic if args.traffic is not None else profiled_traffic(args.workload,
+                                                                                  "tc_prefill_kernel")
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": args.traffic,
+                    "frac": achieved / peak, "traffic": traffic,
                     "kernel": "tc_prefill_kernel (tcgen05, spans of 2+ rows)",
                     "flops_per_launch": flops, "launch_us": launch_ms * 1e3,
                     "peak_source": f"{peak_src} bf16_tflops (burst) x nominal fp16/bf16 ratio 1.0"}

@@ -113,7 +113,7 @@ ns_status ns_kv_append(const void *k, const void *v, const int64_t *slot_mapping
 /*
  * Workspace for the attention entry points: split-KV partial results
  * (fp32 running max, running sum and unnormalised output of each piece of a
- * sequence that was cut across CTAs), one arrival counter per (sequence, kv
+ * sequence that was cut across workers, about 8.7 MB), one arrival counter per (sequence, kv
  * head) and a small plan record.  Size it with ns_paged_attn_workspace_bytes
  * for the largest num_seqs you will pass.  It must be zero-filled once before
  * first use (ns_paged_attn_workspace_init or cudaMemsetAsync); every call
@@ -152,9 +152,6 @@ ns_status ns_paged_attn_workspace_init(void *workspace, size_t workspace_bytes,
  * run of them, so a long context is split across CTAs (flash-decoding style)
  * and its partial results are merged by log-sum-exp.  How many CTAs run is
  * decided on the device from the actual context lengths and batch size.
- * Block sizes 16 and 32 run on the tcgen05 tensor cores (S = Q K^T and
- * P V per 128-key tile, one CTA per SM); block sizes 4 and 8 run on the
- * CUDA cores.
  */
 ns_status ns_paged_attn_decode(const void *q, const void *k_pool, const void *v_pool,
                                const int32_t *block_tables, const int32_t *context_lens,
@@ -167,28 +164,18 @@ ns_status ns_paged_attn_decode(const void *q, const void *k_pool, const void *v_
  * Policy overrides for the split-KV decode (tests and measurements).
  *   num_ctas            0 = auto (resident CTAs on this GPU); else the grid size
  *                       (1 .. NS_MAX_CTAS)
- *   min_blocks_per_cta  0 = auto; fewer CTAs are used when the total work
- *                       would give each less than this many KV blocks
- *   whole_sequences     nonzero = never split a (sequence, kv head): CTA c
- *                       takes pairs c, c+G, c+2G, ... (no merge step)
- *   kernel              NS_DECODE_KERNEL_AUTO (0): tensor cores for block
- *                       sizes 16 and 32, CUDA cores otherwise;
- *                       NS_DECODE_KERNEL_CUDA_CORE / _TENSOR_CORE force one
- *                       (the tensor-core kernel with another block size
- *                       returns NS_ERR_UNSUPPORTED).  Both compute the same
- *                       result within the stated tolerance.
- *   reserved            must be zero
+ *   min_blocks_per_cta  0 = auto; fewer workers (warps, 4 per CTA) are used
+ *                       when the total work would give each less than a
+ *                       quarter of this many KV blocks
+ *   whole_sequences     nonzero = never split a (sequence, kv head): worker w
+ *                       of W takes pairs w, w+W, w+2W, ... (no merge step)
  */
 #define NS_MAX_CTAS 1024
-#define NS_DECODE_KERNEL_AUTO 0
-#define NS_DECODE_KERNEL_CUDA_CORE 1
-#define NS_DECODE_KERNEL_TENSOR_CORE 2
 typedef struct ns_decode_config {
     int num_ctas;
     int min_blocks_per_cta;
     int whole_sequences;
-    int kernel;
-    int reserved[4];
+    int reserved[5];
 } ns_decode_config;
 
 /* ns_paged_attn_decode with policy overrides (cfg may be NULL = auto). */
@@ -209,13 +196,11 @@ ns_status ns_paged_attn_decode_ex(const void *q, const void *k_pool, const void 
  *   slot_mapping  int64 [num_seqs]: must be the slot of that position,
  *                 block_tables[s][(L-1)/bs]*bs + (L-1)%bs
  * The result equals the two calls in order: the pool slot is written and the
- * attention includes the new token.  Only the CTA that owns a sequence's
- * last block touches the slot, and it never reads the slot while writing
- * it (the CUDA-core kernel takes the new K/V from k_new/v_new; the
- * tensor-core kernel writes the slot, fences, then loads the block).  A slot
- * that is not the slot of position L-1 sets NS_DEV_FUSED_SLOT: the given
- * slot is still written if it lies in the pool, and the attention result of
- * the sequences involved is then unspecified.
+ * attention includes the new token.  The CTA that owns a sequence's last
+ * block takes the new K/V from k_new/v_new (never from the pool slot it is
+ * writing), so nothing reads the slot while it is written.  A slot that is
+ * not the slot of position L-1 sets NS_DEV_FUSED_SLOT (the slot is still
+ * written; the attention still uses the new token at position L-1).
  */
 ns_status ns_kv_append_paged_attn_decode(const void *q, const void *k_new, const void *v_new,
                                          const int64_t *slot_mapping, void *k_pool,
@@ -229,13 +214,15 @@ ns_status ns_kv_append_paged_attn_decode(const void *q, const void *k_new, const
 
 /*
  * Plan record the decode kernels leave at the start of the workspace (CTA 0
- * writes it during every call).  It shows which split the device chose:
+ * writes it during every call).  It shows which split the device chose.  The
+ * unit of work is a worker: one warp of a CTA (4 workers per CTA).
  *   ctas_launched   grid size
- *   ctas_active     CTAs that received work
+ *   ctas_active     CTAs with at least one worker that received work
  *   total_blocks    KV blocks over all (sequence, kv head) pairs
- *   split_pairs     (sequence, kv head) pairs cut across two or more CTAs
- *   max_pieces      most CTAs sharing one pair
+ *   split_pairs     (sequence, kv head) pairs cut across two or more workers
+ *   max_pieces      most workers sharing one pair
  *   whole_sequences 1 when the no-split policy ran
+ *   workers_active  workers that received work
  */
 typedef struct ns_decode_plan {
     int32_t ctas_launched;
@@ -244,7 +231,8 @@ typedef struct ns_decode_plan {
     int32_t split_pairs;
     int32_t max_pieces;
     int32_t whole_sequences;
-    int32_t reserved[9];
+    int32_t workers_active;
+    int32_t reserved[8];
 } ns_decode_plan;
 
 /* Copy the plan record out of `workspace` (synchronises `stream`). */
@@ -322,7 +310,7 @@ ns_status ns_paged_attn_prefill_ex(const void *q, const int32_t *query_start_loc
  * must not allocate once they run.  It takes the same inputs and output as
  * ns_paged_attn_decode (same checks, same result) but no workspace: the split
  * partial records, arrival counters and plan record live in a scratch array
- * compiled into the library (about 4.4 MB, held by every GPU that loads the
+ * compiled into the library (about 8.7 MB, held by every GPU that loads the
  * library until the process exits).
  *   - num_seqs * num_kv_heads must not exceed NS_NOALLOC_MAX_PAIRS; larger
  *     calls return NS_ERR_UNSUPPORTED and launch nothing.

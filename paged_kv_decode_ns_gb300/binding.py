@@ -41,11 +41,7 @@ class NsError(RuntimeError):
 
 class DecodeConfig(ctypes.Structure):
     _fields_ = [("num_ctas", ctypes.c_int), ("min_blocks_per_cta", ctypes.c_int),
-                ("whole_sequences", ctypes.c_int), ("kernel", ctypes.c_int),
-                ("reserved", ctypes.c_int * 4)]
-
-
-DECODE_KERNEL_AUTO, DECODE_KERNEL_CUDA_CORE, DECODE_KERNEL_TENSOR_CORE = 0, 1, 2
+                ("whole_sequences", ctypes.c_int), ("reserved", ctypes.c_int * 5)]
 
 
 class PrefillConfig(ctypes.Structure):
@@ -57,7 +53,7 @@ class DecodePlan(ctypes.Structure):
     _fields_ = [("ctas_launched", ctypes.c_int32), ("ctas_active", ctypes.c_int32),
                 ("total_blocks", ctypes.c_int64), ("split_pairs", ctypes.c_int32),
                 ("max_pieces", ctypes.c_int32), ("whole_sequences", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 9)]
+                ("workers_active", ctypes.c_int32), ("reserved", ctypes.c_int32 * 8)]
 
 
 _LIB = None

@@ -17,7 +17,6 @@ constexpr int kMaxDevices = 64;
 std::atomic<unsigned *> g_status_ptr[kMaxDevices];
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_ctas_per_sm[kMaxDevices][2][4][ns::kMaxGroup];
-std::atomic<int> g_tc_ctas_per_sm[kMaxDevices][2][2];
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -130,18 +129,6 @@ int resident_ctas(int dev, ns_dtype dt, int bs, int g)
     return (int)(total > NS_MAX_CTAS ? NS_MAX_CTAS : total);
 }
 
-int resident_tc_ctas(int dev, ns_dtype dt, int bs)
-{
-    std::atomic<int> &slot = g_tc_ctas_per_sm[dev][dt == NS_BF16 ? 1 : 0][bs == 16 ? 0 : 1];
-    int n = slot.load(std::memory_order_relaxed);
-    if (n <= 0) {
-        n = ns::tc_decode_ctas_per_sm(dt, bs);
-        slot.store(n, std::memory_order_relaxed);
-    }
-    long long total = (long long)n * sm_count(dev);
-    return (int)(total > NS_MAX_CTAS ? NS_MAX_CTAS : total);
-}
-
 // Workspace layout (byte offsets), for up to `rows` query rows.
 struct WsLayout {
     size_t plan, counters, partials, row_seq, row_len, total;
@@ -153,7 +140,7 @@ WsLayout ws_layout(long long rows, int num_kv_heads)
     L.plan = 0;
     L.counters = 256;
     L.partials = L.counters + align256((size_t)rows * num_kv_heads * sizeof(int32_t));
-    L.row_seq = L.partials + align256((size_t)NS_MAX_CTAS * 2 * ns::kSlotFloats * sizeof(float));
+    L.row_seq = L.partials + align256((size_t)ns::kMaxWorkers * 2 * ns::kSlotFloats * sizeof(float));
     L.row_len = L.row_seq + align256((size_t)rows * sizeof(int32_t));
     L.total = L.row_len + align256((size_t)rows * sizeof(int32_t));
     return L;
@@ -235,8 +222,7 @@ ns_status run_decode(const DecodeCall &c, int dev)
                         ? 1
                         : 0;
 
-    return ns::launch_decode(P, c.dtype, c.block_size, c.cfg ? c.cfg->kernel : NS_DECODE_KERNEL_AUTO,
-                             c.cfg ? c.cfg->num_ctas : 0, c.stream, dev);
+    return ns::launch_decode(P, c.dtype, c.block_size, c.cfg ? c.cfg->num_ctas : 0, c.stream, dev);
 }
 
 ns_status check_decode_args(const void *q, const void *k_pool, const void *v_pool,
@@ -260,12 +246,8 @@ ns_status check_decode_args(const void *q, const void *k_pool, const void *v_poo
         return NS_ERR_INVALID_ARG;
     if (workspace_bytes < ns_paged_attn_workspace_bytes(rows, num_q_heads, num_kv_heads, head_dim))
         return NS_ERR_INVALID_ARG;
-    if (cfg && (cfg->num_ctas < 0 || cfg->num_ctas > NS_MAX_CTAS || cfg->min_blocks_per_cta < 0 ||
-                cfg->kernel < NS_DECODE_KERNEL_AUTO || cfg->kernel > NS_DECODE_KERNEL_TENSOR_CORE))
+    if (cfg && (cfg->num_ctas < 0 || cfg->num_ctas > NS_MAX_CTAS || cfg->min_blocks_per_cta < 0))
         return NS_ERR_INVALID_ARG;
-    if (cfg && cfg->kernel == NS_DECODE_KERNEL_TENSOR_CORE &&
-        !ns::tc_decode_supported(block_size, num_q_heads / num_kv_heads))
-        return NS_ERR_UNSUPPORTED;
     return NS_OK;
 }
 
@@ -273,33 +255,15 @@ ns_status check_decode_args(const void *q, const void *k_pool, const void *v_poo
 
 namespace ns {
 
-ns_status launch_decode(const DecodeParams &P, ns_dtype dtype, int block_size, int kernel,
-                        int num_ctas, cudaStream_t stream, int dev)
+ns_status launch_decode(const DecodeParams &P, ns_dtype dtype, int block_size, int num_ctas,
+                        cudaStream_t stream, int dev)
 {
     const int g = P.group;
-    bool tc;
-    if (kernel == NS_DECODE_KERNEL_TENSOR_CORE) {
-        if (!tc_decode_supported(block_size, g))
-            return NS_ERR_UNSUPPORTED;
-        tc = true;
-    } else if (kernel == NS_DECODE_KERNEL_AUTO) {
-        tc = tc_decode_supported(block_size, g);
-    } else if (kernel == NS_DECODE_KERNEL_CUDA_CORE) {
-        tc = false;
-    } else {
-        return NS_ERR_INVALID_ARG;
-    }
-    int ctas = num_ctas > 0 ? num_ctas
-                            : (tc ? resident_tc_ctas(dev, dtype, block_size)
-                                  : resident_ctas(dev, dtype, block_size, g));
+    int ctas = num_ctas > 0 ? num_ctas : resident_ctas(dev, dtype, block_size, g);
     if (ctas > NS_MAX_CTAS)
         ctas = NS_MAX_CTAS;
-    cudaError_t e;
-    if (tc)
-        e = launch_tc_decode(P, dtype, block_size, ctas, stream);
-    else
-        e = dtype == NS_BF16 ? dispatch_decode<BF16>(block_size, g, P, ctas, stream)
-                             : dispatch_decode<F16>(block_size, g, P, ctas, stream);
+    const cudaError_t e = dtype == NS_BF16 ? dispatch_decode<BF16>(block_size, g, P, ctas, stream)
+                                           : dispatch_decode<F16>(block_size, g, P, ctas, stream);
     return e == cudaSuccess ? NS_OK : NS_ERR_CUDA;
 }
 

@@ -24,16 +24,10 @@ unsigned *device_status_word(int dev);
 
 struct DecodeParams;
 
-// Split-KV decode on the tcgen05 tensor cores (block sizes 16 and 32).
-bool tc_decode_supported(int block_size, int group);
-int tc_decode_ctas_per_sm(ns_dtype dtype, int block_size);
-cudaError_t launch_tc_decode(const DecodeParams &P, ns_dtype dtype, int block_size, int num_ctas,
-                             cudaStream_t stream);
-
-// Launch the decode kernel chosen by `kernel` (NS_DECODE_KERNEL_*) with
-// num_ctas CTAs, or the resident CTAs of device `dev` when num_ctas is 0.
-ns_status launch_decode(const DecodeParams &P, ns_dtype dtype, int block_size, int kernel,
-                        int num_ctas, cudaStream_t stream, int dev);
+// Launch the split-KV decode kernel with num_ctas CTAs, or with the resident
+// CTAs of device `dev` when num_ctas is 0.
+ns_status launch_decode(const DecodeParams &P, ns_dtype dtype, int block_size, int num_ctas,
+                        cudaStream_t stream, int dev);
 
 // Chunked prefill of every span of two or more tokens on the tcgen05 tensor cores.
 bool tc_prefill_supported(int block_size, int group);

@@ -1,44 +1,44 @@
-// paged_decode.cuh -- split-KV paged-attention decode for sm_103a.
+// paged_decode.cuh -- split-KV paged-attention decode for sm_103a (CUDA cores).
 //
 // What it computes: for every sequence s and query head j (kv head h =
 // j / group), out[s][j] = softmax_p(scale * q[s][j] . K_s[p]) . V_s[p] over
 // the L_s tokens found through the sequence's block table (nanoserve project
 // page, "What I built": fused paged-attention decode with online softmax over
-// the block table).  Long walks are split across CTAs and merged by
+// the block table).  Long walks are split and the parts merged by
 // log-sum-exp (the flash-decoding split arm of the nanoserve build log, Day
 // 74 post).
 //
 // How (GB300-first design, not the pages' Triton kernel):
-//  * Persistent grid.  The KV blocks of all (sequence, kv head) pairs are laid
-//    end to end; CTA c of G takes blocks [c*B/G, (c+1)*B/G), so every CTA
-//    gets the same number of blocks whatever the length mix.  A pair cut by a
-//    CTA boundary yields partial (max, sum, unnormalised output) records; the
-//    CTA that finishes a pair's last piece merges them (log-sum-exp) and
-//    writes the output.  G is chosen on the device from the real lengths.
-//  * Per-warp TMA rings.  Each of the 4 warps of a CTA takes every 4th block
-//    of a piece and keeps its own S-slot ring of shared memory fed by TMA bulk
-//    copies (cp.async.bulk) of whole (block, kv head) K and V chunks --
-//    block_size*128 contiguous bytes each -- issued S blocks ahead of use and
-//    completed on the slot's mbarrier.  No warp waits on another warp's
-//    progress except at the merge at the end of a piece.
-//  * Lane layout.  Lane (r, c) = (lane>>3, lane&7) owns dims 8c..8c+7 of token
-//    rows r, r+4, r+8, ... of its block, for all G query heads of the GQA
-//    group, so one 16-byte shared load feeds every head.  Dot products run on
-//    packed fp32 FMA (two per instruction).  The partial sums of a token are
-//    combined by a shuffle reduce-scatter over the row's 8 lanes; the heads
-//    are padded to a power of two N and slot i of lane c holds head
-//    i ^ (c >> (3 - log2 N)), so the halving steps need no lane-dependent
-//    selects and lane c ends with head c >> (3 - log2 N).  All token rows of a
-//    block are scored before any softmax work, so the shuffle chains of the
-//    rows overlap.
-//  * Online softmax per (row, head) in log2 units with lazy rescaling: the
-//    running max moves only when a score exceeds it by more than
-//    kRescaleSlack, and the result is exact because sum and accumulator share
-//    the stale max.
-//  * Every wait is bounded; a timeout sets NS_DEV_WAIT_TIMEOUT and the CTA
-//    winds down (warps meet through an mbarrier with a bounded wait, never
-//    through bar.sync, so a warp that leaves early cannot hang the others),
-//    waiting -- again bounded -- for its own copies in flight before it exits.
+//  * Workers are warps.  The KV blocks of all (sequence, kv head) pairs are
+//    laid end to end and worker w of Gw takes blocks [w*B/Gw, (w+1)*B/Gw),
+//    so every warp gets the same number of blocks whatever the length mix,
+//    and no warp ever waits on another: a pair cut by a worker boundary
+//    yields a partial (max, sum, unnormalised output) record written by the
+//    warp alone, and the warp that finishes a pair's last piece merges the
+//    records (log-sum-exp) and writes the output.  Gw is chosen on the
+//    device from the real lengths; when no pair is long, whole pairs are
+//    dealt round-robin and nothing is merged.
+//  * Per-warp TMA rings.  Each warp streams its range through its own ring
+//    of S slots of 16 tokens: TMA bulk copies (cp.async.bulk) of the K and V
+//    rows of 16/bs whole blocks (half a block at block size 32), issued S
+//    steps ahead of use, L2 evict-first, completed on the slot's mbarrier.
+//    The first step of a piece also brings the group's q rows, and with a
+//    fused append the step that holds the new token brings its K/V rows.
+//    Block-table entries are read 32 at a time, the next 32 prefetched.
+//  * Lane layout.  Lane (r, c) = (lane>>3, lane&7) owns dims 8c..8c+7 of
+//    token rows r, r+4, r+8, r+12 of a step, for all G query heads of the
+//    GQA group, so one 16-byte shared load feeds every head.  Dot products
+//    run on packed fp32 FMA (two per instruction).  The partial sums of a
+//    token are combined by a shuffle reduce-scatter over the row's 8 lanes;
+//    the heads are padded to a power of two N and slot i of lane c holds
+//    head i ^ (c >> (3 - log2 N)), so the halving steps need no
+//    lane-dependent selects and lane c ends with head c >> (3 - log2 N).
+//  * Online softmax per (row group, head) in log2 units with lazy
+//    rescaling: the running max moves only when a score exceeds it by more
+//    than kRescaleSlack, and the result is exact because sum and accumulator
+//    share the stale max.
+//  * Every wait is bounded; a timeout sets NS_DEV_WAIT_TIMEOUT and the warp
+//    stops, waiting -- again bounded -- for its own copies in flight.
 #pragma once
 
 #include "ns_common.cuh"
@@ -49,8 +49,19 @@ namespace ns {
 // log2 units), L[8] (sum of 2^(z-M)), acc[8][64] (unnormalised output).
 constexpr int kSlotFloats = 2 * kMaxGroup + kMaxGroup * kHeadDim;
 constexpr float kRescaleSlack = 8.0f;
-constexpr int kDecodeWarps = 4;
+constexpr int kDecodeWarps = 4;        // workers per CTA
+constexpr int kStepTokens = 32;        // tokens per ring slot (one per lane for the vote)
+constexpr int kMaxWorkers = 2048;      // split workers (each has two record slots)
 constexpr int kDefaultMinBlocksPerCta = 32;
+constexpr int kLensCache = 2048;       // context lengths kept in shared memory
+// Split cost of a (sequence, kv head) pair beyond its blocks: the even split
+// counts kPieceCost virtual blocks at the start of every pair, so a worker
+// whose range crosses many pair boundaries (a piece end, a partial last
+// step, an arrival count and perhaps a merge each) gets fewer real blocks.
+constexpr int kPieceCost = 4;
+
+// Length of a pair in the split's coordinates (0 for a pair with no block).
+__host__ __device__ __forceinline__ int pair_span(int nb) { return nb > 0 ? nb + kPieceCost : 0; }
 
 struct DecodeParams {
     const uint16_t *q;
@@ -74,7 +85,7 @@ struct DecodeParams {
     long long num_blocks;
     float scale_log2;  // scale * log2(e)
     int *counters;     // [num_seqs * num_kv_heads], zero between calls
-    float *partials;   // [NS_MAX_CTAS][2][kSlotFloats]
+    float *partials;   // [kMaxWorkers][2][kSlotFloats]
     ns_decode_plan *plan;
     unsigned *status;
     int min_blocks_per_cta;
@@ -84,7 +95,7 @@ struct DecodeParams {
 
 enum : int {
     kFlagWhole = 4,    // the piece is the whole (sequence, kv head)
-    kFlagWhich1 = 16,  // partial piece stored in the CTA's second slot
+    kFlagWhich1 = 16,  // partial piece stored in the worker's second record slot
 };
 
 // Reduce-scatter slots: the G heads of a group padded to a power of two.
@@ -95,41 +106,39 @@ struct HeadSlots {
     static constexpr int SHIFT = 3 - LOG;  // lane c holds head c >> SHIFT
 };
 
-// Bytes of K/V each warp keeps in flight (its ring); a build-time tuning knob.
-#ifndef NS_DECODE_RING_BYTES
-#define NS_DECODE_RING_BYTES 16384
+// Ring slots per warp; a build-time tuning knob.
+#ifndef NS_DECODE_STAGES
+#define NS_DECODE_STAGES 2
 #endif
 
-// Ring depth per warp: NS_DECODE_RING_BYTES of K/V per warp, 2 to 8 slots.
-constexpr int decode_stages(int BS)
-{
-    return (NS_DECODE_RING_BYTES / (BS * 2 * kRowBytes)) < 2 ? 2
-           : (NS_DECODE_RING_BYTES / (BS * 2 * kRowBytes)) > 8 ? 8
-                                                                : (NS_DECODE_RING_BYTES / (BS * 2 * kRowBytes));
-}
+// One ring slot: K and V rows of one 16-token step, and the extras that ride
+// with it (q rows on a piece's first step, the new token's K/V when fused).
+template <int G>
+struct DecodeSlot {
+    uint16_t k[kStepTokens * kHeadDim];
+    uint16_t v[kStepTokens * kHeadDim];
+    uint16_t q[G * kHeadDim];
+    uint16_t knew[kHeadDim];
+    uint16_t vnew[kHeadDim];
+};
 
 template <int BS, int G, int S>
 struct DecodeSmem {
-    uint16_t k[kDecodeWarps][S][BS * kHeadDim];
-    uint16_t v[kDecodeWarps][S][BS * kHeadDim];
-    uint16_t q[kDecodeWarps][S][G * kHeadDim];
-    uint16_t knew[kDecodeWarps][S][kHeadDim];
-    uint16_t vnew[kDecodeWarps][S][kHeadDim];
-    float2 p[kDecodeWarps][BS][8];  // (p, p) per [token][head]
-    float mrow[kDecodeWarps][4][8];
-    float lrow[kDecodeWarps][4][8];
-    float acc[kDecodeWarps][G][kHeadDim];
-    float mfin[8];
-    float lfin[8];
-    long long new_slot[kDecodeWarps][S];  // fused append: slot of the new token, or -1
+    DecodeSlot<G> ring[kDecodeWarps][S];
+    float2 p[kDecodeWarps][kStepTokens][8];  // (p, p) per [token][head]
     uint64_t full[kDecodeWarps][S];
-    uint64_t cons;  // rendezvous of the 4 warps
+    uint32_t vmask[kDecodeWarps][S];         // bit t: token t of the slot is a key
+    long long new_slot[kDecodeWarps][S];     // fused append: pool slot of the step's new token, or -1
     long long scan[32];
     int maxnb[32];
-    long long b0, b1, total, start_off;
-    int start_s, g_eff, merge_prev, abort_flag;
-    int plan_split, plan_maxp;
+    int npairs[32];
+    long long wb0[kDecodeWarps], wb1[kDecodeWarps], start_off[kDecodeWarps];
+    int start_s[kDecodeWarps];
+    int lens[kLensCache];                    // clamped context lengths of rows 0..kLensCache-1
+    long long total;
+    int g_eff;  // split workers
     int whole;  // 1: whole (sequence, kv head) pairs dealt round-robin, no split
+    int plan_split, plan_maxp;
 };
 
 __device__ __forceinline__ int nblocks_of(int L, int BS) { return (L + BS - 1) / BS; }
@@ -147,7 +156,7 @@ __device__ __forceinline__ int clamped_len(const DecodeParams &P, int s, int BS,
     return L;
 }
 
-// First CTA whose block range contains global block b:  b0(c) = c*B/G.
+// First worker whose block range contains global block b:  b0(c) = c*B/G.
 __device__ __forceinline__ long long cta_of(long long b, long long B, long long G)
 {
     return ((b + 1) * G - 1) / B;
@@ -158,73 +167,49 @@ __device__ __forceinline__ long long range_begin(long long c, long long B, long 
     return c * B / G;
 }
 
-// Bounded wait that also gives up when another warp has aborted.
-__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag)
-{
-    if (mbar_try_wait(bar, parity))
-        return true;
-    const unsigned long long t0 = global_timer_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity))
-            return true;
-        if (*abort_flag)
-            return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs)
-            return false;
-    }
-}
-
-template <class Smem>
-__device__ __forceinline__ void set_abort(const DecodeParams &P, Smem &sm)
-{
-    *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
-    raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
-}
-
-// Rendezvous of all threads of the CTA (4 warps x 32 arrivals per phase).
-template <class Smem>
-__device__ __forceinline__ bool cta_sync(const DecodeParams &P, Smem &sm, uint32_t &phase)
-{
-    mbar_arrive(&sm.cons);
-    const bool ok = wait_or_abort(&sm.cons, phase, &sm.abort_flag);
-    phase ^= 1u;
-    if (!ok)
-        set_abort(P, sm);
-    return ok;
-}
-
 // ---------------------------------------------------------------------------
-// Walk over the pieces of this CTA: in split mode the runs of one (sequence,
-// kv head) pair inside [b0, b1); with whole_sequences the pairs
-// blockIdx.x, blockIdx.x + gridDim.x, ...  Every warp runs the same walk.
+// Walk over the pieces of one worker: in split mode the runs of one
+// (sequence, kv head) pair inside [b0, b1); with whole pairs the pairs
+// w, w + stride, w + 2 stride, ...
 // ---------------------------------------------------------------------------
 struct PieceWalk {
-    long long pos, end, soff;
+    const int *lens;  // shared-memory copy of the first kLensCache clamped lengths
+    long long pos, end, soff, stride;
     int s, h, L, nb;
     bool first;
     bool whole;
-    // the current piece
-    int ps, ph, pL, pnb, lo, hi, flags;
+    // the current piece: real blocks [lo, hi) of pair (ps, ph); pstart and
+    // pspan place the whole pair in the split's coordinates
+    int ps, ph, pL, pnb, lo, hi, flags, pspan;
     long long pstart;
 };
 
 template <class Smem>
-__device__ __forceinline__ void walk_init(const DecodeParams &P, const Smem &sm, PieceWalk &w)
+__device__ __forceinline__ void walk_init(const DecodeParams &P, const Smem &sm, int warp, PieceWalk &w)
 {
+    w.lens = sm.lens;
     w.whole = sm.whole != 0;
     if (w.whole) {
-        w.pos = blockIdx.x;
+        w.pos = (long long)blockIdx.x * kDecodeWarps + warp;
+        w.stride = (long long)gridDim.x * kDecodeWarps;
         w.end = (long long)P.num_seqs * P.num_kv_heads;
     } else {
-        w.pos = sm.b0;
-        w.end = sm.b1;
+        w.pos = sm.wb0[warp];
+        w.end = sm.wb1[warp];
+        w.stride = 0;
     }
-    w.soff = sm.start_off;
-    w.s = sm.start_s;
+    w.soff = sm.start_off[warp];
+    w.s = sm.start_s[warp];
     w.h = 0;
     w.L = -1;
     w.nb = 0;
     w.first = true;
+}
+
+template <int BS>
+__device__ __forceinline__ int len_at(const DecodeParams &P, const PieceWalk &w, int s)
+{
+    return s < kLensCache ? w.lens[s] : clamped_len(P, s, BS, false);
 }
 
 template <int BS>
@@ -234,9 +219,9 @@ __device__ __forceinline__ bool walk_next(const DecodeParams &P, PieceWalk &w)
     if (w.whole) {
         while (w.pos < w.end) {
             const long long pair = w.pos;
-            w.pos += gridDim.x;
+            w.pos += w.stride;
             const int s = (int)(pair / Hkv);
-            const int L = clamped_len(P, s, BS, false);
+            const int L = len_at<BS>(P, w, s);
             const int nb = nblocks_of(L, BS);
             if (nb == 0)
                 continue;
@@ -248,183 +233,256 @@ __device__ __forceinline__ bool walk_next(const DecodeParams &P, PieceWalk &w)
             w.hi = nb;
             w.flags = kFlagWhole;
             w.pstart = -1;
+            w.pspan = pair_span(nb);
             return true;
         }
         return false;
     }
     while (w.pos < w.end && w.s < P.num_seqs) {
         if (w.L < 0) {
-            w.L = clamped_len(P, w.s, BS, false);
+            w.L = len_at<BS>(P, w, w.s);
             w.nb = nblocks_of(w.L, BS);
             w.h = 0;
         }
+        const int span = pair_span(w.nb);
         if (w.h >= Hkv) {
-            w.soff += (long long)Hkv * w.nb;
+            w.soff += (long long)Hkv * span;
             ++w.s;
             w.L = -1;
             continue;
         }
-        const long long pstart = w.soff + (long long)w.h * w.nb;
-        const long long pend = pstart + w.nb;
+        const long long pstart = w.soff + (long long)w.h * span;
+        const long long pend = pstart + span;
         const int h = w.h++;
         if (pend <= w.pos)
             continue;
+        const int lo_v = (int)(w.pos - pstart);
+        const int hi_v = (int)(min(w.end, pend) - pstart);
         w.ps = w.s;
         w.ph = h;
         w.pL = w.L;
         w.pnb = w.nb;
-        w.lo = (int)(w.pos - pstart);
-        w.hi = (int)(min(w.end, pend) - pstart);
-        const bool whole = (w.lo == 0 && w.hi == w.nb);
+        w.lo = max(lo_v - kPieceCost, 0);  // the virtual blocks hold no keys
+        w.hi = max(hi_v - kPieceCost, 0);
+        const bool whole = (lo_v == 0 && hi_v == span);
         w.flags = whole ? kFlagWhole : (w.first ? 0 : kFlagWhich1);
         w.first = false;
         w.pstart = pstart;
-        w.pos = pstart + w.hi;
+        w.pspan = span;
+        w.pos = pstart + hi_v;
         return true;
     }
     return false;
 }
 
+// One past the last key of a piece (inside the pair).
+template <int BS>
+__device__ __forceinline__ int piece_end_token(const PieceWalk &w)
+{
+    return min(w.hi * BS, w.pL);
+}
+
+// Steps (32-token ring slots) of a piece: step i covers keys
+// lo*bs + 32i .. lo*bs + 32i + 31 of the pair, i.e. 32/bs whole blocks.
+template <int BS>
+__device__ __forceinline__ int steps_of(const PieceWalk &w)
+{
+    return max(0, (piece_end_token<BS>(w) - w.lo * BS + kStepTokens - 1) / kStepTokens);
+}
+
+// First token (inside the pair) of step i of the piece.
+template <int BS>
+__device__ __forceinline__ int step_token0(const PieceWalk &w, int i)
+{
+    return w.lo * BS + i * kStepTokens;
+}
+
 // ---------------------------------------------------------------------------
 // Issue side of a warp's ring: walks the same pieces as the consumer and
-// issues the TMA copies of this warp's blocks, up to S blocks ahead.
+// issues the TMA copies of each 32-token step, up to S steps ahead.
 // ---------------------------------------------------------------------------
 template <typename T, int BS, int G, int S>
 struct Issuer {
-    PieceWalk w;
-    int i;             // this warp's next block index inside the piece
-    bool has;          // a piece is open
+    static constexpr int KB = kStepTokens / BS;  // blocks per step
+    PieceWalk w;       // the piece being issued
+    PieceWalk nw;      // the next piece (looked up one piece ahead)
+    bool nvalid;
+    int step, nsteps;
+    bool has;
     bool done;
-    int issued;        // blocks issued so far
-    int tab_first;     // first block of the cached table chunk (-1: none)
-    int tab_val;       // lane l: phys block of tab_first + 4*l (-1: invalid)
-    long long slot_v;  // fused: slot_mapping of the piece's sequence
+    int issued;
+    long long trow, ntrow;
+    long long slot_v, nslot_v;  // fused append: slot_mapping of the piece's sequence
+    int tab_first;     // first block of the cached table chunk
+    int tab_val;       // lane l: table entry of block tab_first + l (-1 past the piece)
+    int nxt_val;       // lane l: table entry of block tab_first + 32 + l
+    int ntab;          // lane l: table entry of block nw.lo + l
     uint64_t policy;
 
-    __device__ void init(const DecodeParams &P, const DecodeSmem<BS, G, S> &sm)
+    // Raw table entry (checked where it is used, so that the load does not
+    // stall the warp here); -1 past the piece.
+    __device__ int table_raw(const DecodeParams &P, long long row, int blk, int hi) const
     {
-        walk_init(P, sm, w);
-        i = 0;
+        return blk < hi ? __ldg(P.block_tables + row * P.max_blocks_per_seq + blk) : -1;
+    }
+
+    __device__ void look_ahead(const DecodeParams &P, int lane)
+    {
+        nvalid = walk_next<BS>(P, nw);
+        if (nvalid) {
+            ntrow = P.table_row != nullptr ? __ldg(P.table_row + nw.ps) : nw.ps;
+            ntab = table_raw(P, ntrow, nw.lo + lane, nw.hi);
+            nslot_v = (P.k_new != nullptr && nw.hi == nw.pnb) ? __ldg(P.slot_mapping + nw.ps) : -1;
+        }
+    }
+
+    template <class Smem>
+    __device__ void init(const DecodeParams &P, const Smem &sm, int warp, int lane)
+    {
+        walk_init(P, sm, warp, nw);
+        look_ahead(P, lane);
         has = false;
         done = false;
         issued = 0;
-        tab_first = -1;
-        tab_val = -1;
-        slot_v = -1;
+        step = nsteps = 0;
         policy = l2_evict_first_policy();
     }
 
-    // Issue this warp's next block; false when the walk is exhausted.
+    // Move to the looked-up piece and look up the one after it.
+    __device__ bool next_piece(const DecodeParams &P, int lane)
+    {
+        if (!nvalid)
+            return false;
+        w = nw;
+        trow = ntrow;
+        slot_v = nslot_v;
+        tab_first = w.lo;
+        tab_val = ntab;
+        nxt_val = table_raw(P, trow, w.lo + 32 + lane, w.hi);
+        step = 0;
+        nsteps = steps_of<BS>(w);
+        look_ahead(P, lane);
+        return true;
+    }
+
+    // Issue this warp's next step; false when the walk is exhausted.
     __device__ bool issue_one(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int warp, int lane)
     {
-        int blk;
-        while (true) {
-            if (!has) {
-                if (!walk_next<BS>(P, w)) {
-                    done = true;
-                    return false;
-                }
-                has = true;
-                i = 0;
-                tab_first = -1;
-                if (P.k_new != nullptr && w.hi == w.pnb)
-                    slot_v = __ldg(P.slot_mapping + w.ps);  // read early, used at the last block
+        while (!has || step >= nsteps) {
+            if (!next_piece(P, lane)) {
+                done = true;
+                return false;
             }
-            blk = w.lo + warp + kDecodeWarps * i;
-            if (blk < w.hi)
-                break;
-            has = false;
+            has = true;
         }
-        if (tab_first < 0 || blk >= tab_first + kDecodeWarps * 32) {
-            tab_first = blk;
-            const int b = blk + kDecodeWarps * lane;
-            tab_val = -1;
-            if (b < w.hi) {
-                const long long trow = P.table_row != nullptr ? __ldg(P.table_row + w.ps) : w.ps;
-                const int v = __ldg(P.block_tables + trow * P.max_blocks_per_seq + b);
-                if (v < 0 || (long long)v >= P.num_blocks)
-                    raise_status(P.status, NS_DEV_BAD_BLOCK_ID);
-                else
-                    tab_val = v;
-            }
+        // blocks of this step: KB whole blocks from `first`
+        const int first = w.lo + step * KB;
+        if (first >= tab_first + 32) {
+            tab_first += 32;
+            tab_val = nxt_val;
+            nxt_val = table_raw(P, trow, tab_first + 32 + lane, w.hi);
         }
-        const int phys = __shfl_sync(0xffffffffu, tab_val, (blk - tab_first) / kDecodeWarps);
-        const int slot = issued % S;
-        const bool first_of_mine = (i == 0);
-        const bool last_of_seq = P.k_new != nullptr && blk == w.pnb - 1;
-        const uint32_t bytes = (phys >= 0 ? 2u * BS * kRowBytes : 0u) +
-                               (first_of_mine ? (uint32_t)G * kRowBytes : 0u) +
-                               (last_of_seq ? 2u * kRowBytes : 0u);
-        __syncwarp();  // every lane is done reading this slot's previous contents
-        if (lane == 0) {
-            long long ns = -1;
-            if (last_of_seq) {
-                ns = slot_v;
-                const long long want = (long long)phys * BS + (w.pL - 1) % BS;
-                if (ns != want || phys < 0)
-                    raise_status(P.status, NS_DEV_FUSED_SLOT);
-                if (ns >= P.num_blocks * BS) {
+        int phys = __shfl_sync(0xffffffffu, tab_val, (first - tab_first + (lane < KB ? lane : 0)) & 31);
+        const bool mine = lane < KB && first + lane < w.hi;
+        if (mine && (phys < 0 || (long long)phys >= P.num_blocks)) {
+            raise_status(P.status, NS_DEV_BAD_BLOCK_ID);
+            phys = -1;
+        }
+        const unsigned loaded = __ballot_sync(0xffffffffu, mine && phys >= 0);
+        const int tok0 = step_token0<BS>(w, step);
+        const int nval = min(kStepTokens, piece_end_token<BS>(w) - tok0);  // >= 1
+        // valid keys: the first nval tokens whose block was loaded
+        uint32_t vm = nval >= 32 ? 0xffffffffu : ((1u << nval) - 1u);
+        if (KB > 1) {
+            uint32_t bm = 0;
+#pragma unroll
+            for (int u = 0; u < KB; ++u)
+                if ((loaded >> u) & 1u)
+                    bm |= (BS >= 32 ? 0xffffffffu : ((1u << BS) - 1u)) << (u * BS);
+            vm &= bm;
+        } else if (!(loaded & 1u)) {
+            vm = 0;
+        }
+        const bool first_step = step == 0;
+        const bool new_tok = P.k_new != nullptr && w.hi == w.pnb && step == nsteps - 1;
+        long long ns = -1;
+        if (new_tok) {
+            // the pool slot of position L-1 must be the one slot_mapping names
+            const int u_last = (w.pL - 1) / BS - first;
+            const int phys_last = __shfl_sync(0xffffffffu, phys, u_last & 31);
+            const long long want = (long long)phys_last * BS + (w.pL - 1) % BS;
+            ns = slot_v;
+            if (lane == 0 && (ns != want || phys_last < 0))
+                raise_status(P.status, NS_DEV_FUSED_SLOT);
+            if (ns >= P.num_blocks * BS) {
+                if (lane == 0)
                     raise_status(P.status, NS_DEV_BAD_SLOT);
-                    ns = -1;
-                }
+                ns = -1;
             }
-            sm.new_slot[warp][slot] = ns;
-            fence_async_smem();  // generic-proxy reads of the slot before the async-proxy refill
-            uint64_t *bar = &sm.full[warp][slot];
-            if (bytes == 0) {
+        }
+        const uint32_t bytes = (uint32_t)__popc(loaded) * 2u * BS * kRowBytes +
+                               (first_step ? (uint32_t)G * kRowBytes : 0u) + (new_tok ? 2u * kRowBytes : 0u);
+        const int slot = issued % S;
+        DecodeSlot<G> &sl = sm.ring[warp][slot];
+        uint64_t *bar = &sm.full[warp][slot];
+        // every lane is done with this slot's previous contents, and its
+        // generic-proxy accesses are ordered before the async-proxy refill
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            sm.vmask[warp][slot] = vm;
+            sm.new_slot[warp][slot] = new_tok ? ns : -1;
+            if (bytes == 0)
                 mbar_arrive(bar);
-            } else {
+            else
                 mbar_arrive_expect_tx(bar, bytes);
-                if (phys >= 0) {
-                    const long long off = ((long long)phys * P.num_kv_heads + w.ph) * BS * kHeadDim;
-                    bulk_load(sm.k[warp][slot], P.k_pool + off, BS * kRowBytes, bar, policy);
-                    bulk_load(sm.v[warp][slot], P.v_pool + off, BS * kRowBytes, bar, policy);
-                }
-                if (first_of_mine) {
-                    const long long qoff = ((long long)w.ps * P.num_q_heads + (long long)w.ph * G) * kHeadDim;
-                    bulk_load(sm.q[warp][slot], P.q + qoff, G * kRowBytes, bar);
-                }
-                if (last_of_seq) {
-                    const long long noff = ((long long)w.ps * P.num_kv_heads + w.ph) * kHeadDim;
-                    bulk_load(sm.knew[warp][slot], P.k_new + noff, kRowBytes, bar);
-                    bulk_load(sm.vnew[warp][slot], P.v_new + noff, kRowBytes, bar);
-                }
-            }
         }
         __syncwarp();
+        if (mine && phys >= 0) {
+            const long long off = ((long long)phys * P.num_kv_heads + w.ph) * BS * kHeadDim;
+            bulk_load(sl.k + lane * BS * kHeadDim, P.k_pool + off, BS * kRowBytes, bar, policy);
+            bulk_load(sl.v + lane * BS * kHeadDim, P.v_pool + off, BS * kRowBytes, bar, policy);
+        }
+        if (lane == 0) {
+            if (first_step) {
+                const long long qoff = ((long long)w.ps * P.num_q_heads + (long long)w.ph * G) * kHeadDim;
+                bulk_load(sl.q, P.q + qoff, G * kRowBytes, bar);
+            }
+            if (new_tok) {
+                const long long noff = ((long long)w.ps * P.num_kv_heads + w.ph) * kHeadDim;
+                bulk_load(sl.knew, P.k_new + noff, kRowBytes, bar);
+                bulk_load(sl.vnew, P.v_new + noff, kRowBytes, bar);
+            }
+        }
         ++issued;
-        ++i;
+        ++step;
         return true;
     }
 };
 
 // ---------------------------------------------------------------------------
-// One block of BS tokens for one warp.  LAST: the sequence's last block
-// (tokens >= valid are masked; with a fused append, token t_new comes from
-// the new-token buffers instead of the pool copy).
+// One 32-token step for one warp.  MASKED: some tokens of the step are not
+// keys (bit t of vmask clear): their scores are -inf and their values 0.
 // ---------------------------------------------------------------------------
-template <typename T, int BS, int G, bool LAST>
-__device__ __forceinline__ void process_block(const uint16_t *__restrict__ kb,
-                                              const uint16_t *__restrict__ vb, int valid, int t_new,
-                                              const uint16_t *knew, const uint16_t *vnew,
-                                              const float2 (&q2)[HeadSlots<G>::N][4],
-                                              float2 (&acc)[G][4], float &m_run, float &l_run,
-                                              float2 *pbuf, int lane)
+template <typename T, int G, bool MASKED>
+__device__ __forceinline__ void process_step(const uint16_t *__restrict__ kb,
+                                             const uint16_t *__restrict__ vb, uint32_t vmask,
+                                             const float2 (&q2)[HeadSlots<G>::N][4],
+                                             float2 (&acc)[G][4], float &m_run, float &l_run,
+                                             float2 *pbuf, int lane)
 {
     constexpr int NS = HeadSlots<G>::N;
     constexpr int SHIFT = HeadSlots<G>::SHIFT;
-    constexpr int STEPS = BS / 4;
+    constexpr int STEPS = kStepTokens / 4;
     const int c = lane & 7;
     const int r = lane >> 3;
 
-    // ---- scores of all token rows of the block
+    // ---- scores of all token rows of the step
     float z[STEPS];
 #pragma unroll
     for (int st = 0; st < STEPS; ++st) {
         const int t = st * 4 + r;
-        uint4 kw = lds128(kb + t * kHeadDim + c * 8);
-        if (LAST && t == t_new)
-            kw = lds128(knew + c * 8);
+        const uint4 kw = lds128(kb + t * kHeadDim + c * 8);
         const float2 k0 = unpack2<T>(kw.x), k1 = unpack2<T>(kw.y);
         const float2 k2 = unpack2<T>(kw.z), k3 = unpack2<T>(kw.w);
         // breadth-first over the head slots: NS independent chains between
@@ -458,7 +516,7 @@ __device__ __forceinline__ void process_block(const uint16_t *__restrict__ kb,
 #pragma unroll
         for (int m = 4 >> HeadSlots<G>::LOG; m >= 1; m >>= 1)
             zz += __shfl_xor_sync(0xffffffffu, zz, m);
-        z[st] = (LAST && t >= valid) ? -INFINITY : zz;
+        z[st] = (MASKED && !((vmask >> t) & 1u)) ? -INFINITY : zz;
     }
 
     // ---- online softmax over this lane's rows, lazily rescaled
@@ -486,7 +544,7 @@ __device__ __forceinline__ void process_block(const uint16_t *__restrict__ kb,
 #pragma unroll
     for (int st = 0; st < STEPS; ++st) {
         p[st] = fast_exp2(z[st] - m_run);
-        if (LAST && !(z[st] > -INFINITY))
+        if (MASKED && !(z[st] > -INFINITY))
             p[st] = 0.f;
         l_run += p[st];
     }
@@ -502,12 +560,10 @@ __device__ __forceinline__ void process_block(const uint16_t *__restrict__ kb,
 #pragma unroll
     for (int st = 0; st < STEPS; ++st) {
         const int t = st * 4 + r;
-        uint4 vw = lds128(vb + t * kHeadDim + c * 8);
-        if (LAST && t == t_new)
-            vw = lds128(vnew + c * 8);
+        const uint4 vw = lds128(vb + t * kHeadDim + c * 8);
         float2 v0 = unpack2<T>(vw.x), v1 = unpack2<T>(vw.y);
         float2 v2 = unpack2<T>(vw.z), v3 = unpack2<T>(vw.w);
-        if (LAST && t >= valid)
+        if (MASKED && !((vmask >> t) & 1u))
             v0 = v1 = v2 = v3 = make_float2(0.f, 0.f);
         const float4 *prow = reinterpret_cast<const float4 *>(pbuf + t * 8);
         float4 pp[(G + 1) / 2];
@@ -524,110 +580,175 @@ __device__ __forceinline__ void process_block(const uint16_t *__restrict__ kb,
             acc[j][3] = ffma2(pj, v3, acc[j][3]);
         }
     }
-    __syncwarp();  // the next block rewrites pbuf
+    __syncwarp();  // the next step rewrites pbuf
 }
 
 // ---------------------------------------------------------------------------
-// Log-sum-exp merge of the partial records of one (sequence, kv head) pair,
-// pieces c0..c1 (the first in its CTA's second slot when c0_second), written
-// to out[out_row + j*64 + d] for the G heads.  Threads tid = 0..NT-1 of the
-// calling CTA share the G*64 outputs.
+// Log-sum-exp merge of the partial records of one (sequence, kv head) pair by
+// one warp: pieces c0..c1 (the first in its worker's second slot when
+// c0_second), written to out[out_row + j*64 + d] for the G heads.
+//  1. lane k reads piece k's maxima and sums (32 pieces per round); per-head
+//     maxima and weighted sums are warp reductions;
+//  2. lane l owns outputs (head 2i + l/16, dims 4(l%16)..+3), i = 0..3, and
+//     accumulates them over the pieces with 16-byte loads, several pieces in
+//     flight, each scaled by its factor taken from the lane that read it.
 // ---------------------------------------------------------------------------
 template <typename T>
-__device__ __forceinline__ void merge_pieces(const DecodeParams &P, long long c0, long long c1,
-                                             bool c0_second, long long out_row, int G, int tid, int NT)
+__device__ __forceinline__ const float *piece_record(const DecodeParams &P, long long c0, int k, bool c0_second)
+{
+    const int wh = (k == 0 && c0_second) ? 1 : 0;
+    return P.partials + ((c0 + k) * 2 + wh) * kSlotFloats;
+}
+
+template <typename T>
+__device__ void merge_pieces(const DecodeParams &P, long long c0, long long c1, bool c0_second,
+                             long long out_row, int G, int lane)
 {
     const int npieces = (int)(c1 - c0 + 1);
-    constexpr int U = 8;  // records read per round, so their latencies overlap
-    for (int idx = tid; idx < G * kHeadDim; idx += NT) {
-        const int j = idx >> 6;
-        float M = -INFINITY;
-        for (int k0 = 0; k0 < npieces; k0 += U) {
-            float mk[U];
+    float M[kMaxGroup];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int k = k0 + u;
-                const long long cc = c0 + k;
-                const int wh = (k == 0 && c0_second) ? 1 : 0;
-                mk[u] = k < npieces ? __ldcg(P.partials + (cc * 2 + wh) * kSlotFloats + j) : -INFINITY;
-            }
+    for (int j = 0; j < kMaxGroup; ++j)
+        M[j] = -INFINITY;
+    for (int k0 = 0; k0 < npieces; k0 += 32) {
+        float m[kMaxGroup];
+        if (k0 + lane < npieces) {
+            const float4 *r = reinterpret_cast<const float4 *>(piece_record<T>(P, c0, k0 + lane, c0_second));
+            const float4 a = __ldcg(r), b = __ldcg(r + 1);
+            m[0] = a.x; m[1] = a.y; m[2] = a.z; m[3] = a.w; m[4] = b.x; m[5] = b.y; m[6] = b.z; m[7] = b.w;
+        } else {
 #pragma unroll
-            for (int u = 0; u < U; ++u)
-                M = fmaxf(M, mk[u]);
+            for (int j = 0; j < kMaxGroup; ++j)
+                m[j] = -INFINITY;
         }
-        float Ls = 0.f, o = 0.f;
-        for (int k0 = 0; k0 < npieces; k0 += U) {
-            float mk[U], lk[U], ak[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int k = k0 + u;
-                const long long cc = c0 + k;
-                const int wh = (k == 0 && c0_second) ? 1 : 0;
-                const float *sl = P.partials + (cc * 2 + wh) * kSlotFloats;
-                const bool in = k < npieces;
-                mk[u] = in ? __ldcg(sl + j) : -INFINITY;
-                lk[u] = in ? __ldcg(sl + kMaxGroup + j) : 0.f;
-                ak[u] = in ? __ldcg(sl + 2 * kMaxGroup + idx) : 0.f;
+        for (int j = 0; j < kMaxGroup; ++j) {
+            float x = m[j];
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1)
+                x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+            M[j] = fmaxf(M[j], x);
+        }
+    }
+    const int hsel = lane >> 4;  // this lane's heads are 2i + hsel
+    float Lsum[kMaxGroup];
+#pragma unroll
+    for (int j = 0; j < kMaxGroup; ++j)
+        Lsum[j] = 0.f;
+    float4 o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k0 = 0; k0 < npieces; k0 += 32) {
+        // lane k: factors of piece k0 + k
+        float f[kMaxGroup];
+        if (k0 + lane < npieces) {
+            const float4 *r = reinterpret_cast<const float4 *>(piece_record<T>(P, c0, k0 + lane, c0_second));
+            const float4 a = __ldcg(r), b = __ldcg(r + 1), c = __ldcg(r + 2), d = __ldcg(r + 3);
+            const float mm[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            const float ll[8] = {c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
+#pragma unroll
+            for (int j = 0; j < kMaxGroup; ++j) {
+                f[j] = (j < G && mm[j] > -INFINITY) ? fast_exp2(mm[j] - M[j]) : 0.f;
+                Lsum[j] += f[j] * ll[j];
             }
+        } else {
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const float f = (mk[u] > -INFINITY) ? fast_exp2(mk[u] - M) : 0.f;
-                Ls += f * lk[u];
-                o += f * ak[u];
+            for (int j = 0; j < kMaxGroup; ++j)
+                f[j] = 0.f;
+        }
+        const int nk = min(32, npieces - k0);
+#pragma unroll 4
+        for (int kk = 0; kk < nk; ++kk) {
+            const float4 *r = reinterpret_cast<const float4 *>(piece_record<T>(P, c0, k0 + kk, c0_second) +
+                                                               2 * kMaxGroup) + lane;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float fe = __shfl_sync(0xffffffffu, f[2 * i], kk);
+                const float fo = __shfl_sync(0xffffffffu, f[2 * i + 1], kk);
+                const float fk = hsel ? fo : fe;
+                const float4 a = (2 * i + hsel < G) ? __ldcg(r + 32 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                o[i].x = fmaf(fk, a.x, o[i].x);
+                o[i].y = fmaf(fk, a.y, o[i].y);
+                o[i].z = fmaf(fk, a.z, o[i].z);
+                o[i].w = fmaf(fk, a.w, o[i].w);
             }
         }
-        P.out[out_row + idx] = pack1<T>(o / Ls);
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxGroup; ++j) {
+        float x = Lsum[j];
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1)
+            x += __shfl_xor_sync(0xffffffffu, x, m);
+        Lsum[j] = x;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int h = 2 * i + hsel;
+        if (h < G) {
+            const float inv = 1.f / (hsel ? Lsum[2 * i + 1] : Lsum[2 * i]);
+            uint2 w;
+            w.x = pack2<T>(o[i].x * inv, o[i].y * inv);
+            w.y = pack2<T>(o[i].z * inv, o[i].w * inv);
+            *reinterpret_cast<uint2 *>(P.out + out_row + h * kHeadDim + 4 * (lane & 15)) = w;
+        }
+    }
+}
+
+// An arrival count whose result this warp has not looked at yet: the warp
+// that brings a pair's count to its number of pieces merges the pair.
+struct PendingMerge {
+    int prev;  // lane 0: the count before this warp's arrival
+    int pair;  // -1: nothing pending
+    int pspan;
+    long long pstart;
+};
+
+template <typename T>
+__device__ __forceinline__ void resolve_merge(const DecodeParams &P, PendingMerge &pm, long long B,
+                                              long long Gw, int G, int lane)
+{
+    if (pm.pair < 0)
+        return;
+    const int pair = pm.pair;
+    pm.pair = -1;
+    const long long c0 = cta_of(pm.pstart, B, Gw);
+    const long long c1 = cta_of(pm.pstart + pm.pspan - 1, B, Gw);
+    const int prev = __shfl_sync(0xffffffffu, pm.prev, 0);
+    if (prev == (int)(c1 - c0)) {
+        __threadfence();
+        const int s = pair / P.num_kv_heads, h = pair % P.num_kv_heads;
+        const long long out_row = ((long long)s * P.num_q_heads + (long long)h * G) * kHeadDim;
+        merge_pieces<T>(P, c0, c1, range_begin(c0, B, Gw) != pm.pstart, out_row, G, lane);
+        if (lane == 0)
+            P.counters[pair] = 0;
     }
 }
 
 // ---------------------------------------------------------------------------
-// End of a piece: merge the 4 rows x 4 warps, then write the output (whole
-// pair) or a partial record and, if this CTA completes the pair, merge every
-// piece.  Returns false if a rendezvous gave up.
+// End of a piece for one warp: combine the 4 row groups (shuffles), then
+// write the output (whole pair) or a partial record and count its arrival;
+// the result of the count is looked at later (resolve_merge), so the warp
+// does not wait for the atomic here.
 // ---------------------------------------------------------------------------
-template <typename T, int BS, int G, int S>
-__device__ bool piece_epilogue(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
-                               const PieceWalk &pc, float2 (&acc)[G][4], float m_run, float l_run,
-                               int warp, int lane, uint32_t &phase)
+template <typename T, int BS, int G>
+__device__ void piece_end(const DecodeParams &P, const PieceWalk &pc, long long worker, long long B,
+                          long long Gw, float2 (&acc)[G][4], float m_run, float l_run, int lane,
+                          PendingMerge &pm)
 {
     constexpr int SHIFT = HeadSlots<G>::SHIFT;
-    constexpr int NT = kDecodeWarps * 32;
     const int c = lane & 7;
-    const int r = lane >> 3;
-    const int tid = warp * 32 + lane;
-
-    if ((c & ((1 << SHIFT) - 1)) == 0 && (c >> SHIFT) < G) {
-        sm.mrow[warp][r][c >> SHIFT] = m_run;
-        sm.lrow[warp][r][c >> SHIFT] = l_run;
-    }
-    if (!cta_sync(P, sm, phase))
-        return false;
-    if (tid < G) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kDecodeWarps; ++w)
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr)
-                M = fmaxf(M, sm.mrow[w][rr][tid]);
-        float Ls = 0.f;
-#pragma unroll
-        for (int w = 0; w < kDecodeWarps; ++w)
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-                const float m = sm.mrow[w][rr][tid];
-                if (m > -INFINITY)
-                    Ls += sm.lrow[w][rr][tid] * fast_exp2(m - M);
-            }
-        sm.mfin[tid] = M;
-        sm.lfin[tid] = Ls;
-    }
-    if (!cta_sync(P, sm, phase))
-        return false;
+    // lane (r, c) with (c & ((1 << SHIFT) - 1)) == 0 owns (row group r, head c >> SHIFT)
+    float M = fmaxf(m_run, __shfl_xor_sync(0xffffffffu, m_run, 8));
+    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 16));
+    const float f = (m_run > -INFINITY) ? fast_exp2(m_run - M) : 0.f;
+    float Ls = f * l_run;
+    Ls += __shfl_xor_sync(0xffffffffu, Ls, 8);
+    Ls += __shfl_xor_sync(0xffffffffu, Ls, 16);
 #pragma unroll
     for (int j = 0; j < G; ++j) {
-        const float mj = sm.mrow[warp][r][j];
-        const float f = (mj > -INFINITY) ? fast_exp2(mj - sm.mfin[j]) : 0.f;
-        const float2 f2 = make_float2(f, f);
+        const float fj = __shfl_sync(0xffffffffu, f, (lane & ~7) | (j << SHIFT));
+        const float2 f2 = make_float2(fj, fj);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             float2 a = fmul2(acc[j][k], f2);
@@ -635,66 +756,58 @@ __device__ bool piece_epilogue(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
             a.y += __shfl_xor_sync(0xffffffffu, a.y, 8);
             a.x += __shfl_xor_sync(0xffffffffu, a.x, 16);
             a.y += __shfl_xor_sync(0xffffffffu, a.y, 16);
-            if (r == 0)
-                *reinterpret_cast<float2 *>(&sm.acc[warp][j][c * 8 + 2 * k]) = a;
+            acc[j][k] = a;
         }
     }
-    if (!cta_sync(P, sm, phase))
-        return false;
-
+    // every lane now holds, for dims 8c..8c+7: the merged acc of all heads;
+    // head j's max and sum are in lane (j << SHIFT)
     const int s = pc.ps, h = pc.ph;
     const long long out_row = ((long long)s * P.num_q_heads + (long long)h * G) * kHeadDim;
     if (pc.flags & kFlagWhole) {
-        for (int idx = tid; idx < G * kHeadDim; idx += NT) {
-            const int j = idx >> 6, d = idx & 63;
-            float o = 0.f;
+        if (lane < 8) {
 #pragma unroll
-            for (int w = 0; w < kDecodeWarps; ++w)
-                o += sm.acc[w][j][d];
-            P.out[out_row + idx] = pack1<T>(o / sm.lfin[j]);
+            for (int j = 0; j < G; ++j) {
+                const float inv = 1.f / __shfl_sync(0xffu, Ls, j << SHIFT);
+                uint4 w;
+                w.x = pack2<T>(acc[j][0].x * inv, acc[j][0].y * inv);
+                w.y = pack2<T>(acc[j][1].x * inv, acc[j][1].y * inv);
+                w.z = pack2<T>(acc[j][2].x * inv, acc[j][2].y * inv);
+                w.w = pack2<T>(acc[j][3].x * inv, acc[j][3].y * inv);
+                *reinterpret_cast<uint4 *>(P.out + out_row + j * kHeadDim + c * 8) = w;
+            }
         }
-        return cta_sync(P, sm, phase);
+        return;
     }
 
     // ---- partial piece: store the record, count arrivals, merge if last.
     const int which = (pc.flags & kFlagWhich1) ? 1 : 0;
-    float *slot = P.partials + ((long long)blockIdx.x * 2 + which) * kSlotFloats;
-    for (int idx = tid; idx < G * kHeadDim; idx += NT) {
-        const int j = idx >> 6, d = idx & 63;
-        float o = 0.f;
+    float *rec = P.partials + (worker * 2 + which) * kSlotFloats;
+    if (lane < 8) {
 #pragma unroll
-        for (int w = 0; w < kDecodeWarps; ++w)
-            o += sm.acc[w][j][d];
-        __stcg(slot + 2 * kMaxGroup + idx, o);
-    }
-    if (tid < G) {
-        __stcg(slot + tid, sm.mfin[tid]);
-        __stcg(slot + kMaxGroup + tid, sm.lfin[tid]);
+        for (int j = 0; j < G; ++j) {
+            float *a = rec + 2 * kMaxGroup + j * kHeadDim + c * 8;
+            __stcg(reinterpret_cast<float4 *>(a), make_float4(acc[j][0].x, acc[j][0].y, acc[j][1].x, acc[j][1].y));
+            __stcg(reinterpret_cast<float4 *>(a + 4), make_float4(acc[j][2].x, acc[j][2].y, acc[j][3].x, acc[j][3].y));
+        }
+        if ((c & ((1 << SHIFT) - 1)) == 0 && (c >> SHIFT) < G) {
+            __stcg(rec + (c >> SHIFT), M);
+            __stcg(rec + kMaxGroup + (c >> SHIFT), Ls);
+        }
     }
     __threadfence();
-    if (!cta_sync(P, sm, phase))
-        return false;
-    const long long B = sm.total, Gc = sm.g_eff;
-    const long long c0 = cta_of(pc.pstart, B, Gc);
-    const long long c1 = cta_of(pc.pstart + pc.pnb - 1, B, Gc);
+    __syncwarp();
+    resolve_merge<T>(P, pm, B, Gw, G, lane);  // at most one count is left open
     const int pair = s * P.num_kv_heads + h;
-    if (tid == 0) {
-        __threadfence();
-        sm.merge_prev = atomicAdd(P.counters + pair, 1);
-    }
-    if (!cta_sync(P, sm, phase))
-        return false;
-    if (sm.merge_prev == (int)(c1 - c0)) {
-        __threadfence();
-        merge_pieces<T>(P, c0, c1, range_begin(c0, B, Gc) != pc.pstart, out_row, G, tid, NT);
-        if (tid == 0)
-            P.counters[pair] = 0;
-    }
-    return cta_sync(P, sm, phase);
+    pm.prev = 0;
+    if (lane == 0)
+        pm.prev = atomicAdd(P.counters + pair, 1);
+    pm.pair = pair;
+    pm.pspan = pc.pspan;
+    pm.pstart = pc.pstart;
 }
 
 // ---------------------------------------------------------------------------
-// One warp: consume its blocks piece by piece, keeping its ring S blocks ahead.
+// One warp: consume its steps piece by piece, keeping its ring S steps ahead.
 // ---------------------------------------------------------------------------
 template <typename T, int BS, int G, int S>
 __device__ void decode_warp(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int warp, int lane)
@@ -702,10 +815,10 @@ __device__ void decode_warp(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int
     constexpr int NS = HeadSlots<G>::N;
     constexpr int SHIFT = HeadSlots<G>::SHIFT;
     const int c = lane & 7;
+    const long long worker = (long long)blockIdx.x * kDecodeWarps + warp;
+    const long long B = sm.total, Gw = sm.g_eff;
     float2 q2[NS][4];
     float2 acc[G][4];
-    float m_run = -INFINITY, l_run = 0.f;
-    uint32_t phase = 0;
 #pragma unroll
     for (int i = 0; i < NS; ++i)
 #pragma unroll
@@ -713,12 +826,15 @@ __device__ void decode_warp(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int
             q2[i][k] = make_float2(0.f, 0.f);
 
     Issuer<T, BS, G, S> is;
-    is.init(P, sm);
+    is.init(P, sm, warp, lane);
     while (is.issued < S && is.issue_one(P, sm, warp, lane)) {
     }
 
     PieceWalk pc;
-    walk_init(P, sm, pc);
+    walk_init(P, sm, warp, pc);
+    float2 *pbuf = &sm.p[warp][0][0];
+    PendingMerge pm;
+    pm.pair = -1;
     int consumed = 0;
     bool ok = true;
     while (ok && walk_next<BS>(P, pc)) {
@@ -727,24 +843,24 @@ __device__ void decode_warp(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 acc[j][k] = make_float2(0.f, 0.f);
-        m_run = -INFINITY;
-        l_run = 0.f;
-        for (int blk = pc.lo + warp; blk < pc.hi; blk += kDecodeWarps) {
-            while (!is.done && is.issued < consumed + S)
-                is.issue_one(P, sm, warp, lane);
+        float m_run = -INFINITY, l_run = 0.f;
+        const int nsteps = steps_of<BS>(pc);
+        const bool fused_here = P.k_new != nullptr && pc.hi == pc.pnb;
+        for (int step = 0; step < nsteps; ++step) {
             const int slot = consumed % S;
-            if (!wait_or_abort(&sm.full[warp][slot], (uint32_t)(consumed / S) & 1u, &sm.abort_flag)) {
-                set_abort(P, sm);
+            if (!mbar_wait(&sm.full[warp][slot], (uint32_t)(consumed / S) & 1u)) {
+                raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
                 ok = false;
                 break;
             }
-            if (blk == pc.lo + warp) {
-                const uint16_t *qs = sm.q[warp][slot];
+            DecodeSlot<G> &sl = sm.ring[warp][slot];
+            const uint32_t vmask = sm.vmask[warp][slot];
+            if (step == 0) {
 #pragma unroll
                 for (int i = 0; i < NS; ++i) {
                     const int head = i ^ (c >> SHIFT);
                     if (head < G) {
-                        const uint4 w = lds128(qs + head * kHeadDim + c * 8);
+                        const uint4 w = lds128(sl.q + head * kHeadDim + c * 8);
                         const float2 sc = make_float2(P.scale_log2, P.scale_log2);
                         q2[i][0] = fmul2(unpack2<T>(w.x), sc);
                         q2[i][1] = fmul2(unpack2<T>(w.y), sc);
@@ -757,30 +873,37 @@ __device__ void decode_warp(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int
                     }
                 }
             }
-            float2 *pbuf = &sm.p[warp][0][0];
-            if (blk == pc.pnb - 1) {
-                const int valid = pc.pL - blk * BS;
-                const int t_new = P.k_new != nullptr ? valid - 1 : -1;
-                process_block<T, BS, G, true>(sm.k[warp][slot], sm.v[warp][slot], valid, t_new,
-                                              sm.knew[warp][slot], sm.vnew[warp][slot], q2, acc,
-                                              m_run, l_run, pbuf, lane);
-                const long long ns = sm.new_slot[warp][slot];
-                // fused append: the lanes of the new token's row write it to its slot
-                if (P.k_new != nullptr && ns >= 0 && (t_new & 3) == (lane >> 3)) {
-                    const long long dst =
-                        (((ns / BS) * P.num_kv_heads + pc.ph) * BS + ns % BS) * kHeadDim + c * 8;
-                    *reinterpret_cast<uint4 *>(P.k_pool_w + dst) = lds128(sm.knew[warp][slot] + c * 8);
-                    *reinterpret_cast<uint4 *>(P.v_pool_w + dst) = lds128(sm.vnew[warp][slot] + c * 8);
+            const long long ns = sm.new_slot[warp][slot];
+            if (fused_here && step == nsteps - 1) {
+                // fused append: the new token's K/V replace its row in the slot
+                // and go to the pool slot the issuer checked
+                const int t_new = (pc.pL - 1) - step_token0<BS>(pc, step);
+                if (lane < 16) {
+                    const int cc = lane & 7;
+                    const uint4 val = lds128((lane < 8 ? sl.knew : sl.vnew) + cc * 8);
+                    *reinterpret_cast<uint4 *>((lane < 8 ? sl.k : sl.v) + t_new * kHeadDim + cc * 8) = val;
+                    if (ns >= 0) {
+                        const long long dst =
+                            (((ns / BS) * P.num_kv_heads + pc.ph) * BS + ns % BS) * kHeadDim + cc * 8;
+                        *reinterpret_cast<uint4 *>((lane < 8 ? P.k_pool_w : P.v_pool_w) + dst) = val;
+                    }
                 }
-            } else {
-                process_block<T, BS, G, false>(sm.k[warp][slot], sm.v[warp][slot], BS, -1, nullptr,
-                                               nullptr, q2, acc, m_run, l_run, pbuf, lane);
+                __syncwarp();
             }
+            if (vmask == 0xffffffffu)
+                process_step<T, G, false>(sl.k, sl.v, vmask, q2, acc, m_run, l_run, pbuf, lane);
+            else
+                process_step<T, G, true>(sl.k, sl.v, vmask, q2, acc, m_run, l_run, pbuf, lane);
             ++consumed;
+            if (!is.done)
+                is.issue_one(P, sm, warp, lane);
         }
-        if (ok)
-            ok = piece_epilogue<T, BS, G, S>(P, sm, pc, acc, m_run, l_run, warp, lane, phase);
+        if (!ok)
+            break;
+        piece_end<T, BS, G>(P, pc, worker, B, Gw, acc, m_run, l_run, lane, pm);
     }
+    if (ok)
+        resolve_merge<T>(P, pm, B, Gw, G, lane);
     // Never leave with copies still landing in this warp's slots.
     if (!ok && lane == 0) {
         for (int k = consumed; k < is.issued; ++k)
@@ -793,11 +916,10 @@ __device__ void decode_warp(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int
 }
 
 // ---------------------------------------------------------------------------
-// Prologue: total work, active CTAs, this CTA's range and starting pair.
-// Returns false if this CTA has no work.
+// Prologue: total work, active workers, each warp's range and starting pair.
 // ---------------------------------------------------------------------------
 template <class Smem, int BS>
-__device__ bool decode_prologue(const DecodeParams &P, Smem &sm)
+__device__ void decode_prologue(const DecodeParams &P, Smem &sm)
 {
     constexpr int NT = kDecodeWarps * 32;
     const int tid = threadIdx.x;
@@ -809,10 +931,13 @@ __device__ bool decode_prologue(const DecodeParams &P, Smem &sm)
     const bool report = blockIdx.x == 0;
 
     long long mine = 0;
-    int my_maxnb = 0;
+    int my_maxnb = 0, my_pairs = 0;
     for (int s = s_lo; s < s_hi; ++s) {
         const int L = clamped_len(P, s, BS, report);
-        mine += (long long)Hkv * nblocks_of(L, BS);
+        my_pairs += L > 0 ? Hkv : 0;
+        if (s < kLensCache)
+            sm.lens[s] = L;
+        mine += (long long)Hkv * pair_span(nblocks_of(L, BS));
         my_maxnb = max(my_maxnb, nblocks_of(L, BS));
         if (L == 0 && (s % (int)gridDim.x) == (int)blockIdx.x &&
             (P.table_row == nullptr || __ldg(P.table_row + s) >= 0)) {
@@ -829,81 +954,95 @@ __device__ bool decode_prologue(const DecodeParams &P, Smem &sm)
         if (lane >= o)
             incl += y;
     }
-    int wmax = my_maxnb;
+    int wmax = my_maxnb, wpairs = my_pairs;
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1)
+    for (int o = 16; o >= 1; o >>= 1) {
         wmax = max(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+        wpairs += __shfl_xor_sync(0xffffffffu, wpairs, o);
+    }
     if (lane == 31)
         sm.scan[warp] = incl;
-    if (lane == 0)
+    if (lane == 0) {
         sm.maxnb[warp] = wmax;
-    if (tid == 0)
-        sm.abort_flag = 0;
+        sm.npairs[warp] = wpairs;
+    }
     __syncthreads();
-    long long before = 0, total = 0;
+    long long before = 0, total = 0, live_pairs = 0;
     int maxnb = 0;
     for (int w = 0; w < kDecodeWarps; ++w) {
         if (w < warp)
             before += sm.scan[w];
         total += sm.scan[w];
+        live_pairs += sm.npairs[w];
         maxnb = max(maxnb, sm.maxnb[w]);
     }
     const long long excl = before + incl - mine;
 
     // Split policy from the real lengths and batch size: an even split over
-    // G CTAs unless no pair is longer than twice the even share, in which
-    // case whole pairs dealt round-robin need no merge at all.
+    // Gw workers (each at least min_blocks_per_cta / 4 blocks) unless no pair
+    // is longer than twice the even share, in which case whole pairs dealt
+    // round-robin need no merge at all.
+    const long long W = (long long)gridDim.x * kDecodeWarps;
     const long long minb = P.min_blocks_per_cta > 0 ? P.min_blocks_per_cta : 1;
-    long long G = (total + minb - 1) / minb;
-    if (G > (long long)gridDim.x)
-        G = gridDim.x;
-    if (G < 1)
-        G = 1;
+    long long Gw = (kDecodeWarps * total + minb - 1) / minb;
+    if (Gw > W)
+        Gw = W;
+    if (Gw > kMaxWorkers)
+        Gw = kMaxWorkers;
+    if (Gw > total)
+        Gw = total;  // no empty ranges: every worker between a pair's first and last holds a piece
+    if (Gw < 1)
+        Gw = 1;
     const long long pairs = (long long)P.num_seqs * Hkv;
     const bool whole = P.whole_sequences ||
                        (P.auto_policy && total > 0 &&
-                        (long long)maxnb <= 2 * ((total + G - 1) / G) && pairs <= (long long)gridDim.x);
-    if (whole)
-        G = gridDim.x;
-    const long long c = blockIdx.x;
-    const long long b0 = range_begin(c, total, G);
-    const long long b1 = range_begin(c + 1, total, G);
+                        (long long)maxnb <= 2 * ((total + Gw - 1) / Gw) && pairs <= W);
     if (tid == 0) {
         sm.whole = whole ? 1 : 0;
         sm.total = total;
-        sm.g_eff = (int)G;
-        sm.b0 = b0;
-        sm.b1 = b1;
-        sm.start_s = P.num_seqs;
-        sm.start_off = total;
+        sm.g_eff = (int)Gw;
         sm.plan_split = 0;
         sm.plan_maxp = 1;
     }
+    if (tid < kDecodeWarps) {
+        const long long wk = (long long)blockIdx.x * kDecodeWarps + tid;
+        sm.wb0[tid] = (!whole && wk < Gw) ? range_begin(wk, total, Gw) : 0;
+        sm.wb1[tid] = (!whole && wk < Gw) ? range_begin(wk + 1, total, Gw) : 0;
+        sm.start_s[tid] = P.num_seqs;
+        sm.start_off[tid] = total;
+    }
     __syncthreads();
-    if (!whole && c < G && mine > 0 && b0 >= excl && b0 < excl + mine) {
-        long long cum = excl;
-        for (int s = s_lo; s < s_hi; ++s) {
-            const long long w = (long long)Hkv * nblocks_of(clamped_len(P, s, BS, false), BS);
-            if (b0 < cum + w) {
-                sm.start_s = s;
-                sm.start_off = cum;
-                break;
+    if (!whole && mine > 0) {
+        for (int w = 0; w < kDecodeWarps; ++w) {
+            const long long b0 = sm.wb0[w];
+            if (sm.wb1[w] > b0 && b0 >= excl && b0 < excl + mine) {
+                long long cum = excl;
+                for (int s = s_lo; s < s_hi; ++s) {
+                    const int L = s < kLensCache ? sm.lens[s] : clamped_len(P, s, BS, false);
+                    const long long n = (long long)Hkv * pair_span(nblocks_of(L, BS));
+                    if (b0 < cum + n) {
+                        sm.start_s[w] = s;
+                        sm.start_off[w] = cum;
+                        break;
+                    }
+                    cum += n;
+                }
             }
-            cum += w;
         }
     }
     if (blockIdx.x == 0 && !whole && total > 0) {
         long long cum = excl;
         int split = 0, maxp = 1;
         for (int s = s_lo; s < s_hi; ++s) {
-            const int nb = nblocks_of(clamped_len(P, s, BS, false), BS);
+            const int nb = nblocks_of(s < kLensCache ? sm.lens[s] : clamped_len(P, s, BS, false), BS);
+            const int span = pair_span(nb);
             for (int h = 0; h < Hkv && nb > 0; ++h) {
-                const long long ps = cum + (long long)h * nb;
-                const long long np = cta_of(ps + nb - 1, total, G) - cta_of(ps, total, G) + 1;
+                const long long ps = cum + (long long)h * span;
+                const long long np = cta_of(ps + span - 1, total, Gw) - cta_of(ps, total, Gw) + 1;
                 split += np > 1;
                 maxp = max(maxp, (int)np);
             }
-            cum += (long long)Hkv * nb;
+            cum += (long long)Hkv * span;
         }
         atomicAdd(&sm.plan_split, split);
         atomicMax(&sm.plan_maxp, maxp);
@@ -911,19 +1050,18 @@ __device__ bool decode_prologue(const DecodeParams &P, Smem &sm)
     __syncthreads();
     if (blockIdx.x == 0 && tid == 0) {
         ns_decode_plan pl;
+        const long long wact = whole ? min(W, pairs) : Gw;
         pl.ctas_launched = gridDim.x;
-        pl.ctas_active = whole ? (int)min((long long)gridDim.x, pairs) : (int)G;
-        pl.total_blocks = total;
+        pl.ctas_active = (int)((wact + kDecodeWarps - 1) / kDecodeWarps);
+        pl.total_blocks = total - (long long)kPieceCost * live_pairs;  // real blocks
         pl.split_pairs = whole ? 0 : sm.plan_split;
         pl.max_pieces = whole ? 1 : sm.plan_maxp;
         pl.whole_sequences = whole ? 1 : 0;
-        for (int i = 0; i < 9; ++i)
+        pl.workers_active = (int)wact;
+        for (int i = 0; i < 8; ++i)
             pl.reserved[i] = 0;
         *P.plan = pl;
     }
-    if (whole)
-        return c < pairs;
-    return c < G && b0 < b1;
 }
 
 // CTAs per SM the register allocation is sized for; a build-time tuning knob.
@@ -941,11 +1079,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, NS_DECODE_MIN_CTAS) paged_d
         for (int w = 0; w < kDecodeWarps; ++w)
             for (int i = 0; i < S; ++i)
                 mbar_init(&sm.full[w][i], 1);
-        mbar_init(&sm.cons, kDecodeWarps * 32);
         mbar_init_fence();
     }
-    if (!decode_prologue<DecodeSmem<BS, G, S>, BS>(P, sm))
-        return;
+    decode_prologue<DecodeSmem<BS, G, S>, BS>(P, sm);
     decode_warp<T, BS, G, S>(P, sm, warp, lane);
 }
 

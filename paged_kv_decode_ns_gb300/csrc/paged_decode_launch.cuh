@@ -8,7 +8,7 @@ namespace ns {
 
 template <typename T, int BS, int G>
 struct DecodeKernel {
-    static constexpr int S = decode_stages(BS);
+    static constexpr int S = NS_DECODE_STAGES;
     static constexpr int THREADS = kDecodeWarps * 32;
     static constexpr size_t SMEM = sizeof(DecodeSmem<BS, G, S>);
     static void (*fn())(const DecodeParams) { return paged_decode_kernel<T, BS, G, S>; }

@@ -7,12 +7,11 @@
 // while a CUDA graph is being captured (allocation is not capturable), plugins
 // embedded in a host runtime that owns every device allocation, and serving
 // loops that forbid allocation after start-up.  This file gives them
-// ns_paged_attn_decode_noalloc, which runs the same kernels (same choice of
-// tensor-core or CUDA-core kernel, same grid) over a fixed-size scratch array
-// that lives in the library image itself.
+// ns_paged_attn_decode_noalloc, which runs the same kernel (and grid) over a
+// fixed-size scratch array that lives in the library image itself.
 //
 // The scratch is a file-scope __device__ array: every GPU that loads the
-// library holds it (about 4.4 MB) until the process exits.  Host code cannot
+// library holds it (about 8.7 MB) until the process exits.  Host code cannot
 // use the array's name as a device address, so the first call on each device
 // asks the runtime for that device's address (cudaGetSymbolAddress) with the
 // device current, checks the result and caches it; that first call should come
@@ -31,7 +30,7 @@ namespace {
 
 constexpr size_t kPlanBytes = 256;
 constexpr size_t kCounterBytes = (size_t)NS_NOALLOC_MAX_PAIRS * sizeof(int32_t);
-constexpr size_t kPartialBytes = (size_t)NS_MAX_CTAS * 2 * ns::kSlotFloats * sizeof(float);
+constexpr size_t kPartialBytes = (size_t)ns::kMaxWorkers * 2 * ns::kSlotFloats * sizeof(float);
 constexpr size_t kScratchBytes = kPlanBytes + kCounterBytes + kPartialBytes;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
@@ -120,5 +119,5 @@ extern "C" ns_status ns_paged_attn_decode_noalloc(const void *q, const void *k_p
     P.whole_sequences = 0;
     P.auto_policy = 1;
 
-    return ns::launch_decode(P, dtype, block_size, NS_DECODE_KERNEL_AUTO, 0, st, dev);
+    return ns::launch_decode(P, dtype, block_size, 0, st, dev);
 }

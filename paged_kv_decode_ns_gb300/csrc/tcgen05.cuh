@@ -64,22 +64,6 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr)
     return d;
 }
 
-// The same with an explicit stride between 8-row groups.  A stride of 0
-// makes every 8-row group of an operand re-read the same 1024-byte atom: an
-// 8-row matrix presented to a 128-row MMA, whose D rows then repeat with
-// period 8.
-__device__ __forceinline__ uint64_t desc_sw128_rows(uint32_t saddr, uint32_t group_stride_bytes)
-{
-    constexpr uint64_t kAtom = 1024;
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)((kAtom >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((group_stride_bytes >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-
 // Instruction descriptor, kind::f16: D fp32, A and B fp16 (fmt 0) or bf16
 // (fmt 1), A K-major, B K-major or MN-major, shape M x N (K = 16).
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int ab_fmt, bool b_mn_major)
@@ -128,15 +112,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
         : "r"(taddr));
 }
 
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8])
-{
-    uint32_t *r = reinterpret_cast<uint32_t *>(v);
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                   "=r"(r[7])
-                 : "r"(taddr));
-}
-
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
 {
     const uint32_t *r = reinterpret_cast<const uint32_t *>(v);
@@ -181,17 +156,6 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *m
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(smem_dst)),
         "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
-        : "memory");
-}
-
-// 3-D tile load with an L2 cache policy (e.g. evict-first for streamed data).
-__device__ __forceinline__ void tma_load_3d_hint(void *smem_dst, const CUtensorMap *map, int x, int y,
-                                                 int z, uint64_t *bar, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(smem_dst)),
-        "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "l"(policy)
         : "memory");
 }
 

@@ -119,14 +119,9 @@ def assert_no_device_status():
     assert bits == 0, f"device status 0x{bits:x}"
 
 
-def config(num_ctas=0, min_blocks_per_cta=0, whole_sequences=0, kernel=nb.DECODE_KERNEL_AUTO):
+def config(num_ctas=0, min_blocks_per_cta=0, whole_sequences=0):
     c = nb.DecodeConfig()
     c.num_ctas = num_ctas
     c.min_blocks_per_cta = min_blocks_per_cta
     c.whole_sequences = whole_sequences
-    c.kernel = kernel
     return c
-
-
-# The two decode kernels: tensor cores (block sizes 16, 32) and CUDA cores (all).
-KERNELS = {"tc": nb.DECODE_KERNEL_TENSOR_CORE, "cuda": nb.DECODE_KERNEL_CUDA_CORE}

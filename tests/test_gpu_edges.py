@@ -33,20 +33,7 @@ def test_block_sizes_and_ragged_tails(bs, dtype, orc):
     for fused in (False, True):
         d, out, ref, kp, vp = run_decode(st, orc, fused=fused)
         compare(out, ref, dtype, f"bs={bs} fused={fused}")
-    if bs in (16, 32):
-        for k in ("tc", "cuda"):
-            d, out, ref, kp, vp = run_decode(st, orc, config(kernel=_gpu.KERNELS[k]))
-            compare(out, ref, dtype, f"bs={bs} {k}")
     _gpu.assert_no_device_status()
-
-
-@pytest.mark.parametrize("bs", [4, 8])
-def test_tensor_core_kernel_rejects_small_blocks(bs):
-    st = make([5, 9], bs=bs, seed=bs)
-    d = DevStep(st)
-    with pytest.raises(nb.NsError) as e:
-        d.decode(config(kernel=_gpu.KERNELS["tc"]))
-    assert e.value.status == -2
 
 
 @pytest.mark.parametrize("hq,hkv", [(1, 1), (2, 1), (3, 1), (4, 2), (10, 2), (12, 2), (14, 2),
@@ -57,15 +44,12 @@ def test_group_sizes(hq, hkv, orc):
     compare(out, ref, st.dtype, f"Hq={hq} Hkv={hkv}")
     d, out, ref, *_ = run_decode(st, orc, fused=True)
     compare(out, ref, st.dtype, f"Hq={hq} Hkv={hkv} fused")
-    d, out, ref, *_ = run_decode(st, orc, config(kernel=_gpu.KERNELS["cuda"]))
-    compare(out, ref, st.dtype, f"Hq={hq} Hkv={hkv} cuda-core")
     _gpu.assert_no_device_status()
 
 
 def test_single_sequence_at_table_capacity(orc):
     st = make([8192], dtype=wl.BF16, seed=3, max_blocks_per_seq=512)
-    for cfg in (None, config(num_ctas=1), config(min_blocks_per_cta=1),
-                config(num_ctas=1, kernel=_gpu.KERNELS["cuda"])):
+    for cfg in (None, config(num_ctas=1), config(min_blocks_per_cta=1)):
         d, out, ref, *_ = run_decode(st, orc, cfg)
         compare(out, ref, st.dtype, "L=8192")
     _gpu.assert_no_device_status()
