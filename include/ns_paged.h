@@ -164,9 +164,9 @@ ns_status ns_paged_attn_decode(const void *q, const void *k_pool, const void *v_
  * Policy overrides for the split-KV decode (tests and measurements).
  *   num_ctas            0 = auto (resident CTAs on this GPU); else the grid size
  *                       (1 .. NS_MAX_CTAS)
- *   min_blocks_per_cta  0 = auto; fewer workers (warps, 4 per CTA) are used
- *                       when the total work would give each less than a
- *                       quarter of this many KV blocks
+ *   min_blocks_per_cta  0 = auto; fewer workers (warps, 8 per CTA) are used
+ *                       when the total work would give each less than an
+ *                       eighth of this many KV blocks
  *   whole_sequences     nonzero = never split a (sequence, kv head): worker w
  *                       of W takes pairs w, w+W, w+2W, ... (no merge step)
  */
@@ -215,7 +215,7 @@ ns_status ns_kv_append_paged_attn_decode(const void *q, const void *k_new, const
 /*
  * Plan record the decode kernels leave at the start of the workspace (CTA 0
  * writes it during every call).  It shows which split the device chose.  The
- * unit of work is a worker: one warp of a CTA (4 workers per CTA).
+ * unit of work is a worker: one warp of a CTA (8 workers per CTA).
  *   ctas_launched   grid size
  *   ctas_active     CTAs with at least one worker that received work
  *   total_blocks    KV blocks over all (sequence, kv head) pairs

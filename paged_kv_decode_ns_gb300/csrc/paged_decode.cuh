@@ -49,16 +49,29 @@ namespace ns {
 // log2 units), L[8] (sum of 2^(z-M)), acc[8][64] (unnormalised output).
 constexpr int kSlotFloats = 2 * kMaxGroup + kMaxGroup * kHeadDim;
 constexpr float kRescaleSlack = 8.0f;
-constexpr int kDecodeWarps = 4;        // workers per CTA
+// Workers (warps) per CTA and CTAs per SM, build-time knobs.  One CTA of 8
+// warps per SM: with two CTAs of 4, the warps of one CTA got the larger share
+// of issue slots and finished ~12 us before the other CTA's (measured),
+// which then ran with too few warps to hide latency.
+#ifndef NS_DECODE_WARPS
+#define NS_DECODE_WARPS 8
+#endif
+#ifndef NS_DECODE_MIN_CTAS
+#define NS_DECODE_MIN_CTAS (8 / NS_DECODE_WARPS)
+#endif
+constexpr int kDecodeWarps = NS_DECODE_WARPS;
 constexpr int kStepTokens = 32;        // tokens per ring slot (one per lane for the vote)
 constexpr int kMaxWorkers = 2048;      // split workers (each has two record slots)
-constexpr int kDefaultMinBlocksPerCta = 32;
+constexpr int kDefaultMinBlocksPerCta = 8 * kDecodeWarps;  // 8 blocks per worker
 constexpr int kLensCache = 2048;       // context lengths kept in shared memory
 // Split cost of a (sequence, kv head) pair beyond its blocks: the even split
 // counts kPieceCost virtual blocks at the start of every pair, so a worker
 // whose range crosses many pair boundaries (a piece end, a partial last
 // step, an arrival count and perhaps a merge each) gets fewer real blocks.
-constexpr int kPieceCost = 4;
+#ifndef NS_DECODE_PIECE_COST
+#define NS_DECODE_PIECE_COST 4
+#endif
+constexpr int kPieceCost = NS_DECODE_PIECE_COST;
 
 // Length of a pair in the split's coordinates (0 for a pair with no block).
 __host__ __device__ __forceinline__ int pair_span(int nb) { return nb > 0 ? nb + kPieceCost : 0; }
@@ -138,10 +151,20 @@ struct DecodeSmem {
     long long total;
     int g_eff;  // split workers
     int whole;  // 1: whole (sequence, kv head) pairs dealt round-robin, no split
+    int wmajor;  // 1: workers numbered warp-major (see worker_id)
     int plan_split, plan_maxp;
 };
 
 __device__ __forceinline__ int nblocks_of(int L, int BS) { return (L + BS - 1) / BS; }
+
+// Worker number of warp `warp` of this CTA.  When only some workers have
+// work (wmajor), warp-major, so that they are spread over every SM before any
+// SM gets two; when all have work, CTA-major, so that the warps of a CTA walk
+// neighbouring runs of the same sequences.
+__device__ __forceinline__ long long worker_id(int warp, bool wmajor)
+{
+    return wmajor ? (long long)warp * gridDim.x + blockIdx.x : (long long)blockIdx.x * kDecodeWarps + warp;
+}
 
 // Context length of row s, clamped to what the table can address.
 __device__ __forceinline__ int clamped_len(const DecodeParams &P, int s, int BS, bool report)
@@ -190,7 +213,7 @@ __device__ __forceinline__ void walk_init(const DecodeParams &P, const Smem &sm,
     w.lens = sm.lens;
     w.whole = sm.whole != 0;
     if (w.whole) {
-        w.pos = (long long)blockIdx.x * kDecodeWarps + warp;
+        w.pos = worker_id(warp, sm.wmajor != 0);
         w.stride = (long long)gridDim.x * kDecodeWarps;
         w.end = (long long)P.num_seqs * P.num_kv_heads;
     } else {
@@ -815,7 +838,7 @@ __device__ void decode_warp(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int
     constexpr int NS = HeadSlots<G>::N;
     constexpr int SHIFT = HeadSlots<G>::SHIFT;
     const int c = lane & 7;
-    const long long worker = (long long)blockIdx.x * kDecodeWarps + warp;
+    const long long worker = worker_id(warp, sm.wmajor != 0);
     const long long B = sm.total, Gw = sm.g_eff;
     float2 q2[NS][4];
     float2 acc[G][4];
@@ -997,7 +1020,13 @@ __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
     const bool whole = P.whole_sequences ||
                        (P.auto_policy && total > 0 &&
                         (long long)maxnb <= 2 * ((total + Gw - 1) / Gw) && pairs <= W);
+#ifndef NS_DECODE_WMAJOR_ALWAYS
+    const bool wmajor = whole ? pairs < W : Gw < W;
+#else
+    const bool wmajor = true;
+#endif
     if (tid == 0) {
+        sm.wmajor = wmajor ? 1 : 0;
         sm.whole = whole ? 1 : 0;
         sm.total = total;
         sm.g_eff = (int)Gw;
@@ -1005,7 +1034,7 @@ __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
         sm.plan_maxp = 1;
     }
     if (tid < kDecodeWarps) {
-        const long long wk = (long long)blockIdx.x * kDecodeWarps + tid;
+        const long long wk = worker_id(tid, wmajor);
         sm.wb0[tid] = (!whole && wk < Gw) ? range_begin(wk, total, Gw) : 0;
         sm.wb1[tid] = (!whole && wk < Gw) ? range_begin(wk + 1, total, Gw) : 0;
         sm.start_s[tid] = P.num_seqs;
@@ -1052,7 +1081,8 @@ __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
         ns_decode_plan pl;
         const long long wact = whole ? min(W, pairs) : Gw;
         pl.ctas_launched = gridDim.x;
-        pl.ctas_active = (int)((wact + kDecodeWarps - 1) / kDecodeWarps);
+        pl.ctas_active = (int)(wmajor ? min((long long)gridDim.x, wact)
+                                      : (wact + kDecodeWarps - 1) / kDecodeWarps);
         pl.total_blocks = total - (long long)kPieceCost * live_pairs;  // real blocks
         pl.split_pairs = whole ? 0 : sm.plan_split;
         pl.max_pieces = whole ? 1 : sm.plan_maxp;
@@ -1064,10 +1094,6 @@ __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
     }
 }
 
-// CTAs per SM the register allocation is sized for; a build-time tuning knob.
-#ifndef NS_DECODE_MIN_CTAS
-#define NS_DECODE_MIN_CTAS 2
-#endif
 
 template <typename T, int BS, int G, int S>
 __global__ void __launch_bounds__(kDecodeWarps * 32, NS_DECODE_MIN_CTAS) paged_decode_kernel(const DecodeParams P)
