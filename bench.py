@@ -55,7 +55,16 @@ KERNEL_SOURCES = {
                           "paged_kv_decode_ns_gb300/csrc/ns_common.cuh",
                           "paged_kv_decode_ns_gb300/csrc/tcgen05.cuh", "include/ns_paged.h"],
 }
-PROFILED_TRAFFIC = {}
+PROFILED_TRAFFIC = {
+    # profiles/paged_decode_b256_bf16.md: 240.11 MB read + 4.09 MB written
+    ("decode_b256", "paged_decode_kernel"): {
+        "sources_sha256": "c1e08ca6fb017d0477b2742f81698f2a54222a758797d63b3822d3357b8db12c",
+        "bytes": 244204288},
+    # profiles/tc_prefill_mixed_f16.md: 4.75 MB read, 0 written
+    ("mixed_chunked_prefill", "tc_prefill_kernel"): {
+        "sources_sha256": "0c142170defeda595e23ea141dfcfb47710039ea3f721412a0b258bf4d2e9f41",
+        "bytes": 4748288},
+}
 
 
 def kernel_sources_sha(kernel: str) -> str:
@@ -454,10 +463,14 @@ def bench_ours(args):
         cores = host_cores()
         max_seqs = None if step.decode else 16
         secs, kvb, n, thr = run_cpu_oracle(st, cores, max_seqs=max_seqs)
+        # one thread on a bounded sample (the first 32 sequences)
+        secs1, kvb1, n1, _ = run_cpu_oracle(st, 1, max_seqs=32 if max_seqs is None else min(32, max_seqs))
         cpu = {"value": kvb / secs / 1e9, "unit": "GB/s", "cores": thr, "kind": "oracle",
                "sample": f"{'all' if n == st.num_seqs else 'first'} {n} sequences of the "
                          f"batch (decode rows), attention only, one pass, {secs:.2f} s "
-                         f"(fp64 C oracle, OpenMP over (row, head))"}
+                         f"(fp64 C oracle, OpenMP over (row, head))",
+               "value_1thread": kvb1 / secs1 / 1e9,
+               "sample_1thread": f"first {n1} sequences, one thread, {secs1:.2f} s"}
     return {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
