@@ -63,7 +63,7 @@ constexpr int kDecodeWarps = NS_DECODE_WARPS;
 constexpr int kStepTokens = 32;        // tokens per ring slot (one per lane for the vote)
 constexpr int kMaxWorkers = 2048;      // split workers (each has two record slots)
 constexpr int kDefaultMinBlocksPerCta = 8 * kDecodeWarps;  // 8 blocks per worker
-constexpr int kLensCache = 2048;       // context lengths kept in shared memory
+constexpr int kLensCache = 512;        // context lengths kept in shared memory
 // Split cost of a (sequence, kv head) pair beyond its blocks: the even split
 // counts kPieceCost virtual blocks at the start of every pair, so a worker
 // whose range crosses many pair boundaries (a piece end, a partial last
@@ -106,9 +106,52 @@ struct DecodeParams {
     int auto_policy;  // no override given: the device may deal whole pairs instead of splitting
 };
 
+// Thread block: two consumer warpgroups (one warp per worker) and one
+// producer warpgroup of which one warp works.
+constexpr int kDecodeThreads = (kDecodeWarps + 4) * 32;
+constexpr int kLaunchRegs = 65536 / kDecodeThreads / 8 * 8;  // 168
+// Producer warps (of the producer warpgroup's four); each serves
+// kDecodeWarps / NS_DECODE_PRODUCER_WARPS consumers, one lane each.
+#ifndef NS_DECODE_PRODUCER_WARPS
+#define NS_DECODE_PRODUCER_WARPS 4
+#endif
+constexpr int kProducerWarps = NS_DECODE_PRODUCER_WARPS;
+#ifndef NS_DECODE_IDLE_NS
+#define NS_DECODE_IDLE_NS 32  // producer back-off when no slot is free
+#endif
+constexpr int kServedPerProducer = kDecodeWarps / kProducerWarps;
+static_assert(kProducerWarps >= 1 && kProducerWarps <= 4 && kDecodeWarps % kProducerWarps == 0, "producer warps");
+#ifndef NS_DECODE_PRODUCER_REGS
+#define NS_DECODE_PRODUCER_REGS 88
+#endif
+constexpr int kProducerRegs = NS_DECODE_PRODUCER_REGS;
+constexpr int kConsumerRegs = (kLaunchRegs * kDecodeThreads - kProducerRegs * 128) / (kDecodeWarps * 32) / 8 * 8;
+static_assert(kDecodeWarps == 8, "two consumer warpgroups");
+static_assert(kConsumerRegs * kDecodeWarps * 32 + kProducerRegs * 128 <= kLaunchRegs * kDecodeThreads,
+              "register shares exceed the launch allocation");
+
 enum : int {
     kFlagWhole = 4,    // the piece is the whole (sequence, kv head)
     kFlagWhich1 = 16,  // partial piece stored in the worker's second record slot
+    kFlagNewTok = 64,  // fused append: this step holds the new token
+};
+
+// What the producer tells a consumer about one ring slot.
+struct SlotMeta {
+    int ps, ph, pL, flags;      // the pair; piece flags (kFlag*)
+    int pspan, step, nsteps;    // nsteps: steps of the piece; 0 = a piece with no key
+                                // (record only); -1 = no more work
+    int t_new;                  // fused append: the new token's row in the step
+    long long pstart;           // the pair's place in the split
+    long long new_slot;         // fused append: checked pool slot, or -1
+    uint32_t vmask;             // bit t: token t of the step is a key
+    int pad[3];
+};
+
+// The fields of a piece that its end needs.
+struct PieceRef {
+    int ps, ph, flags, pspan;
+    long long pstart;
 };
 
 // Reduce-scatter slots: the G heads of a group padded to a power of two.
@@ -119,29 +162,24 @@ struct HeadSlots {
     static constexpr int SHIFT = 3 - LOG;  // lane c holds head c >> SHIFT
 };
 
-// Ring slots per warp; a build-time tuning knob.
-#ifndef NS_DECODE_STAGES
-#define NS_DECODE_STAGES 2
-#endif
 
-// One ring slot: K and V rows of one 16-token step, and the extras that ride
-// with it (q rows on a piece's first step, the new token's K/V when fused).
+// One ring slot: K and V rows of one 32-token step and the q rows that ride
+// with a piece's first step.  With a fused append the new token's K/V are
+// copied straight into their row of the step.
 template <int G>
 struct DecodeSlot {
     uint16_t k[kStepTokens * kHeadDim];
     uint16_t v[kStepTokens * kHeadDim];
     uint16_t q[G * kHeadDim];
-    uint16_t knew[kHeadDim];
-    uint16_t vnew[kHeadDim];
 };
 
 template <int BS, int G, int S>
 struct DecodeSmem {
     DecodeSlot<G> ring[kDecodeWarps][S];
-    float2 p[kDecodeWarps][kStepTokens][8];  // (p, p) per [token][head]
-    uint64_t full[kDecodeWarps][S];
-    uint32_t vmask[kDecodeWarps][S];         // bit t: token t of the slot is a key
-    long long new_slot[kDecodeWarps][S];     // fused append: pool slot of the step's new token, or -1
+    float p[kDecodeWarps][kStepTokens][8];   // p per [token][head]
+    SlotMeta meta[kDecodeWarps][S];
+    uint64_t full[kDecodeWarps][S];          // producer -> consumer: the step has landed
+    uint64_t empty[kDecodeWarps][S];         // consumer -> producer: the slot may be refilled
     long long scan[32];
     int maxnb[32];
     int npairs[32];
@@ -151,9 +189,23 @@ struct DecodeSmem {
     long long total;
     int g_eff;  // split workers
     int whole;  // 1: whole (sequence, kv head) pairs dealt round-robin, no split
+    int abort_flag;  // set by a warp that gave up waiting
     int wmajor;  // 1: workers numbered warp-major (see worker_id)
     int plan_split, plan_maxp;
 };
+
+// Ring slots per warp: three where they fit in a CTA's shared memory (two
+// steps stream while one is computed), else two.
+constexpr size_t kMaxDynSmem = 227 * 1024;
+template <int BS, int G>
+constexpr int decode_stages()
+{
+#ifdef NS_DECODE_STAGES
+    return NS_DECODE_STAGES;
+#else
+    return sizeof(DecodeSmem<BS, G, 3>) <= kMaxDynSmem ? 3 : 2;
+#endif
+}
 
 __device__ __forceinline__ int nblocks_of(int L, int BS) { return (L + BS - 1) / BS; }
 
@@ -321,169 +373,6 @@ __device__ __forceinline__ int step_token0(const PieceWalk &w, int i)
 }
 
 // ---------------------------------------------------------------------------
-// Issue side of a warp's ring: walks the same pieces as the consumer and
-// issues the TMA copies of each 32-token step, up to S steps ahead.
-// ---------------------------------------------------------------------------
-template <typename T, int BS, int G, int S>
-struct Issuer {
-    static constexpr int KB = kStepTokens / BS;  // blocks per step
-    PieceWalk w;       // the piece being issued
-    PieceWalk nw;      // the next piece (looked up one piece ahead)
-    bool nvalid;
-    int step, nsteps;
-    bool has;
-    bool done;
-    int issued;
-    long long trow, ntrow;
-    long long slot_v, nslot_v;  // fused append: slot_mapping of the piece's sequence
-    int tab_first;     // first block of the cached table chunk
-    int tab_val;       // lane l: table entry of block tab_first + l (-1 past the piece)
-    int nxt_val;       // lane l: table entry of block tab_first + 32 + l
-    int ntab;          // lane l: table entry of block nw.lo + l
-    uint64_t policy;
-
-    // Raw table entry (checked where it is used, so that the load does not
-    // stall the warp here); -1 past the piece.
-    __device__ int table_raw(const DecodeParams &P, long long row, int blk, int hi) const
-    {
-        return blk < hi ? __ldg(P.block_tables + row * P.max_blocks_per_seq + blk) : -1;
-    }
-
-    __device__ void look_ahead(const DecodeParams &P, int lane)
-    {
-        nvalid = walk_next<BS>(P, nw);
-        if (nvalid) {
-            ntrow = P.table_row != nullptr ? __ldg(P.table_row + nw.ps) : nw.ps;
-            ntab = table_raw(P, ntrow, nw.lo + lane, nw.hi);
-            nslot_v = (P.k_new != nullptr && nw.hi == nw.pnb) ? __ldg(P.slot_mapping + nw.ps) : -1;
-        }
-    }
-
-    template <class Smem>
-    __device__ void init(const DecodeParams &P, const Smem &sm, int warp, int lane)
-    {
-        walk_init(P, sm, warp, nw);
-        look_ahead(P, lane);
-        has = false;
-        done = false;
-        issued = 0;
-        step = nsteps = 0;
-        policy = l2_evict_first_policy();
-    }
-
-    // Move to the looked-up piece and look up the one after it.
-    __device__ bool next_piece(const DecodeParams &P, int lane)
-    {
-        if (!nvalid)
-            return false;
-        w = nw;
-        trow = ntrow;
-        slot_v = nslot_v;
-        tab_first = w.lo;
-        tab_val = ntab;
-        nxt_val = table_raw(P, trow, w.lo + 32 + lane, w.hi);
-        step = 0;
-        nsteps = steps_of<BS>(w);
-        look_ahead(P, lane);
-        return true;
-    }
-
-    // Issue this warp's next step; false when the walk is exhausted.
-    __device__ bool issue_one(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int warp, int lane)
-    {
-        while (!has || step >= nsteps) {
-            if (!next_piece(P, lane)) {
-                done = true;
-                return false;
-            }
-            has = true;
-        }
-        // blocks of this step: KB whole blocks from `first`
-        const int first = w.lo + step * KB;
-        if (first >= tab_first + 32) {
-            tab_first += 32;
-            tab_val = nxt_val;
-            nxt_val = table_raw(P, trow, tab_first + 32 + lane, w.hi);
-        }
-        int phys = __shfl_sync(0xffffffffu, tab_val, (first - tab_first + (lane < KB ? lane : 0)) & 31);
-        const bool mine = lane < KB && first + lane < w.hi;
-        if (mine && (phys < 0 || (long long)phys >= P.num_blocks)) {
-            raise_status(P.status, NS_DEV_BAD_BLOCK_ID);
-            phys = -1;
-        }
-        const unsigned loaded = __ballot_sync(0xffffffffu, mine && phys >= 0);
-        const int tok0 = step_token0<BS>(w, step);
-        const int nval = min(kStepTokens, piece_end_token<BS>(w) - tok0);  // >= 1
-        // valid keys: the first nval tokens whose block was loaded
-        uint32_t vm = nval >= 32 ? 0xffffffffu : ((1u << nval) - 1u);
-        if (KB > 1) {
-            uint32_t bm = 0;
-#pragma unroll
-            for (int u = 0; u < KB; ++u)
-                if ((loaded >> u) & 1u)
-                    bm |= (BS >= 32 ? 0xffffffffu : ((1u << BS) - 1u)) << (u * BS);
-            vm &= bm;
-        } else if (!(loaded & 1u)) {
-            vm = 0;
-        }
-        const bool first_step = step == 0;
-        const bool new_tok = P.k_new != nullptr && w.hi == w.pnb && step == nsteps - 1;
-        long long ns = -1;
-        if (new_tok) {
-            // the pool slot of position L-1 must be the one slot_mapping names
-            const int u_last = (w.pL - 1) / BS - first;
-            const int phys_last = __shfl_sync(0xffffffffu, phys, u_last & 31);
-            const long long want = (long long)phys_last * BS + (w.pL - 1) % BS;
-            ns = slot_v;
-            if (lane == 0 && (ns != want || phys_last < 0))
-                raise_status(P.status, NS_DEV_FUSED_SLOT);
-            if (ns >= P.num_blocks * BS) {
-                if (lane == 0)
-                    raise_status(P.status, NS_DEV_BAD_SLOT);
-                ns = -1;
-            }
-        }
-        const uint32_t bytes = (uint32_t)__popc(loaded) * 2u * BS * kRowBytes +
-                               (first_step ? (uint32_t)G * kRowBytes : 0u) + (new_tok ? 2u * kRowBytes : 0u);
-        const int slot = issued % S;
-        DecodeSlot<G> &sl = sm.ring[warp][slot];
-        uint64_t *bar = &sm.full[warp][slot];
-        // every lane is done with this slot's previous contents, and its
-        // generic-proxy accesses are ordered before the async-proxy refill
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            sm.vmask[warp][slot] = vm;
-            sm.new_slot[warp][slot] = new_tok ? ns : -1;
-            if (bytes == 0)
-                mbar_arrive(bar);
-            else
-                mbar_arrive_expect_tx(bar, bytes);
-        }
-        __syncwarp();
-        if (mine && phys >= 0) {
-            const long long off = ((long long)phys * P.num_kv_heads + w.ph) * BS * kHeadDim;
-            bulk_load(sl.k + lane * BS * kHeadDim, P.k_pool + off, BS * kRowBytes, bar, policy);
-            bulk_load(sl.v + lane * BS * kHeadDim, P.v_pool + off, BS * kRowBytes, bar, policy);
-        }
-        if (lane == 0) {
-            if (first_step) {
-                const long long qoff = ((long long)w.ps * P.num_q_heads + (long long)w.ph * G) * kHeadDim;
-                bulk_load(sl.q, P.q + qoff, G * kRowBytes, bar);
-            }
-            if (new_tok) {
-                const long long noff = ((long long)w.ps * P.num_kv_heads + w.ph) * kHeadDim;
-                bulk_load(sl.knew, P.k_new + noff, kRowBytes, bar);
-                bulk_load(sl.vnew, P.v_new + noff, kRowBytes, bar);
-            }
-        }
-        ++issued;
-        ++step;
-        return true;
-    }
-};
-
-// ---------------------------------------------------------------------------
 // One 32-token step for one warp.  MASKED: some tokens of the step are not
 // keys (bit t of vmask clear): their scores are -inf and their values 0.
 // ---------------------------------------------------------------------------
@@ -492,7 +381,7 @@ __device__ __forceinline__ void process_step(const uint16_t *__restrict__ kb,
                                              const uint16_t *__restrict__ vb, uint32_t vmask,
                                              const float2 (&q2)[HeadSlots<G>::N][4],
                                              float2 (&acc)[G][4], float &m_run, float &l_run,
-                                             float2 *pbuf, int lane)
+                                             float *pbuf, int lane)
 {
     constexpr int NS = HeadSlots<G>::N;
     constexpr int SHIFT = HeadSlots<G>::SHIFT;
@@ -576,7 +465,7 @@ __device__ __forceinline__ void process_step(const uint16_t *__restrict__ kb,
     // write the same value; a padding head lands in an unused slot)
 #pragma unroll
     for (int st = 0; st < STEPS; ++st)
-        pbuf[(st * 4 + r) * 8 + (c >> SHIFT)] = make_float2(p[st], p[st]);
+        pbuf[(st * 4 + r) * 8 + (c >> SHIFT)] = p[st];
     __syncwarp();
 
     // ---- values
@@ -589,14 +478,15 @@ __device__ __forceinline__ void process_step(const uint16_t *__restrict__ kb,
         if (MASKED && !((vmask >> t) & 1u))
             v0 = v1 = v2 = v3 = make_float2(0.f, 0.f);
         const float4 *prow = reinterpret_cast<const float4 *>(pbuf + t * 8);
-        float4 pp[(G + 1) / 2];
+        float4 pp[(G + 3) / 4];
 #pragma unroll
-        for (int i = 0; i < (G + 1) / 2; ++i)
+        for (int i = 0; i < (G + 3) / 4; ++i)
             pp[i] = prow[i];
 #pragma unroll
         for (int j = 0; j < G; ++j) {
-            const float2 pj = (j & 1) ? make_float2(pp[j >> 1].z, pp[j >> 1].w)
-                                      : make_float2(pp[j >> 1].x, pp[j >> 1].y);
+            const float4 &q4 = pp[j >> 2];
+            const float pv = (j & 3) == 0 ? q4.x : (j & 3) == 1 ? q4.y : (j & 3) == 2 ? q4.z : q4.w;
+            const float2 pj = make_float2(pv, pv);
             acc[j][0] = ffma2(pj, v0, acc[j][0]);
             acc[j][1] = ffma2(pj, v1, acc[j][1]);
             acc[j][2] = ffma2(pj, v2, acc[j][2]);
@@ -755,7 +645,7 @@ __device__ __forceinline__ void resolve_merge(const DecodeParams &P, PendingMerg
 // does not wait for the atomic here.
 // ---------------------------------------------------------------------------
 template <typename T, int BS, int G>
-__device__ void piece_end(const DecodeParams &P, const PieceWalk &pc, long long worker, long long B,
+__device__ void piece_end(const DecodeParams &P, const PieceRef &pc, long long worker, long long B,
                           long long Gw, float2 (&acc)[G][4], float m_run, float l_run, int lane,
                           PendingMerge &pm)
 {
@@ -829,11 +719,235 @@ __device__ void piece_end(const DecodeParams &P, const PieceWalk &pc, long long 
     pm.pstart = pc.pstart;
 }
 
+// Table row, first-step table entries and slot_mapping entry of a piece.
+template <int BS, int KB>
+__device__ __forceinline__ void piece_prefetch(const DecodeParams &P, const PieceWalk &pc, long long &trow,
+                                               int (&phys)[KB], long long &slot)
+{
+    trow = P.table_row != nullptr ? __ldg(P.table_row + pc.ps) : pc.ps;
+    slot = (P.k_new != nullptr && pc.hi == pc.pnb) ? __ldg(P.slot_mapping + pc.ps) : -1;
+#pragma unroll
+    for (int u = 0; u < KB; ++u)
+        phys[u] = pc.lo + u < pc.hi ? __ldg(P.block_tables + trow * P.max_blocks_per_seq + pc.lo + u) : -1;
+}
+
 // ---------------------------------------------------------------------------
-// One warp: consume its steps piece by piece, keeping its ring S steps ahead.
+// Producer warps: lane i of producer warp p serves consumer warp
+// w = p * kServedPerProducer + i.  It walks w's pieces one piece ahead,
+// reads the block-table entries of each step one step ahead, and issues the
+// TMA copies of the next step into w's ring as soon as w frees a slot, with
+// the step's description (piece, valid keys, fused slot) in the slot's
+// SlotMeta.  Consumers then hold no walk or issue state: their registers go
+// to the scores and accumulators.
 // ---------------------------------------------------------------------------
 template <typename T, int BS, int G, int S>
-__device__ void decode_warp(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int warp, int lane)
+__device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int pwarp, int lane)
+{
+    constexpr int KB = kStepTokens / BS;  // blocks per step
+    const int w = pwarp * kServedPerProducer + (lane < kServedPerProducer ? lane : 0);
+    const uint64_t pol = l2_evict_first_policy();
+    bool done = lane >= kServedPerProducer;
+    // `walk` runs one piece ahead of `cur`: the table entries of the next
+    // piece's first step (and its slot_mapping entry) load while the current
+    // piece streams.
+    PieceWalk walk;
+    walk_init(P, sm, w, walk);
+    long long a_trow = 0, a_slot = -1;
+    int aphys[KB];
+    bool ahead = !done && walk_next<BS>(P, walk);
+    if (ahead)
+        piece_prefetch<BS, KB>(P, walk, a_trow, aphys, a_slot);
+    PieceWalk cur;
+    bool has = false;
+    int step = 0, nsteps = 0, issued = 0;
+    long long trow = 0, slot_v = -1;
+    int nphys[KB];  // raw table entries of the next step
+    bool ok = true;
+    unsigned long long idle_since = 0;
+    bool idle = false;
+    // The lanes go round in step: each round, every lane whose next slot is
+    // free fills it; a round where no lane could sleeps briefly.
+    while (__any_sync(0xffffffffu, !done)) {
+        const int slot = issued % S;
+        const bool ready = !done && mbar_test(&sm.empty[w][slot], ((uint32_t)(issued / S) & 1u) ^ 1u);
+        if (__ballot_sync(0xffffffffu, ready) == 0) {
+            const bool abort = *reinterpret_cast<volatile int *>(&sm.abort_flag) != 0;
+            const unsigned long long now = global_timer_ns();
+            if (!idle) {
+                idle = true;
+                idle_since = now;
+            }
+            if (__any_sync(0xffffffffu, abort || now - idle_since > kWaitLimitNs)) {
+                ok = false;
+                break;
+            }
+            __nanosleep(NS_DECODE_IDLE_NS);
+            continue;
+        }
+        idle = false;
+        if (!ready)
+            continue;
+        SlotMeta &mt = sm.meta[w][slot];
+        DecodeSlot<G> &sl = sm.ring[w][slot];
+        uint64_t *bar = &sm.full[w][slot];
+        if (!has || step >= nsteps) {
+            if (!ahead) {
+                mt.nsteps = -1;  // no more work for this consumer
+                mbar_arrive(bar);
+                ++issued;
+                done = true;
+                continue;
+            }
+            cur = walk;
+            has = true;
+            step = 0;
+            nsteps = steps_of<BS>(cur);
+            trow = a_trow;
+            slot_v = a_slot;
+#pragma unroll
+            for (int u = 0; u < KB; ++u)
+                nphys[u] = aphys[u];
+            ahead = walk_next<BS>(P, walk);
+            if (ahead)
+                piece_prefetch<BS, KB>(P, walk, a_trow, aphys, a_slot);
+            mt.ps = cur.ps;
+            mt.ph = cur.ph;
+            mt.pL = cur.pL;
+            mt.pspan = cur.pspan;
+            mt.pstart = cur.pstart;
+            if (nsteps == 0) {
+                // only virtual blocks of the pair: the consumer writes an empty record
+                mt.flags = cur.flags;
+                mt.step = 0;
+                mt.nsteps = 0;
+                mbar_arrive(bar);
+                ++issued;
+                has = false;
+                continue;
+            }
+        } else {
+            mt.ps = cur.ps;
+            mt.ph = cur.ph;
+            mt.pL = cur.pL;
+            mt.pspan = cur.pspan;
+            mt.pstart = cur.pstart;
+        }
+        // this step's blocks: KB whole blocks from `first`
+        const int first = cur.lo + step * KB;
+        int phys[KB];
+        unsigned loaded = 0;
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+            phys[u] = nphys[u];
+            if (first + u < cur.hi && (phys[u] < 0 || (long long)phys[u] >= P.num_blocks)) {
+                raise_status(P.status, NS_DEV_BAD_BLOCK_ID);
+                phys[u] = -1;
+            }
+            if (first + u >= cur.hi)
+                phys[u] = -1;
+            loaded |= (phys[u] >= 0 ? 1u : 0u) << u;
+        }
+        if (step + 1 < nsteps) {
+#pragma unroll
+            for (int u = 0; u < KB; ++u)
+                nphys[u] = first + KB + u < cur.hi
+                               ? __ldg(P.block_tables + trow * P.max_blocks_per_seq + first + KB + u)
+                               : -1;
+        }
+        const int tok0 = step_token0<BS>(cur, step);
+        const int nval = min(kStepTokens, piece_end_token<BS>(cur) - tok0);  // >= 1
+        uint32_t vm = nval >= 32 ? 0xffffffffu : ((1u << nval) - 1u);
+        if (KB > 1) {
+            uint32_t bm = 0;
+#pragma unroll
+            for (int u = 0; u < KB; ++u)
+                if ((loaded >> u) & 1u)
+                    bm |= (BS >= 32 ? 0xffffffffu : ((1u << BS) - 1u)) << (u * BS);
+            vm &= bm;
+        } else if (!(loaded & 1u)) {
+            vm = 0;
+        }
+        const bool first_step = step == 0;
+        const bool new_tok = P.k_new != nullptr && cur.hi == cur.pnb && step == nsteps - 1;
+        long long ns = -1;
+        // fused append: block u_last of the step holds position L-1; only its
+        // rows before r_new come from the pool, row r_new is the new token
+        int u_last = -1, r_new = 0;
+        if (new_tok) {
+            // the pool slot of position L-1 must be the one slot_mapping names
+            u_last = (cur.pL - 1) / BS - first;
+            r_new = (cur.pL - 1) % BS;
+            int phys_last = -1;
+#pragma unroll
+            for (int u = 0; u < KB; ++u)
+                phys_last = u == u_last ? phys[u] : phys_last;
+            const long long want = (long long)phys_last * BS + (cur.pL - 1) % BS;
+            ns = slot_v;
+            if (ns != want || phys_last < 0)
+                raise_status(P.status, NS_DEV_FUSED_SLOT);
+            if (ns >= P.num_blocks * BS) {
+                raise_status(P.status, NS_DEV_BAD_SLOT);
+                ns = -1;
+            }
+        }
+        mt.flags = cur.flags | (new_tok ? kFlagNewTok : 0);
+        mt.step = step;
+        mt.nsteps = nsteps;
+        mt.t_new = (cur.pL - 1) - tok0;
+        mt.new_slot = ns;
+        mt.vmask = vm;
+        int rows[KB];  // rows of each block copied from the pool
+        uint32_t bytes = (first_step ? (uint32_t)G * kRowBytes : 0u) + (new_tok ? 2u * kRowBytes : 0u);
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+            rows[u] = phys[u] < 0 ? 0 : (u == u_last ? r_new : BS);
+            bytes += 2u * (uint32_t)rows[u] * kRowBytes;
+        }
+        if (bytes == 0)
+            mbar_arrive(bar);
+        else
+            mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+        for (int u = 0; u < KB; ++u) {
+            if (rows[u] > 0) {
+                const long long off = ((long long)phys[u] * P.num_kv_heads + cur.ph) * BS * kHeadDim;
+                bulk_load(sl.k + u * BS * kHeadDim, P.k_pool + off, rows[u] * kRowBytes, bar, pol);
+                bulk_load(sl.v + u * BS * kHeadDim, P.v_pool + off, rows[u] * kRowBytes, bar, pol);
+            }
+        }
+        if (first_step) {
+            const long long qoff = ((long long)cur.ps * P.num_q_heads + (long long)cur.ph * G) * kHeadDim;
+            bulk_load(sl.q, P.q + qoff, G * kRowBytes, bar);
+        }
+        if (new_tok) {
+            const long long noff = ((long long)cur.ps * P.num_kv_heads + cur.ph) * kHeadDim;
+            const int t_new = (cur.pL - 1) - tok0;
+            bulk_load(sl.k + t_new * kHeadDim, P.k_new + noff, kRowBytes, bar);
+            bulk_load(sl.v + t_new * kHeadDim, P.v_new + noff, kRowBytes, bar);
+        }
+        ++issued;
+        ++step;
+    }
+    if (lane >= kServedPerProducer)
+        return;
+    if (!ok) {
+        *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
+        raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
+    }
+    // Never leave with copies still landing in this consumer's slots.
+    for (int k = (issued > S ? issued - S : 0); k < issued; ++k)
+        if (!mbar_wait(&sm.full[w][k % S], (uint32_t)(k / S) & 1u)) {
+            raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
+            break;
+        }
+}
+
+// ---------------------------------------------------------------------------
+// Consumer warp: takes its slots in order, computes each step and frees the
+// slot; at the end of each piece it writes the output or a partial record.
+// ---------------------------------------------------------------------------
+template <typename T, int BS, int G, int S>
+__device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int warp, int lane)
 {
     constexpr int NS = HeadSlots<G>::N;
     constexpr int SHIFT = HeadSlots<G>::SHIFT;
@@ -842,53 +956,49 @@ __device__ void decode_warp(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int
     const long long B = sm.total, Gw = sm.g_eff;
     float2 q2[NS][4];
     float2 acc[G][4];
+    float m_run = -INFINITY, l_run = 0.f;
 #pragma unroll
     for (int i = 0; i < NS; ++i)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
             q2[i][k] = make_float2(0.f, 0.f);
-
-    Issuer<T, BS, G, S> is;
-    is.init(P, sm, warp, lane);
-    while (is.issued < S && is.issue_one(P, sm, warp, lane)) {
-    }
-
-    PieceWalk pc;
-    walk_init(P, sm, warp, pc);
-    float2 *pbuf = &sm.p[warp][0][0];
+    float *pbuf = &sm.p[warp][0][0];
     PendingMerge pm;
     pm.pair = -1;
     int consumed = 0;
     bool ok = true;
-    while (ok && walk_next<BS>(P, pc)) {
+    while (true) {
+        const int slot = consumed % S;
+        if (!mbar_wait(&sm.full[warp][slot], (uint32_t)(consumed / S) & 1u)) {
+            *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
+            raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
+            ok = false;
+            break;
+        }
+        // fields are read where used: the slot is freed only after its piece end
+        const SlotMeta &mt = sm.meta[warp][slot];
+        if (mt.nsteps < 0)
+            break;  // no more work
+        DecodeSlot<G> &sl = sm.ring[warp][slot];
+        if (mt.step == 0) {
 #pragma unroll
-        for (int j = 0; j < G; ++j)
+            for (int j = 0; j < G; ++j)
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                acc[j][k] = make_float2(0.f, 0.f);
-        float m_run = -INFINITY, l_run = 0.f;
-        const int nsteps = steps_of<BS>(pc);
-        const bool fused_here = P.k_new != nullptr && pc.hi == pc.pnb;
-        for (int step = 0; step < nsteps; ++step) {
-            const int slot = consumed % S;
-            if (!mbar_wait(&sm.full[warp][slot], (uint32_t)(consumed / S) & 1u)) {
-                raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
-                ok = false;
-                break;
-            }
-            DecodeSlot<G> &sl = sm.ring[warp][slot];
-            const uint32_t vmask = sm.vmask[warp][slot];
-            if (step == 0) {
+                for (int k = 0; k < 4; ++k)
+                    acc[j][k] = make_float2(0.f, 0.f);
+            m_run = -INFINITY;
+            l_run = 0.f;
+            if (mt.nsteps > 0) {
 #pragma unroll
                 for (int i = 0; i < NS; ++i) {
                     const int head = i ^ (c >> SHIFT);
                     if (head < G) {
-                        const uint4 w = lds128(sl.q + head * kHeadDim + c * 8);
+                        const uint4 wq = lds128(sl.q + head * kHeadDim + c * 8);
                         const float2 sc = make_float2(P.scale_log2, P.scale_log2);
-                        q2[i][0] = fmul2(unpack2<T>(w.x), sc);
-                        q2[i][1] = fmul2(unpack2<T>(w.y), sc);
-                        q2[i][2] = fmul2(unpack2<T>(w.z), sc);
-                        q2[i][3] = fmul2(unpack2<T>(w.w), sc);
+                        q2[i][0] = fmul2(unpack2<T>(wq.x), sc);
+                        q2[i][1] = fmul2(unpack2<T>(wq.y), sc);
+                        q2[i][2] = fmul2(unpack2<T>(wq.z), sc);
+                        q2[i][3] = fmul2(unpack2<T>(wq.w), sc);
                     } else {
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
@@ -896,45 +1006,35 @@ __device__ void decode_warp(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int
                     }
                 }
             }
-            const long long ns = sm.new_slot[warp][slot];
-            if (fused_here && step == nsteps - 1) {
-                // fused append: the new token's K/V replace its row in the slot
-                // and go to the pool slot the issuer checked
-                const int t_new = (pc.pL - 1) - step_token0<BS>(pc, step);
-                if (lane < 16) {
-                    const int cc = lane & 7;
-                    const uint4 val = lds128((lane < 8 ? sl.knew : sl.vnew) + cc * 8);
-                    *reinterpret_cast<uint4 *>((lane < 8 ? sl.k : sl.v) + t_new * kHeadDim + cc * 8) = val;
-                    if (ns >= 0) {
-                        const long long dst =
-                            (((ns / BS) * P.num_kv_heads + pc.ph) * BS + ns % BS) * kHeadDim + cc * 8;
-                        *reinterpret_cast<uint4 *>((lane < 8 ? P.k_pool_w : P.v_pool_w) + dst) = val;
-                    }
-                }
-                __syncwarp();
-            }
-            if (vmask == 0xffffffffu)
-                process_step<T, G, false>(sl.k, sl.v, vmask, q2, acc, m_run, l_run, pbuf, lane);
-            else
-                process_step<T, G, true>(sl.k, sl.v, vmask, q2, acc, m_run, l_run, pbuf, lane);
-            ++consumed;
-            if (!is.done)
-                is.issue_one(P, sm, warp, lane);
         }
-        if (!ok)
-            break;
-        piece_end<T, BS, G>(P, pc, worker, B, Gw, acc, m_run, l_run, lane, pm);
+        if (mt.nsteps > 0) {
+            if ((mt.flags & kFlagNewTok) && lane < 16 && mt.new_slot >= 0) {
+                // fused append: the new token's K/V landed in its row of the
+                // slot; they also go to the pool slot the producer checked
+                const int cc = lane & 7;
+                const uint4 val = lds128((lane < 8 ? sl.k : sl.v) + mt.t_new * kHeadDim + cc * 8);
+                const long long ns = mt.new_slot;
+                const long long dst = (((ns / BS) * P.num_kv_heads + mt.ph) * BS + ns % BS) * kHeadDim + cc * 8;
+                *reinterpret_cast<uint4 *>((lane < 8 ? P.k_pool_w : P.v_pool_w) + dst) = val;
+            }
+            if (mt.vmask == 0xffffffffu)
+                process_step<T, G, false>(sl.k, sl.v, mt.vmask, q2, acc, m_run, l_run, pbuf, lane);
+            else
+                process_step<T, G, true>(sl.k, sl.v, mt.vmask, q2, acc, m_run, l_run, pbuf, lane);
+        }
+        if (mt.nsteps == 0 || mt.step == mt.nsteps - 1) {
+            const PieceRef pr{mt.ps, mt.ph, mt.flags, mt.pspan, mt.pstart};
+            piece_end<T, BS, G>(P, pr, worker, B, Gw, acc, m_run, l_run, lane, pm);
+        }
+        // the slot's generic-proxy accesses are ordered before its async-proxy refill
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&sm.empty[warp][slot]);
+        ++consumed;
     }
     if (ok)
         resolve_merge<T>(P, pm, B, Gw, G, lane);
-    // Never leave with copies still landing in this warp's slots.
-    if (!ok && lane == 0) {
-        for (int k = consumed; k < is.issued; ++k)
-            if (!mbar_wait(&sm.full[warp][k % S], (uint32_t)(k / S) & 1u)) {
-                raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
-                break;
-            }
-    }
     __syncwarp();
 }
 
@@ -1026,6 +1126,7 @@ __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
     const bool wmajor = true;
 #endif
     if (tid == 0) {
+        sm.abort_flag = 0;
         sm.wmajor = wmajor ? 1 : 0;
         sm.whole = whole ? 1 : 0;
         sm.total = total;
@@ -1096,19 +1197,30 @@ __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
 
 
 template <typename T, int BS, int G, int S>
-__global__ void __launch_bounds__(kDecodeWarps * 32, NS_DECODE_MIN_CTAS) paged_decode_kernel(const DecodeParams P)
+__global__ void __launch_bounds__(kDecodeThreads, 1) paged_decode_kernel(const DecodeParams P)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     auto &sm = *reinterpret_cast<DecodeSmem<BS, G, S> *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int w = 0; w < kDecodeWarps; ++w)
-            for (int i = 0; i < S; ++i)
+            for (int i = 0; i < S; ++i) {
                 mbar_init(&sm.full[w][i], 1);
+                mbar_init(&sm.empty[w][i], 1);
+            }
         mbar_init_fence();
     }
     decode_prologue<DecodeSmem<BS, G, S>, BS>(P, sm);
-    decode_warp<T, BS, G, S>(P, sm, warp, lane);
+    // Registers move from the producer warpgroup (one working warp) to the
+    // two consumer warpgroups; the shares add up to the launch allocation.
+    if (warp < kDecodeWarps) {
+        regs_grow<kConsumerRegs>();
+        decode_consumer<T, BS, G, S>(P, sm, warp, lane);
+    } else {
+        regs_shrink<kProducerRegs>();
+        if (warp - kDecodeWarps < kProducerWarps)
+            decode_producer<T, BS, G, S>(P, sm, warp - kDecodeWarps, lane);
+    }
 }
 
 // Host-side launch helpers (defined in the per-type instantiation files).

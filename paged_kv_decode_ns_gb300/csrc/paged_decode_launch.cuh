@@ -8,8 +8,9 @@ namespace ns {
 
 template <typename T, int BS, int G>
 struct DecodeKernel {
-    static constexpr int S = NS_DECODE_STAGES;
-    static constexpr int THREADS = kDecodeWarps * 32;
+    static constexpr int S = decode_stages<BS, G>();
+    static_assert(sizeof(DecodeSmem<BS, G, S>) <= kMaxDynSmem, "decode shared memory");
+    static constexpr int THREADS = kDecodeThreads;  // consumers + producer warpgroup
     static constexpr size_t SMEM = sizeof(DecodeSmem<BS, G, S>);
     static void (*fn())(const DecodeParams) { return paged_decode_kernel<T, BS, G, S>; }
 
@@ -23,6 +24,14 @@ struct DecodeKernel {
             return e;
         if (dev < 31 && ((__atomic_load_n(&done_mask, __ATOMIC_RELAXED) >> dev) & 1))
             return cudaSuccess;
+        // The warpgroups trade registers with setmaxnreg; the trade balances
+        // only at exactly kLaunchRegs registers a thread, so refuse any other.
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, fn());
+        if (e != cudaSuccess)
+            return e;
+        if (fa.numRegs != kLaunchRegs)
+            return cudaErrorInvalidConfiguration;
         e = cudaFuncSetAttribute(fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
         if (e == cudaSuccess && dev < 31)
             __atomic_fetch_or(&done_mask, 1 << dev, __ATOMIC_RELAXED);
