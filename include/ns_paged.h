@@ -81,6 +81,7 @@ typedef enum ns_dtype { NS_F16 = 0, NS_BF16 = 1 } ns_dtype;
 #define NS_DEV_WAIT_TIMEOUT 0x8u     /* a bounded wait inside a kernel expired */
 #define NS_DEV_FUSED_SLOT 0x10u      /* fused append: slot is not the slot of position L-1 */
 #define NS_DEV_BAD_QUERY_SPAN 0x20u  /* prefill: query span longer than the context, or negative */
+#define NS_DEV_MERGE_QUEUE 0x40u     /* decode: a CTA's merge queue overflowed (a merge was skipped) */
 
 /* Human-readable name of a status code (static string). */
 const char *ns_status_string(ns_status status);

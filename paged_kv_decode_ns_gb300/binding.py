@@ -29,6 +29,7 @@ DEV_BITS = {
     0x8: "NS_DEV_WAIT_TIMEOUT",
     0x10: "NS_DEV_FUSED_SLOT",
     0x20: "NS_DEV_BAD_QUERY_SPAN",
+    0x40: "NS_DEV_MERGE_QUEUE",
 }
 
 

@@ -103,6 +103,18 @@ __device__ __forceinline__ void regs_shrink()
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+__device__ __forceinline__ int ld_acquire_cta(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_cta(int *p, int v)
+{
+    asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+
 // Non-blocking: has the phase with the given parity completed?
 __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
 {

@@ -49,21 +49,29 @@ namespace ns {
 // log2 units), L[8] (sum of 2^(z-M)), acc[8][64] (unnormalised output).
 constexpr int kSlotFloats = 2 * kMaxGroup + kMaxGroup * kHeadDim;
 constexpr float kRescaleSlack = 8.0f;
-// Workers (warps) per CTA and CTAs per SM, build-time knobs.  One CTA of 8
-// warps per SM: with two CTAs of 4, the warps of one CTA got the larger share
-// of issue slots and finished ~12 us before the other CTA's (measured),
-// which then ran with too few warps to hide latency.
-#ifndef NS_DECODE_WARPS
-#define NS_DECODE_WARPS 8
+// One CTA per SM: consumer warps in whole warpgroups and a producer
+// warpgroup.  Build-time knobs: NS_DECODE_CONSUMER_WARPS (8 or 12) and
+// NS_DECODE_SPLIT_HEADS (for G > 4, two warps share each ring and split the
+// query heads, so that 12 consumers fit in the register file).  Measured on
+// the batch-256 decode: 8 consumers with one ring each were fastest; the
+// split issued 22% more instructions (both warps unpack every K/V element).
+#ifndef NS_DECODE_CONSUMER_WARPS
+#define NS_DECODE_CONSUMER_WARPS 8
 #endif
-#ifndef NS_DECODE_MIN_CTAS
-#define NS_DECODE_MIN_CTAS (8 / NS_DECODE_WARPS)
+#ifndef NS_DECODE_SPLIT_HEADS
+#define NS_DECODE_SPLIT_HEADS 0
 #endif
-constexpr int kDecodeWarps = NS_DECODE_WARPS;
+// 1: one step path (the masked one, for every step) instead of an unmasked
+// copy besides: the smaller instruction footprint measured 4% faster on the
+// batch-256 decode than the two paths (instruction-fetch stalls).
+#ifndef NS_DECODE_ONE_STEP_PATH
+#define NS_DECODE_ONE_STEP_PATH 1
+#endif
+constexpr int kConsumerWarps = NS_DECODE_CONSUMER_WARPS;
 constexpr int kStepTokens = 32;        // tokens per ring slot (one per lane for the vote)
 constexpr int kMaxWorkers = 2048;      // split workers (each has two record slots)
-constexpr int kDefaultMinBlocksPerCta = 8 * kDecodeWarps;  // 8 blocks per worker
-constexpr int kLensCache = 512;        // context lengths kept in shared memory
+constexpr int kDefaultMinBlocksPerCta = 64;  // spread over a CTA's workers
+constexpr int kLensCache = 256;        // context lengths kept in shared memory
 // Split cost of a (sequence, kv head) pair beyond its blocks: the even split
 // counts kPieceCost virtual blocks at the start of every pair, so a worker
 // whose range crosses many pair boundaries (a piece end, a partial last
@@ -106,29 +114,68 @@ struct DecodeParams {
     int auto_policy;  // no override given: the device may deal whole pairs instead of splitting
 };
 
-// Thread block: two consumer warpgroups (one warp per worker) and one
-// producer warpgroup of which one warp works.
-constexpr int kDecodeThreads = (kDecodeWarps + 4) * 32;
-constexpr int kLaunchRegs = 65536 / kDecodeThreads / 8 * 8;  // 168
-// Producer warps (of the producer warpgroup's four); each serves
-// kDecodeWarps / NS_DECODE_PRODUCER_WARPS consumers, one lane each.
-#ifndef NS_DECODE_PRODUCER_WARPS
-#define NS_DECODE_PRODUCER_WARPS 4
-#endif
-constexpr int kProducerWarps = NS_DECODE_PRODUCER_WARPS;
+// Merges queued by consumers (run by the merger warp, or by consumers whose
+// rings are done).  A ring holds at most two partial pieces (the first and
+// last of its range), so at most 2 x 12 merges fall to one CTA.
+constexpr int kMergeQueue = 32;
+struct MergeJob {
+    long long c0, c1, out_row;
+    int pair, c0_second;
+};
+struct MergeQueue {
+    MergeJob job[kMergeQueue];
+    int ready[kMergeQueue];
+    int tail;  // entries taken by producers of jobs
+    int head;  // entries taken by mergers
+    int done;  // consumer warps finished
+};
+
+// Thread block: the consumer warpgroups and one producer warpgroup; the
+// registers a thread gets at launch, then the shares setmaxnreg moves to.
+constexpr int kDecodeThreads = (kConsumerWarps + 4) * 32;
+constexpr int kLaunchRegs = 65536 / kDecodeThreads / 8 * 8;  // 168 for 8 consumers
 #ifndef NS_DECODE_IDLE_NS
 #define NS_DECODE_IDLE_NS 32  // producer back-off when no slot is free
 #endif
-constexpr int kServedPerProducer = kDecodeWarps / kProducerWarps;
-static_assert(kProducerWarps >= 1 && kProducerWarps <= 4 && kDecodeWarps % kProducerWarps == 0, "producer warps");
 #ifndef NS_DECODE_PRODUCER_REGS
 #define NS_DECODE_PRODUCER_REGS 88
 #endif
 constexpr int kProducerRegs = NS_DECODE_PRODUCER_REGS;
-constexpr int kConsumerRegs = (kLaunchRegs * kDecodeThreads - kProducerRegs * 128) / (kDecodeWarps * 32) / 8 * 8;
-static_assert(kDecodeWarps == 8, "two consumer warpgroups");
-static_assert(kConsumerRegs * kDecodeWarps * 32 + kProducerRegs * 128 <= kLaunchRegs * kDecodeThreads,
+constexpr int kConsumerRegs = (kLaunchRegs * kDecodeThreads - kProducerRegs * 128) / (kConsumerWarps * 32) / 8 * 8;
+static_assert(kConsumerWarps % 4 == 0, "consumer warpgroups");
+static_assert(kConsumerRegs * kConsumerWarps * 32 + kProducerRegs * 128 <= kLaunchRegs * kDecodeThreads,
               "register shares exceed the launch allocation");
+
+// Reduce-scatter slots: the G heads of a group padded to a power of two.
+// PSTRIDE: floats per token row of the p buffer, at least 4 so that rows
+// stay 16-byte aligned for the float4 loads of the values pass.
+template <int G>
+struct HeadSlots {
+    static constexpr int N = G <= 1 ? 1 : (G <= 2 ? 2 : (G <= 4 ? 4 : 8));
+    static constexpr int LOG = N == 1 ? 0 : (N == 2 ? 1 : (N == 4 ? 2 : 3));
+    static constexpr int SHIFT = 3 - LOG;  // lane c holds head c >> SHIFT
+    static constexpr int PSTRIDE = N < 4 ? 4 : N;
+};
+
+// How a group of G query heads maps onto consumer warps.  Each ring (one
+// worker's stream of K/V steps) is read by WPG warps; warp i of the group
+// owns heads [i * GH0, ...) (with the head split, G > 4 splits 4 + (G - 4)
+// so that a warp holds q and accumulators of at most 4 heads).  Producer warp
+// p serves rings p * SERVED ... p * SERVED + SERVED - 1, one lane each; a
+// producer-warpgroup warp left over runs queued merges (else the consumers
+// run them when their rings are done).
+template <int G>
+struct DecodeShape {
+    static constexpr int WPG = (NS_DECODE_SPLIT_HEADS && G > 4) ? 2 : 1;
+    static constexpr int NG = kConsumerWarps / WPG;  // rings = workers per CTA
+    static constexpr int GH0 = WPG == 2 ? 4 : G;
+    static constexpr int GH1 = G - GH0;
+    static constexpr int SERVED = (NG + 3) / 4;
+    static constexpr int PW = NG / SERVED;  // producer warps
+    static constexpr bool MERGER = PW < 4;  // warp kConsumerWarps + 3 merges
+    static constexpr int PSTRIDE = HeadSlots<GH0>::PSTRIDE;  // p buffer row of a warp
+    static_assert(NG % SERVED == 0 && PW <= 4, "producer lanes");
+};
 
 enum : int {
     kFlagWhole = 4,    // the piece is the whole (sequence, kv head)
@@ -137,7 +184,7 @@ enum : int {
 };
 
 // What the producer tells a consumer about one ring slot.
-struct SlotMeta {
+struct alignas(16) SlotMeta {
     int ps, ph, pL, flags;      // the pair; piece flags (kFlag*)
     int pspan, step, nsteps;    // nsteps: steps of the piece; 0 = a piece with no key
                                 // (record only); -1 = no more work
@@ -148,19 +195,23 @@ struct SlotMeta {
     int pad[3];
 };
 
+__device__ __forceinline__ void put_meta(SlotMeta &mt, int ps, int ph, int pL, int flags, int pspan, int step,
+                                         int nsteps, int t_new, long long pstart, long long new_slot,
+                                         uint32_t vmask)
+{
+    int4 *v = reinterpret_cast<int4 *>(&mt);
+    v[0] = make_int4(ps, ph, pL, flags);
+    v[1] = make_int4(pspan, step, nsteps, t_new);
+    *reinterpret_cast<longlong2 *>(&mt.pstart) = make_longlong2(pstart, new_slot);
+    mt.vmask = vmask;
+}
+
 // The fields of a piece that its end needs.
 struct PieceRef {
     int ps, ph, flags, pspan;
     long long pstart;
 };
 
-// Reduce-scatter slots: the G heads of a group padded to a power of two.
-template <int G>
-struct HeadSlots {
-    static constexpr int N = G <= 1 ? 1 : (G <= 2 ? 2 : (G <= 4 ? 4 : 8));
-    static constexpr int LOG = N == 1 ? 0 : (N == 2 ? 1 : (N == 4 ? 2 : 3));
-    static constexpr int SHIFT = 3 - LOG;  // lane c holds head c >> SHIFT
-};
 
 
 // One ring slot: K and V rows of one 32-token step and the q rows that ride
@@ -175,16 +226,18 @@ struct DecodeSlot {
 
 template <int BS, int G, int S>
 struct DecodeSmem {
-    DecodeSlot<G> ring[kDecodeWarps][S];
-    float p[kDecodeWarps][kStepTokens][8];   // p per [token][head]
-    SlotMeta meta[kDecodeWarps][S];
-    uint64_t full[kDecodeWarps][S];          // producer -> consumer: the step has landed
-    uint64_t empty[kDecodeWarps][S];         // consumer -> producer: the slot may be refilled
+    static constexpr int NG = DecodeShape<G>::NG;
+    DecodeSlot<G> ring[NG][S];
+    float p[kConsumerWarps][kStepTokens][DecodeShape<G>::PSTRIDE];  // p per consumer warp [token][head]
+    SlotMeta meta[NG][S];
+    uint64_t full[NG][S];                    // producer -> consumers: the step has landed
+    uint64_t empty[NG][S];                   // consumers -> producer: the slot may be refilled
     long long scan[32];
     int maxnb[32];
     int npairs[32];
-    long long wb0[kDecodeWarps], wb1[kDecodeWarps], start_off[kDecodeWarps];
-    int start_s[kDecodeWarps];
+    long long wb0[NG], wb1[NG], start_off[NG];
+    int start_s[NG];
+    MergeQueue mq;
     int lens[kLensCache];                    // clamped context lengths of rows 0..kLensCache-1
     long long total;
     int g_eff;  // split workers
@@ -194,8 +247,7 @@ struct DecodeSmem {
     int plan_split, plan_maxp;
 };
 
-// Ring slots per warp: three where they fit in a CTA's shared memory (two
-// steps stream while one is computed), else two.
+// Slots per ring: as many (up to four) as fit in a CTA's shared memory.
 constexpr size_t kMaxDynSmem = 227 * 1024;
 template <int BS, int G>
 constexpr int decode_stages()
@@ -203,19 +255,19 @@ constexpr int decode_stages()
 #ifdef NS_DECODE_STAGES
     return NS_DECODE_STAGES;
 #else
-    return sizeof(DecodeSmem<BS, G, 3>) <= kMaxDynSmem ? 3 : 2;
+    return sizeof(DecodeSmem<BS, G, 4>) <= kMaxDynSmem ? 4 : sizeof(DecodeSmem<BS, G, 3>) <= kMaxDynSmem ? 3 : 2;
 #endif
 }
 
 __device__ __forceinline__ int nblocks_of(int L, int BS) { return (L + BS - 1) / BS; }
 
-// Worker number of warp `warp` of this CTA.  When only some workers have
+// Worker number of ring `ring` of this CTA (ng rings).  When only some workers have
 // work (wmajor), warp-major, so that they are spread over every SM before any
 // SM gets two; when all have work, CTA-major, so that the warps of a CTA walk
 // neighbouring runs of the same sequences.
-__device__ __forceinline__ long long worker_id(int warp, bool wmajor)
+__device__ __forceinline__ long long worker_id(int ring, bool wmajor, int ng)
 {
-    return wmajor ? (long long)warp * gridDim.x + blockIdx.x : (long long)blockIdx.x * kDecodeWarps + warp;
+    return wmajor ? (long long)ring * gridDim.x + blockIdx.x : (long long)blockIdx.x * ng + ring;
 }
 
 // Context length of row s, clamped to what the table can address.
@@ -265,8 +317,8 @@ __device__ __forceinline__ void walk_init(const DecodeParams &P, const Smem &sm,
     w.lens = sm.lens;
     w.whole = sm.whole != 0;
     if (w.whole) {
-        w.pos = worker_id(warp, sm.wmajor != 0);
-        w.stride = (long long)gridDim.x * kDecodeWarps;
+        w.pos = worker_id(warp, sm.wmajor != 0, Smem::NG);
+        w.stride = (long long)gridDim.x * Smem::NG;
         w.end = (long long)P.num_seqs * P.num_kv_heads;
     } else {
         w.pos = sm.wb0[warp];
@@ -465,7 +517,7 @@ __device__ __forceinline__ void process_step(const uint16_t *__restrict__ kb,
     // write the same value; a padding head lands in an unused slot)
 #pragma unroll
     for (int st = 0; st < STEPS; ++st)
-        pbuf[(st * 4 + r) * 8 + (c >> SHIFT)] = p[st];
+        pbuf[(st * 4 + r) * HeadSlots<G>::PSTRIDE + (c >> SHIFT)] = p[st];
     __syncwarp();
 
     // ---- values
@@ -477,7 +529,7 @@ __device__ __forceinline__ void process_step(const uint16_t *__restrict__ kb,
         float2 v2 = unpack2<T>(vw.z), v3 = unpack2<T>(vw.w);
         if (MASKED && !((vmask >> t) & 1u))
             v0 = v1 = v2 = v3 = make_float2(0.f, 0.f);
-        const float4 *prow = reinterpret_cast<const float4 *>(pbuf + t * 8);
+        const float4 *prow = reinterpret_cast<const float4 *>(pbuf + t * HeadSlots<G>::PSTRIDE);
         float4 pp[(G + 3) / 4];
 #pragma unroll
         for (int i = 0; i < (G + 3) / 4; ++i)
@@ -608,8 +660,9 @@ __device__ void merge_pieces(const DecodeParams &P, long long c0, long long c1, 
     }
 }
 
-// An arrival count whose result this warp has not looked at yet: the warp
-// that brings a pair's count to its number of pieces merges the pair.
+// An arrival count whose result this warp has not looked at yet: each warp
+// of each piece arrives once, and the warp that brings a pair's count to
+// (pieces x warps per ring) merges the pair.
 struct PendingMerge {
     int prev;  // lane 0: the count before this warp's arrival
     int pair;  // -1: nothing pending
@@ -619,7 +672,7 @@ struct PendingMerge {
 
 template <typename T>
 __device__ __forceinline__ void resolve_merge(const DecodeParams &P, PendingMerge &pm, long long B,
-                                              long long Gw, int G, int lane)
+                                              long long Gw, int G, int wpg, MergeQueue &mq, int lane)
 {
     if (pm.pair < 0)
         return;
@@ -628,28 +681,137 @@ __device__ __forceinline__ void resolve_merge(const DecodeParams &P, PendingMerg
     const long long c0 = cta_of(pm.pstart, B, Gw);
     const long long c1 = cta_of(pm.pstart + pm.pspan - 1, B, Gw);
     const int prev = __shfl_sync(0xffffffffu, pm.prev, 0);
-    if (prev == (int)(c1 - c0)) {
+    if (prev == (int)((c1 - c0 + 1) * wpg - 1)) {  // every warp of every piece has arrived
+        // the other pieces' records (published before their counts) are
+        // ordered before the hand-off to the merger
         __threadfence();
         const int s = pair / P.num_kv_heads, h = pair % P.num_kv_heads;
         const long long out_row = ((long long)s * P.num_q_heads + (long long)h * G) * kHeadDim;
-        merge_pieces<T>(P, c0, c1, range_begin(c0, B, Gw) != pm.pstart, out_row, G, lane);
+        const bool c0_second = range_begin(c0, B, Gw) != pm.pstart;
+        int idx = kMergeQueue;
         if (lane == 0)
-            P.counters[pair] = 0;
+            idx = atomicAdd(&mq.tail, 1);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        // A ring holds at most two partial pieces, so a CTA queues at most
+        // 2 x 12 merges and the queue cannot fill; the check guards the bound.
+        if (idx >= kMergeQueue) {
+            if (lane == 0)
+                raise_status(P.status, NS_DEV_MERGE_QUEUE);
+        } else {
+            if (lane == 0) {
+                MergeJob &j = mq.job[idx];
+                j.c0 = c0;
+                j.c1 = c1;
+                j.out_row = out_row;
+                j.pair = pair;
+                j.c0_second = c0_second ? 1 : 0;
+                st_release_cta(&mq.ready[idx], 1);
+            }
+        }
+    }
+}
+
+// Take the next queued merge (lane 0's result, broadcast), or -1 when every
+// queued entry is taken.
+__device__ __forceinline__ int merge_pop(MergeQueue &mq, int lane)
+{
+    int idx = -1;
+    if (lane == 0) {
+        while (true) {
+            const int h = ld_acquire_cta(&mq.head);
+            const int t = min(ld_acquire_cta(&mq.tail), kMergeQueue);
+            if (h >= t)
+                break;
+            if (atomicCAS(&mq.head, h, h + 1) == h) {
+                idx = h;
+                break;
+            }
+        }
+    }
+    return __shfl_sync(0xffffffffu, idx, 0);
+}
+
+// Run queued merge `idx` (its entry may still be being written: wait,
+// bounded, for its ready flag).
+template <typename T>
+__device__ __forceinline__ bool merge_run(const DecodeParams &P, MergeQueue &mq, int idx, int G, int lane)
+{
+    int ok = 1;
+    if (lane == 0) {
+        const unsigned long long t0 = global_timer_ns();
+        while (ld_acquire_cta(&mq.ready[idx]) == 0)
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                ok = 0;
+                break;
+            }
+    }
+    if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
+        return false;
+    }
+    const MergeJob j = mq.job[idx];
+    __threadfence();
+    merge_pieces<T>(P, j.c0, j.c1, j.c0_second != 0, j.out_row, G, lane);
+    if (lane == 0)
+        P.counters[j.pair] = 0;
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// Merger warp: runs queued merges while the consumers stream, until every
+// consumer warp has finished and the queue is empty (consumers that have
+// finished help drain it).
+// ---------------------------------------------------------------------------
+template <typename T>
+__device__ void decode_merger(const DecodeParams &P, MergeQueue &mq, volatile int *abort_flag, int G, int lane)
+{
+    unsigned long long idle_since = 0;
+    bool idle = false;
+    while (true) {
+        const int idx = merge_pop(mq, lane);
+        if (idx >= 0) {
+            idle = false;
+            if (!merge_run<T>(P, mq, idx, G, lane))
+                break;
+            continue;
+        }
+        int done = 0;
+        if (lane == 0)
+            done = ld_acquire_cta(&mq.done);
+        done = __shfl_sync(0xffffffffu, done, 0);
+        // a finished consumer queued its jobs before counting itself done
+        if (done == kConsumerWarps) {
+            if (merge_pop(mq, lane) < 0)
+                break;
+            continue;  // unreachable in practice: a pop would have found it
+        }
+        const unsigned long long now = global_timer_ns();
+        if (!idle) {
+            idle = true;
+            idle_since = now;
+        }
+        if (__any_sync(0xffffffffu, *abort_flag != 0 || now - idle_since > kWaitLimitNs)) {
+            raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
+            break;
+        }
+        __nanosleep(64);
     }
 }
 
 // ---------------------------------------------------------------------------
-// End of a piece for one warp: combine the 4 row groups (shuffles), then
-// write the output (whole pair) or a partial record and count its arrival;
+// End of a piece for one warp (heads hbase .. hbase + gvalid - 1 of the
+// group, computed in GH head slots):
+// combine the 4 row groups (shuffles), then write the output (whole pair) or
+// its part of the partial record and count its arrival;
 // the result of the count is looked at later (resolve_merge), so the warp
 // does not wait for the atomic here.
 // ---------------------------------------------------------------------------
-template <typename T, int BS, int G>
+template <typename T, int BS, int G, int GH>
 __device__ void piece_end(const DecodeParams &P, const PieceRef &pc, long long worker, long long B,
-                          long long Gw, float2 (&acc)[G][4], float m_run, float l_run, int lane,
-                          PendingMerge &pm)
+                          long long Gw, float2 (&acc)[GH][4], float m_run, float l_run, int hbase, int gvalid,
+                          int lane, PendingMerge &pm, MergeQueue &mq)
 {
-    constexpr int SHIFT = HeadSlots<G>::SHIFT;
+    constexpr int SHIFT = HeadSlots<GH>::SHIFT;
     const int c = lane & 7;
     // lane (r, c) with (c & ((1 << SHIFT) - 1)) == 0 owns (row group r, head c >> SHIFT)
     float M = fmaxf(m_run, __shfl_xor_sync(0xffffffffu, m_run, 8));
@@ -659,7 +821,7 @@ __device__ void piece_end(const DecodeParams &P, const PieceRef &pc, long long w
     Ls += __shfl_xor_sync(0xffffffffu, Ls, 8);
     Ls += __shfl_xor_sync(0xffffffffu, Ls, 16);
 #pragma unroll
-    for (int j = 0; j < G; ++j) {
+    for (int j = 0; j < GH; ++j) {
         const float fj = __shfl_sync(0xffffffffu, f, (lane & ~7) | (j << SHIFT));
         const float2 f2 = make_float2(fj, fj);
 #pragma unroll
@@ -672,15 +834,17 @@ __device__ void piece_end(const DecodeParams &P, const PieceRef &pc, long long w
             acc[j][k] = a;
         }
     }
-    // every lane now holds, for dims 8c..8c+7: the merged acc of all heads;
-    // head j's max and sum are in lane (j << SHIFT)
+    // every lane now holds, for dims 8c..8c+7: the merged acc of this warp's
+    // heads; head j's max and sum are in lane (j << SHIFT)
     const int s = pc.ps, h = pc.ph;
-    const long long out_row = ((long long)s * P.num_q_heads + (long long)h * G) * kHeadDim;
+    const long long out_row = ((long long)s * P.num_q_heads + (long long)h * G + hbase) * kHeadDim;
     if (pc.flags & kFlagWhole) {
         if (lane < 8) {
 #pragma unroll
-            for (int j = 0; j < G; ++j) {
+            for (int j = 0; j < GH; ++j) {
                 const float inv = 1.f / __shfl_sync(0xffu, Ls, j << SHIFT);
+                if (j >= gvalid)
+                    break;
                 uint4 w;
                 w.x = pack2<T>(acc[j][0].x * inv, acc[j][0].y * inv);
                 w.y = pack2<T>(acc[j][1].x * inv, acc[j][1].y * inv);
@@ -697,19 +861,21 @@ __device__ void piece_end(const DecodeParams &P, const PieceRef &pc, long long w
     float *rec = P.partials + (worker * 2 + which) * kSlotFloats;
     if (lane < 8) {
 #pragma unroll
-        for (int j = 0; j < G; ++j) {
-            float *a = rec + 2 * kMaxGroup + j * kHeadDim + c * 8;
+        for (int j = 0; j < GH; ++j) {
+            if (j >= gvalid)
+                break;
+            float *a = rec + 2 * kMaxGroup + (hbase + j) * kHeadDim + c * 8;
             __stcg(reinterpret_cast<float4 *>(a), make_float4(acc[j][0].x, acc[j][0].y, acc[j][1].x, acc[j][1].y));
             __stcg(reinterpret_cast<float4 *>(a + 4), make_float4(acc[j][2].x, acc[j][2].y, acc[j][3].x, acc[j][3].y));
         }
-        if ((c & ((1 << SHIFT) - 1)) == 0 && (c >> SHIFT) < G) {
-            __stcg(rec + (c >> SHIFT), M);
-            __stcg(rec + kMaxGroup + (c >> SHIFT), Ls);
+        if ((c & ((1 << SHIFT) - 1)) == 0 && (c >> SHIFT) < gvalid) {
+            __stcg(rec + hbase + (c >> SHIFT), M);
+            __stcg(rec + kMaxGroup + hbase + (c >> SHIFT), Ls);
         }
     }
     __threadfence();
     __syncwarp();
-    resolve_merge<T>(P, pm, B, Gw, G, lane);  // at most one count is left open
+    resolve_merge<T>(P, pm, B, Gw, G, DecodeShape<G>::WPG, mq, lane);  // at most one count is left open
     const int pair = s * P.num_kv_heads + h;
     pm.prev = 0;
     if (lane == 0)
@@ -732,10 +898,10 @@ __device__ __forceinline__ void piece_prefetch(const DecodeParams &P, const Piec
 }
 
 // ---------------------------------------------------------------------------
-// Producer warps: lane i of producer warp p serves consumer warp
-// w = p * kServedPerProducer + i.  It walks w's pieces one piece ahead,
-// reads the block-table entries of each step one step ahead, and issues the
-// TMA copies of the next step into w's ring as soon as w frees a slot, with
+// Producer warps: lane i of producer warp p serves ring (worker)
+// w = p * SERVED + i.  It walks w's pieces one piece ahead, reads the
+// block-table entries of each step one step ahead, and issues the TMA copies
+// of the next step into w's ring as soon as its consumers free a slot, with
 // the step's description (piece, valid keys, fused slot) in the slot's
 // SlotMeta.  Consumers then hold no walk or issue state: their registers go
 // to the scores and accumulators.
@@ -744,9 +910,10 @@ template <typename T, int BS, int G, int S>
 __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int pwarp, int lane)
 {
     constexpr int KB = kStepTokens / BS;  // blocks per step
-    const int w = pwarp * kServedPerProducer + (lane < kServedPerProducer ? lane : 0);
+    constexpr int SERVED = DecodeShape<G>::SERVED;
+    const int w = pwarp * SERVED + (lane < SERVED ? lane : 0);
     const uint64_t pol = l2_evict_first_policy();
-    bool done = lane >= kServedPerProducer;
+    bool done = lane >= SERVED;
     // `walk` runs one piece ahead of `cur`: the table entries of the next
     // piece's first step (and its slot_mapping entry) load while the current
     // piece streams.
@@ -792,7 +959,7 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
         uint64_t *bar = &sm.full[w][slot];
         if (!has || step >= nsteps) {
             if (!ahead) {
-                mt.nsteps = -1;  // no more work for this consumer
+                mt.nsteps = -1;  // no more work for this ring
                 mbar_arrive(bar);
                 ++issued;
                 done = true;
@@ -810,27 +977,14 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
             ahead = walk_next<BS>(P, walk);
             if (ahead)
                 piece_prefetch<BS, KB>(P, walk, a_trow, aphys, a_slot);
-            mt.ps = cur.ps;
-            mt.ph = cur.ph;
-            mt.pL = cur.pL;
-            mt.pspan = cur.pspan;
-            mt.pstart = cur.pstart;
             if (nsteps == 0) {
-                // only virtual blocks of the pair: the consumer writes an empty record
-                mt.flags = cur.flags;
-                mt.step = 0;
-                mt.nsteps = 0;
+                // only virtual blocks of the pair: the consumers write an empty record
+                put_meta(mt, cur.ps, cur.ph, cur.pL, cur.flags, cur.pspan, 0, 0, 0, cur.pstart, -1, 0u);
                 mbar_arrive(bar);
                 ++issued;
                 has = false;
                 continue;
             }
-        } else {
-            mt.ps = cur.ps;
-            mt.ph = cur.ph;
-            mt.pL = cur.pL;
-            mt.pspan = cur.pspan;
-            mt.pstart = cur.pstart;
         }
         // this step's blocks: KB whole blocks from `first`
         const int first = cur.lo + step * KB;
@@ -890,12 +1044,8 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
                 ns = -1;
             }
         }
-        mt.flags = cur.flags | (new_tok ? kFlagNewTok : 0);
-        mt.step = step;
-        mt.nsteps = nsteps;
-        mt.t_new = (cur.pL - 1) - tok0;
-        mt.new_slot = ns;
-        mt.vmask = vm;
+        put_meta(mt, cur.ps, cur.ph, cur.pL, cur.flags | (new_tok ? kFlagNewTok : 0), cur.pspan, step, nsteps,
+                 (cur.pL - 1) - tok0, cur.pstart, ns, vm);
         int rows[KB];  // rows of each block copied from the pool
         uint32_t bytes = (first_step ? (uint32_t)G * kRowBytes : 0u) + (new_tok ? 2u * kRowBytes : 0u);
 #pragma unroll
@@ -928,7 +1078,7 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
         ++issued;
         ++step;
     }
-    if (lane >= kServedPerProducer)
+    if (lane >= SERVED)
         return;
     if (!ok) {
         *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
@@ -943,19 +1093,23 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
 }
 
 // ---------------------------------------------------------------------------
-// Consumer warp: takes its slots in order, computes each step and frees the
-// slot; at the end of each piece it writes the output or a partial record.
+// Consumer warp: heads hbase .. hbase + gvalid - 1 of ring `ring`, computed
+// in GH head slots (both warps of a ring run the same code).  Takes the
+// ring's slots in order, computes each step, and at the end of each piece
+// writes the output or its part of a partial record; then frees the slot
+// (every warp of the ring arrives on its empty barrier).
 // ---------------------------------------------------------------------------
-template <typename T, int BS, int G, int S>
-__device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int warp, int lane)
+template <typename T, int BS, int G, int S, int GH>
+__device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int ring, int hbase, int gvalid,
+                                int warp, int lane)
 {
-    constexpr int NS = HeadSlots<G>::N;
-    constexpr int SHIFT = HeadSlots<G>::SHIFT;
+    constexpr int NS = HeadSlots<GH>::N;
+    constexpr int SHIFT = HeadSlots<GH>::SHIFT;
     const int c = lane & 7;
-    const long long worker = worker_id(warp, sm.wmajor != 0);
+    const long long worker = worker_id(ring, sm.wmajor != 0, DecodeShape<G>::NG);
     const long long B = sm.total, Gw = sm.g_eff;
     float2 q2[NS][4];
-    float2 acc[G][4];
+    float2 acc[GH][4];
     float m_run = -INFINITY, l_run = 0.f;
 #pragma unroll
     for (int i = 0; i < NS; ++i)
@@ -965,35 +1119,37 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
     float *pbuf = &sm.p[warp][0][0];
     PendingMerge pm;
     pm.pair = -1;
-    int consumed = 0;
+    int slot = 0;
+    uint32_t phase = 0;
     bool ok = true;
     while (true) {
-        const int slot = consumed % S;
-        if (!mbar_wait(&sm.full[warp][slot], (uint32_t)(consumed / S) & 1u)) {
+        if (!mbar_wait(&sm.full[ring][slot], phase)) {
             *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
             raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
             ok = false;
             break;
         }
         // fields are read where used: the slot is freed only after its piece end
-        const SlotMeta &mt = sm.meta[warp][slot];
-        if (mt.nsteps < 0)
+        const SlotMeta &mt = sm.meta[ring][slot];
+        const int4 m1 = *reinterpret_cast<const int4 *>(&mt.pspan);  // pspan, step, nsteps, t_new
+        const int nsteps = m1.z, step = m1.y;
+        if (nsteps < 0)
             break;  // no more work
-        DecodeSlot<G> &sl = sm.ring[warp][slot];
-        if (mt.step == 0) {
+        DecodeSlot<G> &sl = sm.ring[ring][slot];
+        if (step == 0) {
 #pragma unroll
-            for (int j = 0; j < G; ++j)
+            for (int j = 0; j < GH; ++j)
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     acc[j][k] = make_float2(0.f, 0.f);
             m_run = -INFINITY;
             l_run = 0.f;
-            if (mt.nsteps > 0) {
+            if (nsteps > 0) {
 #pragma unroll
                 for (int i = 0; i < NS; ++i) {
                     const int head = i ^ (c >> SHIFT);
-                    if (head < G) {
-                        const uint4 wq = lds128(sl.q + head * kHeadDim + c * 8);
+                    if (head < gvalid) {
+                        const uint4 wq = lds128(sl.q + (hbase + head) * kHeadDim + c * 8);
                         const float2 sc = make_float2(P.scale_log2, P.scale_log2);
                         q2[i][0] = fmul2(unpack2<T>(wq.x), sc);
                         q2[i][1] = fmul2(unpack2<T>(wq.y), sc);
@@ -1007,35 +1163,55 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
                 }
             }
         }
-        if (mt.nsteps > 0) {
-            if ((mt.flags & kFlagNewTok) && lane < 16 && mt.new_slot >= 0) {
-                // fused append: the new token's K/V landed in its row of the
-                // slot; they also go to the pool slot the producer checked
+        if (nsteps > 0) {
+            // fused append: the new token's K/V landed in its row of the slot;
+            // the ring's first warp also writes them to the pool slot the
+            // producer checked
+            if (hbase == 0 && (mt.flags & kFlagNewTok) && lane < 16 && mt.new_slot >= 0) {
                 const int cc = lane & 7;
-                const uint4 val = lds128((lane < 8 ? sl.k : sl.v) + mt.t_new * kHeadDim + cc * 8);
+                const uint4 val = lds128((lane < 8 ? sl.k : sl.v) + m1.w * kHeadDim + cc * 8);
                 const long long ns = mt.new_slot;
                 const long long dst = (((ns / BS) * P.num_kv_heads + mt.ph) * BS + ns % BS) * kHeadDim + cc * 8;
                 *reinterpret_cast<uint4 *>((lane < 8 ? P.k_pool_w : P.v_pool_w) + dst) = val;
             }
-            if (mt.vmask == 0xffffffffu)
-                process_step<T, G, false>(sl.k, sl.v, mt.vmask, q2, acc, m_run, l_run, pbuf, lane);
+            const uint32_t vmask = mt.vmask;
+#if NS_DECODE_ONE_STEP_PATH
+            process_step<T, GH, true>(sl.k, sl.v, vmask, q2, acc, m_run, l_run, pbuf, lane);
+#else
+            if (vmask == 0xffffffffu)
+                process_step<T, GH, false>(sl.k, sl.v, vmask, q2, acc, m_run, l_run, pbuf, lane);
             else
-                process_step<T, G, true>(sl.k, sl.v, mt.vmask, q2, acc, m_run, l_run, pbuf, lane);
+                process_step<T, GH, true>(sl.k, sl.v, vmask, q2, acc, m_run, l_run, pbuf, lane);
+#endif
         }
-        if (mt.nsteps == 0 || mt.step == mt.nsteps - 1) {
-            const PieceRef pr{mt.ps, mt.ph, mt.flags, mt.pspan, mt.pstart};
-            piece_end<T, BS, G>(P, pr, worker, B, Gw, acc, m_run, l_run, lane, pm);
+        if (nsteps == 0 || step == nsteps - 1) {
+            const PieceRef pr{mt.ps, mt.ph, mt.flags, m1.x, mt.pstart};
+            piece_end<T, BS, G, GH>(P, pr, worker, B, Gw, acc, m_run, l_run, hbase, gvalid, lane, pm, sm.mq);
         }
-        // the slot's generic-proxy accesses are ordered before its async-proxy refill
-        fence_async_smem();
+        // The slot is only read (the async proxy alone writes it), so the
+        // barrier's release/acquire orders these reads before the refill.
         __syncwarp();
         if (lane == 0)
-            mbar_arrive(&sm.empty[warp][slot]);
-        ++consumed;
+            mbar_arrive(&sm.empty[ring][slot]);
+        if (++slot == S) {
+            slot = 0;
+            phase ^= 1u;
+        }
     }
-    if (ok)
-        resolve_merge<T>(P, pm, B, Gw, G, lane);
+    if (ok) {
+        resolve_merge<T>(P, pm, B, Gw, G, DecodeShape<G>::WPG, sm.mq, lane);
+        // help drain the merge queue: most merges fall due at the end
+        while (true) {
+            const int idx = merge_pop(sm.mq, lane);
+            if (idx < 0 || !merge_run<T>(P, sm.mq, idx, G, lane))
+                break;
+        }
+    }
     __syncwarp();
+    if (lane == 0) {
+        __threadfence_block();  // this warp's queued jobs before its count
+        atomicAdd(&sm.mq.done, 1);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -1044,7 +1220,9 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
 template <class Smem, int BS>
 __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
 {
-    constexpr int NT = kDecodeWarps * 32;
+    constexpr int NT = kDecodeThreads;  // every thread scans lengths
+    constexpr int NWARPS = NT / 32;
+    constexpr int NG = Smem::NG;       // workers of this CTA
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int Hkv = P.num_kv_heads;
@@ -1092,7 +1270,7 @@ __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
     __syncthreads();
     long long before = 0, total = 0, live_pairs = 0;
     int maxnb = 0;
-    for (int w = 0; w < kDecodeWarps; ++w) {
+    for (int w = 0; w < NWARPS; ++w) {
         if (w < warp)
             before += sm.scan[w];
         total += sm.scan[w];
@@ -1105,9 +1283,9 @@ __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
     // Gw workers (each at least min_blocks_per_cta / 4 blocks) unless no pair
     // is longer than twice the even share, in which case whole pairs dealt
     // round-robin need no merge at all.
-    const long long W = (long long)gridDim.x * kDecodeWarps;
+    const long long W = (long long)gridDim.x * NG;
     const long long minb = P.min_blocks_per_cta > 0 ? P.min_blocks_per_cta : 1;
-    long long Gw = (kDecodeWarps * total + minb - 1) / minb;
+    long long Gw = (NG * total + minb - 1) / minb;
     if (Gw > W)
         Gw = W;
     if (Gw > kMaxWorkers)
@@ -1125,7 +1303,12 @@ __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
 #else
     const bool wmajor = true;
 #endif
+    if (tid < kMergeQueue)
+        sm.mq.ready[tid] = 0;
     if (tid == 0) {
+        sm.mq.tail = 0;
+        sm.mq.head = 0;
+        sm.mq.done = 0;
         sm.abort_flag = 0;
         sm.wmajor = wmajor ? 1 : 0;
         sm.whole = whole ? 1 : 0;
@@ -1134,8 +1317,8 @@ __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
         sm.plan_split = 0;
         sm.plan_maxp = 1;
     }
-    if (tid < kDecodeWarps) {
-        const long long wk = worker_id(tid, wmajor);
+    if (tid < NG) {
+        const long long wk = worker_id(tid, wmajor, NG);
         sm.wb0[tid] = (!whole && wk < Gw) ? range_begin(wk, total, Gw) : 0;
         sm.wb1[tid] = (!whole && wk < Gw) ? range_begin(wk + 1, total, Gw) : 0;
         sm.start_s[tid] = P.num_seqs;
@@ -1143,7 +1326,7 @@ __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
     }
     __syncthreads();
     if (!whole && mine > 0) {
-        for (int w = 0; w < kDecodeWarps; ++w) {
+        for (int w = 0; w < NG; ++w) {
             const long long b0 = sm.wb0[w];
             if (sm.wb1[w] > b0 && b0 >= excl && b0 < excl + mine) {
                 long long cum = excl;
@@ -1183,7 +1366,7 @@ __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
         const long long wact = whole ? min(W, pairs) : Gw;
         pl.ctas_launched = gridDim.x;
         pl.ctas_active = (int)(wmajor ? min((long long)gridDim.x, wact)
-                                      : (wact + kDecodeWarps - 1) / kDecodeWarps);
+                                      : (wact + NG - 1) / NG);
         pl.total_blocks = total - (long long)kPieceCost * live_pairs;  // real blocks
         pl.split_pairs = whole ? 0 : sm.plan_split;
         pl.max_pieces = whole ? 1 : sm.plan_maxp;
@@ -1202,24 +1385,30 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) paged_decode_kernel(const D
     extern __shared__ __align__(128) unsigned char smem_raw[];
     auto &sm = *reinterpret_cast<DecodeSmem<BS, G, S> *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    using Shape = DecodeShape<G>;
     if (threadIdx.x == 0) {
-        for (int w = 0; w < kDecodeWarps; ++w)
+        for (int w = 0; w < Shape::NG; ++w)
             for (int i = 0; i < S; ++i) {
                 mbar_init(&sm.full[w][i], 1);
-                mbar_init(&sm.empty[w][i], 1);
+                mbar_init(&sm.empty[w][i], Shape::WPG);
             }
         mbar_init_fence();
     }
     decode_prologue<DecodeSmem<BS, G, S>, BS>(P, sm);
-    // Registers move from the producer warpgroup (one working warp) to the
-    // two consumer warpgroups; the shares add up to the launch allocation.
-    if (warp < kDecodeWarps) {
+    // Registers move from the producer warpgroup to the consumer warpgroups;
+    // the shares add up to the launch allocation.
+    if (warp < kConsumerWarps) {
         regs_grow<kConsumerRegs>();
-        decode_consumer<T, BS, G, S>(P, sm, warp, lane);
+        const int ring = warp / Shape::WPG;
+        const int half = warp % Shape::WPG;
+        decode_consumer<T, BS, G, S, Shape::GH0>(P, sm, ring, half * Shape::GH0, half ? Shape::GH1 : Shape::GH0,
+                                                 warp, lane);
     } else {
         regs_shrink<kProducerRegs>();
-        if (warp - kDecodeWarps < kProducerWarps)
-            decode_producer<T, BS, G, S>(P, sm, warp - kDecodeWarps, lane);
+        if (warp - kConsumerWarps < Shape::PW)
+            decode_producer<T, BS, G, S>(P, sm, warp - kConsumerWarps, lane);
+        else if (Shape::MERGER && warp == kConsumerWarps + 3)
+            decode_merger<T>(P, sm.mq, &sm.abort_flag, G, lane);
     }
 }
 
