@@ -56,14 +56,14 @@ KERNEL_SOURCES = {
                           "paged_kv_decode_ns_gb300/csrc/tcgen05.cuh", "include/ns_paged.h"],
 }
 PROFILED_TRAFFIC = {
-    # profiles/paged_decode_b256_bf16.md: 240.11 MB read + 4.09 MB written
+    # profiles/paged_decode_b256_bf16.md: 238.97 MB read + 3.59 MB written
     ("decode_b256", "paged_decode_kernel"): {
-        "sources_sha256": "c1e08ca6fb017d0477b2742f81698f2a54222a758797d63b3822d3357b8db12c",
-        "bytes": 244204288},
+        "sources_sha256": "4d047ef9677b0b5605bad23ccc3fbcf605ecd9074195547bff95391778a0205d",
+        "bytes": 242556672},
     # profiles/tc_prefill_mixed_f16.md: 4.75 MB read, 0 written
     ("mixed_chunked_prefill", "tc_prefill_kernel"): {
-        "sources_sha256": "0c142170defeda595e23ea141dfcfb47710039ea3f721412a0b258bf4d2e9f41",
-        "bytes": 4748288},
+        "sources_sha256": "27a0c16c4b361e2c641ec001de08657804a0063eb78c9443c526c62768ae7a37",
+        "bytes": 4748032},
 }
 
 
