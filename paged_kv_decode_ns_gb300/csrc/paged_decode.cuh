@@ -114,6 +114,9 @@ struct DecodeParams {
     int auto_policy;  // no override given: the device may deal whole pairs instead of splitting
 };
 
+// Source of the zero-filled rows of a step (32 rows of 64 elements).
+static __device__ __align__(128) uint16_t g_zero_rows[kStepTokens * kHeadDim];
+
 // Merges queued by consumers (run by the merger warp, or by consumers whose
 // rings are done).  A ring holds at most two partial pieces (the first and
 // last of its range), so at most 2 x 12 merges fall to one CTA.
@@ -135,7 +138,7 @@ struct MergeQueue {
 constexpr int kDecodeThreads = (kConsumerWarps + 4) * 32;
 constexpr int kLaunchRegs = 65536 / kDecodeThreads / 8 * 8;  // 168 for 8 consumers
 #ifndef NS_DECODE_IDLE_NS
-#define NS_DECODE_IDLE_NS 32  // producer back-off when no slot is free
+#define NS_DECODE_IDLE_NS 500  // producer back-off when no slot is free (the rings hold 3 steps)
 #endif
 #ifndef NS_DECODE_PRODUCER_REGS
 #define NS_DECODE_PRODUCER_REGS 88
@@ -426,7 +429,8 @@ __device__ __forceinline__ int step_token0(const PieceWalk &w, int i)
 
 // ---------------------------------------------------------------------------
 // One 32-token step for one warp.  MASKED: some tokens of the step are not
-// keys (bit t of vmask clear): their scores are -inf and their values 0.
+// keys (bit t of vmask clear): their scores are -inf, so p = 0; their rows
+// in the slot are zero-filled by the producer, so p * v adds nothing.
 // ---------------------------------------------------------------------------
 template <typename T, int G, bool MASKED>
 __device__ __forceinline__ void process_step(const uint16_t *__restrict__ kb,
@@ -527,8 +531,6 @@ __device__ __forceinline__ void process_step(const uint16_t *__restrict__ kb,
         const uint4 vw = lds128(vb + t * kHeadDim + c * 8);
         float2 v0 = unpack2<T>(vw.x), v1 = unpack2<T>(vw.y);
         float2 v2 = unpack2<T>(vw.z), v3 = unpack2<T>(vw.w);
-        if (MASKED && !((vmask >> t) & 1u))
-            v0 = v1 = v2 = v3 = make_float2(0.f, 0.f);
         const float4 *prow = reinterpret_cast<const float4 *>(pbuf + t * HeadSlots<G>::PSTRIDE);
         float4 pp[(G + 3) / 4];
 #pragma unroll
@@ -1046,12 +1048,20 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
         }
         put_meta(mt, cur.ps, cur.ph, cur.pL, cur.flags | (new_tok ? kFlagNewTok : 0), cur.pspan, step, nsteps,
                  (cur.pL - 1) - tok0, cur.pstart, ns, vm);
-        int rows[KB];  // rows of each block copied from the pool
+        // Rows of each block: the first rows[u] come from the pool; in the new
+        // token's block row r_new comes from k_new/v_new; every other row is
+        // zero-filled, so that each row of the slot is finite and a masked
+        // token (p = 0) adds nothing.  Zero ranges: [rows, za) and [zb, BS).
+        const int pend_tok = piece_end_token<BS>(cur);
+        int rows[KB], za[KB], zb[KB];
         uint32_t bytes = (first_step ? (uint32_t)G * kRowBytes : 0u) + (new_tok ? 2u * kRowBytes : 0u);
 #pragma unroll
         for (int u = 0; u < KB; ++u) {
-            rows[u] = phys[u] < 0 ? 0 : (u == u_last ? r_new : BS);
-            bytes += 2u * (uint32_t)rows[u] * kRowBytes;
+            const int keys = min(max(pend_tok - (tok0 + u * BS), 0), BS);
+            rows[u] = phys[u] < 0 ? 0 : (u == u_last ? r_new : keys);
+            za[u] = u == u_last ? r_new : BS;      // zero rows [rows, za)
+            zb[u] = u == u_last ? r_new + 1 : BS;  // and [zb, BS)
+            bytes += 2u * (uint32_t)(rows[u] + (za[u] - rows[u]) + (BS - zb[u])) * kRowBytes;
         }
         if (bytes == 0)
             mbar_arrive(bar);
@@ -1063,6 +1073,16 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
                 const long long off = ((long long)phys[u] * P.num_kv_heads + cur.ph) * BS * kHeadDim;
                 bulk_load(sl.k + u * BS * kHeadDim, P.k_pool + off, rows[u] * kRowBytes, bar, pol);
                 bulk_load(sl.v + u * BS * kHeadDim, P.v_pool + off, rows[u] * kRowBytes, bar, pol);
+            }
+            if (za[u] > rows[u]) {
+                const uint32_t n = (uint32_t)(za[u] - rows[u]) * kRowBytes;
+                bulk_load(sl.k + (u * BS + rows[u]) * kHeadDim, g_zero_rows, n, bar);
+                bulk_load(sl.v + (u * BS + rows[u]) * kHeadDim, g_zero_rows, n, bar);
+            }
+            if (zb[u] < BS) {
+                const uint32_t n = (uint32_t)(BS - zb[u]) * kRowBytes;
+                bulk_load(sl.k + (u * BS + zb[u]) * kHeadDim, g_zero_rows, n, bar);
+                bulk_load(sl.v + (u * BS + zb[u]) * kHeadDim, g_zero_rows, n, bar);
             }
         }
         if (first_step) {
