@@ -200,17 +200,25 @@ def make_workload(name: str):
     return wl.WORKLOADS[name]()
 
 
-def workload_config(st, name, pools):
+def workload_config(st, name, pools, layers=1):
     step = ("fused kv_append + split-KV paged decode" if st.is_decode
             else "kv_append + chunked prefill (tensor-core spans, decode-walk rows)")
-    return {"workload": f"{st.name}: {name}", "num_seqs": st.num_seqs,
+    if layers > 1:
+        step = (f"{layers} attention layers (Qwen2.5-0.5B stack), each a fused kv_append + "
+                f"split-KV paged decode over its own pool; tables, lengths and slots shared")
+        l2 = (f"inputs larger than L2: {layers} layer pools of "
+              f"{2 * st.k_pool.nbytes / 1e6:.0f} MB each (L2 129 MB)")
+    else:
+        l2 = (f"inputs larger than L2: {pools} rotating pool copies of "
+              f"{2 * st.k_pool.nbytes / 1e6:.0f} MB each (L2 129 MB)")
+    return {"workload": f"{st.name}: {name}" + (f" x {layers} layers" if layers > 1 else ""),
+            "layers": layers, "num_seqs": st.num_seqs,
             "context_tokens": int(st.context_lens.sum()),
             "max_context": int(st.context_lens.max()),
             "num_q_heads": st.num_q_heads, "num_kv_heads": st.num_kv_heads,
             "head_dim": st.head_dim, "block_size": st.block_size,
             "num_blocks": st.num_blocks, "step": step, "query_tokens": st.num_tokens,
-            "l2": (f"inputs larger than L2: {pools} rotating pool copies of "
-                   f"{2 * st.k_pool.nbytes / 1e6:.0f} MB each (L2 129 MB)")}
+            "l2": l2}
 
 
 def run_cpu_oracle(st, num_threads: int, max_seqs: int | None = None):
@@ -255,10 +263,13 @@ class Step:
 
     Decode workloads: one fused call (append the new token of every sequence
     and run the split-KV decode).  The mixed workload: ns_kv_append of all new
-    tokens, then ns_paged_attn_prefill over every span.
+    tokens, then ns_paged_attn_prefill over every span.  With ``layers`` > 1
+    (decode only) a step is that many fused calls, one per attention layer,
+    each over its own pool, q and new K/V (drawn on the device from a seeded
+    generator); block tables, lengths and slots are shared.
     """
 
-    def __init__(self, st, dev, npools):
+    def __init__(self, st, dev, npools, layers=1):
         import torch
         from paged_kv_decode_ns_gb300 import binding as nb
         self.nb, self.torch, self.st, self.dev = nb, torch, st, dev
@@ -288,8 +299,35 @@ class Step:
             self.inputs.append(self.qsl)
         # kernels per step: fused decode = 1; append + span rows + walk + tensor-core = 4
         self.launches = 1 if self.decode else 4
+        self.layers = layers
+        self.layer_io = []
+        if layers > 1:
+            if not self.decode:
+                raise ValueError("layers > 1 applies to decode workloads")
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(7000)
+
+            def rnd(t):
+                return torch.randn(t.shape, generator=gen, device=dev, dtype=torch.float32).to(t.dtype)
+            self.layer_io.append((k0, v0, self.q, self.k_new, self.v_new, self.out))
+            for _ in range(1, layers):
+                self.layer_io.append((rnd(k0), rnd(v0), rnd(self.q), rnd(self.k_new), rnd(self.v_new),
+                                      torch.empty_like(self.q)))
+            self.inputs = ([t for io in self.layer_io for t in io[2:5]]
+                           + [self.slots, self.tables, self.lens])
+            self.out = self.layer_io[-1][5]  # read back end to end: the last layer's output
+            self.launches = layers
+
+    def run_layer(self, layer, stream=None):
+        kp, vp, q, kn, vn, out = self.layer_io[layer]
+        self.nb.ns_kv_append_paged_attn_decode(q, kn, vn, self.slots, kp, vp, self.tables, self.lens,
+                                               self.st.scale, out, self.ws, stream=stream)
 
     def run(self, i, stream=None):
+        if self.layers > 1:
+            for layer in range(self.layers):
+                self.run_layer(layer, stream)
+            return
         kp, vp = self.pools[i % self.npools]
         if self.decode:
             self.nb.ns_kv_append_paged_attn_decode(self.q, self.k_new, self.v_new, self.slots, kp,
@@ -301,7 +339,9 @@ class Step:
                                           self.st.scale, self.out, self.ws, stream=stream)
 
     def run_dominant(self, i, stream=None):
-        """The dominant kernel alone: the fused decode, or the tensor-core prefill."""
+        """The dominant kernel alone: the fused decode (one layer's), or the tensor-core prefill."""
+        if self.layers > 1:
+            return self.run_layer(i % self.layers, stream)
         if self.decode:
             return self.run(i, stream)
         kp, vp = self.pools[i % self.npools]
@@ -334,7 +374,9 @@ def bench_ours(args):
     st = make_workload(args.workload)
     pool_bytes = 2 * st.k_pool.nbytes
     npools = max(1, args.pools if args.pools else math.ceil(2 * L2_BYTES / max(pool_bytes, 1)))
-    step = Step(st, dev, npools)
+    if args.layers > 1:
+        npools = 1  # the layers' pools are the rotation
+    step = Step(st, dev, npools, layers=args.layers)
     stream = torch.cuda.current_stream(dev)
 
     sampler = ClockSampler(local) if rank == 0 else None
@@ -427,8 +469,8 @@ def bench_ours(args):
     e2e_ms = e2.elapsed_time(e3)
     nb.raise_on_device_status()
 
-    kv_bytes = st.kv_read_bytes()
-    alg_bytes = st.algorithmic_bytes(with_append=True)
+    kv_bytes = st.kv_read_bytes() * args.layers
+    alg_bytes = st.algorithmic_bytes(with_append=True)  # one launch: one layer
     t_max, units = reduce_max_sum(dist, elapsed_ms, kv_bytes * args.steps, dev)
     te2e_max, units_e2e = reduce_max_sum(dist, e2e_ms, kv_bytes * n_e2e, dev)
     if rank != 0:
@@ -476,9 +518,12 @@ def bench_ours(args):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": t_max / args.steps, "us_per_step": 1e3 * t_max / args.steps,
         "graph_us_per_step": graph_us, "hbm_peak_frac": value / float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS)),
+        "layer_us": ({"eager": 1e3 * t_max / args.steps / args.layers,
+                      "graph": graph_us / args.layers if graph_us else None}
+                     if args.layers > 1 else None),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": st.dtype, "data": "synthetic (seeded; no dataset or weights involved)",
-        "config": workload_config(st, args.workload, npools),
+        "config": workload_config(st, args.workload, npools, args.layers),
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": units_e2e / (te2e_max * 1e-3) / 1e9, "unit": "GB/s",
@@ -534,6 +579,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_b256")
+    ap.add_argument("--layers", type=int, default=1,
+                    help="attention layers per step (decode workloads; 24 = the Qwen2.5-0.5B stack)")
     ap.add_argument("--pools", type=int, default=0, help="rotating pool copies (0 = enough to exceed 2x L2)")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--soak-s", type=float, default=1.0)

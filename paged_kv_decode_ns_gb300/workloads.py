@@ -281,6 +281,29 @@ def mixed_chunked_prefill(seed: int = 1005, **kw) -> PagedStep:
     return make_step(rng, lens, qlens, name="mixed_16dec_2x512chunk", **kw)
 
 
+# Attention layers of the Qwen2.5-0.5B stack (the pages' model): every layer
+# has its own K/V pool and its own q / new K / new V, while the block tables,
+# lengths and slots are the sequences' and so the same in every layer.
+QWEN25_05B_LAYERS = 24
+
+
+def layer_steps(st: PagedStep, num_layers: int, seed: int = 7000) -> list:
+    """``num_layers`` steps sharing ``st``'s block tables, lengths and slots;
+    layer 0 is ``st`` itself, layer l > 0 draws fresh pools, q and new K/V
+    (seeded, standard normal, rounded to the step's type)."""
+    out = [st]
+    for layer in range(1, num_layers):
+        rng = np.random.default_rng(seed + layer)
+        out.append(dataclasses.replace(
+            st, name=f"{st.name}_layer{layer}",
+            q=_randn_bits(rng, st.q.shape, st.dtype),
+            k_pool=_randn_bits(rng, st.k_pool.shape, st.dtype),
+            v_pool=_randn_bits(rng, st.v_pool.shape, st.dtype),
+            k_new=_randn_bits(rng, st.k_new.shape, st.dtype),
+            v_new=_randn_bits(rng, st.v_new.shape, st.dtype)))
+    return out
+
+
 WORKLOADS = {
     "tiny_decode": tiny_decode,
     "decode_b32": decode_batch32,
