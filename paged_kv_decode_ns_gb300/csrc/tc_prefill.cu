@@ -10,19 +10,23 @@
 // heads of one GQA group packed into M = QT*G <= 128 rows (row r = token r/G,
 // head r%G), so every K/V tile is loaded once for all heads of the group.
 //
-//   warp 5   producer: TMA 3D load of the Q tile; per 128-key tile, one TMA 2D
+//   warp 9   producer: TMA 3D load of the Q tile; per 128-key tile, one TMA 2D
 //            load per pool block for K and for V (128-byte swizzle), into a
 //            2-stage ring;
-//   warp 4   allocates 256 TMEM columns; lane 0 issues tcgen05.mma:
+//   warp 8   allocates 256 TMEM columns; lane 0 issues tcgen05.mma:
 //              S[128x128] = Q K^T   (4 steps of K=16, A and B K-major)
 //              O[128x64] += P V     (8 steps of K=16, P K-major from shared
 //                                    memory, V MN-major)
 //            and commits each group to an mbarrier;
-//   warps 0-3 softmax: thread t owns row t (TMEM lane t).  It reads its S row
-//            from TMEM, masks keys past its position, keeps a running max and
-//            sum (max moves lazily, by more than 8 in log2 units), writes P as
-//            fp16/bf16 into a 128-byte-swizzled K-major panel, rescales its O
-//            row in TMEM when the max moved, and finally writes O / sum.
+//   warps 0-7 softmax: thread t owns row t % 128 (TMEM lane) and key columns
+//            64 (t / 128) .. +63 of each tile.  It reads its half of the S row
+//            from TMEM, masks keys past its position, and with the other half
+//            of the row (through shared memory) keeps a running max (moving
+//            lazily, by more than 8 in log2 units); it keeps its share of the
+//            sum, writes its half of P as fp16/bf16 into its 128-byte-swizzled
+//            K-major panel, rescales its half of the O row in TMEM when the
+//            max moved, and finally writes its half of O / sum.  (Two
+//            warpgroups: one took ~1.5 us of the ~1.9 us per tile.)
 // Values of keys past the context are zeroed in shared memory before the PV
 // product, so undefined (even NaN) pool slots never reach the accumulator.
 #include <cstddef>
@@ -39,8 +43,12 @@ constexpr int kKT = 128;         // keys per K/V tile
 constexpr int kRows = 128;       // MMA M
 constexpr int kTmemCols = 256;   // S: columns [0,128), O: [128,192)
 constexpr int kTmemO = 128;
-constexpr int kStages = 2;
-constexpr int kThreads = 192;    // warps 0-3 softmax, 4 MMA, 5 producer
+constexpr int kStages = 3;       // K/V tiles in flight: a tile's copies take ~2 us under load
+constexpr int kSoftmaxThreads = 256;  // two warpgroups: key columns 0..63 and 64..127 of each row
+constexpr int kHalf = kKT / 2;         // key columns per softmax thread
+constexpr int kMmaWarp = 8;
+constexpr int kProducerWarp = 9;
+constexpr int kThreads = 320;          // warps 0-7 softmax, 8 MMA, 9 producer
 constexpr float kSlack = 8.0f;   // lazy rescale: the max moves by more than this (log2 units)
 
 struct PrefillParams {
@@ -80,6 +88,11 @@ struct alignas(1024) PrefillSmem {
     uint64_t s_free;
     uint64_t p_full;
     uint64_t o_done;
+    // the two softmax halves of a row exchange their maxima every tile (and
+    // their sums at the end) through these, double-buffered by tile parity
+    uint64_t xbar;
+    float xmax[2][2][kRows];  // [tile parity][half][row]
+    float xl[2][kRows];       // [half][row]
     // rank 1's unnormalised rows, written remotely into rank 0 with 16-byte stores
     alignas(16) float rem_o[kRows][kHeadDim];
     float rem_m[kRows];
@@ -102,6 +115,8 @@ constexpr size_t smem_bytes()
 {
     return sizeof(PrefillSmem<NP>) + 1024;  // + alignment slack
 }
+
+static_assert(smem_bytes<1>() <= 227 * 1024 && smem_bytes<2>() <= 227 * 1024, "prefill shared memory");
 
 template <int NP>
 __device__ __forceinline__ PrefillSmem<NP> &smem_of(unsigned char *raw)
@@ -170,7 +185,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = P.group;
 
-    if (warp == 5) {
+    if (warp == kProducerWarp) {
         find_unit(P, sm, lane);
         __syncwarp();
         if (lane == 0 && sm.u_ok == 1) {
@@ -203,10 +218,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(&sm.kv_empty[i], 1);
         }
         mbar_init(&sm.s_full, 1);
-        mbar_init(&sm.s_free, 128);
-        mbar_init(&sm.p_full, 128);
+        mbar_init(&sm.s_free, kSoftmaxThreads);
+        mbar_init(&sm.p_full, kSoftmaxThreads);
         mbar_init(&sm.o_done, 1);
-        mbar_init(&sm.rem_bar, 128);
+        mbar_init(&sm.xbar, kSoftmaxThreads);
+        mbar_init(&sm.rem_bar, kSoftmaxThreads);
         mbar_init_fence();
     }
     __syncthreads();
@@ -221,7 +237,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4 *>(sm.q + threadIdx.x * kRowBytes + b) = make_uint4(0, 0, 0, 0);
         tc::fence_async_smem();
     }
-    if (warp == 4) {
+    if (warp == kMmaWarp) {
         tc::tmem_alloc(&sm.tmem_base, kTmemCols);
         tc::tmem_relinquish();
     }
@@ -236,7 +252,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t tmem = sm.tmem_base;
     const int ab_fmt = T::code == NS_BF16 ? 1 : 0;
 
-    if (warp == 5) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && tiles > 0) {
             tc::prefetch_tensormap(&tm_q);
@@ -292,7 +308,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
         }
         __syncwarp();
-    } else if (warp == 4) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0 && tiles > 0) {
             const uint32_t idesc_s = tc::idesc_f16(kRows, kKT, ab_fmt, false);
@@ -347,14 +363,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax
-        const int r = threadIdx.x;  // row == TMEM lane
+        const int r = threadIdx.x & (kRows - 1);  // row == TMEM lane
+        const int hf = threadIdx.x / kRows;       // 0: key columns 0..63, 1: 64..127
+        const int c0 = hf * kHalf;
         const int tok = r / G;
         const bool row_ok = r < P.qt * G && i0 + tok < n;
         const int pos = row_ok ? prefix + i0 + tok : -1;
         const int pos_lo = prefix + i0;  // smallest position in the tile
-        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-        float m = -INFINITY, l = 0.f;
+        const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        float m = -INFINITY, l = 0.f;  // l: this half's share of the row sum
         bool ok = true;
+        int xphase = 0;  // phases of xbar this thread has completed
         for (int j = 0; j < tiles; ++j) {
             const int stage = j % kStages;
             if (!mbar_wait(&sm.s_full, (uint32_t)j & 1u)) {
@@ -362,28 +381,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 break;
             }
             tc::fence_after_sync();
-            float sv[kKT];
+            float sv[kHalf];
 #pragma unroll
-            for (int c = 0; c < kKT / 32; ++c)
-                tc::tmem_ld32(lane_addr + c * 32, *reinterpret_cast<float(*)[32]>(&sv[c * 32]));
+            for (int c = 0; c < kHalf / 32; ++c)
+                tc::tmem_ld32(lane_addr + c0 + c * 32, *reinterpret_cast<float(*)[32]>(&sv[c * 32]));
             tc::tmem_ld_wait();
             tc::fence_before_sync();
             mbar_arrive(&sm.s_free);
 
-            const int kbase = (j0 + j) * kKT;
-            const bool masked = kbase + kKT - 1 > pos_lo;
-            float tmax = -INFINITY;
+            const int tbase = (j0 + j) * kKT;  // first key of the tile
+            const int kbase = tbase + c0;      // first key of this half
+            const bool masked = tbase + kKT - 1 > pos_lo;
+            // four independent running maxima (no long dependent chain)
+            float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
             if (masked) {
 #pragma unroll
-                for (int c = 0; c < kKT; ++c) {
+                for (int c = 0; c < kHalf; ++c) {
                     sv[c] = (kbase + c <= pos) ? sv[c] : -INFINITY;
-                    tmax = fmaxf(tmax, sv[c]);
+                    tm[c & 3] = fmaxf(tm[c & 3], sv[c]);
                 }
             } else {
 #pragma unroll
-                for (int c = 0; c < kKT; ++c)
-                    tmax = fmaxf(tmax, sv[c]);
+                for (int c = 0; c < kHalf; ++c)
+                    tm[c & 3] = fmaxf(tm[c & 3], sv[c]);
             }
+            const float hmax = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]));
+            // the row max over both halves (the two threads compute the same m)
+            sm.xmax[j & 1][hf][r] = hmax;
+            mbar_arrive(&sm.xbar);
+            if (!mbar_wait(&sm.xbar, (uint32_t)j & 1u)) {
+                ok = false;
+                break;
+            }
+            ++xphase;
+            float tmax = fmaxf(hmax, sm.xmax[j & 1][hf ^ 1][r]);
             tmax *= P.scale_log2;  // scale > 0 keeps the order
             float m_new = m;
             if (tmax > m + kSlack)
@@ -393,10 +424,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             l *= (m_new != m) ? alpha : 1.f;
             m = m_new;
 
-            uint32_t pk[kKT / 2];
-            float lsum = 0.f;
+            uint32_t pk[kHalf / 2];
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};  // four independent partial sums
 #pragma unroll
-            for (int c = 0; c < kKT; c += 2) {
+            for (int c = 0; c < kHalf; c += 2) {
                 // even columns on the MUFU pipe, odd columns on the FMA pipe
                 float p0 = fast_exp2(fmaf(sv[c], P.scale_log2, -m));
                 float p1 = exp2_fma(fmaf(sv[c + 1], P.scale_log2, -m));
@@ -404,7 +435,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     p0 = sv[c] > -INFINITY ? p0 : 0.f;
                     p1 = sv[c + 1] > -INFINITY ? p1 : 0.f;
                 }
-                lsum += p0 + p1;
+                ls[(c >> 1) & 3] += p0 + p1;
                 pk[c >> 1] = pack2<T>(p0, p1);
                 if (NP == 2) {
                     // keep the rounding residue of P for the second product
@@ -413,7 +444,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     sv[c + 1] = p1 - hi.y;
                 }
             }
-            l += lsum;
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
 
             // PV of the previous tile must be done before P and O are touched.
             if (j > 0 && !mbar_wait(&sm.o_done, (uint32_t)(j - 1) & 1u)) {
@@ -422,84 +453,92 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             tc::fence_after_sync();
             if (__any_sync(0xffffffffu, rescale)) {
+                // this half rescales O columns 32 hf .. 32 hf + 31 of the row
                 const float a = rescale ? alpha : 1.f;
+                float ov[32];
+                tc::tmem_ld32(lane_addr + kTmemO + hf * 32, ov);
+                tc::tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < kHeadDim / 32; ++c) {
-                    float ov[32];
-                    tc::tmem_ld32(lane_addr + kTmemO + c * 32, ov);
-                    tc::tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        ov[e] *= a;
-                    tc::tmem_st32(lane_addr + kTmemO + c * 32, ov);
-                }
+                for (int e = 0; e < 32; ++e)
+                    ov[e] *= a;
+                tc::tmem_st32(lane_addr + kTmemO + hf * 32, ov);
                 tc::tmem_st_wait();
             }
-            // P row r: 16-byte chunk q (keys 8q..8q+7) of panel q/8 at chunk (q%8) ^ (r%8)
+            // P row r, this half's keys: 16-byte chunk q (keys c0+8q..+7) of
+            // panel hf at chunk q ^ (r % 8)
 #pragma unroll
-            for (int q = 0; q < kKT / 8; ++q) {
-                uint8_t *dst = sm.p[0][q >> 3] + r * 128 + (((q & 7) ^ (r & 7)) << 4);
+            for (int q = 0; q < kHalf / 8; ++q) {
+                uint8_t *dst = sm.p[0][hf] + r * 128 + ((q ^ (r & 7)) << 4);
                 *reinterpret_cast<uint4 *>(dst) =
                     make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
             }
             if (NP == 2) {
 #pragma unroll
-                for (int q = 0; q < kKT / 8; ++q) {
-                    uint8_t *dst = sm.p[NP - 1][q >> 3] + r * 128 + (((q & 7) ^ (r & 7)) << 4);
+                for (int q = 0; q < kHalf / 8; ++q) {
+                    uint8_t *dst = sm.p[NP - 1][hf] + r * 128 + ((q ^ (r & 7)) << 4);
                     *reinterpret_cast<uint4 *>(dst) =
                         make_uint4(pack2<T>(sv[8 * q], sv[8 * q + 1]), pack2<T>(sv[8 * q + 2], sv[8 * q + 3]),
                                    pack2<T>(sv[8 * q + 4], sv[8 * q + 5]), pack2<T>(sv[8 * q + 6], sv[8 * q + 7]));
                 }
             }
             // Values of keys past the context, or of blocks that were not
-            // loaded, must be zero: P is zero there but 0 * NaN is not.
+            // loaded, must be zero: P is zero there but 0 * NaN is not.  This
+            // half clears bytes 64 hf .. 64 hf + 63 of value row r.
             if (masked || sm.loaded[stage] != (1u << (kKT / BS)) - 1u) {
                 if (!mbar_wait(&sm.kv_full[stage], (uint32_t)(j / kStages) & 1u)) {
                     ok = false;
                     break;
                 }
-                const int key = kbase + r;
+                const int key = tbase + r;
                 const bool blk_loaded = (sm.loaded[stage] >> (r / BS)) & 1u;
                 if (key >= L || !blk_loaded) {
 #pragma unroll
-                    for (int b = 0; b < kRowBytes; b += 16)
-                        *reinterpret_cast<uint4 *>(sm.v[stage] + r * kRowBytes + b) = make_uint4(0, 0, 0, 0);
+                    for (int b = 0; b < kRowBytes / 2; b += 16)
+                        *reinterpret_cast<uint4 *>(sm.v[stage] + r * kRowBytes + hf * (kRowBytes / 2) + b) =
+                            make_uint4(0, 0, 0, 0);
                 }
             }
             tc::fence_async_smem();
             tc::fence_before_sync();
             mbar_arrive(&sm.p_full);
         }
-        // ---- epilogue: this CTA's unnormalised rows (zero when it had no tile)
-        float ov[kHeadDim];
+        // ---- epilogue: this CTA's unnormalised half rows (zero when it had no tile)
+        float ov[32];  // O columns 32 hf .. 32 hf + 31 of row r
         if (ok && tiles > 0) {
             ok = mbar_wait(&sm.o_done, (uint32_t)(tiles - 1) & 1u);
             if (ok) {
                 tc::fence_after_sync();
-#pragma unroll
-                for (int c = 0; c < kHeadDim / 32; ++c)
-                    tc::tmem_ld32(lane_addr + kTmemO + c * 32, *reinterpret_cast<float(*)[32]>(&ov[c * 32]));
+                tc::tmem_ld32(lane_addr + kTmemO + hf * 32, ov);
                 tc::tmem_ld_wait();
             }
         }
         if (!ok || tiles == 0) {
 #pragma unroll
-            for (int c = 0; c < kHeadDim; ++c)
+            for (int c = 0; c < 32; ++c)
                 ov[c] = 0.f;
         }
+        // the row sum over both halves
+        sm.xl[hf][r] = l;
+        mbar_arrive(&sm.xbar);
+        if (ok && mbar_wait(&sm.xbar, (uint32_t)xphase & 1u))
+            l += sm.xl[hf ^ 1][r];
+        else
+            ok = false;
         if (!ok)
             raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
         if (rank != 0) {
-            // rank 1: hand (max, sum, rows) to rank 0 through distributed shared memory
-            const uint32_t dst = tc::map_to_rank(&sm.rem_o[r][0], 0);
+            // rank 1: hand (max, sum, half rows) to rank 0 through distributed shared memory
+            const uint32_t dst = tc::map_to_rank(&sm.rem_o[r][hf * 32], 0);
 #pragma unroll
-            for (int c = 0; c < kHeadDim; c += 4)
+            for (int c = 0; c < 32; c += 4)
                 tc::st_cluster_v4(dst + c * 4, ov[c], ov[c + 1], ov[c + 2], ov[c + 3]);
-            tc::st_cluster_f32(tc::map_to_rank(&sm.rem_m[r], 0), m);
-            tc::st_cluster_f32(tc::map_to_rank(&sm.rem_l[r], 0), l);
+            if (hf == 0) {
+                tc::st_cluster_f32(tc::map_to_rank(&sm.rem_m[r], 0), m);
+                tc::st_cluster_f32(tc::map_to_rank(&sm.rem_l[r], 0), l);
+            }
             tc::mbar_arrive_remote(tc::map_to_rank(&sm.rem_bar, 0));
         } else if (tc::mbar_wait_cluster(&sm.rem_bar, 0)) {
-            // rank 0: log-sum-exp merge of the two halves, then O / l
+            // rank 0: log-sum-exp merge of the two key halves, then O / l
             const float m1 = sm.rem_m[r], l1 = sm.rem_l[r];
             const float M = fmaxf(m, m1);
             const float f0 = (m > -INFINITY) ? fast_exp2(m - M) : 0.f;
@@ -508,10 +547,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const float inv = 1.f / (f0 * l + f1 * l1);
                 const float a0 = f0 * inv, a1 = f1 * inv;
                 const long long tok_g = __ldg(P.qsl + s) + i0 + tok;
-                uint16_t *o = P.out + (tok_g * P.num_q_heads + (long long)h * G + (r % G)) * kHeadDim;
-                const float *o1 = &sm.rem_o[r][0];
+                uint16_t *o = P.out + (tok_g * P.num_q_heads + (long long)h * G + (r % G)) * kHeadDim + hf * 32;
+                const float *o1 = &sm.rem_o[r][hf * 32];
 #pragma unroll
-                for (int c = 0; c < kHeadDim; c += 8) {
+                for (int c = 0; c < 32; c += 8) {
                     uint4 w;
                     w.x = pack2<T>(fmaf(ov[c], a0, o1[c] * a1), fmaf(ov[c + 1], a0, o1[c + 1] * a1));
                     w.y = pack2<T>(fmaf(ov[c + 2], a0, o1[c + 2] * a1), fmaf(ov[c + 3], a0, o1[c + 3] * a1));
@@ -526,7 +565,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 4) {
+    if (warp == kMmaWarp) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
