@@ -244,6 +244,7 @@ __device__ __forceinline__ uint16_t pack1<F16>(float a)
 // Packed fp32 (two lanes per instruction on sm_100-class GPUs).
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 __device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 
 __device__ __forceinline__ float fast_exp2(float x)
 {

@@ -15,18 +15,19 @@
 //            2-stage ring;
 //   warp 8   allocates 256 TMEM columns; lane 0 issues tcgen05.mma:
 //              S[128x128] = Q K^T   (4 steps of K=16, A and B K-major)
-//              O[128x64] += P V     (8 steps of K=16, P K-major from shared
-//                                    memory, V MN-major)
+//              O_h[128x64] += P_h V_h (4 steps of K=16 per key half h,
+//                                    P K-major from shared memory, V MN-major)
 //            and commits each group to an mbarrier;
 //   warps 0-7 softmax: thread t owns row t % 128 (TMEM lane) and key columns
-//            64 (t / 128) .. +63 of each tile.  It reads its half of the S row
-//            from TMEM, masks keys past its position, and with the other half
-//            of the row (through shared memory) keeps a running max (moving
-//            lazily, by more than 8 in log2 units); it keeps its share of the
-//            sum, writes its half of P as fp16/bf16 into its 128-byte-swizzled
-//            K-major panel, rescales its half of the O row in TMEM when the
-//            max moved, and finally writes its half of O / sum.  (Two
-//            warpgroups: one took ~1.5 us of the ~1.9 us per tile.)
+//            64 h .. 64 h + 63 of each tile, h = t / 128.  Each key half has
+//            its own running max (moving lazily, by more than 8 in log2 units),
+//            sum and O accumulator (TMEM), so the halves never wait on each
+//            other; it reads its half of the S row, masks keys past its
+//            position, writes its half of P as fp16/bf16 into its
+//            128-byte-swizzled K-major panel and rescales its O when its max
+//            moved.  At the end the two halves of a row are merged by
+//            log-sum-exp and each writes half of the output row.  (One
+//            warpgroup for all 128 columns took ~1.5 us of ~1.9 us per tile.)
 // Values of keys past the context are zeroed in shared memory before the PV
 // product, so undefined (even NaN) pool slots never reach the accumulator.
 #include <cstddef>
@@ -41,7 +42,7 @@ namespace {
 
 constexpr int kKT = 128;         // keys per K/V tile
 constexpr int kRows = 128;       // MMA M
-constexpr int kTmemCols = 256;   // S: columns [0,128), O: [128,192)
+constexpr int kTmemCols = 256;   // S: columns [0,128); O of key half h: [128 + 64h, 192 + 64h)
 constexpr int kTmemO = 128;
 constexpr int kStages = 3;       // K/V tiles in flight: a tile's copies take ~2 us under load
 constexpr int kSoftmaxThreads = 256;  // two warpgroups: key columns 0..63 and 64..127 of each row
@@ -50,6 +51,10 @@ constexpr int kMmaWarp = 8;
 constexpr int kProducerWarp = 9;
 constexpr int kThreads = 320;          // warps 0-7 softmax, 8 MMA, 9 producer
 constexpr float kSlack = 8.0f;   // lazy rescale: the max moves by more than this (log2 units)
+// 1: every exponential on the MUFU pipe; 0: odd columns as an FMA-pipe polynomial
+#ifndef NS_PREFILL_EXP_MUFU
+#define NS_PREFILL_EXP_MUFU 1  // measured 12% faster: the polynomial's instructions cost more than MUFU
+#endif
 
 struct PrefillParams {
     const int32_t *qsl;
@@ -88,11 +93,11 @@ struct alignas(1024) PrefillSmem {
     uint64_t s_free;
     uint64_t p_full;
     uint64_t o_done;
-    // the two softmax halves of a row exchange their maxima every tile (and
-    // their sums at the end) through these, double-buffered by tile parity
+    // the two softmax halves of a row exchange their maxima and sums once,
+    // at the end, through these
     uint64_t xbar;
-    float xmax[2][2][kRows];  // [tile parity][half][row]
-    float xl[2][kRows];       // [half][row]
+    float xm[2][kRows];  // [half][row]
+    float xl[2][kRows];
     // rank 1's unnormalised rows, written remotely into rank 0 with 16-byte stores
     alignas(16) float rem_o[kRows][kHeadDim];
     float rem_m[kRows];
@@ -349,10 +354,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int part = 0; part < NP; ++part)
 #pragma unroll
                     for (int kk = 0; kk < kKT / 16; ++kk) {
+                        // keys 16 kk ..: key half kk / 4 accumulates into its own O
                         const uint32_t p_addr = smem_addr(sm.p[part][kk >> 2]) + (kk & 3) * 32;
-                        tc::mma_ss(tmem + kTmemO, tc::desc_sw128(p_addr),
+                        tc::mma_ss(tmem + kTmemO + (kk >> 2) * kHeadDim, tc::desc_sw128(p_addr),
                                    tc::desc_sw128(v_addr + kk * 16 * kRowBytes), idesc_o,
-                                   (j > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                                   (j > 0 || part > 0 || (kk & 3) > 0) ? 1u : 0u);
                     }
                 tc::mma_commit(&sm.o_done);
                 tc::mma_commit(&sm.kv_empty[j % kStages]);
@@ -371,9 +377,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int pos = row_ok ? prefix + i0 + tok : -1;
         const int pos_lo = prefix + i0;  // smallest position in the tile
         const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-        float m = -INFINITY, l = 0.f;  // l: this half's share of the row sum
+        float m = -INFINITY, l = 0.f;  // this key half's running max and sum
         bool ok = true;
-        int xphase = 0;  // phases of xbar this thread has completed
         for (int j = 0; j < tiles; ++j) {
             const int stage = j % kStages;
             if (!mbar_wait(&sm.s_full, (uint32_t)j & 1u)) {
@@ -405,16 +410,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < kHalf; ++c)
                     tm[c & 3] = fmaxf(tm[c & 3], sv[c]);
             }
-            const float hmax = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]));
-            // the row max over both halves (the two threads compute the same m)
-            sm.xmax[j & 1][hf][r] = hmax;
-            mbar_arrive(&sm.xbar);
-            if (!mbar_wait(&sm.xbar, (uint32_t)j & 1u)) {
-                ok = false;
-                break;
-            }
-            ++xphase;
-            float tmax = fmaxf(hmax, sm.xmax[j & 1][hf ^ 1][r]);
+            float tmax = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]));
             tmax *= P.scale_log2;  // scale > 0 keeps the order
             float m_new = m;
             if (tmax > m + kSlack)
@@ -425,17 +421,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             m = m_new;
 
             uint32_t pk[kHalf / 2];
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};  // four independent partial sums
+            // pairs of columns in packed fp32 (scale and shift, sums); two
+            // independent partial sums
+            const float2 sc2 = make_float2(P.scale_log2, P.scale_log2);
+            const float2 nm2 = make_float2(-m, -m);
+            float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
             for (int c = 0; c < kHalf; c += 2) {
-                // even columns on the MUFU pipe, odd columns on the FMA pipe
-                float p0 = fast_exp2(fmaf(sv[c], P.scale_log2, -m));
-                float p1 = exp2_fma(fmaf(sv[c + 1], P.scale_log2, -m));
+                const float2 z = ffma2(make_float2(sv[c], sv[c + 1]), sc2, nm2);
+                float p0 = fast_exp2(z.x);
+#if NS_PREFILL_EXP_MUFU
+                float p1 = fast_exp2(z.y);
+#else
+                float p1 = exp2_fma(z.y);  // odd columns on the FMA pipe
+#endif
                 if (masked) {
                     p0 = sv[c] > -INFINITY ? p0 : 0.f;
                     p1 = sv[c + 1] > -INFINITY ? p1 : 0.f;
                 }
-                ls[(c >> 1) & 3] += p0 + p1;
+                ls2[(c >> 1) & 1] = fadd2(ls2[(c >> 1) & 1], make_float2(p0, p1));
                 pk[c >> 1] = pack2<T>(p0, p1);
                 if (NP == 2) {
                     // keep the rounding residue of P for the second product
@@ -444,7 +448,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     sv[c + 1] = p1 - hi.y;
                 }
             }
-            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            l += (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
 
             // PV of the previous tile must be done before P and O are touched.
             if (j > 0 && !mbar_wait(&sm.o_done, (uint32_t)(j - 1) & 1u)) {
@@ -453,15 +457,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             tc::fence_after_sync();
             if (__any_sync(0xffffffffu, rescale)) {
-                // this half rescales O columns 32 hf .. 32 hf + 31 of the row
+                // this key half's O row
                 const float a = rescale ? alpha : 1.f;
-                float ov[32];
-                tc::tmem_ld32(lane_addr + kTmemO + hf * 32, ov);
-                tc::tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    ov[e] *= a;
-                tc::tmem_st32(lane_addr + kTmemO + hf * 32, ov);
+                for (int c = 0; c < kHeadDim / 32; ++c) {
+                    float ov[32];
+                    tc::tmem_ld32(lane_addr + kTmemO + hf * kHeadDim + c * 32, ov);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        ov[e] *= a;
+                    tc::tmem_st32(lane_addr + kTmemO + hf * kHeadDim + c * 32, ov);
+                }
                 tc::tmem_st_wait();
             }
             // P row r, this half's keys: 16-byte chunk q (keys c0+8q..+7) of
@@ -502,14 +509,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc::fence_before_sync();
             mbar_arrive(&sm.p_full);
         }
-        // ---- epilogue: this CTA's unnormalised half rows (zero when it had no tile)
-        float ov[32];  // O columns 32 hf .. 32 hf + 31 of row r
+        // ---- epilogue: merge the row's two key halves (log-sum-exp), then this
+        // CTA's unnormalised output columns 32 hf .. 32 hf + 31 (zero when it had no tile)
+        sm.xm[hf][r] = m;
+        sm.xl[hf][r] = l;
+        mbar_arrive(&sm.xbar);
+        float ov[32];
+        float fa = 0.f, fb = 0.f;  // factors of key halves 0 and 1
+        if (ok && mbar_wait(&sm.xbar, 0)) {
+            const float ma = sm.xm[0][r], mb = sm.xm[1][r];
+            const float M = fmaxf(ma, mb);
+            fa = (ma > -INFINITY) ? fast_exp2(ma - M) : 0.f;
+            fb = (mb > -INFINITY) ? fast_exp2(mb - M) : 0.f;
+            l = fa * sm.xl[0][r] + fb * sm.xl[1][r];
+            m = M;
+        } else {
+            ok = false;
+        }
         if (ok && tiles > 0) {
             ok = mbar_wait(&sm.o_done, (uint32_t)(tiles - 1) & 1u);
             if (ok) {
                 tc::fence_after_sync();
+                float ob[32];
                 tc::tmem_ld32(lane_addr + kTmemO + hf * 32, ov);
+                tc::tmem_ld32(lane_addr + kTmemO + kHeadDim + hf * 32, ob);
                 tc::tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    ov[c] = fmaf(fa, ov[c], fb * ob[c]);
             }
         }
         if (!ok || tiles == 0) {
@@ -517,13 +544,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 32; ++c)
                 ov[c] = 0.f;
         }
-        // the row sum over both halves
-        sm.xl[hf][r] = l;
-        mbar_arrive(&sm.xbar);
-        if (ok && mbar_wait(&sm.xbar, (uint32_t)xphase & 1u))
-            l += sm.xl[hf ^ 1][r];
-        else
-            ok = false;
         if (!ok)
             raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
         if (rank != 0) {
