@@ -56,14 +56,14 @@ KERNEL_SOURCES = {
                           "paged_kv_decode_ns_gb300/csrc/tcgen05.cuh", "include/ns_paged.h"],
 }
 PROFILED_TRAFFIC = {
-    # profiles/paged_decode_b256_bf16.md: 238.97 MB read + 3.59 MB written
+    # profiles/paged_decode_b256_bf16.md: 238.97 MB read + 3.68 MB written
     ("decode_b256", "paged_decode_kernel"): {
-        "sources_sha256": "4d047ef9677b0b5605bad23ccc3fbcf605ecd9074195547bff95391778a0205d",
-        "bytes": 242556672},
-    # profiles/tc_prefill_mixed_f16.md: 4.75 MB read, 0 written
+        "sources_sha256": "891c00d5fbaf05296a11ebd67b61e9559fd9b79b6f357b3b90c225503f1ede0d",
+        "bytes": 242653184},
+    # profiles/tc_prefill_mixed_f16.md: 4.73 MB read, 0 written
     ("mixed_chunked_prefill", "tc_prefill_kernel"): {
-        "sources_sha256": "27a0c16c4b361e2c641ec001de08657804a0063eb78c9443c526c62768ae7a37",
-        "bytes": 4748032},
+        "sources_sha256": "c17804412889bd3c206b568c29b090446dd56245c39cdaba325d857ad01cb873",
+        "bytes": 4729088},
 }
 
 
