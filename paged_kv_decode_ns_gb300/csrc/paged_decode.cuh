@@ -560,6 +560,8 @@ __device__ __forceinline__ void process_step(const uint16_t *__restrict__ kb,
 //     accumulates them over the pieces with 16-byte loads, several pieces in
 //     flight, each scaled by its factor taken from the lane that read it.
 // ---------------------------------------------------------------------------
+constexpr int kMergeBatch = 8;  // pieces whose output loads are in flight together
+
 template <typename T>
 __device__ __forceinline__ const float *piece_record(const DecodeParams &P, long long c0, int k, bool c0_second)
 {
@@ -624,20 +626,31 @@ __device__ void merge_pieces(const DecodeParams &P, long long c0, long long c1, 
                 f[j] = 0.f;
         }
         const int nk = min(32, npieces - k0);
-#pragma unroll 4
-        for (int kk = 0; kk < nk; ++kk) {
-            const float4 *r = reinterpret_cast<const float4 *>(piece_record<T>(P, c0, k0 + kk, c0_second) +
-                                                               2 * kMaxGroup) + lane;
+        // 8 pieces per round: all their loads are issued before any is used,
+        // so a merge of many pieces costs a few L2 round trips, not one each
+        for (int kb = 0; kb < nk; kb += kMergeBatch) {
+            float4 a[kMergeBatch][4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float fe = __shfl_sync(0xffffffffu, f[2 * i], kk);
-                const float fo = __shfl_sync(0xffffffffu, f[2 * i + 1], kk);
-                const float fk = hsel ? fo : fe;
-                const float4 a = (2 * i + hsel < G) ? __ldcg(r + 32 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
-                o[i].x = fmaf(fk, a.x, o[i].x);
-                o[i].y = fmaf(fk, a.y, o[i].y);
-                o[i].z = fmaf(fk, a.z, o[i].z);
-                o[i].w = fmaf(fk, a.w, o[i].w);
+            for (int u = 0; u < kMergeBatch; ++u) {
+                const int kk = kb + u < nk ? kb + u : 0;
+                const float4 *r = reinterpret_cast<const float4 *>(piece_record<T>(P, c0, k0 + kk, c0_second) +
+                                                                   2 * kMaxGroup) + lane;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    a[u][i] = (kb + u < nk && 2 * i + hsel < G) ? __ldcg(r + 32 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < kMergeBatch; ++u) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float fe = __shfl_sync(0xffffffffu, f[2 * i], (kb + u) & 31);
+                    const float fo = __shfl_sync(0xffffffffu, f[2 * i + 1], (kb + u) & 31);
+                    const float fk = kb + u < nk ? (hsel ? fo : fe) : 0.f;
+                    o[i].x = fmaf(fk, a[u][i].x, o[i].x);
+                    o[i].y = fmaf(fk, a[u][i].y, o[i].y);
+                    o[i].z = fmaf(fk, a[u][i].z, o[i].z);
+                    o[i].w = fmaf(fk, a[u][i].w, o[i].w);
+                }
             }
         }
     }
