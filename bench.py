@@ -269,7 +269,7 @@ class Step:
     generator); block tables, lengths and slots are shared.
     """
 
-    def __init__(self, st, dev, npools, layers=1):
+    def __init__(self, st, dev, npools, layers=1, overlap=False):
         import torch
         from paged_kv_decode_ns_gb300 import binding as nb
         self.nb, self.torch, self.st, self.dev = nb, torch, st, dev
@@ -300,6 +300,10 @@ class Step:
         # kernels per step: fused decode = 1; append + span rows + walk + tensor-core = 4
         self.launches = 1 if self.decode else 4
         self.layers = layers
+        self.config = None
+        if overlap:  # programmatic dependent launches (see ns_decode_config.overlap_prologue)
+            self.config = nb.DecodeConfig()
+            self.config.overlap_prologue = 1
         self.layer_io = []
         if layers > 1:
             if not self.decode:
@@ -321,7 +325,8 @@ class Step:
     def run_layer(self, layer, stream=None):
         kp, vp, q, kn, vn, out = self.layer_io[layer]
         self.nb.ns_kv_append_paged_attn_decode(q, kn, vn, self.slots, kp, vp, self.tables, self.lens,
-                                               self.st.scale, out, self.ws, stream=stream)
+                                               self.st.scale, out, self.ws, config=self.config,
+                                               stream=stream)
 
     def run(self, i, stream=None):
         if self.layers > 1:
@@ -332,7 +337,8 @@ class Step:
         if self.decode:
             self.nb.ns_kv_append_paged_attn_decode(self.q, self.k_new, self.v_new, self.slots, kp,
                                                    vp, self.tables, self.lens, self.st.scale,
-                                                   self.out, self.ws, stream=stream)
+                                                   self.out, self.ws, config=self.config,
+                                                   stream=stream)
         else:
             self.nb.ns_kv_append(self.k_new, self.v_new, self.slots, kp, vp, stream=stream)
             self.nb.ns_paged_attn_prefill(self.q, self.qsl, kp, vp, self.tables, self.lens,
@@ -376,7 +382,7 @@ def bench_ours(args):
     npools = max(1, args.pools if args.pools else math.ceil(2 * L2_BYTES / max(pool_bytes, 1)))
     if args.layers > 1:
         npools = 1  # the layers' pools are the rotation
-    step = Step(st, dev, npools, layers=args.layers)
+    step = Step(st, dev, npools, layers=args.layers, overlap=args.overlap)
     stream = torch.cuda.current_stream(dev)
 
     sampler = ClockSampler(local) if rank == 0 else None
@@ -398,6 +404,25 @@ def bench_ours(args):
     torch.cuda.synchronize(dev)
     barrier(dist)
     elapsed_ms = e0.elapsed_time(e1)
+
+    # ---- the same steps launched as programmatic dependents (opt-in in the
+    # API: each launch's prologue may overlap the previous kernel's tail)
+    overlap_us = None
+    if step.decode and not args.overlap and args.steps >= 10:
+        plain_cfg, step.config = step.config, nb.DecodeConfig()
+        step.config.overlap_prologue = 1
+        n_ov = min(args.steps, 2000)
+        for i in range(20):
+            step.run(i)
+        torch.cuda.synchronize(dev)
+        o0, o1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        o0.record(stream)
+        for i in range(n_ov):
+            step.run(i)
+        o1.record(stream)
+        torch.cuda.synchronize(dev)
+        overlap_us = 1e3 * o0.elapsed_time(o1) / n_ov
+        step.config = plain_cfg
 
     # ---- the dominant kernel per launch (events on its stream)
     n_lat = max(3, min(args.steps, 200))
@@ -518,12 +543,14 @@ def bench_ours(args):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": t_max / args.steps, "us_per_step": 1e3 * t_max / args.steps,
         "graph_us_per_step": graph_us, "hbm_peak_frac": value / float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS)),
+        "overlap_us_per_step": overlap_us,
         "layer_us": ({"eager": 1e3 * t_max / args.steps / args.layers,
                       "graph": graph_us / args.layers if graph_us else None}
                      if args.layers > 1 else None),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": st.dtype, "data": "synthetic (seeded; no dataset or weights involved)",
-        "config": workload_config(st, args.workload, npools, args.layers),
+        "config": dict(workload_config(st, args.workload, npools, args.layers),
+                       overlap_prologue=bool(args.overlap)),
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": units_e2e / (te2e_max * 1e-3) / 1e9, "unit": "GB/s",
@@ -579,6 +606,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_b256")
+    ap.add_argument("--overlap", action="store_true",
+                    help="decode launches as programmatic dependents (a prologue may overlap the "
+                         "previous kernel's tail); off for the default line")
     ap.add_argument("--layers", type=int, default=1,
                     help="attention layers per step (decode workloads; 24 = the Qwen2.5-0.5B stack)")
     ap.add_argument("--pools", type=int, default=0, help="rotating pool copies (0 = enough to exceed 2x L2)")

@@ -170,13 +170,24 @@ ns_status ns_paged_attn_decode(const void *q, const void *k_pool, const void *v_
  *                       eighth of this many KV blocks
  *   whole_sequences     nonzero = never split a (sequence, kv head): worker w
  *                       of W takes pairs w, w+W, w+2W, ... (no merge step)
+ *   overlap_prologue    nonzero = launch as a programmatic dependent of the
+ *                       kernel before it on the stream (CUDA programmatic
+ *                       dependent launch): the decode may start while that
+ *                       kernel drains, reads context_lens and block_tables,
+ *                       then waits for it to finish before it touches q, the
+ *                       pools, k_new/v_new, slot_mapping, out or the
+ *                       workspace.  The caller guarantees that the kernel just
+ *                       before it on the stream does not write context_lens or
+ *                       block_tables.  It also lets the kernel after it start
+ *                       early.  Not a policy override: the split stays automatic.
  */
 #define NS_MAX_CTAS 1024
 typedef struct ns_decode_config {
     int num_ctas;
     int min_blocks_per_cta;
     int whole_sequences;
-    int reserved[5];
+    int overlap_prologue;
+    int reserved[4];
 } ns_decode_config;
 
 /* ns_paged_attn_decode with policy overrides (cfg may be NULL = auto). */
@@ -212,6 +223,17 @@ ns_status ns_kv_append_paged_attn_decode(const void *q, const void *k_new, const
                                          ns_stream_t stream, int max_blocks_per_seq,
                                          int64_t num_blocks, ns_dtype dtype, void *workspace,
                                          size_t workspace_bytes);
+
+/* ns_kv_append_paged_attn_decode with policy overrides (cfg may be NULL = auto). */
+ns_status ns_kv_append_paged_attn_decode_ex(const void *q, const void *k_new, const void *v_new,
+                                            const int64_t *slot_mapping, void *k_pool,
+                                            void *v_pool, const int32_t *block_tables,
+                                            const int32_t *context_lens, int num_seqs,
+                                            int num_q_heads, int num_kv_heads, int head_dim,
+                                            int block_size, float scale, void *out,
+                                            ns_stream_t stream, int max_blocks_per_seq,
+                                            int64_t num_blocks, ns_dtype dtype, void *workspace,
+                                            size_t workspace_bytes, const ns_decode_config *cfg);
 
 /*
  * Plan record the decode kernels leave at the start of the workspace (CTA 0

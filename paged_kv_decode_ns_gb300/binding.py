@@ -42,7 +42,8 @@ class NsError(RuntimeError):
 
 class DecodeConfig(ctypes.Structure):
     _fields_ = [("num_ctas", ctypes.c_int), ("min_blocks_per_cta", ctypes.c_int),
-                ("whole_sequences", ctypes.c_int), ("reserved", ctypes.c_int * 5)]
+                ("whole_sequences", ctypes.c_int), ("overlap_prologue", ctypes.c_int),
+                ("reserved", ctypes.c_int * 4)]
 
 
 class PrefillConfig(ctypes.Structure):
@@ -71,6 +72,8 @@ _SIGNATURES = {
                                     ctypes.POINTER(DecodeConfig)]),
     "ns_kv_append_paged_attn_decode": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, I,
                                            I64, I, P, SZ]),
+    "ns_kv_append_paged_attn_decode_ex": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, I,
+                                              I64, I, P, SZ, ctypes.POINTER(DecodeConfig)]),
     "ns_read_decode_plan": (I, [P, ctypes.POINTER(DecodePlan), P]),
     "ns_paged_attn_prefill": (I, [P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, I, I64, I, P, SZ]),
     "ns_paged_attn_prefill_ex": (I, [P, P, P, P, P, P, I, I, I, I, I, I, F, P, P, I, I64, I, P, SZ,
@@ -222,17 +225,18 @@ def ns_paged_attn_decode_noalloc(q, k_pool, v_pool, block_tables, context_lens, 
 
 
 def ns_kv_append_paged_attn_decode(q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables,
-                                   context_lens, scale, out, workspace, stream=None):
+                                   context_lens, scale, out, workspace, config: DecodeConfig | None = None,
+                                   stream=None):
     """Append one new token per sequence and run the decode step, in one kernel."""
     S, hq, hkv, d, bs, nb, dt, p = _attn_common(q, k_pool, v_pool, block_tables, context_lens,
                                                 out, workspace)
     if k_new.shape != (S, hkv, d) or v_new.shape != (S, hkv, d) or slot_mapping.shape != (S,):
         raise ValueError("k_new/v_new must be [num_seqs, Hkv, D], slot_mapping [num_seqs]")
-    st = lib().ns_kv_append_paged_attn_decode(
+    st = lib().ns_kv_append_paged_attn_decode_ex(
         p["q"], _dev(k_new, "k_new", q.dtype), _dev(v_new, "v_new", q.dtype),
         _dev(slot_mapping, "slot_mapping", torch.int64), p["k"], p["v"], p["bt"], p["cl"], S, hq,
         hkv, d, bs, float(scale), p["out"], _stream(stream), block_tables.shape[1], nb, dt,
-        p["ws"], workspace.numel())
+        p["ws"], workspace.numel(), ctypes.byref(config) if config is not None else None)
     _check(st, "ns_kv_append_paged_attn_decode")
 
 

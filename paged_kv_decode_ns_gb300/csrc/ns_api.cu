@@ -217,6 +217,7 @@ ns_status run_decode(const DecodeCall &c, int dev)
     P.min_blocks_per_cta = (c.cfg && c.cfg->min_blocks_per_cta > 0) ? c.cfg->min_blocks_per_cta
                                                                      : ns::kDefaultMinBlocksPerCta;
     P.whole_sequences = (c.cfg && c.cfg->whole_sequences) ? 1 : 0;
+    P.overlap = (c.cfg && c.cfg->overlap_prologue) ? 1 : 0;
     P.auto_policy = (c.cfg == nullptr || (c.cfg->num_ctas == 0 && c.cfg->min_blocks_per_cta == 0 &&
                                           c.cfg->whole_sequences == 0))
                         ? 1
@@ -385,10 +386,27 @@ ns_status ns_kv_append_paged_attn_decode(const void *q, const void *k_new, const
                                          int64_t num_blocks, ns_dtype dtype, void *workspace,
                                          size_t workspace_bytes)
 {
+    return ns_kv_append_paged_attn_decode_ex(q, k_new, v_new, slot_mapping, k_pool, v_pool,
+                                             block_tables, context_lens, num_seqs, num_q_heads,
+                                             num_kv_heads, head_dim, block_size, scale, out, stream,
+                                             max_blocks_per_seq, num_blocks, dtype, workspace,
+                                             workspace_bytes, nullptr);
+}
+
+ns_status ns_kv_append_paged_attn_decode_ex(const void *q, const void *k_new, const void *v_new,
+                                            const int64_t *slot_mapping, void *k_pool,
+                                            void *v_pool, const int32_t *block_tables,
+                                            const int32_t *context_lens, int num_seqs,
+                                            int num_q_heads, int num_kv_heads, int head_dim,
+                                            int block_size, float scale, void *out,
+                                            ns_stream_t stream, int max_blocks_per_seq,
+                                            int64_t num_blocks, ns_dtype dtype, void *workspace,
+                                            size_t workspace_bytes, const ns_decode_config *cfg)
+{
     const ns_status s = check_decode_args(q, k_pool, v_pool, block_tables, context_lens, num_seqs,
                                           num_q_heads, num_kv_heads, head_dim, block_size, scale,
                                           out, max_blocks_per_seq, num_blocks, dtype, workspace,
-                                          workspace_bytes, nullptr);
+                                          workspace_bytes, cfg);
     if (s != NS_OK)
         return s;
     if (num_seqs == 0)
@@ -400,7 +418,7 @@ ns_status ns_kv_append_paged_attn_decode(const void *q, const void *k_new, const
         return NS_ERR_CUDA;
     DecodeCall c{q, k_pool, v_pool, block_tables, context_lens, nullptr, num_seqs, num_q_heads,
                  num_kv_heads, block_size, scale, out, reinterpret_cast<cudaStream_t>(stream),
-                 max_blocks_per_seq, num_blocks, dtype, workspace, nullptr, k_new, v_new,
+                 max_blocks_per_seq, num_blocks, dtype, workspace, cfg, k_new, v_new,
                  slot_mapping};
     return run_decode(c, dev);
 }

@@ -103,6 +103,18 @@ __device__ __forceinline__ void regs_shrink()
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// Programmatic dependent launch: wait for the previous grid on the stream
+// (complete, memory visible) / let the next one be scheduled.  Both are
+// no-ops for a grid launched without the programmatic attribute.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ int ld_acquire_cta(const int *p)
 {
     int v;

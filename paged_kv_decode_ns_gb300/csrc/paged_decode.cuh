@@ -116,6 +116,7 @@ struct DecodeParams {
     int min_blocks_per_cta;
     int whole_sequences;
     int auto_policy;  // no override given: the device may deal whole pairs instead of splitting
+    int overlap;      // launched as a programmatic dependent: wait for the previous grid (see the prologue)
 };
 
 // Source of the zero-filled rows of a step (32 rows of 64 elements).
@@ -1293,12 +1294,6 @@ __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
             sm.lens[s] = L;
         mine += (long long)Hkv * pair_span(nblocks_of(L, BS));
         my_maxnb = max(my_maxnb, nblocks_of(L, BS));
-        if (L == 0 && (s % (int)gridDim.x) == (int)blockIdx.x &&
-            (P.table_row == nullptr || __ldg(P.table_row + s) >= 0)) {
-            uint16_t *o = P.out + (long long)s * P.num_q_heads * kHeadDim;
-            for (int i = 0; i < P.num_q_heads * kHeadDim; ++i)
-                o[i] = 0;
-        }
     }
     // block-wide exclusive scan of `mine`
     long long incl = mine;
@@ -1414,6 +1409,24 @@ __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
         atomicMax(&sm.plan_maxp, maxp);
     }
     __syncthreads();
+    // Launched with programmatic stream serialization, this grid may start
+    // while the previous one on the stream drains: until here it has read
+    // only the lengths and table rows (which the caller guarantees that grid
+    // does not write); from here on it touches q, the pools, the output and
+    // the workspace, so it waits for that grid.  A plain launch returns at once.
+    if (P.overlap)
+        grid_dependency_wait();
+    // rows with no key get zeros (the rows this CTA owns: s = blockIdx.x mod grid)
+    for (int s = s_lo; s < s_hi; ++s) {
+        if ((s % (int)gridDim.x) != (int)blockIdx.x)
+            continue;
+        const int L = s < kLensCache ? sm.lens[s] : clamped_len(P, s, BS, false);
+        if (L == 0 && (P.table_row == nullptr || __ldg(P.table_row + s) >= 0)) {
+            uint16_t *o = P.out + (long long)s * P.num_q_heads * kHeadDim;
+            for (int i = 0; i < P.num_q_heads * kHeadDim; ++i)
+                o[i] = 0;
+        }
+    }
     if (blockIdx.x == 0 && tid == 0) {
         ns_decode_plan pl;
         const long long wact = whole ? min(W, pairs) : Gw;
@@ -1439,6 +1452,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) paged_decode_kernel(const D
     auto &sm = *reinterpret_cast<DecodeSmem<BS, G, S> *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     using Shape = DecodeShape<G>;
+    // the next grid on the stream may be scheduled on SMs this one frees
+    // (only when it was launched as a programmatic dependent)
+    grid_launch_dependents();
     if (threadIdx.x == 0) {
         for (int w = 0; w < Shape::NG; ++w)
             for (int i = 0; i < S; ++i) {

@@ -46,8 +46,22 @@ cudaError_t launch_paged_decode(const DecodeParams &P, int num_ctas, cudaStream_
     cudaError_t e = K::prepare();
     if (e != cudaSuccess)
         return e;
-    K::fn()<<<num_ctas, K::THREADS, K::SMEM, stream>>>(P);
-    return cudaGetLastError();
+    if (!P.overlap) {
+        K::fn()<<<num_ctas, K::THREADS, K::SMEM, stream>>>(P);
+        return cudaGetLastError();
+    }
+    // programmatic dependent launch: may start while the previous grid drains
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_ctas);
+    cfg.blockDim = dim3(K::THREADS);
+    cfg.dynamicSmemBytes = K::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, K::fn(), P);
 }
 
 template <typename T, int BS, int G>

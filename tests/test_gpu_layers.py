@@ -54,3 +54,47 @@ def test_layer_stack_matches_oracle_and_graph_replay(orc):
     for layer, e, d in zip(layers, eager, devs):
         assert torch.equal(e.view(torch.int16), d.out.view(torch.int16)), layer.name
     _gpu.assert_no_device_status()
+
+
+def test_layer_stack_with_overlapped_prologues_gives_the_same_bits(orc):
+    """Launched as programmatic dependents (each layer's prologue may overlap the
+    previous layer's tail), eagerly and from a CUDA graph, the stack gives the
+    bits of plain launches."""
+    st = wl.WORKLOADS["decode_b32"]()
+    layers = wl.layer_steps(st, 4)
+    plain = [DevStep(layer) for layer in layers]
+    over = [DevStep(layer) for layer in layers]
+    cfg = nb.DecodeConfig()
+    cfg.overlap_prologue = 1
+
+    def run(devs, config):
+        for d in devs:
+            nb.ns_kv_append_paged_attn_decode(d.q, d.k_new, d.v_new, d.slot_mapping, d.k_pool,
+                                              d.v_pool, d.block_tables, d.context_lens, d.st.scale,
+                                              d.out, devs[0].ws, config=config)
+
+    run(plain, None)
+    run(over, cfg)
+    torch.cuda.synchronize()
+    _gpu.assert_no_device_status()
+    for layer, a, b in zip(layers, plain, over):
+        assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16)), layer.name
+        assert torch.equal(a.k_pool.view(torch.int16), b.k_pool.view(torch.int16)), layer.name
+    ref, _, _ = orc.step(layers[2], num_threads=max(1, orc.max_threads()))
+    compare(over[2].out, ref, layers[2].dtype, layers[2].name)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run(over, cfg)
+    torch.cuda.synchronize()
+    for d in over:
+        d.out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run(over, cfg)
+    g.replay()
+    torch.cuda.synchronize()
+    for layer, a, b in zip(layers, plain, over):
+        assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16)), layer.name
+    _gpu.assert_no_device_status()
