@@ -30,12 +30,14 @@ ns_status launch_decode(const DecodeParams &P, ns_dtype dtype, int block_size, i
                         cudaStream_t stream, int dev);
 
 // Chunked prefill of every span of two or more tokens on the tcgen05 tensor cores.
+// after_walk: the kernel just before it on the stream is this call's span walk
+// (whose results it does not read), so it may be launched to overlap it.
 bool tc_prefill_supported(int block_size, int group);
 cudaError_t launch_tc_prefill(const void *q, const int32_t *query_start_loc, const void *k_pool,
                               const void *v_pool, const int32_t *block_tables,
                               const int32_t *context_lens, int num_seqs, int total_q_tokens,
                               int num_q_heads, int num_kv_heads, int block_size, float scale,
                               void *out, int max_blocks_per_seq, long long num_blocks, ns_dtype dtype,
-                              unsigned *status, cudaStream_t stream);
+                              unsigned *status, bool after_walk, cudaStream_t stream);
 
 }  // namespace ns

@@ -636,7 +636,7 @@ bool tc_prefill_supported(int block_size, int group)
 
 template <typename T, int BS>
 static cudaError_t launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                             const PrefillParams &P, int grid, cudaStream_t stream)
+                             const PrefillParams &P, int grid, bool overlap, cudaStream_t stream)
 {
     static int done_mask = 0;
     int dev = 0;
@@ -651,8 +651,24 @@ static cudaError_t launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const
         if (dev < 31)
             __atomic_fetch_or(&done_mask, 1 << dev, __ATOMIC_RELAXED);
     }
-    tc_prefill_kernel<T, BS><<<grid, kThreads, smem_bytes<PParts<T>::N>(), stream>>>(tq, tk, tv, P);
-    return cudaGetLastError();
+    if (!overlap) {
+        tc_prefill_kernel<T, BS><<<grid, kThreads, smem_bytes<PParts<T>::N>(), stream>>>(tq, tk, tv, P);
+        return cudaGetLastError();
+    }
+    // programmatic dependent of the kernel before it (the span walk of the same
+    // call, whose results this kernel does not read): it may start as soon as
+    // SMs free up, with no wait
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_bytes<PParts<T>::N>();
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_prefill_kernel<T, BS>, tq, tk, tv, P);
 }
 
 cudaError_t launch_tc_prefill(const void *q, const int32_t *query_start_loc, const void *k_pool,
@@ -660,7 +676,7 @@ cudaError_t launch_tc_prefill(const void *q, const int32_t *query_start_loc, con
                               const int32_t *context_lens, int num_seqs, int total_q_tokens,
                               int num_q_heads, int num_kv_heads, int block_size, float scale,
                               void *out, int max_blocks_per_seq, long long num_blocks, ns_dtype dtype,
-                              unsigned *status, cudaStream_t stream)
+                              unsigned *status, bool after_walk, cudaStream_t stream)
 {
     const int G = num_q_heads / num_kv_heads;
     const int qt = kRows / G;
@@ -701,10 +717,10 @@ cudaError_t launch_tc_prefill(const void *q, const int32_t *query_start_loc, con
     if (grid == 0)
         return cudaSuccess;
     if (dtype == NS_BF16)
-        return block_size == 16 ? launch_tc<BF16, 16>(tq, tk, tv, P, grid, stream)
-                                : launch_tc<BF16, 32>(tq, tk, tv, P, grid, stream);
-    return block_size == 16 ? launch_tc<F16, 16>(tq, tk, tv, P, grid, stream)
-                            : launch_tc<F16, 32>(tq, tk, tv, P, grid, stream);
+        return block_size == 16 ? launch_tc<BF16, 16>(tq, tk, tv, P, grid, after_walk, stream)
+                                : launch_tc<BF16, 32>(tq, tk, tv, P, grid, after_walk, stream);
+    return block_size == 16 ? launch_tc<F16, 16>(tq, tk, tv, P, grid, after_walk, stream)
+                            : launch_tc<F16, 32>(tq, tk, tv, P, grid, after_walk, stream);
 }
 
 }  // namespace ns
