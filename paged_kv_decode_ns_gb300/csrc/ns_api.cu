@@ -179,6 +179,7 @@ struct DecodeCall {
     const ns_decode_config *cfg;
     const void *k_new, *v_new;
     const int64_t *slot_mapping;
+    bool pack = false;  // keep the workers on the fewest CTAs (another kernel waits for the SMs)
 };
 
 ns_status run_decode(const DecodeCall &c, int dev)
@@ -218,6 +219,7 @@ ns_status run_decode(const DecodeCall &c, int dev)
                                                                      : ns::kDefaultMinBlocksPerCta;
     P.whole_sequences = (c.cfg && c.cfg->whole_sequences) ? 1 : 0;
     P.overlap = (c.cfg && c.cfg->overlap_prologue) ? 1 : 0;
+    P.pack = c.pack ? 1 : 0;
     P.auto_policy = (c.cfg == nullptr || (c.cfg->num_ctas == 0 && c.cfg->min_blocks_per_cta == 0 &&
                                           c.cfg->whole_sequences == 0))
                         ? 1
@@ -477,6 +479,8 @@ ns_status ns_paged_attn_prefill_ex(const void *q, const int32_t *query_start_loc
         DecodeCall c{q, k_pool, v_pool, block_tables, row_len, row_seq, total_q_tokens, num_q_heads,
                      num_kv_heads, block_size, scale, out, st, max_blocks_per_seq, num_blocks, dtype,
                      workspace, nullptr, nullptr, nullptr, nullptr};
+        // the tensor-core kernel after it takes the SMs its idle CTAs leave
+        c.pack = tc_min != 0 && (phases & NS_PREFILL_TENSOR_CORE) != 0;
         const ns_status r = run_decode(c, dev);
         if (r != NS_OK)
             return r;

@@ -117,6 +117,7 @@ struct DecodeParams {
     int whole_sequences;
     int auto_policy;  // no override given: the device may deal whole pairs instead of splitting
     int overlap;      // launched as a programmatic dependent: wait for the previous grid (see the prologue)
+    int pack;         // number workers CTA-major even when only some have work
 };
 
 // Source of the zero-filled rows of a step (32 rows of 64 elements).
@@ -1346,11 +1347,9 @@ __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
     const bool whole = P.whole_sequences ||
                        (P.auto_policy && total > 0 &&
                         (long long)maxnb <= 2 * ((total + Gw - 1) / Gw) && pairs <= W);
-#ifndef NS_DECODE_WMAJOR_ALWAYS
-    const bool wmajor = whole ? pairs < W : Gw < W;
-#else
-    const bool wmajor = true;
-#endif
+    // warp-major spreads a light load over every SM; a packed walk (one whose
+    // SMs another kernel is waiting for) keeps it on the fewest CTAs
+    const bool wmajor = !P.pack && (whole ? pairs < W : Gw < W);
     if (tid < kMergeQueue)
         sm.mq.ready[tid] = 0;
     if (tid == 0) {
