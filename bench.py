@@ -56,14 +56,14 @@ KERNEL_SOURCES = {
                           "paged_kv_decode_ns_gb300/csrc/tcgen05.cuh", "include/ns_paged.h"],
 }
 PROFILED_TRAFFIC = {
-    # profiles/paged_decode_b256_bf16.md: 238.97 MB read + 3.68 MB written
+    # profiles/paged_decode_b256_bf16.md: 238.98 MB read + 3.45 MB written
     ("decode_b256", "paged_decode_kernel"): {
-        "sources_sha256": "891c00d5fbaf05296a11ebd67b61e9559fd9b79b6f357b3b90c225503f1ede0d",
-        "bytes": 242653184},
+        "sources_sha256": "4fc19a346abc90565f160907c30215fafb4b64b911bb4d323a8cff75d8e2107a",
+        "bytes": 242434560},
     # profiles/tc_prefill_mixed_f16.md: 4.73 MB read, 0 written
     ("mixed_chunked_prefill", "tc_prefill_kernel"): {
-        "sources_sha256": "c17804412889bd3c206b568c29b090446dd56245c39cdaba325d857ad01cb873",
-        "bytes": 4729088},
+        "sources_sha256": "0f3c4731b995ef404f1675512c3fb24753812a1db48fd71f499a43acce0aaf79",
+        "bytes": 4729344},
 }
 
 
