@@ -49,18 +49,10 @@ namespace ns {
 // log2 units), L[8] (sum of 2^(z-M)), acc[8][64] (unnormalised output).
 constexpr int kSlotFloats = 2 * kMaxGroup + kMaxGroup * kHeadDim;
 constexpr float kRescaleSlack = 8.0f;
-// One CTA per SM: consumer warps in whole warpgroups and a producer
-// warpgroup.  Build-time knobs: NS_DECODE_CONSUMER_WARPS (8 or 12) and
-// NS_DECODE_SPLIT_HEADS (for G > 4, two warps share each ring and split the
-// query heads, so that 12 consumers fit in the register file).  Measured on
-// the batch-256 decode: 8 consumers with one ring each were fastest; the
-// split issued 22% more instructions (both warps unpack every K/V element).
-#ifndef NS_DECODE_CONSUMER_WARPS
-#define NS_DECODE_CONSUMER_WARPS 8
-#endif
-#ifndef NS_DECODE_SPLIT_HEADS
-#define NS_DECODE_SPLIT_HEADS 0
-#endif
+// One CTA per SM: two consumer warpgroups (8 warps, one worker each) and a
+// producer warpgroup.  (Measured alternative: 12 consumers, two per ring
+// splitting the query heads, issued 22% more instructions and ran slower.)
+constexpr int kConsumerWarps = 8;
 // Row groups (4 tokens each) whose scores are computed together (1, 2 or 4)
 #ifndef NS_DECODE_QK_ROWS
 #define NS_DECODE_QK_ROWS 2  // 2 measured 1.3% faster than 1 and 4 on the batch-256 decode
@@ -71,7 +63,6 @@ constexpr float kRescaleSlack = 8.0f;
 #ifndef NS_DECODE_ONE_STEP_PATH
 #define NS_DECODE_ONE_STEP_PATH 1
 #endif
-constexpr int kConsumerWarps = NS_DECODE_CONSUMER_WARPS;
 constexpr int kStepTokens = 32;        // tokens per ring slot (one per lane for the vote)
 constexpr int kMaxWorkers = 2048;      // split workers (each has two record slots)
 constexpr int kDefaultMinBlocksPerCta = 64;  // spread over a CTA's workers
@@ -123,9 +114,9 @@ struct DecodeParams {
 // Source of the zero-filled rows of a step (32 rows of 64 elements).
 static __device__ __align__(128) uint16_t g_zero_rows[kStepTokens * kHeadDim];
 
-// Merges queued by consumers (run by the merger warp, or by consumers whose
-// rings are done).  A ring holds at most two partial pieces (the first and
-// last of its range), so at most 2 x 12 merges fall to one CTA.
+// Merges queued by consumers and run by the consumers whose rings are done.
+// A ring holds at most two partial pieces (the first and last of its range),
+// so at most 2 x 8 merges fall to one CTA.
 constexpr int kMergeQueue = 32;
 struct MergeJob {
     long long c0, c1, out_row;
@@ -166,24 +157,15 @@ struct HeadSlots {
     static constexpr int PSTRIDE = N < 4 ? 4 : N;
 };
 
-// How a group of G query heads maps onto consumer warps.  Each ring (one
-// worker's stream of K/V steps) is read by WPG warps; warp i of the group
-// owns heads [i * GH0, ...) (with the head split, G > 4 splits 4 + (G - 4)
-// so that a warp holds q and accumulators of at most 4 heads).  Producer warp
-// p serves rings p * SERVED ... p * SERVED + SERVED - 1, one lane each; a
-// producer-warpgroup warp left over runs queued merges (else the consumers
-// run them when their rings are done).
+// Rings (workers) of a CTA and how producer lanes serve them: producer warp
+// p serves rings p * SERVED .. p * SERVED + SERVED - 1, one lane each.
 template <int G>
 struct DecodeShape {
-    static constexpr int WPG = (NS_DECODE_SPLIT_HEADS && G > 4) ? 2 : 1;
-    static constexpr int NG = kConsumerWarps / WPG;  // rings = workers per CTA
-    static constexpr int GH0 = WPG == 2 ? 4 : G;
-    static constexpr int GH1 = G - GH0;
-    static constexpr int SERVED = (NG + 3) / 4;
-    static constexpr int PW = NG / SERVED;  // producer warps
-    static constexpr bool MERGER = PW < 4;  // warp kConsumerWarps + 3 merges
-    static constexpr int PSTRIDE = HeadSlots<GH0>::PSTRIDE;  // p buffer row of a warp
-    static_assert(NG % SERVED == 0 && PW <= 4, "producer lanes");
+    static constexpr int NG = kConsumerWarps;  // rings = workers per CTA
+    static constexpr int SERVED = (NG + 3) / 4;  // two rings per producer warp: three measured slower
+    static constexpr int PW = (NG + SERVED - 1) / SERVED;  // producer warps
+    static constexpr int PSTRIDE = HeadSlots<G>::PSTRIDE;  // p buffer row of a warp
+    static_assert(PW <= 4, "producer lanes");
 };
 
 enum : int {
@@ -697,9 +679,8 @@ __device__ void merge_pieces(const DecodeParams &P, long long c0, long long c1, 
     }
 }
 
-// An arrival count whose result this warp has not looked at yet: each warp
-// of each piece arrives once, and the warp that brings a pair's count to
-// (pieces x warps per ring) merges the pair.
+// An arrival count whose result this warp has not looked at yet: the warp
+// that brings a pair's count to its number of pieces queues the pair's merge.
 struct PendingMerge {
     int prev;  // lane 0: the count before this warp's arrival
     int pair;  // -1: nothing pending
@@ -709,7 +690,7 @@ struct PendingMerge {
 
 template <typename T>
 __device__ __forceinline__ void resolve_merge(const DecodeParams &P, PendingMerge &pm, long long B,
-                                              long long Gw, int G, int wpg, MergeQueue &mq, int lane)
+                                              long long Gw, int G, MergeQueue &mq, int lane)
 {
     if (pm.pair < 0)
         return;
@@ -718,7 +699,7 @@ __device__ __forceinline__ void resolve_merge(const DecodeParams &P, PendingMerg
     const long long c0 = cta_of(pm.pstart, B, Gw);
     const long long c1 = cta_of(pm.pstart + pm.pspan - 1, B, Gw);
     const int prev = __shfl_sync(0xffffffffu, pm.prev, 0);
-    if (prev == (int)((c1 - c0 + 1) * wpg - 1)) {  // every warp of every piece has arrived
+    if (prev == (int)(c1 - c0)) {  // every piece has arrived
         // the other pieces' records (published before their counts) are
         // ordered before the hand-off to the merger
         __threadfence();
@@ -795,60 +776,17 @@ __device__ __forceinline__ bool merge_run(const DecodeParams &P, MergeQueue &mq,
 }
 
 // ---------------------------------------------------------------------------
-// Merger warp: runs queued merges while the consumers stream, until every
-// consumer warp has finished and the queue is empty (consumers that have
-// finished help drain it).
-// ---------------------------------------------------------------------------
-template <typename T>
-__device__ void decode_merger(const DecodeParams &P, MergeQueue &mq, volatile int *abort_flag, int G, int lane)
-{
-    unsigned long long idle_since = 0;
-    bool idle = false;
-    while (true) {
-        const int idx = merge_pop(mq, lane);
-        if (idx >= 0) {
-            idle = false;
-            if (!merge_run<T>(P, mq, idx, G, lane))
-                break;
-            continue;
-        }
-        int done = 0;
-        if (lane == 0)
-            done = ld_acquire_cta(&mq.done);
-        done = __shfl_sync(0xffffffffu, done, 0);
-        // a finished consumer queued its jobs before counting itself done
-        if (done == kConsumerWarps) {
-            if (merge_pop(mq, lane) < 0)
-                break;
-            continue;  // unreachable in practice: a pop would have found it
-        }
-        const unsigned long long now = global_timer_ns();
-        if (!idle) {
-            idle = true;
-            idle_since = now;
-        }
-        if (__any_sync(0xffffffffu, *abort_flag != 0 || now - idle_since > kWaitLimitNs)) {
-            raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
-            break;
-        }
-        __nanosleep(64);
-    }
-}
-
-// ---------------------------------------------------------------------------
-// End of a piece for one warp (heads hbase .. hbase + gvalid - 1 of the
-// group, computed in GH head slots):
-// combine the 4 row groups (shuffles), then write the output (whole pair) or
-// its part of the partial record and count its arrival;
+// End of a piece for one warp: combine the 4 row groups (shuffles), then
+// write the output (whole pair) or the partial record and count its arrival;
 // the result of the count is looked at later (resolve_merge), so the warp
 // does not wait for the atomic here.
 // ---------------------------------------------------------------------------
-template <typename T, int BS, int G, int GH>
+template <typename T, int BS, int G>
 __device__ void piece_end(const DecodeParams &P, const PieceRef &pc, long long worker, long long B,
-                          long long Gw, float2 (&acc)[GH][4], float m_run, float l_run, int hbase, int gvalid,
-                          int lane, PendingMerge &pm, MergeQueue &mq)
+                          long long Gw, float2 (&acc)[G][4], float m_run, float l_run, int lane,
+                          PendingMerge &pm, MergeQueue &mq)
 {
-    constexpr int SHIFT = HeadSlots<GH>::SHIFT;
+    constexpr int SHIFT = HeadSlots<G>::SHIFT;
     const int c = lane & 7;
     // lane (r, c) with (c & ((1 << SHIFT) - 1)) == 0 owns (row group r, head c >> SHIFT)
     float M = fmaxf(m_run, __shfl_xor_sync(0xffffffffu, m_run, 8));
@@ -858,7 +796,7 @@ __device__ void piece_end(const DecodeParams &P, const PieceRef &pc, long long w
     Ls += __shfl_xor_sync(0xffffffffu, Ls, 8);
     Ls += __shfl_xor_sync(0xffffffffu, Ls, 16);
 #pragma unroll
-    for (int j = 0; j < GH; ++j) {
+    for (int j = 0; j < G; ++j) {
         const float fj = __shfl_sync(0xffffffffu, f, (lane & ~7) | (j << SHIFT));
         const float2 f2 = make_float2(fj, fj);
 #pragma unroll
@@ -874,14 +812,12 @@ __device__ void piece_end(const DecodeParams &P, const PieceRef &pc, long long w
     // every lane now holds, for dims 8c..8c+7: the merged acc of this warp's
     // heads; head j's max and sum are in lane (j << SHIFT)
     const int s = pc.ps, h = pc.ph;
-    const long long out_row = ((long long)s * P.num_q_heads + (long long)h * G + hbase) * kHeadDim;
+    const long long out_row = ((long long)s * P.num_q_heads + (long long)h * G) * kHeadDim;
     if (pc.flags & kFlagWhole) {
         if (lane < 8) {
 #pragma unroll
-            for (int j = 0; j < GH; ++j) {
+            for (int j = 0; j < G; ++j) {
                 const float inv = 1.f / __shfl_sync(0xffu, Ls, j << SHIFT);
-                if (j >= gvalid)
-                    break;
                 uint4 w;
                 w.x = pack2<T>(acc[j][0].x * inv, acc[j][0].y * inv);
                 w.y = pack2<T>(acc[j][1].x * inv, acc[j][1].y * inv);
@@ -898,21 +834,19 @@ __device__ void piece_end(const DecodeParams &P, const PieceRef &pc, long long w
     float *rec = P.partials + (worker * 2 + which) * kSlotFloats;
     if (lane < 8) {
 #pragma unroll
-        for (int j = 0; j < GH; ++j) {
-            if (j >= gvalid)
-                break;
-            float *a = rec + 2 * kMaxGroup + (hbase + j) * kHeadDim + c * 8;
+        for (int j = 0; j < G; ++j) {
+            float *a = rec + 2 * kMaxGroup + j * kHeadDim + c * 8;
             __stcg(reinterpret_cast<float4 *>(a), make_float4(acc[j][0].x, acc[j][0].y, acc[j][1].x, acc[j][1].y));
             __stcg(reinterpret_cast<float4 *>(a + 4), make_float4(acc[j][2].x, acc[j][2].y, acc[j][3].x, acc[j][3].y));
         }
-        if ((c & ((1 << SHIFT) - 1)) == 0 && (c >> SHIFT) < gvalid) {
-            __stcg(rec + hbase + (c >> SHIFT), M);
-            __stcg(rec + kMaxGroup + hbase + (c >> SHIFT), Ls);
+        if ((c & ((1 << SHIFT) - 1)) == 0 && (c >> SHIFT) < G) {
+            __stcg(rec + (c >> SHIFT), M);
+            __stcg(rec + kMaxGroup + (c >> SHIFT), Ls);
         }
     }
     __threadfence();
     __syncwarp();
-    resolve_merge<T>(P, pm, B, Gw, G, DecodeShape<G>::WPG, mq, lane);  // at most one count is left open
+    resolve_merge<T>(P, pm, B, Gw, G, mq, lane);  // at most one count is left open
     const int pair = s * P.num_kv_heads + h;
     pm.prev = 0;
     if (lane == 0)
@@ -1148,23 +1082,21 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
 }
 
 // ---------------------------------------------------------------------------
-// Consumer warp: heads hbase .. hbase + gvalid - 1 of ring `ring`, computed
-// in GH head slots (both warps of a ring run the same code).  Takes the
+// Consumer warp: the G heads of ring `ring`.  Takes the
 // ring's slots in order, computes each step, and at the end of each piece
 // writes the output or its part of a partial record; then frees the slot
 // (every warp of the ring arrives on its empty barrier).
 // ---------------------------------------------------------------------------
-template <typename T, int BS, int G, int S, int GH>
-__device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int ring, int hbase, int gvalid,
-                                int warp, int lane)
+template <typename T, int BS, int G, int S>
+__device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int ring, int warp, int lane)
 {
-    constexpr int NS = HeadSlots<GH>::N;
-    constexpr int SHIFT = HeadSlots<GH>::SHIFT;
+    constexpr int NS = HeadSlots<G>::N;
+    constexpr int SHIFT = HeadSlots<G>::SHIFT;
     const int c = lane & 7;
     const long long worker = worker_id(ring, sm.wmajor != 0, DecodeShape<G>::NG);
     const long long B = sm.total, Gw = sm.g_eff;
     float2 q2[NS][4];
-    float2 acc[GH][4];
+    float2 acc[G][4];
     float m_run = -INFINITY, l_run = 0.f;
 #pragma unroll
     for (int i = 0; i < NS; ++i)
@@ -1193,7 +1125,7 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
         DecodeSlot<G> &sl = sm.ring[ring][slot];
         if (step == 0) {
 #pragma unroll
-            for (int j = 0; j < GH; ++j)
+            for (int j = 0; j < G; ++j)
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
                     acc[j][k] = make_float2(0.f, 0.f);
@@ -1203,8 +1135,8 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
 #pragma unroll
                 for (int i = 0; i < NS; ++i) {
                     const int head = i ^ (c >> SHIFT);
-                    if (head < gvalid) {
-                        const uint4 wq = lds128(sl.q + (hbase + head) * kHeadDim + c * 8);
+                    if (head < G) {
+                        const uint4 wq = lds128(sl.q + head * kHeadDim + c * 8);
                         const float2 sc = make_float2(P.scale_log2, P.scale_log2);
                         q2[i][0] = fmul2(unpack2<T>(wq.x), sc);
                         q2[i][1] = fmul2(unpack2<T>(wq.y), sc);
@@ -1222,7 +1154,7 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
             // fused append: the new token's K/V landed in its row of the slot;
             // the ring's first warp also writes them to the pool slot the
             // producer checked
-            if (hbase == 0 && (mt.flags & kFlagNewTok) && lane < 16 && mt.new_slot >= 0) {
+            if ((mt.flags & kFlagNewTok) && lane < 16 && mt.new_slot >= 0) {
                 const int cc = lane & 7;
                 const uint4 val = lds128((lane < 8 ? sl.k : sl.v) + m1.w * kHeadDim + cc * 8);
                 const long long ns = mt.new_slot;
@@ -1231,17 +1163,17 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
             }
             const uint32_t vmask = mt.vmask;
 #if NS_DECODE_ONE_STEP_PATH
-            process_step<T, GH, true>(sl.k, sl.v, vmask, q2, acc, m_run, l_run, pbuf, lane);
+            process_step<T, G, true>(sl.k, sl.v, vmask, q2, acc, m_run, l_run, pbuf, lane);
 #else
             if (vmask == 0xffffffffu)
-                process_step<T, GH, false>(sl.k, sl.v, vmask, q2, acc, m_run, l_run, pbuf, lane);
+                process_step<T, G, false>(sl.k, sl.v, vmask, q2, acc, m_run, l_run, pbuf, lane);
             else
-                process_step<T, GH, true>(sl.k, sl.v, vmask, q2, acc, m_run, l_run, pbuf, lane);
+                process_step<T, G, true>(sl.k, sl.v, vmask, q2, acc, m_run, l_run, pbuf, lane);
 #endif
         }
         if (nsteps == 0 || step == nsteps - 1) {
             const PieceRef pr{mt.ps, mt.ph, mt.flags, m1.x, mt.pstart};
-            piece_end<T, BS, G, GH>(P, pr, worker, B, Gw, acc, m_run, l_run, hbase, gvalid, lane, pm, sm.mq);
+            piece_end<T, BS, G>(P, pr, worker, B, Gw, acc, m_run, l_run, lane, pm, sm.mq);
         }
         // The slot is only read (the async proxy alone writes it), so the
         // barrier's release/acquire orders these reads before the refill.
@@ -1254,7 +1186,7 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
         }
     }
     if (ok) {
-        resolve_merge<T>(P, pm, B, Gw, G, DecodeShape<G>::WPG, sm.mq, lane);
+        resolve_merge<T>(P, pm, B, Gw, G, sm.mq, lane);
         // help drain the merge queue: most merges fall due at the end
         while (true) {
             const int idx = merge_pop(sm.mq, lane);
@@ -1458,7 +1390,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) paged_decode_kernel(const D
         for (int w = 0; w < Shape::NG; ++w)
             for (int i = 0; i < S; ++i) {
                 mbar_init(&sm.full[w][i], 1);
-                mbar_init(&sm.empty[w][i], Shape::WPG);
+                mbar_init(&sm.empty[w][i], 1);
             }
         mbar_init_fence();
     }
@@ -1467,16 +1399,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) paged_decode_kernel(const D
     // the shares add up to the launch allocation.
     if (warp < kConsumerWarps) {
         regs_grow<kConsumerRegs>();
-        const int ring = warp / Shape::WPG;
-        const int half = warp % Shape::WPG;
-        decode_consumer<T, BS, G, S, Shape::GH0>(P, sm, ring, half * Shape::GH0, half ? Shape::GH1 : Shape::GH0,
-                                                 warp, lane);
+        decode_consumer<T, BS, G, S>(P, sm, warp, warp, lane);
     } else {
         regs_shrink<kProducerRegs>();
         if (warp - kConsumerWarps < Shape::PW)
             decode_producer<T, BS, G, S>(P, sm, warp - kConsumerWarps, lane);
-        else if (Shape::MERGER && warp == kConsumerWarps + 3)
-            decode_merger<T>(P, sm.mq, &sm.abort_flag, G, lane);
     }
 }
 
