@@ -58,22 +58,48 @@ KERNEL_SOURCES = {
 PROFILED_TRAFFIC = {
     # profiles/paged_decode_b256_bf16.md: 238.98 MB read + 3.62 MB written
     ("decode_b256", "paged_decode_kernel"): {
-        "sources_sha256": "442659aa9d8880da60013fa4ca81af2b2f92c4d93fcc09566b8dff540baa3a4c",
+        "sources_sha256": "3c26dd70990d2b3c7545686f5ba11b9bb7efb23dbda11ec47bee18f1042ad834",
         "bytes": 242606336},
     # profiles/tc_prefill_mixed_f16.md: 4.73 MB read, 0 written
     ("mixed_chunked_prefill", "tc_prefill_kernel"): {
-        "sources_sha256": "0f3c4731b995ef404f1675512c3fb24753812a1db48fd71f499a43acce0aaf79",
+        "sources_sha256": "e20126070c8f47304a0ba7a9bcb2319d91e95c406bfa58c67735091579ca6d22",
         "bytes": 4729600},
 }
+
+
+def strip_comments(src: str) -> str:
+    """C/C++ source with comments removed and blank lines dropped, so that a
+    comment edit does not count as a change to the kernel."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":  # string or character literal: copy it whole
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    lines = (ln.rstrip() for ln in "".join(out).splitlines())
+    return "\n".join(ln for ln in lines if ln)
 
 
 def kernel_sources_sha(kernel: str) -> str:
     import hashlib
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, rel), "rb") as f:
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
             h.update(rel.encode())
-            h.update(f.read())
+            h.update(strip_comments(f.read()).encode())
     return h.hexdigest()
 
 

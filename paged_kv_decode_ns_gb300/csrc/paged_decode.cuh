@@ -126,7 +126,7 @@ struct MergeQueue {
     MergeJob job[kMergeQueue];
     int ready[kMergeQueue];
     int tail;  // entries taken by producers of jobs
-    int head;  // entries taken by mergers
+    int head;  // entries taken to run
     int done;  // consumer warps finished
 };
 
@@ -701,7 +701,7 @@ __device__ __forceinline__ void resolve_merge(const DecodeParams &P, PendingMerg
     const int prev = __shfl_sync(0xffffffffu, pm.prev, 0);
     if (prev == (int)(c1 - c0)) {  // every piece has arrived
         // the other pieces' records (published before their counts) are
-        // ordered before the hand-off to the merger
+        // ordered before the hand-off to whichever warp runs the merge
         __threadfence();
         const int s = pair / P.num_kv_heads, h = pair % P.num_kv_heads;
         const long long out_row = ((long long)s * P.num_q_heads + (long long)h * G) * kHeadDim;
@@ -711,7 +711,7 @@ __device__ __forceinline__ void resolve_merge(const DecodeParams &P, PendingMerg
             idx = atomicAdd(&mq.tail, 1);
         idx = __shfl_sync(0xffffffffu, idx, 0);
         // A ring holds at most two partial pieces, so a CTA queues at most
-        // 2 x 12 merges and the queue cannot fill; the check guards the bound.
+        // 2 x 8 merges and the queue cannot fill; the check guards the bound.
         if (idx >= kMergeQueue) {
             if (lane == 0)
                 raise_status(P.status, NS_DEV_MERGE_QUEUE);
@@ -1085,7 +1085,7 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
 // Consumer warp: the G heads of ring `ring`.  Takes the
 // ring's slots in order, computes each step, and at the end of each piece
 // writes the output or its part of a partial record; then frees the slot
-// (every warp of the ring arrives on its empty barrier).
+// (its empty barrier).
 // ---------------------------------------------------------------------------
 template <typename T, int BS, int G, int S>
 __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int ring, int warp, int lane)
