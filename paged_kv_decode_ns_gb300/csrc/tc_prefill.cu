@@ -13,19 +13,19 @@
 //   warp 9   producer: TMA 3D load of the Q tile; per 128-key tile, one TMA 2D
 //            load per pool block for K and for V (128-byte swizzle), into a
 //            2-stage ring;
-//   warp 8   allocates 256 TMEM columns; lane 0 issues tcgen05.mma:
+//   warp 8   allocates 512 TMEM columns; lane 0 issues tcgen05.mma:
 //              S[128x128] = Q K^T   (4 steps of K=16, A and B K-major)
 //              O_h[128x64] += P_h V_h (4 steps of K=16 per key half h,
-//                                    P K-major from shared memory, V MN-major)
+//                                    P read from TMEM, V MN-major)
 //            and commits each group to an mbarrier;
 //   warps 0-7 softmax: thread t owns row t % 128 (TMEM lane) and key columns
 //            64 h .. 64 h + 63 of each tile, h = t / 128.  Each key half has
 //            its own running max (moving lazily, by more than 8 in log2 units),
 //            sum and O accumulator (TMEM), so the halves never wait on each
 //            other; it reads its half of the S row, masks keys past its
-//            position, writes its half of P as fp16/bf16 into its
-//            128-byte-swizzled K-major panel and rescales its O when its max
-//            moved.  At the end the two halves of a row are merged by
+//            position, writes its half of P as packed fp16/bf16 pairs into
+//            the P columns of TMEM (the A operand of the PV product) and
+//            rescales its O when its max moved.  At the end the two halves of a row are merged by
 //            log-sum-exp and each writes half of the output row.  (One
 //            warpgroup for all 128 columns took ~1.5 us of ~1.9 us per tile.)
 // Values of keys past the context are zeroed in shared memory before the PV
@@ -42,8 +42,11 @@ namespace {
 
 constexpr int kKT = 128;         // keys per K/V tile
 constexpr int kRows = 128;       // MMA M
-constexpr int kTmemCols = 256;   // S: columns [0,128); O of key half h: [128 + 64h, 192 + 64h)
+// TMEM columns: S [0,128); O of key half h [128 + 64h, 192 + 64h); P part p,
+// key half h [256 + 64p + 32h, 288 + 64p + 32h) (two 16-bit values a column)
+constexpr int kTmemCols = 512;
 constexpr int kTmemO = 128;
+constexpr int kTmemP = 256;
 constexpr int kStages = 3;       // K/V tiles in flight: a tile's copies take ~2 us under load
 constexpr int kSoftmaxThreads = 256;  // two warpgroups: key columns 0..63 and 64..127 of each row
 constexpr int kHalf = kKT / 2;         // key columns per softmax thread
@@ -85,7 +88,6 @@ struct alignas(1024) PrefillSmem {
     uint8_t q[kRows * 128];
     uint8_t k[kStages][kKT * 128];
     uint8_t v[kStages][kKT * 128];
-    uint8_t p[NP][2][kRows * 128];  // [part][keys 0..63 | 64..127]
     uint64_t q_full;
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
@@ -355,8 +357,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kKT / 16; ++kk) {
                         // keys 16 kk ..: key half kk / 4 accumulates into its own O
-                        const uint32_t p_addr = smem_addr(sm.p[part][kk >> 2]) + (kk & 3) * 32;
-                        tc::mma_ss(tmem + kTmemO + (kk >> 2) * kHeadDim, tc::desc_sw128(p_addr),
+                        const uint32_t p_cols = kTmemP + part * (kKT / 2) + (kk >> 2) * (kHalf / 2) + (kk & 3) * 8;
+                        tc::mma_ts(tmem + kTmemO + (kk >> 2) * kHeadDim, tmem + p_cols,
                                    tc::desc_sw128(v_addr + kk * 16 * kRowBytes), idesc_o,
                                    (j > 0 || part > 0 || (kk & 3) > 0) ? 1u : 0u);
                     }
@@ -471,22 +473,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 tc::tmem_st_wait();
             }
-            // P row r, this half's keys: 16-byte chunk q (keys c0+8q..+7) of
-            // panel hf at chunk q ^ (r % 8)
-#pragma unroll
-            for (int q = 0; q < kHalf / 8; ++q) {
-                uint8_t *dst = sm.p[0][hf] + r * 128 + ((q ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4 *>(dst) =
-                    make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            }
+            // P row r, this half's keys c0 .. c0 + 63: column c holds keys
+            // c0 + 2c (low half) and c0 + 2c + 1
+            tc::tmem_st32(lane_addr + kTmemP + hf * (kHalf / 2), pk);
             if (NP == 2) {
+                uint32_t pl[kHalf / 2];
 #pragma unroll
-                for (int q = 0; q < kHalf / 8; ++q) {
-                    uint8_t *dst = sm.p[NP - 1][hf] + r * 128 + ((q ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(dst) =
-                        make_uint4(pack2<T>(sv[8 * q], sv[8 * q + 1]), pack2<T>(sv[8 * q + 2], sv[8 * q + 3]),
-                                   pack2<T>(sv[8 * q + 4], sv[8 * q + 5]), pack2<T>(sv[8 * q + 6], sv[8 * q + 7]));
-                }
+                for (int c = 0; c < kHalf / 2; ++c)
+                    pl[c] = pack2<T>(sv[2 * c], sv[2 * c + 1]);
+                tc::tmem_st32(lane_addr + kTmemP + (NP - 1) * (kKT / 2) + hf * (kHalf / 2), pl);
             }
             // Values of keys past the context, or of blocks that were not
             // loaded, must be zero: P is zero there but 0 * NaN is not.  This
@@ -505,6 +500,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             make_uint4(0, 0, 0, 0);
                 }
             }
+            tc::tmem_st_wait();
             tc::fence_async_smem();
             tc::fence_before_sync();
             mbar_arrive(&sm.p_full);

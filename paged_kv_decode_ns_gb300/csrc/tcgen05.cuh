@@ -87,6 +87,20 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
         : "memory");
 }
 
+// D[tmem] = A[tmem] * B[smem] (+ D when accumulate), issued by one thread.
+// A (M = 128 rows x K = 16) sits in TMEM with row m in lane m and its 16
+// elements packed two per 32-bit column, lower k in the low half: 8 columns
+// starting at a_tmem.
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive on `bar` once every tcgen05.mma issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint64_t *bar)
 {
@@ -112,9 +126,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
         : "r"(taddr));
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
 {
-    const uint32_t *r = reinterpret_cast<const uint32_t *>(v);
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
         "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
@@ -126,6 +139,11 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
         "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
         "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
+{
+    tmem_st32(taddr, reinterpret_cast<const uint32_t(&)[32]>(v));
 }
 
 __device__ __forceinline__ void tmem_ld_wait()
