@@ -62,8 +62,8 @@ PROFILED_TRAFFIC = {
         "bytes": 242606336},
     # profiles/tc_prefill_mixed_f16.md: 4.73 MB read, 0 written
     ("mixed_chunked_prefill", "tc_prefill_kernel"): {
-        "sources_sha256": "e20126070c8f47304a0ba7a9bcb2319d91e95c406bfa58c67735091579ca6d22",
-        "bytes": 4729600},
+        "sources_sha256": "3552f5a02d6dee42418d7d962677d7dc296afe0c5bd6f54467f02d85eeaf77ee",
+        "bytes": 4728576},
 }
 
 
@@ -413,10 +413,18 @@ def stage_inputs(step, torch, dev):
     return d_all, h_all
 
 
-def time_events(torch, stream, fn, n):
-    """Mean device time of fn(i) over n calls, each bracketed by events (ms)."""
+def time_events(torch, stream, fn, n, queue_ahead=False):
+    """Mean device time of fn(i) over n calls, each bracketed by events (ms).
+
+    queue_ahead: first hold the stream with a device-side sleep long enough
+    for the host to enqueue every call, so that no bracket also measures the
+    host preparing a call (a call whose host side takes longer than its
+    kernel would otherwise leave the device idle inside its bracket)."""
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(n)]
+    if queue_ahead and hasattr(torch.cuda, "_sleep"):
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(int(200_000 * n))  # ~100 us of clock cycles per call
     for i, (a, b) in enumerate(evs):
         a.record(stream)
         fn(i)
@@ -482,7 +490,7 @@ def bench_ours(args):
 
     # ---- the dominant kernel per launch (events on its stream)
     n_lat = max(3, min(args.steps, 200))
-    launch_ms = time_events(torch, stream, step.run_dominant, n_lat)
+    launch_ms = time_events(torch, stream, step.run_dominant, n_lat, queue_ahead=True)
 
     # ---- CUDA-graph replay of the same steps (launch overhead removed)
     graph_us = None
