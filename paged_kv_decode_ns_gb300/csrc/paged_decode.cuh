@@ -1261,7 +1261,7 @@ __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
     const long long excl = before + incl - mine;
 
     // Split policy from the real lengths and batch size: an even split over
-    // Gw workers (each at least min_blocks_per_cta / 4 blocks) unless no pair
+    // Gw workers (each at least min_blocks_per_cta / NG blocks) unless no pair
     // is longer than twice the even share, in which case whole pairs dealt
     // round-robin need no merge at all.
     const long long W = (long long)gridDim.x * NG;
