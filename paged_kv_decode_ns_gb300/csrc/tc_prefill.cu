@@ -83,6 +83,7 @@ struct PParts {
     static constexpr int N = T::code == NS_BF16 ? 2 : 1;
 };
 
+// NP (the P parts, 1 or 2) sizes no member: P lives in TMEM.
 template <int NP>
 struct alignas(1024) PrefillSmem {
     uint8_t q[kRows * 128];
@@ -331,8 +332,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc::mma_commit(&sm.s_full);
             };
             // Order: S_0, then per tile j: S_{j+1} as soon as the softmax has
-            // read S_j, then PV_j once P_j is in shared memory -- the softmax
-            // of tile j overlaps S_{j+1} and PV_{j-1} on the tensor core.
+            // read S_j, then PV_j once P_j is in TMEM -- the softmax of tile j
+            // overlaps S_{j+1} and PV_{j-1} on the tensor core.
             bool ok = mbar_wait(&sm.q_full, 0) && mbar_wait(&sm.kv_full[0], 0);
             if (ok) {
                 tc::fence_after_sync();
