@@ -245,6 +245,9 @@ MUTANTS = {
     "append offset swapped": ("b, o = divmod(int(slot), bs)", "o, b = divmod(int(slot), bs)"),
     "slot 0 taken as padding": ("if slot < 0:", "if slot <= 0:"),
     "K codes into V": ("v_codes[b, :, o, :] = vc[t]", "v_codes[b, :, o, :] = kc[t]"),
+    "signed maximum for the scale": ("amax = np.max(np.abs(blk), axis=-1)", "amax = np.max(blk, axis=-1)"),
+    "block scales swapped": ("np.asarray(scales, dtype=np.float16).astype(np.float64)[..., None]",
+                             "np.asarray(scales, dtype=np.float16).astype(np.float64)[..., ::-1, None]"),
     "V read from the K pool": ("V = dequantize_q8_0(v_codes[blk, h, off], v_scales[blk, h, off])",
                                "V = dequantize_q8_0(k_codes[blk, h, off], k_scales[blk, h, off])"),
 }
