@@ -53,16 +53,9 @@ constexpr float kRescaleSlack = 8.0f;
 // producer warpgroup.  (Measured alternative: 12 consumers, two per ring
 // splitting the query heads, issued 22% more instructions and ran slower.)
 constexpr int kConsumerWarps = 8;
-// Row groups (4 tokens each) whose scores are computed together (1, 2 or 4)
-#ifndef NS_DECODE_QK_ROWS
-#define NS_DECODE_QK_ROWS 2  // 2 measured 1.3% faster than 1 and 4 on the batch-256 decode
-#endif
-// 1: one step path (the masked one, for every step) instead of an unmasked
-// copy besides: the smaller instruction footprint measured 4% faster on the
-// batch-256 decode than the two paths (instruction-fetch stalls).
-#ifndef NS_DECODE_ONE_STEP_PATH
-#define NS_DECODE_ONE_STEP_PATH 1
-#endif
+// Row groups (4 tokens each) whose scores are computed together: 2 measured
+// 1.3% faster than 1 and 4 on the batch-256 decode.
+constexpr int kQkRows = 2;
 constexpr int kStepTokens = 32;        // tokens per ring slot (one per lane for the vote)
 constexpr int kMaxWorkers = 2048;      // split workers (each has two record slots)
 constexpr int kDefaultMinBlocksPerCta = 64;  // spread over a CTA's workers
@@ -155,6 +148,16 @@ struct HeadSlots {
     static constexpr int LOG = N == 1 ? 0 : (N == 2 ? 1 : (N == 4 ? 2 : 3));
     static constexpr int SHIFT = 3 - LOG;  // lane c holds head c >> SHIFT
     static constexpr int PSTRIDE = N < 4 ? 4 : N;
+};
+
+// A consumer lane's query registers (pre-scaled by scale * log2 e), for the
+// lane's 8 dims 8c..8c+7:
+//  * two or more head slots: head pairs, q2[m*8 + d] = (q[slot 2m][8c+d],
+//    q[slot 2m+1][8c+d]), so one packed FMA serves two heads;
+//  * one head slot: dim pairs, q2[k] = (q[8c+2k], q[8c+2k+1]).
+template <int G>
+struct QRegs {
+    static constexpr int N = HeadSlots<G>::N * 4;
 };
 
 // Rings (workers) of a CTA and how producer lanes serve them: producer warp
@@ -416,14 +419,14 @@ __device__ __forceinline__ int step_token0(const PieceWalk &w, int i)
 }
 
 // ---------------------------------------------------------------------------
-// One 32-token step for one warp.  MASKED: some tokens of the step are not
-// keys (bit t of vmask clear): their scores are -inf, so p = 0; their rows
-// in the slot are zero-filled by the producer, so p * v adds nothing.
+// One 32-token step for one warp.  Tokens of the step that are not keys
+// (bit t of vmask clear) get score -inf, so p = 0; their rows in the slot are
+// zero-filled by the producer, so p * v adds nothing.
 // ---------------------------------------------------------------------------
-template <typename T, int G, bool MASKED>
+template <typename T, int G>
 __device__ __forceinline__ void process_step(const uint16_t *__restrict__ kb,
                                              const uint16_t *__restrict__ vb, uint32_t vmask,
-                                             const float2 (&q2)[HeadSlots<G>::N][4],
+                                             const float2 (&q2)[QRegs<G>::N],
                                              float2 (&acc)[G][4], float &m_run, float &l_run,
                                              float *pbuf, int lane)
 {
@@ -433,61 +436,78 @@ __device__ __forceinline__ void process_step(const uint16_t *__restrict__ kb,
     const int c = lane & 7;
     const int r = lane >> 3;
 
-    // ---- scores of all token rows of the step, QKR row groups at a time
-    // (their FMA chains and shuffle levels interleave)
-    constexpr int QKR = NS_DECODE_QK_ROWS;
-    static_assert(STEPS % QKR == 0, "row groups per round");
+    // ---- scores of all token rows of the step, kQkRows row groups at a
+    // time (their FMA chains and shuffle levels interleave)
+    static_assert(STEPS % kQkRows == 0, "row groups per round");
     float z[STEPS];
 #pragma unroll
-    for (int st = 0; st < STEPS; st += QKR) {
-        float2 kk[QKR][4];
+    for (int st = 0; st < STEPS; st += kQkRows) {
+        float zz[kQkRows];
+        if constexpr (NS >= 2) {
+            // Head pairs: a[u][m] holds this lane's partial dot products of
+            // head slots 2m and 2m+1 (its 8 dims), one packed FMA per key
+            // element for two heads, so no horizontal add is needed.
+            constexpr int NP = NS / 2;
+            float2 a[kQkRows][NP];
 #pragma unroll
-        for (int u = 0; u < QKR; ++u) {
-            const uint4 kw = lds128(kb + ((st + u) * 4 + r) * kHeadDim + c * 8);
-            kk[u][0] = unpack2<T>(kw.x);
-            kk[u][1] = unpack2<T>(kw.y);
-            kk[u][2] = unpack2<T>(kw.z);
-            kk[u][3] = unpack2<T>(kw.w);
+            for (int u = 0; u < kQkRows; ++u) {
+                const uint4 kw = lds128(kb + ((st + u) * 4 + r) * kHeadDim + c * 8);
+                const uint32_t w[4] = {kw.x, kw.y, kw.z, kw.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 kv = unpack2<T>(w[e]);  // dims 2e, 2e+1 of the lane's 8
+                    const float2 k0 = make_float2(kv.x, kv.x), k1 = make_float2(kv.y, kv.y);
+#pragma unroll
+                    for (int m = 0; m < NP; ++m) {
+                        a[u][m] = e == 0 ? fmul2(q2[m * 8], k0) : ffma2(q2[m * 8 + 2 * e], k0, a[u][m]);
+                        a[u][m] = ffma2(q2[m * 8 + 2 * e + 1], k1, a[u][m]);
+                    }
+                }
+            }
+            // Reduce-scatter over the row's 8 lanes: whole pairs are halved
+            // (lane masks 4, 2, ...) while more than one is left, the last
+            // pair is split at the next mask, and lanes that still share a
+            // head (fewer than 8 slots) sum what is left.
+            int msk = 4;
+#pragma unroll
+            for (int n = NP; n > 1; n >>= 1, msk >>= 1)
+#pragma unroll
+                for (int i = 0; i < n / 2; ++i)
+#pragma unroll
+                    for (int u = 0; u < kQkRows; ++u) {
+                        const float2 o = make_float2(__shfl_xor_sync(0xffffffffu, a[u][i + n / 2].x, msk),
+                                                     __shfl_xor_sync(0xffffffffu, a[u][i + n / 2].y, msk));
+                        a[u][i] = fadd2(a[u][i], o);
+                    }
+#pragma unroll
+            for (int u = 0; u < kQkRows; ++u)
+                zz[u] = a[u][0].x + __shfl_xor_sync(0xffffffffu, a[u][0].y, msk);
+#pragma unroll
+            for (int m = msk >> 1; m >= 1; m >>= 1)
+#pragma unroll
+                for (int u = 0; u < kQkRows; ++u)
+                    zz[u] += __shfl_xor_sync(0xffffffffu, zz[u], m);
+        } else {
+            // One head: dim pairs, then a sum over the row's 8 lanes.
+#pragma unroll
+            for (int u = 0; u < kQkRows; ++u) {
+                const uint4 kw = lds128(kb + ((st + u) * 4 + r) * kHeadDim + c * 8);
+                float2 a = fmul2(q2[0], unpack2<T>(kw.x));
+                a = ffma2(q2[1], unpack2<T>(kw.y), a);
+                a = ffma2(q2[2], unpack2<T>(kw.z), a);
+                a = ffma2(q2[3], unpack2<T>(kw.w), a);
+                zz[u] = a.x + a.y;
+            }
+#pragma unroll
+            for (int m = 4; m >= 1; m >>= 1)
+#pragma unroll
+                for (int u = 0; u < kQkRows; ++u)
+                    zz[u] += __shfl_xor_sync(0xffffffffu, zz[u], m);
         }
-        // breadth-first over the head slots and row groups: NS x QKR
-        // independent chains between each dependent step
-        float2 a[QKR][NS];
 #pragma unroll
-        for (int i = 0; i < NS; ++i)
-#pragma unroll
-            for (int u = 0; u < QKR; ++u)
-                a[u][i] = fmul2(q2[i][0], kk[u][0]);
-#pragma unroll
-        for (int d = 1; d < 4; ++d)
-#pragma unroll
-            for (int i = 0; i < NS; ++i)
-#pragma unroll
-                for (int u = 0; u < QKR; ++u)
-                    a[u][i] = ffma2(q2[i][d], kk[u][d], a[u][i]);
-        float part[QKR][NS];
-#pragma unroll
-        for (int i = 0; i < NS; ++i)
-#pragma unroll
-            for (int u = 0; u < QKR; ++u)
-                part[u][i] = a[u][i].x + a[u][i].y;
-        // halving steps (lane masks 4, 2, 1 from the top), then the lanes that
-        // share a head sum what is left
-#pragma unroll
-        for (int n = NS, m = 4; n > 1; n >>= 1, m >>= 1) {
-#pragma unroll
-            for (int i = 0; i < n / 2; ++i)
-#pragma unroll
-                for (int u = 0; u < QKR; ++u)
-                    part[u][i] += __shfl_xor_sync(0xffffffffu, part[u][i + n / 2], m);
-        }
-#pragma unroll
-        for (int u = 0; u < QKR; ++u) {
-            float zz = part[u][0];
-#pragma unroll
-            for (int m = 4 >> HeadSlots<G>::LOG; m >= 1; m >>= 1)
-                zz += __shfl_xor_sync(0xffffffffu, zz, m);
+        for (int u = 0; u < kQkRows; ++u) {
             const int t = (st + u) * 4 + r;
-            z[st + u] = (MASKED && !((vmask >> t) & 1u)) ? -INFINITY : zz;
+            z[st + u] = !((vmask >> t) & 1u) ? -INFINITY : zz[u];
         }
     }
 
@@ -516,7 +536,7 @@ __device__ __forceinline__ void process_step(const uint16_t *__restrict__ kb,
 #pragma unroll
     for (int st = 0; st < STEPS; ++st) {
         p[st] = fast_exp2(z[st] - m_run);
-        if (MASKED && !(z[st] > -INFINITY))
+        if (!(z[st] > -INFINITY))
             p[st] = 0.f;
         l_run += p[st];
     }
@@ -1095,95 +1115,113 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
     const int c = lane & 7;
     const long long worker = worker_id(ring, sm.wmajor != 0, DecodeShape<G>::NG);
     const long long B = sm.total, Gw = sm.g_eff;
-    float2 q2[NS][4];
+    float2 q2[QRegs<G>::N];
     float2 acc[G][4];
     float m_run = -INFINITY, l_run = 0.f;
 #pragma unroll
-    for (int i = 0; i < NS; ++i)
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            q2[i][k] = make_float2(0.f, 0.f);
+    for (int i = 0; i < QRegs<G>::N; ++i)
+        q2[i] = make_float2(0.f, 0.f);
     float *pbuf = &sm.p[warp][0][0];
     PendingMerge pm;
     pm.pair = -1;
     int slot = 0;
     uint32_t phase = 0;
     bool ok = true;
-    while (true) {
+    // One piece per outer iteration; its steps run in a tight inner loop, so
+    // the per-piece work (query load, record or output) stays off the
+    // per-step path.
+    while (ok) {
         if (!mbar_wait(&sm.full[ring][slot], phase)) {
-            *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
-            raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
             ok = false;
             break;
         }
-        // fields are read where used: the slot is freed only after its piece end
-        const SlotMeta &mt = sm.meta[ring][slot];
-        const int4 m1 = *reinterpret_cast<const int4 *>(&mt.pspan);  // pspan, step, nsteps, t_new
-        const int nsteps = m1.z, step = m1.y;
+        const int4 m0 = *reinterpret_cast<const int4 *>(&sm.meta[ring][slot].ps);     // ps, ph, pL, flags
+        const int4 m1 = *reinterpret_cast<const int4 *>(&sm.meta[ring][slot].pspan);  // pspan, step, nsteps, t_new
+        const int nsteps = m1.z;
         if (nsteps < 0)
             break;  // no more work
-        DecodeSlot<G> &sl = sm.ring[ring][slot];
-        if (step == 0) {
+        const PieceRef pr{m0.x, m0.y, m0.w, m1.x, sm.meta[ring][slot].pstart};
 #pragma unroll
-            for (int j = 0; j < G; ++j)
+        for (int j = 0; j < G; ++j)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                acc[j][k] = make_float2(0.f, 0.f);
+        m_run = -INFINITY;
+        l_run = 0.f;
+        if (nsteps > 0) {
+            // slot i holds head i ^ (c >> SHIFT); slots past the group are 0.
+            // The raw 16-bit words of the slots are paired first (byte
+            // permutes), so that each register pair is one packed product.
+            const uint16_t *qs = sm.ring[ring][slot].q;
+            const float2 sc = make_float2(P.scale_log2, P.scale_log2);
+            uint32_t wq[NS][4];
+#pragma unroll
+            for (int i = 0; i < NS; ++i) {
+                const int head = i ^ (c >> SHIFT);
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                if (head < G)
+                    w = lds128(qs + head * kHeadDim + c * 8);
+                wq[i][0] = w.x;
+                wq[i][1] = w.y;
+                wq[i][2] = w.z;
+                wq[i][3] = w.w;
+            }
+            if constexpr (NS >= 2) {
+#pragma unroll
+                for (int m = 0; m < NS / 2; ++m)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        // dims 2k, 2k+1 of slots 2m, 2m+1
+                        q2[m * 8 + 2 * k] = fmul2(unpack2<T>(__byte_perm(wq[2 * m][k], wq[2 * m + 1][k], 0x5410)), sc);
+                        q2[m * 8 + 2 * k + 1] =
+                            fmul2(unpack2<T>(__byte_perm(wq[2 * m][k], wq[2 * m + 1][k], 0x7632)), sc);
+                    }
+            } else {
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    acc[j][k] = make_float2(0.f, 0.f);
-            m_run = -INFINITY;
-            l_run = 0.f;
+                    q2[k] = fmul2(unpack2<T>(wq[0][k]), sc);
+            }
+        }
+        for (int step = 0;;) {
             if (nsteps > 0) {
-#pragma unroll
-                for (int i = 0; i < NS; ++i) {
-                    const int head = i ^ (c >> SHIFT);
-                    if (head < G) {
-                        const uint4 wq = lds128(sl.q + head * kHeadDim + c * 8);
-                        const float2 sc = make_float2(P.scale_log2, P.scale_log2);
-                        q2[i][0] = fmul2(unpack2<T>(wq.x), sc);
-                        q2[i][1] = fmul2(unpack2<T>(wq.y), sc);
-                        q2[i][2] = fmul2(unpack2<T>(wq.z), sc);
-                        q2[i][3] = fmul2(unpack2<T>(wq.w), sc);
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            q2[i][k] = make_float2(0.f, 0.f);
-                    }
+                const SlotMeta &mt = sm.meta[ring][slot];
+                DecodeSlot<G> &sl = sm.ring[ring][slot];
+                // fused append (the piece's last step): the new token's K/V
+                // landed in its row of the slot; this warp also writes them
+                // to the pool slot the producer checked
+                if (step == nsteps - 1 && (mt.flags & kFlagNewTok) && lane < 16 && mt.new_slot >= 0) {
+                    const int cc = lane & 7;
+                    const uint4 val = lds128((lane < 8 ? sl.k : sl.v) + mt.t_new * kHeadDim + cc * 8);
+                    const long long ns = mt.new_slot;
+                    const long long dst = (((ns / BS) * P.num_kv_heads + mt.ph) * BS + ns % BS) * kHeadDim + cc * 8;
+                    *reinterpret_cast<uint4 *>((lane < 8 ? P.k_pool_w : P.v_pool_w) + dst) = val;
                 }
+                // one step path for full and partial steps: a second, unmasked
+                // copy measured 4% slower (instruction-fetch stalls)
+                process_step<T, G>(sl.k, sl.v, mt.vmask, q2, acc, m_run, l_run, pbuf, lane);
+            }
+            // The slot is only read (the async proxy alone writes it), so the
+            // barrier's release/acquire orders these reads before the refill.
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.empty[ring][slot]);
+            if (++slot == S) {
+                slot = 0;
+                phase ^= 1u;
+            }
+            if (++step >= nsteps)
+                break;
+            if (!mbar_wait(&sm.full[ring][slot], phase)) {
+                ok = false;
+                break;
             }
         }
-        if (nsteps > 0) {
-            // fused append: the new token's K/V landed in its row of the slot;
-            // the ring's first warp also writes them to the pool slot the
-            // producer checked
-            if ((mt.flags & kFlagNewTok) && lane < 16 && mt.new_slot >= 0) {
-                const int cc = lane & 7;
-                const uint4 val = lds128((lane < 8 ? sl.k : sl.v) + m1.w * kHeadDim + cc * 8);
-                const long long ns = mt.new_slot;
-                const long long dst = (((ns / BS) * P.num_kv_heads + mt.ph) * BS + ns % BS) * kHeadDim + cc * 8;
-                *reinterpret_cast<uint4 *>((lane < 8 ? P.k_pool_w : P.v_pool_w) + dst) = val;
-            }
-            const uint32_t vmask = mt.vmask;
-#if NS_DECODE_ONE_STEP_PATH
-            process_step<T, G, true>(sl.k, sl.v, vmask, q2, acc, m_run, l_run, pbuf, lane);
-#else
-            if (vmask == 0xffffffffu)
-                process_step<T, G, false>(sl.k, sl.v, vmask, q2, acc, m_run, l_run, pbuf, lane);
-            else
-                process_step<T, G, true>(sl.k, sl.v, vmask, q2, acc, m_run, l_run, pbuf, lane);
-#endif
-        }
-        if (nsteps == 0 || step == nsteps - 1) {
-            const PieceRef pr{mt.ps, mt.ph, mt.flags, m1.x, mt.pstart};
+        if (ok)
             piece_end<T, BS, G>(P, pr, worker, B, Gw, acc, m_run, l_run, lane, pm, sm.mq);
-        }
-        // The slot is only read (the async proxy alone writes it), so the
-        // barrier's release/acquire orders these reads before the refill.
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&sm.empty[ring][slot]);
-        if (++slot == S) {
-            slot = 0;
-            phase ^= 1u;
-        }
+    }
+    if (!ok) {
+        *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
+        raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
     }
     if (ok) {
         resolve_merge<T>(P, pm, B, Gw, G, sm.mq, lane);
