@@ -247,6 +247,8 @@ ns_status check_decode_args(const void *q, const void *k_pool, const void *v_poo
         return NS_ERR_INVALID_ARG;
     if (max_blocks_per_seq < 1 || num_blocks < 1 || !std::isfinite(scale))
         return NS_ERR_INVALID_ARG;
+    if (!ns::split_fits(rows, num_kv_heads, max_blocks_per_seq))
+        return NS_ERR_UNSUPPORTED;
     if (workspace_bytes < ns_paged_attn_workspace_bytes(rows, num_q_heads, num_kv_heads, head_dim))
         return NS_ERR_INVALID_ARG;
     if (cfg && (cfg->num_ctas < 0 || cfg->num_ctas > NS_MAX_CTAS || cfg->min_blocks_per_cta < 0))

@@ -72,6 +72,13 @@ constexpr int kPieceCost = NS_DECODE_PIECE_COST;
 // Length of a pair in the split's coordinates (0 for a pair with no block).
 __host__ __device__ __forceinline__ int pair_span(int nb) { return nb > 0 ? nb + kPieceCost : 0; }
 
+// The split's coordinates are 32-bit: a call fits when its pairs, each at
+// most max_blocks_per_seq + kPieceCost long, add up to at most INT32_MAX.
+inline bool split_fits(long long rows, long long num_kv_heads, long long max_blocks_per_seq)
+{
+    return rows * num_kv_heads * (max_blocks_per_seq + kPieceCost) <= 0x7fffffffLL;
+}
+
 struct DecodeParams {
     const uint16_t *q;
     const uint16_t *k_pool;
@@ -202,8 +209,7 @@ __device__ __forceinline__ void put_meta(SlotMeta &mt, int ps, int ph, int pL, i
 
 // The fields of a piece that its end needs.
 struct PieceRef {
-    int ps, ph, flags, pspan;
-    long long pstart;
+    int ps, ph, flags, pspan, pstart;
 };
 
 
@@ -226,18 +232,17 @@ struct DecodeSmem {
     SlotMeta meta[NG][S];
     uint64_t full[NG][S];                    // producer -> consumers: the step has landed
     uint64_t empty[NG][S];                   // consumers -> producer: the slot may be refilled
-    long long scan[32];
-    int maxnb[32];
-    int npairs[32];
-    long long wb0[NG], wb1[NG], start_off[NG];
-    int start_s[NG];
+    static constexpr int STAGES = S;
+    // prologue scan of the split coordinates (pair blocks plus piece costs):
+    // per warp its total, largest pair and live pairs; per thread its
+    // exclusive offset inside its warp
+    int wtot[kDecodeThreads / 32];
+    int wmax[kDecodeThreads / 32];
+    int wpairs[kDecodeThreads / 32];
+    int toff[kDecodeThreads];
     MergeQueue mq;
     int lens[kLensCache];                    // clamped context lengths of rows 0..kLensCache-1
-    long long total;
-    int g_eff;  // split workers
-    int whole;  // 1: whole (sequence, kv head) pairs dealt round-robin, no split
     int abort_flag;  // set by a warp that gave up waiting
-    int wmajor;  // 1: workers numbered warp-major (see worker_id)
     int plan_split, plan_maxp;
 };
 
@@ -259,9 +264,33 @@ __device__ __forceinline__ int nblocks_of(int L, int BS) { return (L + BS - 1) /
 // work (wmajor), warp-major, so that they are spread over every SM before any
 // SM gets two; when all have work, CTA-major, so that the warps of a CTA walk
 // neighbouring runs of the same sequences.
-__device__ __forceinline__ long long worker_id(int ring, bool wmajor, int ng)
+__device__ __forceinline__ int worker_id(int ring, bool wmajor, int ng)
 {
-    return wmajor ? (long long)ring * gridDim.x + blockIdx.x : (long long)blockIdx.x * ng + ring;
+    return wmajor ? ring * (int)gridDim.x + (int)blockIdx.x : (int)blockIdx.x * ng + ring;
+}
+
+// The split of the KV work over the workers.  Every CTA computes the same one
+// from the context lengths.  The pairs' blocks (each pair counted kPieceCost
+// blocks longer) are laid end to end and cut into gw ranges; the
+// coordinates are 32-bit because the host refuses calls whose
+// pairs * (max_blocks_per_seq + kPieceCost) exceed INT32_MAX.
+struct Split {
+    int total;        // blocks plus piece costs over all (sequence, kv head) pairs
+    int gw;           // split workers
+    int q, r;         // total = q * gw + r: workers c < r hold q + 1 blocks, the rest q
+    int live_pairs;   // pairs with at least one key
+    bool whole;       // whole pairs dealt round-robin, nothing merged
+    bool wmajor;      // workers numbered warp-major
+};
+
+// First block of worker c's range.
+__device__ __forceinline__ int range_begin(int c, int q, int r) { return c * q + min(c, r); }
+
+// The worker whose range holds block b (0 <= b < total).
+__device__ __forceinline__ int worker_of(int b, int q, int r)
+{
+    const int big = r * (q + 1);
+    return b < big ? b / (q + 1) : r + (b - big) / q;
 }
 
 // Context length of row s, clamped to what the table can address.
@@ -277,16 +306,6 @@ __device__ __forceinline__ int clamped_len(const DecodeParams &P, int s, int BS,
     return L;
 }
 
-// First worker whose block range contains global block b:  b0(c) = c*B/G.
-__device__ __forceinline__ long long cta_of(long long b, long long B, long long G)
-{
-    return ((b + 1) * G - 1) / B;
-}
-
-__device__ __forceinline__ long long range_begin(long long c, long long B, long long G)
-{
-    return c * B / G;
-}
 
 // ---------------------------------------------------------------------------
 // Walk over the pieces of one worker: in split mode the runs of one
@@ -295,42 +314,83 @@ __device__ __forceinline__ long long range_begin(long long c, long long B, long 
 // ---------------------------------------------------------------------------
 struct PieceWalk {
     const int *lens;  // shared-memory copy of the first kLensCache clamped lengths
-    long long pos, end, soff, stride;
+    int pos, end, soff, stride;
     int s, h, L, nb;
     bool first;
     bool whole;
     // the current piece: real blocks [lo, hi) of pair (ps, ph); pstart and
     // pspan place the whole pair in the split's coordinates
     int ps, ph, pL, pnb, lo, hi, flags, pspan;
-    long long pstart;
+    int pstart;
 };
-
-template <class Smem>
-__device__ __forceinline__ void walk_init(const DecodeParams &P, const Smem &sm, int warp, PieceWalk &w)
-{
-    w.lens = sm.lens;
-    w.whole = sm.whole != 0;
-    if (w.whole) {
-        w.pos = worker_id(warp, sm.wmajor != 0, Smem::NG);
-        w.stride = (long long)gridDim.x * Smem::NG;
-        w.end = (long long)P.num_seqs * P.num_kv_heads;
-    } else {
-        w.pos = sm.wb0[warp];
-        w.end = sm.wb1[warp];
-        w.stride = 0;
-    }
-    w.soff = sm.start_off[warp];
-    w.s = sm.start_s[warp];
-    w.h = 0;
-    w.L = -1;
-    w.nb = 0;
-    w.first = true;
-}
 
 template <int BS>
 __device__ __forceinline__ int len_at(const DecodeParams &P, const PieceWalk &w, int s)
 {
     return s < kLensCache ? w.lens[s] : clamped_len(P, s, BS, false);
+}
+
+// Start of worker wk's walk.  Split mode: the range [b0, b1) and the
+// sequence that holds b0, found from the prologue scan (the warp, then the
+// thread chunk by binary search, then the chunk's sequences).  Whole mode:
+// pairs wk, wk + stride, ...
+template <int BS, class Smem>
+__device__ __forceinline__ void walk_init(const DecodeParams &P, const Smem &sm, const Split &sp, int wk,
+                                          PieceWalk &w)
+{
+    constexpr int NWARPS = kDecodeThreads / 32;
+    const int Hkv = P.num_kv_heads;
+    w.lens = sm.lens;
+    w.whole = sp.whole;
+    w.first = true;
+    w.h = 0;
+    w.L = -1;
+    w.nb = 0;
+    w.s = P.num_seqs;
+    w.soff = 0;
+    w.stride = 0;
+    w.pos = w.end = 0;
+    if (sp.whole) {
+        w.pos = wk;
+        w.stride = (int)gridDim.x * Smem::NG;
+        w.end = P.num_seqs * Hkv;
+        return;
+    }
+    if (wk >= sp.gw)
+        return;
+    const int b0 = range_begin(wk, sp.q, sp.r), b1 = range_begin(wk + 1, sp.q, sp.r);
+    w.pos = b0;
+    w.end = b1;
+    if (b1 <= b0)
+        return;
+    int base = 0, ws = 0;
+    for (; ws < NWARPS - 1; ++ws) {
+        const int t = sm.wtot[ws];
+        if (base + t > b0)
+            break;
+        base += t;
+    }
+    int lo = 0, hi = 31;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (base + sm.toff[ws * 32 + mid] <= b0)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int t = ws * 32 + lo;
+    const int per = (P.num_seqs + kDecodeThreads - 1) / kDecodeThreads;
+    int s = min(P.num_seqs, t * per);
+    int soff = base + sm.toff[t];
+    while (s < P.num_seqs) {  // whole sequences before b0
+        const int n = Hkv * pair_span(nblocks_of(len_at<BS>(P, w, s), BS));
+        if (soff + n > b0)
+            break;
+        soff += n;
+        ++s;
+    }
+    w.s = s;
+    w.soff = soff;
 }
 
 template <int BS>
@@ -339,15 +399,15 @@ __device__ __forceinline__ bool walk_next(const DecodeParams &P, PieceWalk &w)
     const int Hkv = P.num_kv_heads;
     if (w.whole) {
         while (w.pos < w.end) {
-            const long long pair = w.pos;
+            const int pair = w.pos;
             w.pos += w.stride;
-            const int s = (int)(pair / Hkv);
+            const int s = pair / Hkv;
             const int L = len_at<BS>(P, w, s);
             const int nb = nblocks_of(L, BS);
             if (nb == 0)
                 continue;
             w.ps = s;
-            w.ph = (int)(pair % Hkv);
+            w.ph = pair % Hkv;
             w.pL = L;
             w.pnb = nb;
             w.lo = 0;
@@ -367,18 +427,18 @@ __device__ __forceinline__ bool walk_next(const DecodeParams &P, PieceWalk &w)
         }
         const int span = pair_span(w.nb);
         if (w.h >= Hkv) {
-            w.soff += (long long)Hkv * span;
+            w.soff += Hkv * span;
             ++w.s;
             w.L = -1;
             continue;
         }
-        const long long pstart = w.soff + (long long)w.h * span;
-        const long long pend = pstart + span;
+        const int pstart = w.soff + w.h * span;
+        const int pend = pstart + span;
         const int h = w.h++;
         if (pend <= w.pos)
             continue;
-        const int lo_v = (int)(w.pos - pstart);
-        const int hi_v = (int)(min(w.end, pend) - pstart);
+        const int lo_v = w.pos - pstart;
+        const int hi_v = min(w.end, pend) - pstart;
         w.ps = w.s;
         w.ph = h;
         w.pL = w.L;
@@ -705,19 +765,19 @@ struct PendingMerge {
     int prev;  // lane 0: the count before this warp's arrival
     int pair;  // -1: nothing pending
     int pspan;
-    long long pstart;
+    int pstart;
 };
 
 template <typename T>
-__device__ __forceinline__ void resolve_merge(const DecodeParams &P, PendingMerge &pm, long long B,
-                                              long long Gw, int G, MergeQueue &mq, int lane)
+__device__ __forceinline__ void resolve_merge(const DecodeParams &P, PendingMerge &pm, int q, int r, int G,
+                                              MergeQueue &mq, int lane)
 {
     if (pm.pair < 0)
         return;
     const int pair = pm.pair;
     pm.pair = -1;
-    const long long c0 = cta_of(pm.pstart, B, Gw);
-    const long long c1 = cta_of(pm.pstart + pm.pspan - 1, B, Gw);
+    const int c0 = worker_of(pm.pstart, q, r);
+    const int c1 = worker_of(pm.pstart + pm.pspan - 1, q, r);
     const int prev = __shfl_sync(0xffffffffu, pm.prev, 0);
     if (prev == (int)(c1 - c0)) {  // every piece has arrived
         // the other pieces' records (published before their counts) are
@@ -725,7 +785,7 @@ __device__ __forceinline__ void resolve_merge(const DecodeParams &P, PendingMerg
         __threadfence();
         const int s = pair / P.num_kv_heads, h = pair % P.num_kv_heads;
         const long long out_row = ((long long)s * P.num_q_heads + (long long)h * G) * kHeadDim;
-        const bool c0_second = range_begin(c0, B, Gw) != pm.pstart;
+        const bool c0_second = range_begin(c0, q, r) != pm.pstart;
         int idx = kMergeQueue;
         if (lane == 0)
             idx = atomicAdd(&mq.tail, 1);
@@ -802,9 +862,9 @@ __device__ __forceinline__ bool merge_run(const DecodeParams &P, MergeQueue &mq,
 // does not wait for the atomic here.
 // ---------------------------------------------------------------------------
 template <typename T, int BS, int G>
-__device__ void piece_end(const DecodeParams &P, const PieceRef &pc, long long worker, long long B,
-                          long long Gw, float2 (&acc)[G][4], float m_run, float l_run, int lane,
-                          PendingMerge &pm, MergeQueue &mq)
+__device__ void piece_end(const DecodeParams &P, const PieceRef &pc, int worker, int q, int r,
+                          float2 (&acc)[G][4], float m_run, float l_run, int lane, PendingMerge &pm,
+                          MergeQueue &mq)
 {
     constexpr int SHIFT = HeadSlots<G>::SHIFT;
     const int c = lane & 7;
@@ -851,7 +911,7 @@ __device__ void piece_end(const DecodeParams &P, const PieceRef &pc, long long w
 
     // ---- partial piece: store the record, count arrivals, merge if last.
     const int which = (pc.flags & kFlagWhich1) ? 1 : 0;
-    float *rec = P.partials + (worker * 2 + which) * kSlotFloats;
+    float *rec = P.partials + ((long long)worker * 2 + which) * kSlotFloats;
     if (lane < 8) {
 #pragma unroll
         for (int j = 0; j < G; ++j) {
@@ -866,7 +926,7 @@ __device__ void piece_end(const DecodeParams &P, const PieceRef &pc, long long w
     }
     __threadfence();
     __syncwarp();
-    resolve_merge<T>(P, pm, B, Gw, G, mq, lane);  // at most one count is left open
+    resolve_merge<T>(P, pm, q, r, G, mq, lane);  // at most one count is left open
     const int pair = s * P.num_kv_heads + h;
     pm.prev = 0;
     if (lane == 0)
@@ -898,7 +958,8 @@ __device__ __forceinline__ void piece_prefetch(const DecodeParams &P, const Piec
 // to the scores and accumulators.
 // ---------------------------------------------------------------------------
 template <typename T, int BS, int G, int S>
-__device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int pwarp, int lane)
+__device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, const Split &sp, int pwarp,
+                                int lane)
 {
     constexpr int KB = kStepTokens / BS;  // blocks per step
     constexpr int SERVED = DecodeShape<G>::SERVED;
@@ -909,7 +970,7 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
     // piece's first step (and its slot_mapping entry) load while the current
     // piece streams.
     PieceWalk walk;
-    walk_init(P, sm, w, walk);
+    walk_init<BS>(P, sm, sp, worker_id(w, sp.wmajor, DecodeShape<G>::NG), walk);
     long long a_trow = 0, a_slot = -1;
     int aphys[KB];
     bool ahead = !done && walk_next<BS>(P, walk);
@@ -945,6 +1006,10 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
         idle = false;
         if (!ready)
             continue;
+        // launched as a programmatic dependent: the copies touch q, the pools
+        // and the new K/V, which the previous grid may still be writing
+        if (P.overlap && issued == 0)
+            grid_dependency_wait();
         SlotMeta &mt = sm.meta[w][slot];
         DecodeSlot<G> &sl = sm.ring[w][slot];
         uint64_t *bar = &sm.full[w][slot];
@@ -1108,13 +1173,14 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
 // (its empty barrier).
 // ---------------------------------------------------------------------------
 template <typename T, int BS, int G, int S>
-__device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, int ring, int warp, int lane)
+__device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, const Split &sp, int ring,
+                                int warp, int lane)
 {
     constexpr int NS = HeadSlots<G>::N;
     constexpr int SHIFT = HeadSlots<G>::SHIFT;
     const int c = lane & 7;
-    const long long worker = worker_id(ring, sm.wmajor != 0, DecodeShape<G>::NG);
-    const long long B = sm.total, Gw = sm.g_eff;
+    const int worker = worker_id(ring, sp.wmajor, DecodeShape<G>::NG);
+    const int q = sp.q, r = sp.r;
     float2 q2[QRegs<G>::N];
     float2 acc[G][4];
     float m_run = -INFINITY, l_run = 0.f;
@@ -1140,7 +1206,7 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
         const int nsteps = m1.z;
         if (nsteps < 0)
             break;  // no more work
-        const PieceRef pr{m0.x, m0.y, m0.w, m1.x, sm.meta[ring][slot].pstart};
+        const PieceRef pr{m0.x, m0.y, m0.w, m1.x, (int)sm.meta[ring][slot].pstart};
 #pragma unroll
         for (int j = 0; j < G; ++j)
 #pragma unroll
@@ -1217,14 +1283,14 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
             }
         }
         if (ok)
-            piece_end<T, BS, G>(P, pr, worker, B, Gw, acc, m_run, l_run, lane, pm, sm.mq);
+            piece_end<T, BS, G>(P, pr, worker, q, r, acc, m_run, l_run, lane, pm, sm.mq);
     }
     if (!ok) {
         *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
         raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
     }
     if (ok) {
-        resolve_merge<T>(P, pm, B, Gw, G, sm.mq, lane);
+        resolve_merge<T>(P, pm, q, r, G, sm.mq, lane);
         // help drain the merge queue: most merges fall due at the end
         while (true) {
             const int idx = merge_pop(sm.mq, lane);
@@ -1240,40 +1306,46 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
 }
 
 // ---------------------------------------------------------------------------
-// Prologue: total work, active workers, each warp's range and starting pair.
+// Prologue (every thread, one barrier): the ring barriers, the context
+// lengths of this thread's chunk of sequences, and a block-wide scan of their
+// split coordinates.  Each thread then derives the split itself (read_split)
+// and each producer lane its own range (walk_init).
 // ---------------------------------------------------------------------------
 template <class Smem, int BS>
 __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
 {
-    constexpr int NT = kDecodeThreads;  // every thread scans lengths
-    constexpr int NWARPS = NT / 32;
-    constexpr int NG = Smem::NG;       // workers of this CTA
+    constexpr int NT = kDecodeThreads;
+    constexpr int NG = Smem::NG;
+    constexpr int S = Smem::STAGES;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int Hkv = P.num_kv_heads;
+    if (tid < 2 * NG * S) {
+        const int i = tid % (NG * S);
+        mbar_init(tid < NG * S ? &sm.full[i / S][i % S] : &sm.empty[i / S][i % S], 1);
+        mbar_init_fence();
+    }
     const int per = (P.num_seqs + NT - 1) / NT;
     const int s_lo = min(P.num_seqs, tid * per);
     const int s_hi = min(P.num_seqs, s_lo + per);
     const bool report = blockIdx.x == 0;
-
-    long long mine = 0;
-    int my_maxnb = 0, my_pairs = 0;
+    int mine = 0, my_maxnb = 0, my_pairs = 0;
     for (int s = s_lo; s < s_hi; ++s) {
         const int L = clamped_len(P, s, BS, report);
-        my_pairs += L > 0 ? Hkv : 0;
         if (s < kLensCache)
             sm.lens[s] = L;
-        mine += (long long)Hkv * pair_span(nblocks_of(L, BS));
-        my_maxnb = max(my_maxnb, nblocks_of(L, BS));
+        const int nb = nblocks_of(L, BS);
+        mine += P.num_kv_heads * pair_span(nb);
+        my_maxnb = max(my_maxnb, nb);
+        my_pairs += L > 0 ? P.num_kv_heads : 0;
     }
-    // block-wide exclusive scan of `mine`
-    long long incl = mine;
+    int incl = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o)
             incl += y;
     }
+    sm.toff[tid] = incl - mine;
     int wmax = my_maxnb, wpairs = my_pairs;
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) {
@@ -1281,45 +1353,11 @@ __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
         wpairs += __shfl_xor_sync(0xffffffffu, wpairs, o);
     }
     if (lane == 31)
-        sm.scan[warp] = incl;
+        sm.wtot[warp] = incl;
     if (lane == 0) {
-        sm.maxnb[warp] = wmax;
-        sm.npairs[warp] = wpairs;
+        sm.wmax[warp] = wmax;
+        sm.wpairs[warp] = wpairs;
     }
-    __syncthreads();
-    long long before = 0, total = 0, live_pairs = 0;
-    int maxnb = 0;
-    for (int w = 0; w < NWARPS; ++w) {
-        if (w < warp)
-            before += sm.scan[w];
-        total += sm.scan[w];
-        live_pairs += sm.npairs[w];
-        maxnb = max(maxnb, sm.maxnb[w]);
-    }
-    const long long excl = before + incl - mine;
-
-    // Split policy from the real lengths and batch size: an even split over
-    // Gw workers (each at least min_blocks_per_cta / NG blocks) unless no pair
-    // is longer than twice the even share, in which case whole pairs dealt
-    // round-robin need no merge at all.
-    const long long W = (long long)gridDim.x * NG;
-    const long long minb = P.min_blocks_per_cta > 0 ? P.min_blocks_per_cta : 1;
-    long long Gw = (NG * total + minb - 1) / minb;
-    if (Gw > W)
-        Gw = W;
-    if (Gw > kMaxWorkers)
-        Gw = kMaxWorkers;
-    if (Gw > total)
-        Gw = total;  // no empty ranges: every worker between a pair's first and last holds a piece
-    if (Gw < 1)
-        Gw = 1;
-    const long long pairs = (long long)P.num_seqs * Hkv;
-    const bool whole = P.whole_sequences ||
-                       (P.auto_policy && total > 0 &&
-                        (long long)maxnb <= 2 * ((total + Gw - 1) / Gw) && pairs <= W);
-    // warp-major spreads a light load over every SM; a packed walk (one whose
-    // SMs another kernel is waiting for) keeps it on the fewest CTAs
-    const bool wmajor = !P.pack && (whole ? pairs < W : Gw < W);
     if (tid < kMergeQueue)
         sm.mq.ready[tid] = 0;
     if (tid == 0) {
@@ -1327,92 +1365,111 @@ __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
         sm.mq.head = 0;
         sm.mq.done = 0;
         sm.abort_flag = 0;
-        sm.wmajor = wmajor ? 1 : 0;
-        sm.whole = whole ? 1 : 0;
-        sm.total = total;
-        sm.g_eff = (int)Gw;
         sm.plan_split = 0;
         sm.plan_maxp = 1;
     }
-    if (tid < NG) {
-        const long long wk = worker_id(tid, wmajor, NG);
-        sm.wb0[tid] = (!whole && wk < Gw) ? range_begin(wk, total, Gw) : 0;
-        sm.wb1[tid] = (!whole && wk < Gw) ? range_begin(wk + 1, total, Gw) : 0;
-        sm.start_s[tid] = P.num_seqs;
-        sm.start_off[tid] = total;
-    }
     __syncthreads();
-    if (!whole && mine > 0) {
-        for (int w = 0; w < NG; ++w) {
-            const long long b0 = sm.wb0[w];
-            if (sm.wb1[w] > b0 && b0 >= excl && b0 < excl + mine) {
-                long long cum = excl;
-                for (int s = s_lo; s < s_hi; ++s) {
-                    const int L = s < kLensCache ? sm.lens[s] : clamped_len(P, s, BS, false);
-                    const long long n = (long long)Hkv * pair_span(nblocks_of(L, BS));
-                    if (b0 < cum + n) {
-                        sm.start_s[w] = s;
-                        sm.start_off[w] = cum;
-                        break;
-                    }
-                    cum += n;
+}
+
+// The split, from the prologue scan.  An even split over gw workers (each at
+// least min_blocks_per_cta / NG blocks) unless no pair is longer than twice
+// the even share and every pair can have its own worker: then whole pairs
+// dealt round-robin need no merge at all.
+template <class Smem>
+__device__ __forceinline__ Split read_split(const DecodeParams &P, const Smem &sm)
+{
+    constexpr int NWARPS = kDecodeThreads / 32;
+    constexpr int NG = Smem::NG;
+    Split sp;
+    int total = 0, live = 0, maxnb = 0;
+#pragma unroll
+    for (int w = 0; w < NWARPS; ++w) {
+        total += sm.wtot[w];
+        live += sm.wpairs[w];
+        maxnb = max(maxnb, sm.wmax[w]);
+    }
+    const int W = (int)gridDim.x * NG;
+    const unsigned per_worker = (unsigned)max(1, (P.min_blocks_per_cta + NG - 1) / NG);
+    int gw = (int)(((unsigned)total + per_worker - 1u) / per_worker);
+    gw = min(gw, min(W, kMaxWorkers));
+    gw = max(1, min(gw, total));  // no empty ranges: every worker between a pair's first and last holds a piece
+    sp.total = total;
+    sp.live_pairs = live;
+    sp.gw = gw;
+    sp.q = total / gw;
+    sp.r = total % gw;
+    const int pairs = P.num_seqs * P.num_kv_heads;
+    const int share = (int)(((unsigned)total + (unsigned)gw - 1u) / (unsigned)gw);
+    sp.whole = P.whole_sequences || (P.auto_policy && total > 0 && maxnb <= 2 * share && pairs <= W);
+    sp.wmajor = !P.pack && (sp.whole ? pairs < W : gw < W);
+    return sp;
+}
+
+// Side work of the consumer warps while the first steps are in flight: rows
+// of sequences with no key get zeros (CTA s mod grid writes row s), and CTA 0
+// records the plan (workers, pairs cut across workers, most pieces of one pair).
+template <class Smem, int BS>
+__device__ void decode_side_work(const DecodeParams &P, Smem &sm, const Split &sp)
+{
+    constexpr int NT = kDecodeThreads;
+    constexpr int NC = kConsumerWarps * 32;
+    constexpr int NG = Smem::NG;
+    const int tid = threadIdx.x;
+    const int per = (P.num_seqs + NT - 1) / NT;
+    const int Hkv = P.num_kv_heads;
+    int split = 0, maxp = 1;
+    for (int t = tid; t < NT; t += NC) {
+        const int s_lo = min(P.num_seqs, t * per);
+        const int s_hi = min(P.num_seqs, s_lo + per);
+        int cum = 0;
+        if (blockIdx.x == 0 && !sp.whole) {
+            for (int w = 0; w < (t >> 5); ++w)
+                cum += sm.wtot[w];
+            cum += sm.toff[t];
+        }
+        for (int s = s_lo; s < s_hi; ++s) {
+            const int L = s < kLensCache ? sm.lens[s] : clamped_len(P, s, BS, false);
+            if (L == 0 && (s % (int)gridDim.x) == (int)blockIdx.x &&
+                (P.table_row == nullptr || __ldg(P.table_row + s) >= 0)) {
+                uint16_t *o = P.out + (long long)s * P.num_q_heads * kHeadDim;
+                for (int i = 0; i < P.num_q_heads * kHeadDim; ++i)
+                    o[i] = 0;
+            }
+            const int nb = nblocks_of(L, BS);
+            const int span = pair_span(nb);
+            if (blockIdx.x == 0 && !sp.whole && nb > 0) {
+                for (int h = 0; h < Hkv; ++h) {
+                    const int ps = cum + h * span;
+                    const int np = worker_of(ps + span - 1, sp.q, sp.r) - worker_of(ps, sp.q, sp.r) + 1;
+                    split += np > 1;
+                    maxp = max(maxp, np);
                 }
             }
+            cum += Hkv * span;
         }
     }
-    if (blockIdx.x == 0 && !whole && total > 0) {
-        long long cum = excl;
-        int split = 0, maxp = 1;
-        for (int s = s_lo; s < s_hi; ++s) {
-            const int nb = nblocks_of(s < kLensCache ? sm.lens[s] : clamped_len(P, s, BS, false), BS);
-            const int span = pair_span(nb);
-            for (int h = 0; h < Hkv && nb > 0; ++h) {
-                const long long ps = cum + (long long)h * span;
-                const long long np = cta_of(ps + span - 1, total, Gw) - cta_of(ps, total, Gw) + 1;
-                split += np > 1;
-                maxp = max(maxp, (int)np);
-            }
-            cum += (long long)Hkv * span;
-        }
-        atomicAdd(&sm.plan_split, split);
-        atomicMax(&sm.plan_maxp, maxp);
-    }
-    __syncthreads();
-    // Launched with programmatic stream serialization, this grid may start
-    // while the previous one on the stream drains: until here it has read
-    // only the lengths and table rows (which the caller guarantees that grid
-    // does not write); from here on it touches q, the pools, the output and
-    // the workspace, so it waits for that grid.  A plain launch returns at once.
-    if (P.overlap)
-        grid_dependency_wait();
-    // rows with no key get zeros (the rows this CTA owns: s = blockIdx.x mod grid)
-    for (int s = s_lo; s < s_hi; ++s) {
-        if ((s % (int)gridDim.x) != (int)blockIdx.x)
-            continue;
-        const int L = s < kLensCache ? sm.lens[s] : clamped_len(P, s, BS, false);
-        if (L == 0 && (P.table_row == nullptr || __ldg(P.table_row + s) >= 0)) {
-            uint16_t *o = P.out + (long long)s * P.num_q_heads * kHeadDim;
-            for (int i = 0; i < P.num_q_heads * kHeadDim; ++i)
-                o[i] = 0;
-        }
-    }
-    if (blockIdx.x == 0 && tid == 0) {
+    if (blockIdx.x != 0)
+        return;
+    atomicAdd(&sm.plan_split, split);
+    atomicMax(&sm.plan_maxp, maxp);
+    named_barrier_sync(1, NC);  // the consumer warps of CTA 0
+    if (tid == 0) {
         ns_decode_plan pl;
-        const long long wact = whole ? min(W, pairs) : Gw;
+        const int W = (int)gridDim.x * NG;
+        const int pairs = P.num_seqs * Hkv;
+        const int wact = sp.whole ? min(W, pairs) : sp.gw;
         pl.ctas_launched = gridDim.x;
-        pl.ctas_active = (int)(wmajor ? min((long long)gridDim.x, wact)
-                                      : (wact + NG - 1) / NG);
-        pl.total_blocks = total - (long long)kPieceCost * live_pairs;  // real blocks
-        pl.split_pairs = whole ? 0 : sm.plan_split;
-        pl.max_pieces = whole ? 1 : sm.plan_maxp;
-        pl.whole_sequences = whole ? 1 : 0;
-        pl.workers_active = (int)wact;
+        pl.ctas_active = sp.wmajor ? min((int)gridDim.x, wact) : (wact + NG - 1) / NG;
+        pl.total_blocks = (long long)sp.total - (long long)kPieceCost * sp.live_pairs;  // real blocks
+        pl.split_pairs = sp.whole ? 0 : sm.plan_split;
+        pl.max_pieces = sp.whole ? 1 : sm.plan_maxp;
+        pl.whole_sequences = sp.whole ? 1 : 0;
+        pl.workers_active = wact;
         for (int i = 0; i < 8; ++i)
             pl.reserved[i] = 0;
         *P.plan = pl;
     }
 }
-
 
 template <typename T, int BS, int G, int S>
 __global__ void __launch_bounds__(kDecodeThreads, 1) paged_decode_kernel(const DecodeParams P)
@@ -1424,24 +1481,22 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) paged_decode_kernel(const D
     // the next grid on the stream may be scheduled on SMs this one frees
     // (only when it was launched as a programmatic dependent)
     grid_launch_dependents();
-    if (threadIdx.x == 0) {
-        for (int w = 0; w < Shape::NG; ++w)
-            for (int i = 0; i < S; ++i) {
-                mbar_init(&sm.full[w][i], 1);
-                mbar_init(&sm.empty[w][i], 1);
-            }
-        mbar_init_fence();
-    }
     decode_prologue<DecodeSmem<BS, G, S>, BS>(P, sm);
+    const Split sp = read_split(P, sm);
     // Registers move from the producer warpgroup to the consumer warpgroups;
     // the shares add up to the launch allocation.
     if (warp < kConsumerWarps) {
         regs_grow<kConsumerRegs>();
-        decode_consumer<T, BS, G, S>(P, sm, warp, warp, lane);
+        // launched as a programmatic dependent: the side work writes the
+        // output and the plan, which the previous grid may still be using
+        if (P.overlap)
+            grid_dependency_wait();
+        decode_side_work<DecodeSmem<BS, G, S>, BS>(P, sm, sp);
+        decode_consumer<T, BS, G, S>(P, sm, sp, warp, warp, lane);
     } else {
         regs_shrink<kProducerRegs>();
         if (warp - kConsumerWarps < Shape::PW)
-            decode_producer<T, BS, G, S>(P, sm, warp - kConsumerWarps, lane);
+            decode_producer<T, BS, G, S>(P, sm, sp, warp - kConsumerWarps, lane);
     }
 }
 

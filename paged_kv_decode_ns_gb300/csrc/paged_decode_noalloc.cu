@@ -21,6 +21,7 @@
 // cudaMemsetAsync on its own stream before the kernel; the partial records need
 // no clearing.
 #include <atomic>
+#include <cmath>
 #include <cstring>
 
 #include "ns_internal.h"
@@ -80,8 +81,10 @@ extern "C" ns_status ns_paged_attn_decode_noalloc(const void *q, const void *k_p
         return NS_ERR_INVALID_ARG;
     if (!aligned(q) || !aligned(k_pool) || !aligned(v_pool) || !aligned(out))
         return NS_ERR_INVALID_ARG;
-    if (max_blocks_per_seq < 1 || num_blocks < 1 || !(scale == scale))
+    if (max_blocks_per_seq < 1 || num_blocks < 1 || !std::isfinite(scale))
         return NS_ERR_INVALID_ARG;
+    if (!ns::split_fits(num_seqs, num_kv_heads, max_blocks_per_seq))
+        return NS_ERR_UNSUPPORTED;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
