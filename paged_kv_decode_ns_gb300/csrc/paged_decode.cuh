@@ -637,120 +637,104 @@ __device__ __forceinline__ void process_step(const uint16_t *__restrict__ kb,
 // ---------------------------------------------------------------------------
 // Log-sum-exp merge of the partial records of one (sequence, kv head) pair by
 // one warp: pieces c0..c1 (the first in its worker's second slot when
-// c0_second), written to out[out_row + j*64 + d] for the G heads.
-//  1. lane k reads piece k's maxima and sums (32 pieces per round); per-head
-//     maxima and weighted sums are warp reductions;
-//  2. lane l owns outputs (head 2i + l/16, dims 4(l%16)..+3), i = 0..3, and
-//     accumulates them over the pieces with 16-byte loads, several pieces in
-//     flight, each scaled by its factor taken from the lane that read it.
+// c0_second), written to out[out_row + j*64 + d] for the G heads.  Pieces
+// go in chunks of kMergeChunk: lane k loads piece k's maxima and sums, and
+// lane l loads its outputs (head 2i + l/16, dims 4(l%16)..+3, i = 0..3) of
+// every piece of the chunk, all before any is used, so a chunk costs one
+// round trip to L2.  Chunks are merged online: a chunk with a larger maximum
+// rescales what came before.
 // ---------------------------------------------------------------------------
-constexpr int kMergeBatch = 8;  // pieces whose output loads are in flight together
+constexpr int kMergeChunk = 8;
 
-template <typename T>
-__device__ __forceinline__ const float *piece_record(const DecodeParams &P, long long c0, int k, bool c0_second)
+__device__ __forceinline__ const float *piece_record(const DecodeParams &P, int c0, int k, bool c0_second)
 {
     const int wh = (k == 0 && c0_second) ? 1 : 0;
-    return P.partials + ((c0 + k) * 2 + wh) * kSlotFloats;
+    return P.partials + ((long long)(c0 + k) * 2 + wh) * kSlotFloats;
 }
 
 template <typename T>
-__device__ void merge_pieces(const DecodeParams &P, long long c0, long long c1, bool c0_second,
-                             long long out_row, int G, int lane)
+__device__ void merge_pieces(const DecodeParams &P, int c0, int c1, bool c0_second, long long out_row, int G,
+                             int lane)
 {
-    const int npieces = (int)(c1 - c0 + 1);
-    float M[kMaxGroup];
-#pragma unroll
-    for (int j = 0; j < kMaxGroup; ++j)
-        M[j] = -INFINITY;
-    for (int k0 = 0; k0 < npieces; k0 += 32) {
-        float m[kMaxGroup];
-        if (k0 + lane < npieces) {
-            const float4 *r = reinterpret_cast<const float4 *>(piece_record<T>(P, c0, k0 + lane, c0_second));
-            const float4 a = __ldcg(r), b = __ldcg(r + 1);
-            m[0] = a.x; m[1] = a.y; m[2] = a.z; m[3] = a.w; m[4] = b.x; m[5] = b.y; m[6] = b.z; m[7] = b.w;
-        } else {
-#pragma unroll
-            for (int j = 0; j < kMaxGroup; ++j)
-                m[j] = -INFINITY;
-        }
-#pragma unroll
-        for (int j = 0; j < kMaxGroup; ++j) {
-            float x = m[j];
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1)
-                x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-            M[j] = fmaxf(M[j], x);
-        }
-    }
+    const int npieces = c1 - c0 + 1;
     const int hsel = lane >> 4;  // this lane's heads are 2i + hsel
-    float Lsum[kMaxGroup];
+    float mr[kMaxGroup], lr[kMaxGroup];
 #pragma unroll
-    for (int j = 0; j < kMaxGroup; ++j)
-        Lsum[j] = 0.f;
+    for (int j = 0; j < kMaxGroup; ++j) {
+        mr[j] = -INFINITY;
+        lr[j] = 0.f;
+    }
     float4 o[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
         o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k0 = 0; k0 < npieces; k0 += 32) {
-        // lane k: factors of piece k0 + k
-        float f[kMaxGroup];
-        if (k0 + lane < npieces) {
-            const float4 *r = reinterpret_cast<const float4 *>(piece_record<T>(P, c0, k0 + lane, c0_second));
-            const float4 a = __ldcg(r), b = __ldcg(r + 1), c = __ldcg(r + 2), d = __ldcg(r + 3);
-            const float mm[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            const float ll[8] = {c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
-#pragma unroll
-            for (int j = 0; j < kMaxGroup; ++j) {
-                f[j] = (j < G && mm[j] > -INFINITY) ? fast_exp2(mm[j] - M[j]) : 0.f;
-                Lsum[j] += f[j] * ll[j];
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < kMaxGroup; ++j)
-                f[j] = 0.f;
+    for (int k0 = 0; k0 < npieces; k0 += kMergeChunk) {
+        const int nk = min(kMergeChunk, npieces - k0);
+        float4 ma = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), mb = ma;
+        float4 la = make_float4(0.f, 0.f, 0.f, 0.f), lb = la;
+        if (lane < nk) {
+            const float4 *r = reinterpret_cast<const float4 *>(piece_record(P, c0, k0 + lane, c0_second));
+            ma = __ldcg(r);
+            mb = __ldcg(r + 1);
+            la = __ldcg(r + 2);
+            lb = __ldcg(r + 3);
         }
-        const int nk = min(32, npieces - k0);
-        // 8 pieces per round: all their loads are issued before any is used,
-        // so a merge of many pieces costs a few L2 round trips, not one each
-        for (int kb = 0; kb < nk; kb += kMergeBatch) {
-            float4 a[kMergeBatch][4];
+        float4 a[kMergeChunk][4];
 #pragma unroll
-            for (int u = 0; u < kMergeBatch; ++u) {
-                const int kk = kb + u < nk ? kb + u : 0;
-                const float4 *r = reinterpret_cast<const float4 *>(piece_record<T>(P, c0, k0 + kk, c0_second) +
-                                                                   2 * kMaxGroup) + lane;
+        for (int k = 0; k < kMergeChunk; ++k) {
+            const float4 *r = reinterpret_cast<const float4 *>(piece_record(P, c0, k0 + (k < nk ? k : 0), c0_second) +
+                                                               2 * kMaxGroup) + lane;
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    a[u][i] = (kb + u < nk && 2 * i + hsel < G) ? __ldcg(r + 32 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+            for (int i = 0; i < 4; ++i)
+                a[k][i] = (k < nk && 2 * i + hsel < G) ? __ldcg(r + 32 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        const float mk[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+        const float lk[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
+        float f[kMaxGroup], sc[kMaxGroup];
 #pragma unroll
-            for (int u = 0; u < kMergeBatch; ++u) {
+        for (int j = 0; j < kMaxGroup; ++j) {
+            float n = mk[j];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float fe = __shfl_sync(0xffffffffu, f[2 * i], (kb + u) & 31);
-                    const float fo = __shfl_sync(0xffffffffu, f[2 * i + 1], (kb + u) & 31);
-                    const float fk = kb + u < nk ? (hsel ? fo : fe) : 0.f;
-                    o[i].x = fmaf(fk, a[u][i].x, o[i].x);
-                    o[i].y = fmaf(fk, a[u][i].y, o[i].y);
-                    o[i].z = fmaf(fk, a[u][i].z, o[i].z);
-                    o[i].w = fmaf(fk, a[u][i].w, o[i].w);
-                }
+            for (int o2 = 16; o2 >= 1; o2 >>= 1)
+                n = fmaxf(n, __shfl_xor_sync(0xffffffffu, n, o2));
+            n = fmaxf(n, mr[j]);
+            // weights of what came before and of lane k's piece (0 for an empty one)
+            sc[j] = mr[j] > -INFINITY ? fast_exp2(mr[j] - n) : 0.f;
+            f[j] = (j < G && mk[j] > -INFINITY) ? fast_exp2(mk[j] - n) : 0.f;
+            float w = f[j] * lk[j];
+#pragma unroll
+            for (int o2 = 16; o2 >= 1; o2 >>= 1)
+                w += __shfl_xor_sync(0xffffffffu, w, o2);
+            lr[j] = lr[j] * sc[j] + w;
+            mr[j] = n;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float s = hsel ? sc[2 * i + 1] : sc[2 * i];
+            o[i].x *= s;
+            o[i].y *= s;
+            o[i].z *= s;
+            o[i].w *= s;
+        }
+#pragma unroll
+        for (int k = 0; k < kMergeChunk; ++k) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float fe = __shfl_sync(0xffffffffu, f[2 * i], k);
+                const float fo = __shfl_sync(0xffffffffu, f[2 * i + 1], k);
+                const float fk = hsel ? fo : fe;
+                o[i].x = fmaf(fk, a[k][i].x, o[i].x);
+                o[i].y = fmaf(fk, a[k][i].y, o[i].y);
+                o[i].z = fmaf(fk, a[k][i].z, o[i].z);
+                o[i].w = fmaf(fk, a[k][i].w, o[i].w);
             }
         }
-    }
-#pragma unroll
-    for (int j = 0; j < kMaxGroup; ++j) {
-        float x = Lsum[j];
-#pragma unroll
-        for (int m = 16; m >= 1; m >>= 1)
-            x += __shfl_xor_sync(0xffffffffu, x, m);
-        Lsum[j] = x;
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int h = 2 * i + hsel;
         if (h < G) {
-            const float inv = 1.f / (hsel ? Lsum[2 * i + 1] : Lsum[2 * i]);
+            const float inv = 1.f / (hsel ? lr[2 * i + 1] : lr[2 * i]);
             uint2 w;
             w.x = pack2<T>(o[i].x * inv, o[i].y * inv);
             w.y = pack2<T>(o[i].z * inv, o[i].w * inv);
@@ -849,7 +833,7 @@ __device__ __forceinline__ bool merge_run(const DecodeParams &P, MergeQueue &mq,
     }
     const MergeJob j = mq.job[idx];
     __threadfence();
-    merge_pieces<T>(P, j.c0, j.c1, j.c0_second != 0, j.out_row, G, lane);
+    merge_pieces<T>(P, (int)j.c0, (int)j.c1, j.c0_second != 0, j.out_row, G, lane);
     if (lane == 0)
         P.counters[j.pair] = 0;
     return true;
