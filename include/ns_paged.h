@@ -5,9 +5,9 @@
  * every query head of every running sequence walks its block table over a
  * paged K/V pool with online softmax (nanoserve project page, "What I built":
  * paged KV cache with block tables; fused paged-attention decode kernel with
- * online softmax over the block table), after the step's new tokens have been
- * written into their slots ("updates the KV cache with the new key and value
- * vectors": Inference Engineering Day 11 short, "How does vLLM work").  Long
+ * online softmax over the block table), after the step's new K/V rows have
+ * been written to their pool slots (Inference Engineering Day 11 short, "How
+ * does vLLM work": the engine's cache update of each step).  Long
  * contexts are split across CTAs and merged by log-sum-exp, the flash-decoding
  * split arm of the nanoserve author's build log (Day 74 post).  A chunked
  * prefill variant takes a span of query tokens per sequence (nanoserve project
@@ -92,9 +92,9 @@ int ns_version(void);
 /*
  * ns_kv_append -- write the step's new tokens into their pool slots.
  *
- * Definition (Inference Engineering Day 11 short, "How does vLLM work": the
- * engine updates the KV cache with the new key and value vectors; paged
- * layout from the nanoserve project page, "What I built"):
+ * Definition (Inference Engineering Day 11 short, "How does vLLM work": each
+ * step stores its tokens' new K/V rows in the cache; paged layout from the
+ * nanoserve project page, "What I built"):
  *   for every token t with slot_mapping[t] >= 0 and every kv head h:
  *     k_pool[slot/bs][h][slot%bs][:] = k[t][h][:]   (same for v)
  * A bit-exact copy.  A negative slot marks a padding token and is skipped.
@@ -180,6 +180,15 @@ ns_status ns_paged_attn_decode(const void *q, const void *k_pool, const void *v_
  *                       before it on the stream does not write context_lens or
  *                       block_tables.  It also lets the kernel after it start
  *                       early.  Not a policy override: the split stays automatic.
+ *   wait_limit_ns       0 = default (about one second); else the limit, in ns, of
+ *                       each wait of a computing warp for its next K/V step.  On
+ *                       expiry the kernel sets NS_DEV_WAIT_TIMEOUT, stops issuing
+ *                       copies, waits (with the default limit) for the copies it
+ *                       has in flight and returns; the outputs of that call are
+ *                       undefined and the workspace must be zero-filled again
+ *                       (ns_paged_attn_workspace_init) before its next use.  For
+ *                       testing the failure path: a limit shorter than a copy's
+ *                       latency makes every call time out.
  */
 #define NS_MAX_CTAS 1024
 typedef struct ns_decode_config {
@@ -187,7 +196,8 @@ typedef struct ns_decode_config {
     int min_blocks_per_cta;
     int whole_sequences;
     int overlap_prologue;
-    int reserved[4];
+    int wait_limit_ns;
+    int reserved[3];
 } ns_decode_config;
 
 /* ns_paged_attn_decode with policy overrides (cfg may be NULL = auto). */

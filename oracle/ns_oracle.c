@@ -9,9 +9,8 @@
  *
  * What it computes (the plain definitions, no blocking, no online softmax):
  *
- *  kv_append -- the serving engine "updates the KV cache with the new key and
- *    value vectors" (Inference Engineering Day 11 short, "How does vLLM
- *    work"); with the paged layout of the nanoserve project page ("What I
+ *  kv_append -- each step stores its tokens' new K/V rows in the cache
+ *    (Inference Engineering Day 11 short, "How does vLLM work"); with the paged layout of the nanoserve project page ("What I
  *    built", paged KV cache bullet) a token's slot s lives in block s / bs at
  *    offset s % bs.  Pool layout [num_blocks][Hkv][bs][D].  A negative slot
  *    marks a padding token and is skipped.  Pure copy of bit patterns.

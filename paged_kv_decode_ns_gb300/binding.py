@@ -43,7 +43,7 @@ class NsError(RuntimeError):
 class DecodeConfig(ctypes.Structure):
     _fields_ = [("num_ctas", ctypes.c_int), ("min_blocks_per_cta", ctypes.c_int),
                 ("whole_sequences", ctypes.c_int), ("overlap_prologue", ctypes.c_int),
-                ("reserved", ctypes.c_int * 4)]
+                ("wait_limit_ns", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
 
 
 class PrefillConfig(ctypes.Structure):

@@ -1,8 +1,7 @@
 // kv_append.cu -- scatter the step's new tokens into their pool slots.
 //
-// The serving engine "updates the KV cache with the new key and value
-// vectors" (Inference Engineering Day 11 short, "How does vLLM work"); in the
-// paged layout (nanoserve project page, "What I built") slot s of a token is
+// Each step stores its tokens' new K/V rows in the cache (Inference
+// Engineering Day 11 short, "How does vLLM work"); in the paged layout (nanoserve project page, "What I built") slot s of a token is
 // block s / bs, offset s % bs.  A bit-exact copy: one thread moves 16 bytes,
 // eight threads move one 64-element head row, so both the reads of the new
 // rows and the writes into the pool are whole 128-byte lines.

@@ -220,6 +220,8 @@ ns_status run_decode(const DecodeCall &c, int dev)
     P.whole_sequences = (c.cfg && c.cfg->whole_sequences) ? 1 : 0;
     P.overlap = (c.cfg && c.cfg->overlap_prologue) ? 1 : 0;
     P.pack = c.pack ? 1 : 0;
+    P.wait_limit_ns = (c.cfg && c.cfg->wait_limit_ns > 0) ? (unsigned long long)c.cfg->wait_limit_ns
+                                                           : ns::kWaitLimitNs;
     P.auto_policy = (c.cfg == nullptr || (c.cfg->num_ctas == 0 && c.cfg->min_blocks_per_cta == 0 &&
                                           c.cfg->whole_sequences == 0))
                         ? 1
@@ -251,7 +253,8 @@ ns_status check_decode_args(const void *q, const void *k_pool, const void *v_poo
         return NS_ERR_UNSUPPORTED;
     if (workspace_bytes < ns_paged_attn_workspace_bytes(rows, num_q_heads, num_kv_heads, head_dim))
         return NS_ERR_INVALID_ARG;
-    if (cfg && (cfg->num_ctas < 0 || cfg->num_ctas > NS_MAX_CTAS || cfg->min_blocks_per_cta < 0))
+    if (cfg && (cfg->num_ctas < 0 || cfg->num_ctas > NS_MAX_CTAS || cfg->min_blocks_per_cta < 0 ||
+                cfg->wait_limit_ns < 0))
         return NS_ERR_INVALID_ARG;
     return NS_OK;
 }

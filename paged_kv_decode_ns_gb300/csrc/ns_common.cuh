@@ -149,16 +149,27 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity)
 }
 
 // Wait for the phase with the given parity to complete; false after
-// kWaitLimitNs of waiting (the caller then reports NS_DEV_WAIT_TIMEOUT).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+// limit_ns of waiting (the caller then reports NS_DEV_WAIT_TIMEOUT).
+// try_wait may hold the thread inside the instruction for a window the
+// hardware picks (microseconds); a limit shorter than the default polls with
+// the non-blocking test instead, so that the limit itself is what expires.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs)
 {
+    if (limit_ns < kWaitLimitNs) {
+        const unsigned long long t0 = global_timer_ns();
+        while (!mbar_test(bar, parity))
+            if (global_timer_ns() - t0 > limit_ns)
+                return false;
+        return true;
+    }
     if (mbar_try_wait(bar, parity))
         return true;
     const unsigned long long t0 = global_timer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity))
             return true;
-        if (global_timer_ns() - t0 > kWaitLimitNs)
+        if (global_timer_ns() - t0 > limit_ns)
             return false;
     }
 }
@@ -168,19 +179,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
 // multiple of 16), completing on an mbarrier.  The L2 policy marks the
 // streamed K/V as evict-first so they do not push out reused data.
 // ---------------------------------------------------------------------------
-// Build-time knob: 0 gives the streamed K/V the default (evict-normal) policy.
-#ifndef NS_KV_EVICT_FIRST
-#define NS_KV_EVICT_FIRST 1
-#endif
-
 __device__ __forceinline__ uint64_t l2_evict_first_policy()
 {
     uint64_t pol;
-#if NS_KV_EVICT_FIRST
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-#else
-    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
-#endif
     return pol;
 }
 
@@ -270,25 +272,6 @@ __device__ __forceinline__ float fast_exp2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// 2^x on the FMA pipe, for x <= 8: Cody-Waite split x = n + f with n =
-// floor(x), f in [0, 1); 2^f from a degree-4 polynomial fitted here by
-// least squares at Chebyshev nodes (max relative error 2.8e-6 in fp32
-// Horner form); 2^n added to the exponent field.  Inputs below -127 give a
-// value under 2^-126 (not exactly 0): callers that need 0 select it.  Half of
-// a softmax's exponentials go here so that the MUFU pipe is not the limit
-// (the split FlashAttention-4 uses on Blackwell).
-__device__ __forceinline__ float exp2_fma(float x)
-{
-    x = fmaxf(x, -127.0f);
-    const float n = floorf(x);
-    const float f = x - n;
-    float p = fmaf(0.013520603f, f, 0.052037429f);
-    p = fmaf(p, f, 0.241427496f);
-    p = fmaf(p, f, 0.693006635f);
-    p = fmaf(p, f, 1.000002503f);
-    return __int_as_float(__float_as_int(p) + (static_cast<int>(n) << 23));
 }
 
 __device__ __forceinline__ uint4 lds128(const void *p)

@@ -64,10 +64,8 @@ constexpr int kLensCache = 256;        // context lengths kept in shared memory
 // counts kPieceCost virtual blocks at the start of every pair, so a worker
 // whose range crosses many pair boundaries (a piece end, a partial last
 // step, an arrival count and perhaps a merge each) gets fewer real blocks.
-#ifndef NS_DECODE_PIECE_COST
-#define NS_DECODE_PIECE_COST 4
-#endif
-constexpr int kPieceCost = NS_DECODE_PIECE_COST;
+// (2, 3 and 4 measured alike on the batch-256 decode; 1 and 6 slower.)
+constexpr int kPieceCost = 4;
 
 // Length of a pair in the split's coordinates (0 for a pair with no block).
 __host__ __device__ __forceinline__ int pair_span(int nb) { return nb > 0 ? nb + kPieceCost : 0; }
@@ -109,6 +107,7 @@ struct DecodeParams {
     int auto_policy;  // no override given: the device may deal whole pairs instead of splitting
     int overlap;      // launched as a programmatic dependent: wait for the previous grid (see the prologue)
     int pack;         // number workers CTA-major even when only some have work
+    unsigned long long wait_limit_ns;  // consumers' waits for a ring step (the producer's own drain keeps kWaitLimitNs)
 };
 
 // Source of the zero-filled rows of a step (32 rows of 64 elements).
@@ -134,13 +133,12 @@ struct MergeQueue {
 // registers a thread gets at launch, then the shares setmaxnreg moves to.
 constexpr int kDecodeThreads = (kConsumerWarps + 4) * 32;
 constexpr int kLaunchRegs = 65536 / kDecodeThreads / 8 * 8;  // 168 for 8 consumers
-#ifndef NS_DECODE_IDLE_NS
-#define NS_DECODE_IDLE_NS 500  // producer back-off when no slot is free (the rings hold 3 steps)
-#endif
-#ifndef NS_DECODE_PRODUCER_REGS
-#define NS_DECODE_PRODUCER_REGS 88
-#endif
-constexpr int kProducerRegs = NS_DECODE_PRODUCER_REGS;
+// Producer back-off when no slot is free (ns; the rings hold 3 steps): 200 and
+// 1000 measured alike.
+constexpr unsigned kProducerIdleNs = 500;
+// The producer warpgroup's registers (the consumers get the rest of the
+// launch allocation).
+constexpr int kProducerRegs = 88;
 constexpr int kConsumerRegs = (kLaunchRegs * kDecodeThreads - kProducerRegs * 128) / (kConsumerWarps * 32) / 8 * 8;
 static_assert(kConsumerWarps % 4 == 0, "consumer warpgroups");
 static_assert(kConsumerRegs * kConsumerWarps * 32 + kProducerRegs * 128 <= kLaunchRegs * kDecodeThreads,
@@ -251,11 +249,7 @@ constexpr size_t kMaxDynSmem = 227 * 1024;
 template <int BS, int G>
 constexpr int decode_stages()
 {
-#ifdef NS_DECODE_STAGES
-    return NS_DECODE_STAGES;
-#else
     return sizeof(DecodeSmem<BS, G, 4>) <= kMaxDynSmem ? 4 : sizeof(DecodeSmem<BS, G, 3>) <= kMaxDynSmem ? 3 : 2;
-#endif
 }
 
 __device__ __forceinline__ int nblocks_of(int L, int BS) { return (L + BS - 1) / BS; }
@@ -984,7 +978,7 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
                 ok = false;
                 break;
             }
-            __nanosleep(NS_DECODE_IDLE_NS);
+            __nanosleep(kProducerIdleNs);
             continue;
         }
         idle = false;
@@ -1181,7 +1175,7 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
     // the per-piece work (query load, record or output) stays off the
     // per-step path.
     while (ok) {
-        if (!mbar_wait(&sm.full[ring][slot], phase)) {
+        if (!mbar_wait(&sm.full[ring][slot], phase, P.wait_limit_ns)) {
             ok = false;
             break;
         }
@@ -1261,7 +1255,7 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
             }
             if (++step >= nsteps)
                 break;
-            if (!mbar_wait(&sm.full[ring][slot], phase)) {
+            if (!mbar_wait(&sm.full[ring][slot], phase, P.wait_limit_ns)) {
                 ok = false;
                 break;
             }

@@ -121,6 +121,7 @@ extern "C" ns_status ns_paged_attn_decode_noalloc(const void *q, const void *k_p
     P.min_blocks_per_cta = ns::kDefaultMinBlocksPerCta;
     P.whole_sequences = 0;
     P.auto_policy = 1;
+    P.wait_limit_ns = ns::kWaitLimitNs;
 
     return ns::launch_decode(P, dtype, block_size, 0, st, dev);
 }

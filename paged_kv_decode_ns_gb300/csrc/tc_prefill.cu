@@ -54,10 +54,8 @@ constexpr int kMmaWarp = 8;
 constexpr int kProducerWarp = 9;
 constexpr int kThreads = 320;          // warps 0-7 softmax, 8 MMA, 9 producer
 constexpr float kSlack = 8.0f;   // lazy rescale: the max moves by more than this (log2 units)
-// 1: every exponential on the MUFU pipe; 0: odd columns as an FMA-pipe polynomial
-#ifndef NS_PREFILL_EXP_MUFU
-#define NS_PREFILL_EXP_MUFU 1  // measured 12% faster: the polynomial's instructions cost more than MUFU
-#endif
+// Every exponential runs on the MUFU pipe: an FMA-pipe polynomial for half of
+// them measured 12% slower (its instructions cost more than MUFU).
 
 struct PrefillParams {
     const int32_t *qsl;
@@ -433,11 +431,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int c = 0; c < kHalf; c += 2) {
                 const float2 z = ffma2(make_float2(sv[c], sv[c + 1]), sc2, nm2);
                 float p0 = fast_exp2(z.x);
-#if NS_PREFILL_EXP_MUFU
                 float p1 = fast_exp2(z.y);
-#else
-                float p1 = exp2_fma(z.y);  // odd columns on the FMA pipe
-#endif
                 if (masked) {
                     p0 = sv[c] > -INFINITY ? p0 : 0.f;
                     p1 = sv[c + 1] > -INFINITY ? p1 : 0.f;
