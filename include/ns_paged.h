@@ -364,6 +364,68 @@ ns_status ns_paged_attn_decode_noalloc(const void *q, const void *k_pool, const 
                                        int64_t num_blocks, ns_dtype dtype);
 
 /*
+ * 8-bit (q8_0) KV cache.  The video-shorts aggregator page's post on serving
+ * a 26B model on one 24 GB GPU ("q8 kv cache") keeps K and V in llama.cpp's
+ * q8_0 format, 8 bits instead of 16, dequantised on the fly by every
+ * attention step.  The pages name the format without defining it; the reading
+ * taken here is the q8_0 block format:
+ *   - a block is 32 consecutive elements of one token's head row (a 64-wide
+ *     row holds two);
+ *   - its scale d = max|x| / 127 in fp32, stored as fp16 (nearest even,
+ *     saturating at 65504); an all-zero block has d = 0;
+ *   - code = rint(x * (1/d)) with both products rounded to fp32, ties to even,
+ *     clamped to [-127, 127]; the code q stands for fp16(d) * q.
+ * Pools: k_codes, v_codes int8 [num_blocks][num_kv_heads][block_size][64];
+ * k_scales, v_scales fp16 [num_blocks][num_kv_heads][block_size][2] (the
+ * scale of elements 0-31, then of 32-63).  All four 16-byte aligned.
+ */
+
+/*
+ * ns_kv_append_q8_0 -- ns_kv_append into a q8_0 pool: each new token's K and
+ * V rows (fp16 or bf16, [num_tokens][num_kv_heads][64]) are quantised as
+ * above and their codes and scales written at slot_mapping (negative: skipped;
+ * outside the pool: skipped, NS_DEV_BAD_SLOT).  The codes and scales match the
+ * q8_0 definition bit for bit.  block_size 4, 8, 16 or 32.
+ */
+ns_status ns_kv_append_q8_0(const void *k, const void *v, const int64_t *slot_mapping,
+                            void *k_codes, void *k_scales, void *v_codes, void *v_scales,
+                            int num_tokens, int num_kv_heads, int head_dim, int block_size,
+                            int64_t num_blocks, ns_dtype dtype, ns_stream_t stream);
+
+/*
+ * ns_paged_attn_decode_q8_0 -- ns_paged_attn_decode over a q8_0 pool: the
+ * same definition with K_s[p] and V_s[p] the dequantised rows
+ * (fp16(d) * code).  q and out are fp16 or bf16 (dtype); the arithmetic is
+ * fp32.  block_size must be 16.  Same workspace, split and merge as the
+ * 16-bit decode; the copies move 64 code bytes and 4 scale bytes per row
+ * instead of 128.
+ */
+ns_status ns_paged_attn_decode_q8_0(const void *q, const void *k_codes, const void *k_scales,
+                                   const void *v_codes, const void *v_scales,
+                                   const int32_t *block_tables, const int32_t *context_lens,
+                                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, float scale, void *out, ns_stream_t stream,
+                                   int max_blocks_per_seq, int64_t num_blocks, ns_dtype dtype,
+                                   void *workspace, size_t workspace_bytes);
+
+/*
+ * ns_kv_append_paged_attn_decode_q8_0 -- ns_kv_append_q8_0 of one new token
+ * per sequence followed by ns_paged_attn_decode_q8_0, in one kernel (the q8_0
+ * form of ns_kv_append_paged_attn_decode: the same slot rule and status
+ * bits).  The attention sees the new token quantised, as the two calls would.
+ */
+ns_status ns_kv_append_paged_attn_decode_q8_0(const void *q, const void *k_new, const void *v_new,
+                                             const int64_t *slot_mapping, void *k_codes,
+                                             void *k_scales, void *v_codes, void *v_scales,
+                                             const int32_t *block_tables,
+                                             const int32_t *context_lens, int num_seqs,
+                                             int num_q_heads, int num_kv_heads, int head_dim,
+                                             int block_size, float scale, void *out,
+                                             ns_stream_t stream, int max_blocks_per_seq,
+                                             int64_t num_blocks, ns_dtype dtype, void *workspace,
+                                             size_t workspace_bytes);
+
+/*
  * Device status word of the current device: OR of NS_DEV_* bits raised by
  * kernels since the last clear.  Synchronises `stream`, copies the word to
  * *bits, and zeroes it when `clear` is nonzero.  Returns NS_OK (whatever the

@@ -80,6 +80,10 @@ _SIGNATURES = {
                                      ctypes.POINTER(PrefillConfig)]),
     "ns_get_device_status": (I, [P, ctypes.POINTER(ctypes.c_uint32), I]),
     "ns_paged_attn_decode_noalloc": (I, [P, P, P, P, P, I, I, I, I, I, F, P, P, I, I64, I]),
+    "ns_kv_append_q8_0": (I, [P, P, P, P, P, P, P, I, I, I, I, I64, I, P]),
+    "ns_paged_attn_decode_q8_0": (I, [P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, I, I64, I, P, SZ]),
+    "ns_kv_append_paged_attn_decode_q8_0": (I, [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P, P, I,
+                                                I64, I, P, SZ]),
 }
 
 
@@ -256,6 +260,60 @@ def ns_paged_attn_prefill(q, query_start_loc, k_pool, v_pool, block_tables, cont
     else:
         _check(lib().ns_paged_attn_prefill_ex(*args, ctypes.byref(config)),
                "ns_paged_attn_prefill_ex")
+
+
+def _q8_pools(k_codes, k_scales, v_codes, v_scales):
+    nb, hkv, bs, d = k_codes.shape
+    if v_codes.shape != k_codes.shape or k_scales.shape != (nb, hkv, bs, d // 32) \
+            or v_scales.shape != k_scales.shape:
+        raise ValueError("q8_0 pools: codes [NB, Hkv, bs, D] int8, scales [NB, Hkv, bs, D/32] fp16")
+    return (nb, hkv, bs, d, _dev(k_codes, "k_codes", torch.int8), _dev(k_scales, "k_scales", torch.float16),
+            _dev(v_codes, "v_codes", torch.int8), _dev(v_scales, "v_scales", torch.float16))
+
+
+def ns_kv_append_q8_0(k, v, slot_mapping, k_codes, k_scales, v_codes, v_scales, stream=None):
+    """Quantise k/v [T, Hkv, D] to q8_0 and write codes and scales at slot_mapping [T] (int64)."""
+    T, hkv, d = k.shape
+    nb, hkv2, bs, d2, kc, ks, vc, vs = _q8_pools(k_codes, k_scales, v_codes, v_scales)
+    if v.shape != k.shape or hkv2 != hkv or d2 != d or slot_mapping.shape != (T,):
+        raise ValueError("shape mismatch")
+    st = lib().ns_kv_append_q8_0(_dev(k, "k"), _dev(v, "v", k.dtype),
+                                 _dev(slot_mapping, "slot_mapping", torch.int64), kc, ks, vc, vs, T, hkv, d,
+                                 bs, nb, _dtype_code(k), _stream(stream))
+    _check(st, "ns_kv_append_q8_0")
+
+
+def ns_paged_attn_decode_q8_0(q, k_codes, k_scales, v_codes, v_scales, block_tables, context_lens, scale,
+                              out, workspace, stream=None):
+    """Decode attention of q [S, Hq, D] over a q8_0 pool (block size 16)."""
+    S, hq, d = q.shape
+    nb, hkv, bs, d2, kc, ks, vc, vs = _q8_pools(k_codes, k_scales, v_codes, v_scales)
+    if d2 != d or out.shape != q.shape or context_lens.shape != (S,) or block_tables.shape[0] != S:
+        raise ValueError("shape mismatch")
+    st = lib().ns_paged_attn_decode_q8_0(
+        _dev(q, "q"), kc, ks, vc, vs, _dev(block_tables, "block_tables", torch.int32),
+        _dev(context_lens, "context_lens", torch.int32), S, hq, hkv, d, bs, float(scale),
+        _dev(out, "out", q.dtype), _stream(stream), block_tables.shape[1], nb, _dtype_code(q),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel())
+    _check(st, "ns_paged_attn_decode_q8_0")
+
+
+def ns_kv_append_paged_attn_decode_q8_0(q, k_new, v_new, slot_mapping, k_codes, k_scales, v_codes, v_scales,
+                                        block_tables, context_lens, scale, out, workspace, stream=None):
+    """Quantise and append one new token per sequence, then decode over the q8_0 pool, in one kernel."""
+    S, hq, d = q.shape
+    nb, hkv, bs, d2, kc, ks, vc, vs = _q8_pools(k_codes, k_scales, v_codes, v_scales)
+    if k_new.shape != (S, hkv, d) or v_new.shape != (S, hkv, d) or slot_mapping.shape != (S,):
+        raise ValueError("k_new/v_new must be [num_seqs, Hkv, D], slot_mapping [num_seqs]")
+    if d2 != d or out.shape != q.shape or context_lens.shape != (S,) or block_tables.shape[0] != S:
+        raise ValueError("shape mismatch")
+    st = lib().ns_kv_append_paged_attn_decode_q8_0(
+        _dev(q, "q"), _dev(k_new, "k_new", q.dtype), _dev(v_new, "v_new", q.dtype),
+        _dev(slot_mapping, "slot_mapping", torch.int64), kc, ks, vc, vs,
+        _dev(block_tables, "block_tables", torch.int32), _dev(context_lens, "context_lens", torch.int32), S, hq,
+        hkv, d, bs, float(scale), _dev(out, "out", q.dtype), _stream(stream), block_tables.shape[1], nb,
+        _dtype_code(q), _dev(workspace, "workspace", torch.uint8), workspace.numel())
+    _check(st, "ns_kv_append_paged_attn_decode_q8_0")
 
 
 def ns_read_decode_plan(workspace, stream=None) -> dict:

@@ -17,6 +17,7 @@ constexpr int kMaxDevices = 64;
 std::atomic<unsigned *> g_status_ptr[kMaxDevices];
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_ctas_per_sm[kMaxDevices][2][4][ns::kMaxGroup];
+std::atomic<int> g_ctas_per_sm_q8[kMaxDevices][2][ns::kMaxGroup];
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -106,6 +107,37 @@ int ctas_per_sm_g(int g)
     }
 }
 
+// q8_0 pools: block size 16 only.
+template <typename T>
+cudaError_t dispatch_decode_q8(int g, const ns::DecodeParams &P, int ctas, cudaStream_t s)
+{
+    switch (g) {
+    case 1: return ns::launch_paged_decode<T, 16, 1, true>(P, ctas, s);
+    case 2: return ns::launch_paged_decode<T, 16, 2, true>(P, ctas, s);
+    case 3: return ns::launch_paged_decode<T, 16, 3, true>(P, ctas, s);
+    case 4: return ns::launch_paged_decode<T, 16, 4, true>(P, ctas, s);
+    case 5: return ns::launch_paged_decode<T, 16, 5, true>(P, ctas, s);
+    case 6: return ns::launch_paged_decode<T, 16, 6, true>(P, ctas, s);
+    case 7: return ns::launch_paged_decode<T, 16, 7, true>(P, ctas, s);
+    default: return ns::launch_paged_decode<T, 16, 8, true>(P, ctas, s);
+    }
+}
+
+template <typename T>
+int ctas_per_sm_q8(int g)
+{
+    switch (g) {
+    case 1: return ns::decode_ctas_per_sm<T, 16, 1, true>();
+    case 2: return ns::decode_ctas_per_sm<T, 16, 2, true>();
+    case 3: return ns::decode_ctas_per_sm<T, 16, 3, true>();
+    case 4: return ns::decode_ctas_per_sm<T, 16, 4, true>();
+    case 5: return ns::decode_ctas_per_sm<T, 16, 5, true>();
+    case 6: return ns::decode_ctas_per_sm<T, 16, 6, true>();
+    case 7: return ns::decode_ctas_per_sm<T, 16, 7, true>();
+    default: return ns::decode_ctas_per_sm<T, 16, 8, true>();
+    }
+}
+
 template <typename T>
 int dispatch_ctas_per_sm(int bs, int g)
 {
@@ -117,12 +149,16 @@ int dispatch_ctas_per_sm(int bs, int g)
     }
 }
 
-int resident_ctas(int dev, ns_dtype dt, int bs, int g)
+int resident_ctas(int dev, ns_dtype dt, int bs, int g, bool q8)
 {
-    std::atomic<int> &slot = g_ctas_per_sm[dev][dt == NS_BF16 ? 1 : 0][bs_index(bs)][g - 1];
+    std::atomic<int> &slot = q8 ? g_ctas_per_sm_q8[dev][dt == NS_BF16 ? 1 : 0][g - 1]
+                                : g_ctas_per_sm[dev][dt == NS_BF16 ? 1 : 0][bs_index(bs)][g - 1];
     int n = slot.load(std::memory_order_relaxed);
     if (n <= 0) {
-        n = dt == NS_BF16 ? dispatch_ctas_per_sm<ns::BF16>(bs, g) : dispatch_ctas_per_sm<ns::F16>(bs, g);
+        if (q8)
+            n = dt == NS_BF16 ? ctas_per_sm_q8<ns::BF16>(g) : ctas_per_sm_q8<ns::F16>(g);
+        else
+            n = dt == NS_BF16 ? dispatch_ctas_per_sm<ns::BF16>(bs, g) : dispatch_ctas_per_sm<ns::F16>(bs, g);
         slot.store(n, std::memory_order_relaxed);
     }
     long long total = (long long)n * sm_count(dev);
@@ -180,6 +216,9 @@ struct DecodeCall {
     const void *k_new, *v_new;
     const int64_t *slot_mapping;
     bool pack = false;  // keep the workers on the fewest CTAs (another kernel waits for the SMs)
+    // q8_0 pools (k_pool and v_pool unused then)
+    bool q8 = false;
+    const void *k_codes = nullptr, *k_scales = nullptr, *v_codes = nullptr, *v_scales = nullptr;
 };
 
 ns_status run_decode(const DecodeCall &c, int dev)
@@ -222,12 +261,16 @@ ns_status run_decode(const DecodeCall &c, int dev)
     P.pack = c.pack ? 1 : 0;
     P.wait_limit_ns = (c.cfg && c.cfg->wait_limit_ns > 0) ? (unsigned long long)c.cfg->wait_limit_ns
                                                            : ns::kWaitLimitNs;
+    P.k_codes = static_cast<const int8_t *>(c.k_codes);
+    P.v_codes = static_cast<const int8_t *>(c.v_codes);
+    P.k_scales = static_cast<const uint16_t *>(c.k_scales);
+    P.v_scales = static_cast<const uint16_t *>(c.v_scales);
     P.auto_policy = (c.cfg == nullptr || (c.cfg->num_ctas == 0 && c.cfg->min_blocks_per_cta == 0 &&
                                           c.cfg->whole_sequences == 0))
                         ? 1
                         : 0;
 
-    return ns::launch_decode(P, c.dtype, c.block_size, c.cfg ? c.cfg->num_ctas : 0, c.stream, dev);
+    return ns::launch_decode(P, c.dtype, c.block_size, c.cfg ? c.cfg->num_ctas : 0, c.stream, dev, c.q8);
 }
 
 ns_status check_decode_args(const void *q, const void *k_pool, const void *v_pool,
@@ -264,14 +307,18 @@ ns_status check_decode_args(const void *q, const void *k_pool, const void *v_poo
 namespace ns {
 
 ns_status launch_decode(const DecodeParams &P, ns_dtype dtype, int block_size, int num_ctas,
-                        cudaStream_t stream, int dev)
+                        cudaStream_t stream, int dev, bool q8)
 {
     const int g = P.group;
-    int ctas = num_ctas > 0 ? num_ctas : resident_ctas(dev, dtype, block_size, g);
+    int ctas = num_ctas > 0 ? num_ctas : resident_ctas(dev, dtype, block_size, g, q8);
     if (ctas > NS_MAX_CTAS)
         ctas = NS_MAX_CTAS;
-    const cudaError_t e = dtype == NS_BF16 ? dispatch_decode<BF16>(block_size, g, P, ctas, stream)
-                                           : dispatch_decode<F16>(block_size, g, P, ctas, stream);
+    cudaError_t e;
+    if (q8)
+        e = dtype == NS_BF16 ? dispatch_decode_q8<BF16>(g, P, ctas, stream) : dispatch_decode_q8<F16>(g, P, ctas, stream);
+    else
+        e = dtype == NS_BF16 ? dispatch_decode<BF16>(block_size, g, P, ctas, stream)
+                             : dispatch_decode<F16>(block_size, g, P, ctas, stream);
     return e == cudaSuccess ? NS_OK : NS_ERR_CUDA;
 }
 
@@ -281,6 +328,46 @@ unsigned *ns::device_status_word(int dev)
 {
     return (dev >= 0 && dev < kMaxDevices) ? status_word(dev) : nullptr;
 }
+
+namespace {
+
+ns_status decode_q8_0(const void *q, const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                      const void *k_codes, const void *k_scales, const void *v_codes, const void *v_scales,
+                      const int32_t *block_tables, const int32_t *context_lens, int num_seqs, int num_q_heads,
+                      int num_kv_heads, int head_dim, int block_size, float scale, void *out,
+                      ns_stream_t stream, int max_blocks_per_seq, int64_t num_blocks, ns_dtype dtype,
+                      void *workspace, size_t workspace_bytes, const ns_decode_config *cfg)
+{
+    if (!k_codes || !k_scales || !v_codes || !v_scales)
+        return NS_ERR_INVALID_ARG;
+    const ns_status s = check_decode_args(q, k_codes, v_codes, block_tables, context_lens, num_seqs, num_q_heads,
+                                          num_kv_heads, head_dim, block_size, scale, out, max_blocks_per_seq,
+                                          num_blocks, dtype, workspace, workspace_bytes, cfg);
+    if (s != NS_OK)
+        return s;
+    if (block_size != 16)
+        return NS_ERR_UNSUPPORTED;
+    if (!aligned16(k_scales) || !aligned16(v_scales))
+        return NS_ERR_INVALID_ARG;
+    if (num_seqs == 0)
+        return NS_OK;
+    if (k_new && (!v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new)))
+        return NS_ERR_INVALID_ARG;
+    int dev = 0;
+    if (current_device(&dev) != cudaSuccess)
+        return NS_ERR_CUDA;
+    DecodeCall c{q, nullptr, nullptr, block_tables, context_lens, nullptr, num_seqs, num_q_heads, num_kv_heads,
+                 block_size, scale, out, reinterpret_cast<cudaStream_t>(stream), max_blocks_per_seq, num_blocks,
+                 dtype, workspace, cfg, k_new, v_new, k_new ? slot_mapping : nullptr};
+    c.q8 = true;
+    c.k_codes = k_codes;
+    c.k_scales = k_scales;
+    c.v_codes = v_codes;
+    c.v_scales = v_scales;
+    return run_decode(c, dev);
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -512,6 +599,65 @@ ns_status ns_paged_attn_prefill(const void *q, const int32_t *query_start_loc, c
                                     num_seqs, total_q_tokens, num_q_heads, num_kv_heads, head_dim,
                                     block_size, scale, out, stream, max_blocks_per_seq, num_blocks,
                                     dtype, workspace, workspace_bytes, nullptr);
+}
+
+ns_status ns_kv_append_q8_0(const void *k, const void *v, const int64_t *slot_mapping, void *k_codes,
+                            void *k_scales, void *v_codes, void *v_scales, int num_tokens, int num_kv_heads,
+                            int head_dim, int block_size, int64_t num_blocks, ns_dtype dtype, ns_stream_t stream)
+{
+    if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks < 1)
+        return NS_ERR_INVALID_ARG;
+    if (dtype != NS_F16 && dtype != NS_BF16)
+        return NS_ERR_UNSUPPORTED;
+    if (head_dim != ns::kHeadDim || bs_index(block_size) < 0)
+        return NS_ERR_UNSUPPORTED;
+    if (num_tokens == 0)
+        return NS_OK;
+    if (!k || !v || !slot_mapping || !k_codes || !k_scales || !v_codes || !v_scales)
+        return NS_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_codes) || !aligned16(k_scales) || !aligned16(v_codes) ||
+        !aligned16(v_scales))
+        return NS_ERR_INVALID_ARG;
+    int dev = 0;
+    if (current_device(&dev) != cudaSuccess)
+        return NS_ERR_CUDA;
+    unsigned *status = status_word(dev);
+    if (status == nullptr)
+        return NS_ERR_CUDA;
+    return ns::launch_kv_append_q8(k, v, slot_mapping, k_codes, k_scales, v_codes, v_scales, num_tokens,
+                                   num_kv_heads, block_size, num_blocks, dtype, status,
+                                   reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? NS_OK
+               : NS_ERR_CUDA;
+}
+
+
+ns_status ns_paged_attn_decode_q8_0(const void *q, const void *k_codes, const void *k_scales,
+                                   const void *v_codes, const void *v_scales, const int32_t *block_tables,
+                                   const int32_t *context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                                   int head_dim, int block_size, float scale, void *out, ns_stream_t stream,
+                                   int max_blocks_per_seq, int64_t num_blocks, ns_dtype dtype, void *workspace,
+                                   size_t workspace_bytes)
+{
+    return decode_q8_0(q, nullptr, nullptr, nullptr, k_codes, k_scales, v_codes, v_scales, block_tables,
+                       context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, scale, out,
+                       stream, max_blocks_per_seq, num_blocks, dtype, workspace, workspace_bytes, nullptr);
+}
+
+ns_status ns_kv_append_paged_attn_decode_q8_0(const void *q, const void *k_new, const void *v_new,
+                                             const int64_t *slot_mapping, void *k_codes, void *k_scales,
+                                             void *v_codes, void *v_scales, const int32_t *block_tables,
+                                             const int32_t *context_lens, int num_seqs, int num_q_heads,
+                                             int num_kv_heads, int head_dim, int block_size, float scale,
+                                             void *out, ns_stream_t stream, int max_blocks_per_seq,
+                                             int64_t num_blocks, ns_dtype dtype, void *workspace,
+                                             size_t workspace_bytes)
+{
+    if (!k_new)
+        return NS_ERR_INVALID_ARG;
+    return decode_q8_0(q, k_new, v_new, slot_mapping, k_codes, k_scales, v_codes, v_scales, block_tables,
+                       context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, scale, out,
+                       stream, max_blocks_per_seq, num_blocks, dtype, workspace, workspace_bytes, nullptr);
 }
 
 ns_status ns_get_device_status(ns_stream_t stream, uint32_t *bits, int clear)

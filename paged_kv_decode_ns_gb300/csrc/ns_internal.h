@@ -12,6 +12,12 @@ cudaError_t launch_kv_append(const void *k, const void *v, const int64_t *slot_m
                              void *v_pool, int num_tokens, int num_kv_heads, int block_size,
                              long long num_blocks, unsigned *status, cudaStream_t stream);
 
+// q8_0 append: quantise each new token's K/V rows and scatter codes and scales.
+cudaError_t launch_kv_append_q8(const void *k, const void *v, const int64_t *slot_mapping, void *k_codes,
+                                void *k_scales, void *v_codes, void *v_scales, int num_tokens, int num_kv_heads,
+                                int block_size, long long num_blocks, ns_dtype dtype, unsigned *status,
+                                cudaStream_t stream);
+
 // Query spans -> per-row table row and key count (prefill through the decode
 // walk).  Rows of spans with at least `tc_min_span` tokens (tc_min_span > 0)
 // are marked for the tensor-core kernel: table row -1, key count 0.
@@ -27,7 +33,7 @@ struct DecodeParams;
 // Launch the split-KV decode kernel with num_ctas CTAs, or with the resident
 // CTAs of device `dev` when num_ctas is 0.
 ns_status launch_decode(const DecodeParams &P, ns_dtype dtype, int block_size, int num_ctas,
-                        cudaStream_t stream, int dev);
+                        cudaStream_t stream, int dev, bool q8 = false);
 
 // Chunked prefill of every span of two or more tokens on the tcgen05 tensor cores.
 // after_walk: the kernel just before it on the stream is this call's span walk

@@ -91,6 +91,12 @@ struct DecodeParams {
     const int64_t *slot_mapping;
     uint16_t *k_pool_w;
     uint16_t *v_pool_w;
+    // q8_0 pools (the Q8 kernels): int8 codes [NB][Hkv][bs][64] and fp16
+    // scales [NB][Hkv][bs][2], one scale per 32 consecutive elements of a row
+    const int8_t *k_codes;
+    const int8_t *v_codes;
+    const uint16_t *k_scales;
+    const uint16_t *v_scales;
     int num_seqs;
     int num_q_heads;
     int num_kv_heads;
@@ -215,17 +221,34 @@ struct PieceRef {
 // One ring slot: K and V rows of one 32-token step and the q rows that ride
 // with a piece's first step.  With a fused append the new token's K/V are
 // copied straight into their row of the step.
-template <int G>
+template <int G, bool Q8>
 struct DecodeSlot {
     uint16_t k[kStepTokens * kHeadDim];
     uint16_t v[kStepTokens * kHeadDim];
     uint16_t q[G * kHeadDim];
 };
 
-template <int BS, int G, int S>
+// q8_0 pools: a step holds each row's 64 int8 codes and 2 fp16 scales, and the
+// new token's 16-bit K/V rows (fused append), which the consumer quantises.
+constexpr int kQ8Block = 32;                        // elements per scale
+constexpr int kQ8Scales = kHeadDim / kQ8Block;      // scales per row
+constexpr int kQ8CodeRow = kHeadDim;                // bytes of a row's codes
+constexpr int kQ8ScaleRow = kQ8Scales * 2;          // bytes of a row's scales
+template <int G>
+struct DecodeSlot<G, true> {
+    int8_t k[kStepTokens * kHeadDim];
+    int8_t v[kStepTokens * kHeadDim];
+    uint16_t ks[kStepTokens * kQ8Scales];
+    uint16_t vs[kStepTokens * kQ8Scales];
+    uint16_t q[G * kHeadDim];
+    uint16_t knew[kHeadDim];
+    uint16_t vnew[kHeadDim];
+};
+
+template <int BS, int G, int S, bool Q8 = false>
 struct DecodeSmem {
     static constexpr int NG = DecodeShape<G>::NG;
-    DecodeSlot<G> ring[NG][S];
+    DecodeSlot<G, Q8> ring[NG][S];
     float p[kConsumerWarps][kStepTokens][DecodeShape<G>::PSTRIDE];  // p per consumer warp [token][head]
     SlotMeta meta[NG][S];
     uint64_t full[NG][S];                    // producer -> consumers: the step has landed
@@ -246,10 +269,12 @@ struct DecodeSmem {
 
 // Slots per ring: as many (up to four) as fit in a CTA's shared memory.
 constexpr size_t kMaxDynSmem = 227 * 1024;
-template <int BS, int G>
+template <int BS, int G, bool Q8 = false>
 constexpr int decode_stages()
 {
-    return sizeof(DecodeSmem<BS, G, 4>) <= kMaxDynSmem ? 4 : sizeof(DecodeSmem<BS, G, 3>) <= kMaxDynSmem ? 3 : 2;
+    return sizeof(DecodeSmem<BS, G, 4, Q8>) <= kMaxDynSmem   ? 4
+           : sizeof(DecodeSmem<BS, G, 3, Q8>) <= kMaxDynSmem ? 3
+                                                              : 2;
 }
 
 __device__ __forceinline__ int nblocks_of(int L, int BS) { return (L + BS - 1) / BS; }
@@ -477,9 +502,68 @@ __device__ __forceinline__ int step_token0(const PieceWalk &w, int i)
 // (bit t of vmask clear) get score -inf, so p = 0; their rows in the slot are
 // zero-filled by the producer, so p * v adds nothing.
 // ---------------------------------------------------------------------------
+// A row's 8 elements of this lane (dims 8c..8c+7) from a ring slot, as four
+// fp32 pairs, and (q8_0) the row's scale for those dims.  16-bit pools: the
+// elements themselves, scale 1.  q8_0: the codes, converted exactly (a code
+// byte, offset by 128, is placed in the mantissa of 2^23 and 2^23 + 128 is
+// subtracted), and the fp16 scale of the 32-element block.
+template <typename T, int G, bool Q8>
+struct RowLoad;
+
 template <typename T, int G>
-__device__ __forceinline__ void process_step(const uint16_t *__restrict__ kb,
-                                             const uint16_t *__restrict__ vb, uint32_t vmask,
+struct RowLoad<T, G, false> {
+    static __device__ __forceinline__ void k(const DecodeSlot<G, false> &sl, int row, int c, float2 (&x)[4], float &d)
+    {
+        const uint4 w = lds128(sl.k + row * kHeadDim + c * 8);
+        x[0] = unpack2<T>(w.x);
+        x[1] = unpack2<T>(w.y);
+        x[2] = unpack2<T>(w.z);
+        x[3] = unpack2<T>(w.w);
+        d = 1.f;
+    }
+    static __device__ __forceinline__ void v(const DecodeSlot<G, false> &sl, int row, int c, float2 (&x)[4], float &d)
+    {
+        const uint4 w = lds128(sl.v + row * kHeadDim + c * 8);
+        x[0] = unpack2<T>(w.x);
+        x[1] = unpack2<T>(w.y);
+        x[2] = unpack2<T>(w.z);
+        x[3] = unpack2<T>(w.w);
+        d = 1.f;
+    }
+};
+
+__device__ __forceinline__ float2 q8_code_pair(uint32_t biased, int k)
+{
+    const float2 f = make_float2(__int_as_float(__byte_perm(biased, 0x4B000000u, 0x7540u + k)),
+                                 __int_as_float(__byte_perm(biased, 0x4B000000u, 0x7541u + k)));
+    return fadd2(f, make_float2(-8388736.0f, -8388736.0f));
+}
+
+template <typename T, int G>
+struct RowLoad<T, G, true> {
+    static __device__ __forceinline__ void load(const int8_t *codes, const uint16_t *scales, int row, int c,
+                                                float2 (&x)[4], float &d)
+    {
+        const uint2 w = *reinterpret_cast<const uint2 *>(codes + row * kQ8CodeRow + c * 8);
+        const uint32_t lo = w.x ^ 0x80808080u, hi = w.y ^ 0x80808080u;
+        x[0] = q8_code_pair(lo, 0);
+        x[1] = q8_code_pair(lo, 2);
+        x[2] = q8_code_pair(hi, 0);
+        x[3] = q8_code_pair(hi, 2);
+        d = __half2float(__ushort_as_half(scales[row * kQ8Scales + (c >> 2)]));
+    }
+    static __device__ __forceinline__ void k(const DecodeSlot<G, true> &sl, int row, int c, float2 (&x)[4], float &d)
+    {
+        load(sl.k, sl.ks, row, c, x, d);
+    }
+    static __device__ __forceinline__ void v(const DecodeSlot<G, true> &sl, int row, int c, float2 (&x)[4], float &d)
+    {
+        load(sl.v, sl.vs, row, c, x, d);
+    }
+};
+
+template <typename T, int G, bool Q8>
+__device__ __forceinline__ void process_step(const DecodeSlot<G, Q8> &sl, uint32_t vmask,
                                              const float2 (&q2)[QRegs<G>::N],
                                              float2 (&acc)[G][4], float &m_run, float &l_run,
                                              float *pbuf, int lane)
@@ -505,17 +589,22 @@ __device__ __forceinline__ void process_step(const uint16_t *__restrict__ kb,
             float2 a[kQkRows][NP];
 #pragma unroll
             for (int u = 0; u < kQkRows; ++u) {
-                const uint4 kw = lds128(kb + ((st + u) * 4 + r) * kHeadDim + c * 8);
-                const uint32_t w[4] = {kw.x, kw.y, kw.z, kw.w};
+                float2 kx[4];  // dims 2e, 2e+1 of the lane's 8
+                float kd;
+                RowLoad<T, G, Q8>::k(sl, (st + u) * 4 + r, c, kx, kd);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float2 kv = unpack2<T>(w[e]);  // dims 2e, 2e+1 of the lane's 8
-                    const float2 k0 = make_float2(kv.x, kv.x), k1 = make_float2(kv.y, kv.y);
+                    const float2 k0 = make_float2(kx[e].x, kx[e].x), k1 = make_float2(kx[e].y, kx[e].y);
 #pragma unroll
                     for (int m = 0; m < NP; ++m) {
                         a[u][m] = e == 0 ? fmul2(q2[m * 8], k0) : ffma2(q2[m * 8 + 2 * e], k0, a[u][m]);
                         a[u][m] = ffma2(q2[m * 8 + 2 * e + 1], k1, a[u][m]);
                     }
+                }
+                if constexpr (Q8) {  // the row's scale for this lane's dims, before lanes combine
+#pragma unroll
+                    for (int m = 0; m < NP; ++m)
+                        a[u][m] = fmul2(a[u][m], make_float2(kd, kd));
                 }
             }
             // Reduce-scatter over the row's 8 lanes: whole pairs are halved
@@ -545,12 +634,16 @@ __device__ __forceinline__ void process_step(const uint16_t *__restrict__ kb,
             // One head: dim pairs, then a sum over the row's 8 lanes.
 #pragma unroll
             for (int u = 0; u < kQkRows; ++u) {
-                const uint4 kw = lds128(kb + ((st + u) * 4 + r) * kHeadDim + c * 8);
-                float2 a = fmul2(q2[0], unpack2<T>(kw.x));
-                a = ffma2(q2[1], unpack2<T>(kw.y), a);
-                a = ffma2(q2[2], unpack2<T>(kw.z), a);
-                a = ffma2(q2[3], unpack2<T>(kw.w), a);
+                float2 kx[4];
+                float kd;
+                RowLoad<T, G, Q8>::k(sl, (st + u) * 4 + r, c, kx, kd);
+                float2 a = fmul2(q2[0], kx[0]);
+                a = ffma2(q2[1], kx[1], a);
+                a = ffma2(q2[2], kx[2], a);
+                a = ffma2(q2[3], kx[3], a);
                 zz[u] = a.x + a.y;
+                if constexpr (Q8)
+                    zz[u] *= kd;
             }
 #pragma unroll
             for (int m = 4; m >= 1; m >>= 1)
@@ -606,9 +699,18 @@ __device__ __forceinline__ void process_step(const uint16_t *__restrict__ kb,
 #pragma unroll
     for (int st = 0; st < STEPS; ++st) {
         const int t = st * 4 + r;
-        const uint4 vw = lds128(vb + t * kHeadDim + c * 8);
-        float2 v0 = unpack2<T>(vw.x), v1 = unpack2<T>(vw.y);
-        float2 v2 = unpack2<T>(vw.z), v3 = unpack2<T>(vw.w);
+        float2 vx[4];
+        float vd;
+        RowLoad<T, G, Q8>::v(sl, t, c, vx, vd);
+        if constexpr (Q8) {
+            // a row that holds no key has p = 0 and zero codes, but its pool
+            // scale may be anything: use 0
+            const float d = ((vmask >> t) & 1u) ? vd : 0.f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                vx[k] = fmul2(vx[k], make_float2(d, d));
+        }
+        const float2 v0 = vx[0], v1 = vx[1], v2 = vx[2], v3 = vx[3];
         const float4 *prow = reinterpret_cast<const float4 *>(pbuf + t * HeadSlots<G>::PSTRIDE);
         float4 pp[(G + 3) / 4];
 #pragma unroll
@@ -935,8 +1037,8 @@ __device__ __forceinline__ void piece_prefetch(const DecodeParams &P, const Piec
 // SlotMeta.  Consumers then hold no walk or issue state: their registers go
 // to the scores and accumulators.
 // ---------------------------------------------------------------------------
-template <typename T, int BS, int G, int S>
-__device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, const Split &sp, int pwarp,
+template <typename T, int BS, int G, int S, bool Q8>
+__device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8> &sm, const Split &sp, int pwarp,
                                 int lane)
 {
     constexpr int KB = kStepTokens / BS;  // blocks per step
@@ -989,7 +1091,7 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
         if (P.overlap && issued == 0)
             grid_dependency_wait();
         SlotMeta &mt = sm.meta[w][slot];
-        DecodeSlot<G> &sl = sm.ring[w][slot];
+        DecodeSlot<G, Q8> &sl = sm.ring[w][slot];
         uint64_t *bar = &sm.full[w][slot];
         if (!has || step >= nsteps) {
             if (!ahead) {
@@ -1084,7 +1186,12 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
         // token's block row r_new comes from k_new/v_new; every other row is
         // zero-filled, so that each row of the slot is finite and a masked
         // token (p = 0) adds nothing.  Zero ranges: [rows, za) and [zb, BS).
+        // (q8_0: the codes likewise; the scales of a loaded block are copied
+        // whole, a 16-byte multiple, and the consumer ignores those of rows
+        // without a key; the new token's rows land in the slot's staging rows
+        // and the consumer quantises them into row r_new.)
         const int pend_tok = piece_end_token<BS>(cur);
+        constexpr uint32_t kRowB = Q8 ? (uint32_t)kQ8CodeRow : (uint32_t)kRowBytes;
         int rows[KB], za[KB], zb[KB];
         uint32_t bytes = (first_step ? (uint32_t)G * kRowBytes : 0u) + (new_tok ? 2u * kRowBytes : 0u);
 #pragma unroll
@@ -1093,7 +1200,9 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
             rows[u] = phys[u] < 0 ? 0 : (u == u_last ? r_new : keys);
             za[u] = u == u_last ? r_new : BS;      // zero rows [rows, za)
             zb[u] = u == u_last ? r_new + 1 : BS;  // and [zb, BS)
-            bytes += 2u * (uint32_t)(rows[u] + (za[u] - rows[u]) + (BS - zb[u])) * kRowBytes;
+            bytes += 2u * (uint32_t)(rows[u] + (za[u] - rows[u]) + (BS - zb[u])) * kRowB;
+            if (Q8)
+                bytes += 2u * (uint32_t)(BS * kQ8ScaleRow);
         }
         if (bytes == 0)
             mbar_arrive(bar);
@@ -1101,18 +1210,32 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
             mbar_arrive_expect_tx(bar, bytes);
 #pragma unroll
         for (int u = 0; u < KB; ++u) {
-            if (rows[u] > 0) {
-                const long long off = ((long long)phys[u] * P.num_kv_heads + cur.ph) * BS * kHeadDim;
-                bulk_load(sl.k + u * BS * kHeadDim, P.k_pool + off, rows[u] * kRowBytes, bar, pol);
-                bulk_load(sl.v + u * BS * kHeadDim, P.v_pool + off, rows[u] * kRowBytes, bar, pol);
+            const long long row0 = ((long long)phys[u] * P.num_kv_heads + cur.ph) * BS;  // pool row of the block
+            if constexpr (!Q8) {
+                if (rows[u] > 0) {
+                    bulk_load(sl.k + u * BS * kHeadDim, P.k_pool + row0 * kHeadDim, rows[u] * kRowBytes, bar, pol);
+                    bulk_load(sl.v + u * BS * kHeadDim, P.v_pool + row0 * kHeadDim, rows[u] * kRowBytes, bar, pol);
+                }
+            } else {
+                if (rows[u] > 0) {
+                    bulk_load(sl.k + u * BS * kHeadDim, P.k_codes + row0 * kQ8CodeRow, rows[u] * kQ8CodeRow, bar, pol);
+                    bulk_load(sl.v + u * BS * kHeadDim, P.v_codes + row0 * kQ8CodeRow, rows[u] * kQ8CodeRow, bar, pol);
+                }
+                if (phys[u] >= 0) {
+                    bulk_load(sl.ks + u * BS * kQ8Scales, P.k_scales + row0 * kQ8Scales, BS * kQ8ScaleRow, bar, pol);
+                    bulk_load(sl.vs + u * BS * kQ8Scales, P.v_scales + row0 * kQ8Scales, BS * kQ8ScaleRow, bar, pol);
+                } else {
+                    bulk_load(sl.ks + u * BS * kQ8Scales, g_zero_rows, BS * kQ8ScaleRow, bar);
+                    bulk_load(sl.vs + u * BS * kQ8Scales, g_zero_rows, BS * kQ8ScaleRow, bar);
+                }
             }
             if (za[u] > rows[u]) {
-                const uint32_t n = (uint32_t)(za[u] - rows[u]) * kRowBytes;
+                const uint32_t n = (uint32_t)(za[u] - rows[u]) * kRowB;
                 bulk_load(sl.k + (u * BS + rows[u]) * kHeadDim, g_zero_rows, n, bar);
                 bulk_load(sl.v + (u * BS + rows[u]) * kHeadDim, g_zero_rows, n, bar);
             }
             if (zb[u] < BS) {
-                const uint32_t n = (uint32_t)(BS - zb[u]) * kRowBytes;
+                const uint32_t n = (uint32_t)(BS - zb[u]) * kRowB;
                 bulk_load(sl.k + (u * BS + zb[u]) * kHeadDim, g_zero_rows, n, bar);
                 bulk_load(sl.v + (u * BS + zb[u]) * kHeadDim, g_zero_rows, n, bar);
             }
@@ -1123,9 +1246,14 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
         }
         if (new_tok) {
             const long long noff = ((long long)cur.ps * P.num_kv_heads + cur.ph) * kHeadDim;
-            const int t_new = (cur.pL - 1) - tok0;
-            bulk_load(sl.k + t_new * kHeadDim, P.k_new + noff, kRowBytes, bar);
-            bulk_load(sl.v + t_new * kHeadDim, P.v_new + noff, kRowBytes, bar);
+            if constexpr (!Q8) {
+                const int t_new = (cur.pL - 1) - tok0;
+                bulk_load(sl.k + t_new * kHeadDim, P.k_new + noff, kRowBytes, bar);
+                bulk_load(sl.v + t_new * kHeadDim, P.v_new + noff, kRowBytes, bar);
+            } else {
+                bulk_load(sl.knew, P.k_new + noff, kRowBytes, bar);
+                bulk_load(sl.vnew, P.v_new + noff, kRowBytes, bar);
+            }
         }
         ++issued;
         ++step;
@@ -1150,8 +1278,55 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
 // writes the output or its part of a partial record; then frees the slot
 // (its empty barrier).
 // ---------------------------------------------------------------------------
-template <typename T, int BS, int G, int S>
-__device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm, const Split &sp, int ring,
+// q8_0 quantisation of the new token's K (lanes 0-7) and V (lanes 8-15) rows,
+// staged in the slot as 16-bit rows, into row t of the slot and, for a valid
+// slot, into the pool.  A block of 32 elements is four lanes' eight: its
+// scale d = max|x| / 127 and every code rint(x * (1/d)) (ties to even,
+// clamped to +-127) are rounded to fp32 at each step, and d is stored as
+// fp16 (nearest even, saturating), the decisions the CPU oracle takes.
+template <typename T, int BS, int G>
+__device__ __forceinline__ void quantize_new_row(const DecodeParams &P, DecodeSlot<G, true> &sl, int t,
+                                                 long long new_slot, int ph, int lane)
+{
+    const int cc = lane & 7;
+    const bool isv = (lane & 8) != 0;
+    const uint4 w = lds128((isv ? sl.vnew : sl.knew) + cc * 8);
+    const float2 x0 = unpack2<T>(w.x), x1 = unpack2<T>(w.y), x2 = unpack2<T>(w.z), x3 = unpack2<T>(w.w);
+    const float x[8] = {x0.x, x0.y, x1.x, x1.y, x2.x, x2.y, x3.x, x3.y};
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        amax = fmaxf(amax, fabsf(x[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const float d = __fdiv_rn(amax, 127.f);
+    const float inv = d > 0.f ? __fdiv_rn(1.f, d) : 0.f;
+    uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int code = max(-127, min(127, __float2int_rn(__fmul_rn(x[i], inv))));
+        packed[i >> 2] |= (uint32_t)(code & 0xff) << (8 * (i & 3));
+    }
+    const uint16_t d16 = __half_as_ushort(__float2half_rn(fminf(d, 65504.f)));
+    if (lane < 16) {
+        int8_t *row = (isv ? sl.v : sl.k) + t * kQ8CodeRow + cc * 8;
+        *reinterpret_cast<uint2 *>(row) = make_uint2(packed[0], packed[1]);
+        if ((cc & 3) == 0)
+            (isv ? sl.vs : sl.ks)[t * kQ8Scales + (cc >> 2)] = d16;
+        if (new_slot >= 0) {
+            const long long prow = ((new_slot / BS) * P.num_kv_heads + ph) * BS + new_slot % BS;
+            int8_t *codes = const_cast<int8_t *>(isv ? P.v_codes : P.k_codes);
+            uint16_t *scales = const_cast<uint16_t *>(isv ? P.v_scales : P.k_scales);
+            *reinterpret_cast<uint2 *>(codes + prow * kQ8CodeRow + cc * 8) = make_uint2(packed[0], packed[1]);
+            if ((cc & 3) == 0)
+                scales[prow * kQ8Scales + (cc >> 2)] = d16;
+        }
+    }
+    __syncwarp();
+}
+
+template <typename T, int BS, int G, int S, bool Q8>
+__device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8> &sm, const Split &sp, int ring,
                                 int warp, int lane)
 {
     constexpr int NS = HeadSlots<G>::N;
@@ -1229,20 +1404,27 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S> &sm,
         for (int step = 0;;) {
             if (nsteps > 0) {
                 const SlotMeta &mt = sm.meta[ring][slot];
-                DecodeSlot<G> &sl = sm.ring[ring][slot];
+                DecodeSlot<G, Q8> &sl = sm.ring[ring][slot];
                 // fused append (the piece's last step): the new token's K/V
-                // landed in its row of the slot; this warp also writes them
-                // to the pool slot the producer checked
-                if (step == nsteps - 1 && (mt.flags & kFlagNewTok) && lane < 16 && mt.new_slot >= 0) {
-                    const int cc = lane & 7;
-                    const uint4 val = lds128((lane < 8 ? sl.k : sl.v) + mt.t_new * kHeadDim + cc * 8);
-                    const long long ns = mt.new_slot;
-                    const long long dst = (((ns / BS) * P.num_kv_heads + mt.ph) * BS + ns % BS) * kHeadDim + cc * 8;
-                    *reinterpret_cast<uint4 *>((lane < 8 ? P.k_pool_w : P.v_pool_w) + dst) = val;
+                // landed in the slot; this warp also writes them to the pool
+                // slot the producer checked (q8_0: quantised first)
+                if (step == nsteps - 1 && (mt.flags & kFlagNewTok)) {
+                    if constexpr (!Q8) {
+                        if (lane < 16 && mt.new_slot >= 0) {
+                            const int cc = lane & 7;
+                            const uint4 val = lds128((lane < 8 ? sl.k : sl.v) + mt.t_new * kHeadDim + cc * 8);
+                            const long long ns = mt.new_slot;
+                            const long long dst =
+                                (((ns / BS) * P.num_kv_heads + mt.ph) * BS + ns % BS) * kHeadDim + cc * 8;
+                            *reinterpret_cast<uint4 *>((lane < 8 ? P.k_pool_w : P.v_pool_w) + dst) = val;
+                        }
+                    } else {
+                        quantize_new_row<T, BS, G>(P, sl, mt.t_new, mt.new_slot, mt.ph, lane);
+                    }
                 }
                 // one step path for full and partial steps: a second, unmasked
                 // copy measured 4% slower (instruction-fetch stalls)
-                process_step<T, G>(sl.k, sl.v, mt.vmask, q2, acc, m_run, l_run, pbuf, lane);
+                process_step<T, G, Q8>(sl, mt.vmask, q2, acc, m_run, l_run, pbuf, lane);
             }
             // The slot is only read (the async proxy alone writes it), so the
             // barrier's release/acquire orders these reads before the refill.
@@ -1449,17 +1631,18 @@ __device__ void decode_side_work(const DecodeParams &P, Smem &sm, const Split &s
     }
 }
 
-template <typename T, int BS, int G, int S>
+template <typename T, int BS, int G, int S, bool Q8>
 __global__ void __launch_bounds__(kDecodeThreads, 1) paged_decode_kernel(const DecodeParams P)
 {
+    using Smem = DecodeSmem<BS, G, S, Q8>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    auto &sm = *reinterpret_cast<DecodeSmem<BS, G, S> *>(smem_raw);
+    auto &sm = *reinterpret_cast<Smem *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     using Shape = DecodeShape<G>;
     // the next grid on the stream may be scheduled on SMs this one frees
     // (only when it was launched as a programmatic dependent)
     grid_launch_dependents();
-    decode_prologue<DecodeSmem<BS, G, S>, BS>(P, sm);
+    decode_prologue<Smem, BS>(P, sm);
     const Split sp = read_split(P, sm);
     // Registers move from the producer warpgroup to the consumer warpgroups;
     // the shares add up to the launch allocation.
@@ -1469,20 +1652,21 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) paged_decode_kernel(const D
         // output and the plan, which the previous grid may still be using
         if (P.overlap)
             grid_dependency_wait();
-        decode_side_work<DecodeSmem<BS, G, S>, BS>(P, sm, sp);
-        decode_consumer<T, BS, G, S>(P, sm, sp, warp, warp, lane);
+        decode_side_work<Smem, BS>(P, sm, sp);
+        decode_consumer<T, BS, G, S, Q8>(P, sm, sp, warp, warp, lane);
     } else {
         regs_shrink<kProducerRegs>();
         if (warp - kConsumerWarps < Shape::PW)
-            decode_producer<T, BS, G, S>(P, sm, sp, warp - kConsumerWarps, lane);
+            decode_producer<T, BS, G, S, Q8>(P, sm, sp, warp - kConsumerWarps, lane);
     }
 }
 
 // Host-side launch helpers (defined in the per-type instantiation files).
-template <typename T, int BS, int G>
+// Q8: the pools are q8_0 codes and scales (DecodeParams.k_codes ...).
+template <typename T, int BS, int G, bool Q8 = false>
 cudaError_t launch_paged_decode(const DecodeParams &P, int num_ctas, cudaStream_t stream);
 
-template <typename T, int BS, int G>
+template <typename T, int BS, int G, bool Q8 = false>
 int decode_ctas_per_sm();
 
 }  // namespace ns
