@@ -226,7 +226,7 @@ def make_workload(name: str):
     return wl.WORKLOADS[name]()
 
 
-def workload_config(st, name, pools, layers=1):
+def workload_config(st, name, pools, layers=1, kv="native"):
     step = ("fused kv_append + split-KV paged decode" if st.is_decode
             else "kv_append + chunked prefill (tensor-core spans, decode-walk rows)")
     if layers > 1:
@@ -235,8 +235,9 @@ def workload_config(st, name, pools, layers=1):
         l2 = (f"inputs larger than L2: {layers} layer pools of "
               f"{2 * st.k_pool.nbytes / 1e6:.0f} MB each (L2 129 MB)")
     else:
+        pool_mb = 2 * st.k_pool.size * st.kv_row_bytes(kv) // st.head_dim / 1e6
         l2 = (f"inputs larger than L2: {pools} rotating pool copies of "
-              f"{2 * st.k_pool.nbytes / 1e6:.0f} MB each (L2 129 MB)")
+              f"{pool_mb:.0f} MB each (L2 129 MB)")
     return {"workload": f"{st.name}: {name}" + (f" x {layers} layers" if layers > 1 else ""),
             "layers": layers, "num_seqs": st.num_seqs,
             "context_tokens": int(st.context_lens.sum()),
@@ -244,6 +245,7 @@ def workload_config(st, name, pools, layers=1):
             "num_q_heads": st.num_q_heads, "num_kv_heads": st.num_kv_heads,
             "head_dim": st.head_dim, "block_size": st.block_size,
             "num_blocks": st.num_blocks, "step": step, "query_tokens": st.num_tokens,
+            "kv_cache": "q8_0 (int8 codes, fp16 scale per 32 elements)" if kv == "q8_0" else st.dtype,
             "l2": l2}
 
 
@@ -295,10 +297,11 @@ class Step:
     generator); block tables, lengths and slots are shared.
     """
 
-    def __init__(self, st, dev, npools, layers=1, overlap=False):
+    def __init__(self, st, dev, npools, layers=1, overlap=False, kv="native"):
         import torch
         from paged_kv_decode_ns_gb300 import binding as nb
         self.nb, self.torch, self.st, self.dev = nb, torch, st, dev
+        self.kv = kv
 
         def dt_of(bits):
             t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev)
@@ -331,6 +334,14 @@ class Step:
             self.config = nb.DecodeConfig()
             self.config.overlap_prologue = 1
         self.layer_io = []
+        self.q8pools = []
+        if kv == "q8_0":
+            if not self.decode or layers > 1:
+                raise ValueError("--kv q8_0 applies to single-layer decode workloads")
+            # each pool copy quantised on the device by the library's own append
+            # (every pool slot is a token), then the 16-bit copies are dropped
+            self.q8pools = [self.quantize_pool(kp, vp) for kp, vp in self.pools]
+            self.pools = [self.pools[0]]
         if layers > 1:
             if not self.decode:
                 raise ValueError("layers > 1 applies to decode workloads")
@@ -348,6 +359,19 @@ class Step:
             self.out = self.layer_io[-1][5]  # read back end to end: the last layer's output
             self.launches = layers
 
+    def quantize_pool(self, kp, vp):
+        torch, nb = self.torch, self.nb
+        NB, Hkv, bs, D = kp.shape
+        kc = torch.empty((NB, Hkv, bs, D), dtype=torch.int8, device=self.dev)
+        vc = torch.empty_like(kc)
+        ks = torch.empty((NB, Hkv, bs, D // 32), dtype=torch.float16, device=self.dev)
+        vs = torch.empty_like(ks)
+        rows_k = kp.permute(0, 2, 1, 3).contiguous().view(NB * bs, Hkv, D)
+        rows_v = vp.permute(0, 2, 1, 3).contiguous().view(NB * bs, Hkv, D)
+        slots = torch.arange(NB * bs, dtype=torch.int64, device=self.dev)
+        nb.ns_kv_append_q8_0(rows_k, rows_v, slots, kc, ks, vc, vs)
+        return kc, ks, vc, vs
+
     def run_layer(self, layer, stream=None):
         kp, vp, q, kn, vn, out = self.layer_io[layer]
         self.nb.ns_kv_append_paged_attn_decode(q, kn, vn, self.slots, kp, vp, self.tables, self.lens,
@@ -358,6 +382,12 @@ class Step:
         if self.layers > 1:
             for layer in range(self.layers):
                 self.run_layer(layer, stream)
+            return
+        if self.q8pools:
+            kc, ks, vc, vs = self.q8pools[i % len(self.q8pools)]
+            self.nb.ns_kv_append_paged_attn_decode_q8_0(self.q, self.k_new, self.v_new, self.slots, kc, ks, vc,
+                                                        vs, self.tables, self.lens, self.st.scale, self.out,
+                                                        self.ws, stream=stream)
             return
         kp, vp = self.pools[i % self.npools]
         if self.decode:
@@ -413,24 +443,27 @@ def stage_inputs(step, torch, dev):
     return d_all, h_all
 
 
-def time_events(torch, stream, fn, n, queue_ahead=False):
-    """Mean device time of fn(i) over n calls, each bracketed by events (ms).
-
-    queue_ahead: first hold the stream with a device-side sleep long enough
-    for the host to enqueue every call, so that no bracket also measures the
-    host preparing a call (a call whose host side takes longer than its
-    kernel would otherwise leave the device idle inside its bracket)."""
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(n)]
-    if queue_ahead and hasattr(torch.cuda, "_sleep"):
+def hold_stream(torch, stream, calls):
+    """Hold the stream with a device-side sleep long enough for the host to
+    enqueue `calls` calls behind it, so that the device never waits for the
+    host inside a timed region (a call's host side can take longer than its
+    kernel)."""
+    if hasattr(torch.cuda, "_sleep"):
         with torch.cuda.stream(stream):
-            torch.cuda._sleep(int(200_000 * n))  # ~100 us of clock cycles per call
-    for i, (a, b) in enumerate(evs):
-        a.record(stream)
+            torch.cuda._sleep(int(200_000 * calls))  # ~100 us of clock cycles per call
+
+
+def time_events(torch, stream, fn, n):
+    """Mean device time of fn(i) over n back-to-back calls between two events
+    on the launch stream (ms), queued behind a hold of the stream."""
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    hold_stream(torch, stream, n)
+    a.record(stream)
+    for i in range(n):
         fn(i)
-        b.record(stream)
+    b.record(stream)
     torch.cuda.synchronize()
-    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+    return a.elapsed_time(b) / n
 
 
 def bench_ours(args):
@@ -442,11 +475,11 @@ def bench_ours(args):
     dist = init_dist(world, "nccl")
     dev = torch.device("cuda", local)
     st = make_workload(args.workload)
-    pool_bytes = 2 * st.k_pool.nbytes
+    pool_bytes = 2 * st.k_pool.size * st.kv_row_bytes(args.kv) // st.head_dim
     npools = max(1, args.pools if args.pools else math.ceil(2 * L2_BYTES / max(pool_bytes, 1)))
     if args.layers > 1:
         npools = 1  # the layers' pools are the rotation
-    step = Step(st, dev, npools, layers=args.layers, overlap=args.overlap)
+    step = Step(st, dev, npools, layers=args.layers, overlap=args.overlap, kv=args.kv)
     stream = torch.cuda.current_stream(dev)
 
     sampler = ClockSampler(local) if rank == 0 else None
@@ -461,6 +494,7 @@ def bench_ours(args):
     barrier(dist)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    hold_stream(torch, stream, min(args.steps, 4000))
     e0.record(stream)
     for i in range(args.steps):
         step.run(i)
@@ -472,7 +506,7 @@ def bench_ours(args):
     # ---- the same steps launched as programmatic dependents (opt-in in the
     # API: each launch's prologue may overlap the previous kernel's tail)
     overlap_us = None
-    if step.decode and not args.overlap and args.steps >= 10:
+    if step.decode and not args.overlap and args.steps >= 10 and args.kv == "native":
         plain_cfg, step.config = step.config, nb.DecodeConfig()
         step.config.overlap_prologue = 1
         n_ov = min(args.steps, 2000)
@@ -490,7 +524,7 @@ def bench_ours(args):
 
     # ---- the dominant kernel per launch (events on its stream)
     n_lat = max(3, min(args.steps, 200))
-    launch_ms = time_events(torch, stream, step.run_dominant, n_lat, queue_ahead=True)
+    launch_ms = time_events(torch, stream, step.run_dominant, n_lat)
 
     # ---- CUDA-graph replay of the same steps (launch overhead removed)
     graph_us = None
@@ -557,8 +591,8 @@ def bench_ours(args):
     e2e_ms = e2.elapsed_time(e3)
     nb.raise_on_device_status()
 
-    kv_bytes = st.kv_read_bytes() * args.layers
-    alg_bytes = st.algorithmic_bytes(with_append=True)  # one launch: one layer
+    kv_bytes = st.kv_read_bytes(args.kv) * args.layers
+    alg_bytes = st.algorithmic_bytes(with_append=True, kv=args.kv)  # one launch: one layer
     t_max, units = reduce_max_sum(dist, elapsed_ms, kv_bytes * args.steps, dev)
     te2e_max, units_e2e = reduce_max_sum(dist, e2e_ms, kv_bytes * n_e2e, dev)
     if rank != 0:
@@ -569,11 +603,12 @@ def bench_ours(args):
     if step.decode:
         peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
         achieved = alg_bytes / (launch_ms * 1e-3) / 1e9
-        traffic = args.traffic if args.traffic is not None else profiled_traffic(args.workload,
-                                                                                  "paged_decode_kernel")
+        traffic = args.traffic if args.traffic is not None else (
+            profiled_traffic(args.workload, "paged_decode_kernel") if args.kv == "native" else None)
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                     "frac": achieved / peak, "traffic": traffic,
-                    "kernel": "paged_decode_kernel (fused kv_append + split-KV decode)",
+                    "kernel": "paged_decode_kernel (fused kv_append + split-KV decode"
+                              + (", q8_0 pools)" if args.kv == "q8_0" else ")"),
                     "bytes_per_launch": alg_bytes, "launch_us": launch_ms * 1e3,
                     "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"}
     else:
@@ -612,7 +647,7 @@ def bench_ours(args):
                      if args.layers > 1 else None),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": st.dtype, "data": "synthetic (seeded; no dataset or weights involved)",
-        "config": dict(workload_config(st, args.workload, npools, args.layers),
+        "config": dict(workload_config(st, args.workload, npools, args.layers, args.kv),
                        overlap_prologue=bool(args.overlap)),
         "roofline": roofline,
         "cpu_baseline": cpu,
@@ -672,6 +707,8 @@ def main(argv=None):
     ap.add_argument("--overlap", action="store_true",
                     help="decode launches as programmatic dependents (a prologue may overlap the "
                          "previous kernel's tail); off for the default line")
+    ap.add_argument("--kv", choices=["native", "q8_0"], default="native",
+                    help="KV pool format: the workload's 16-bit type, or the 8-bit q8_0 cache")
     ap.add_argument("--layers", type=int, default=1,
                     help="attention layers per step (decode workloads; 24 = the Qwen2.5-0.5B stack)")
     ap.add_argument("--pools", type=int, default=0, help="rotating pool copies (0 = enough to exceed 2x L2)")

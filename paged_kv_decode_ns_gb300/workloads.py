@@ -127,27 +127,36 @@ class PagedStep:
     def is_decode(self) -> bool:
         return bool(np.all(self.query_lens == 1))
 
-    def kv_read_bytes(self) -> int:
-        """K and V bytes one attention pass over every context reads."""
-        return int(self.context_lens.astype(np.int64).sum()) * self.num_kv_heads * self.head_dim * 2 * 2
+    def kv_row_bytes(self, kv: str = "native") -> int:
+        """Bytes of one token's K (or V) row of one kv head in the pool: 2 per
+        element for the 16-bit pools; for q8_0 one code per element plus an
+        fp16 scale per 32 elements."""
+        if kv == "q8_0":
+            return self.head_dim + 2 * (self.head_dim // 32)
+        return 2 * self.head_dim
 
-    def algorithmic_bytes(self, with_append: bool = True) -> int:
+    def kv_read_bytes(self, kv: str = "native") -> int:
+        """K and V bytes one attention pass over every context reads."""
+        return int(self.context_lens.astype(np.int64).sum()) * self.num_kv_heads * 2 * self.kv_row_bytes(kv)
+
+    def algorithmic_bytes(self, with_append: bool = True, kv: str = "native") -> int:
         """Bytes the step must move at minimum (each input read once, output written once).
 
         K/V of every context token + q in + out + the block-table entries in
         use + context lengths (+ new K/V read, pool slots written and slots read
-        when the append is part of the step).
+        when the append is part of the step).  ``kv`` is the pool format.
         """
         esz = 2
-        b = self.kv_read_bytes()
+        b = self.kv_read_bytes(kv)
         b += 2 * self.num_tokens * self.num_q_heads * self.head_dim * esz
         nb = sum(blocks_needed(L, self.block_size) for L in self.context_lens)
         b += 4 * nb + 4 * self.num_seqs
         if not self.is_decode:
             b += 4 * (self.num_seqs + 1)
         if with_append:
-            per_tok = self.num_kv_heads * self.head_dim * esz * 2  # K and V
-            b += self.num_tokens * (2 * per_tok + 8)
+            new_rows = self.num_kv_heads * self.head_dim * esz * 2      # K and V read (16-bit)
+            pool_rows = self.num_kv_heads * self.kv_row_bytes(kv) * 2   # K and V written
+            b += self.num_tokens * (new_rows + pool_rows + 8)
         return int(b)
 
 
