@@ -26,10 +26,14 @@
  *               stream) and the call returns without synchronising.  Inputs
  *               must stay valid until the work completes.
  *  Elements     K, V, q and out are fp16 or bf16 (`ns_dtype`), all of one type.
- *  Shapes       head_dim must be 64.  num_q_heads must be a multiple of
- *               num_kv_heads with at most 8 query heads per KV head; query
- *               head j reads KV head j / (num_q_heads / num_kv_heads).
- *               block_size must be 4, 8, 16 or 32.
+ *  Shapes       head_dim is 64, or 128 with block_size 16 (the split-KV
+ *               decode, its fused append and the prefill, whose spans then
+ *               all take the split-KV walk; the tensor-core prefill, the
+ *               q8_0 pools and the allocation-free entry point take 64).
+ *               num_q_heads must be a multiple of num_kv_heads with at most
+ *               8 query heads per KV head; query head j reads KV head
+ *               j / (num_q_heads / num_kv_heads).  block_size must be 4, 8,
+ *               16 or 32.
  *  Pool layout  k_pool and v_pool are [num_blocks][num_kv_heads][block_size]
  *               [head_dim]: one (block, kv head) is block_size*head_dim
  *               contiguous elements.  Token slot s lives in block
@@ -114,9 +118,10 @@ ns_status ns_kv_append(const void *k, const void *v, const int64_t *slot_mapping
 /*
  * Workspace for the attention entry points: split-KV partial results
  * (fp32 running max, running sum and unnormalised output of each piece of a
- * sequence that was cut across workers, about 8.7 MB), one arrival counter per (sequence, kv
- * head) and a small plan record.  Size it with ns_paged_attn_workspace_bytes
- * for the largest num_seqs you will pass.  It must be zero-filled once before
+ * sequence that was cut across workers: about 8.7 MB for head_dim 64, 17 MB
+ * for 128), one arrival counter per (sequence, kv head) and a small plan
+ * record.  Size it with ns_paged_attn_workspace_bytes for the largest
+ * num_seqs and the head_dim you will pass.  It must be zero-filled once before
  * first use (ns_paged_attn_workspace_init or cudaMemsetAsync); every call
  * that completes without a device status bit leaves it ready for the next
  * call.  Two calls that share a workspace must not run concurrently.

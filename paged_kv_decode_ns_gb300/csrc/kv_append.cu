@@ -16,9 +16,10 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4 *__restrict_
                                                         uint4 *__restrict__ k_pool,
                                                         uint4 *__restrict__ v_pool, long long n_chunks,
                                                         int num_kv_heads, int block_size,
-                                                        long long num_slots, unsigned *status)
+                                                        long long num_slots, unsigned *status,
+                                                        int chunks_per_row)
 {
-    constexpr int kChunksPerRow = kRowBytes / 16;
+    const int kChunksPerRow = chunks_per_row;  // 16-byte chunks of a head row
     const long long stride = (long long)gridDim.x * blockDim.x;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n_chunks; i += stride) {
         const long long row = i / kChunksPerRow;  // (token, kv head)
@@ -133,10 +134,11 @@ cudaError_t launch_kv_append_q8(const void *k, const void *v, const int64_t *slo
 }
 
 cudaError_t launch_kv_append(const void *k, const void *v, const int64_t *slot_mapping, void *k_pool,
-                             void *v_pool, int num_tokens, int num_kv_heads, int block_size,
+                             void *v_pool, int num_tokens, int num_kv_heads, int head_dim, int block_size,
                              long long num_blocks, unsigned *status, cudaStream_t stream)
 {
-    const long long n_chunks = (long long)num_tokens * num_kv_heads * (kRowBytes / 16);
+    const int chunks_per_row = head_dim * 2 / 16;
+    const long long n_chunks = (long long)num_tokens * num_kv_heads * chunks_per_row;
     if (n_chunks == 0)
         return cudaSuccess;
     const int threads = 256;
@@ -146,7 +148,7 @@ cudaError_t launch_kv_append(const void *k, const void *v, const int64_t *slot_m
     kv_append_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
         static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping,
         static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool), n_chunks, num_kv_heads,
-        block_size, num_blocks * block_size, status);
+        block_size, num_blocks * block_size, status, chunks_per_row);
     return cudaGetLastError();
 }
 

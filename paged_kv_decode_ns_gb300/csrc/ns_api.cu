@@ -18,6 +18,7 @@ std::atomic<unsigned *> g_status_ptr[kMaxDevices];
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_ctas_per_sm[kMaxDevices][2][4][ns::kMaxGroup];
 std::atomic<int> g_ctas_per_sm_q8[kMaxDevices][2][ns::kMaxGroup];
+std::atomic<int> g_ctas_per_sm_d128[kMaxDevices][2][ns::kMaxGroup];
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -107,6 +108,37 @@ int ctas_per_sm_g(int g)
     }
 }
 
+// head_dim 128: block size 16, 16-bit pools.
+template <typename T>
+cudaError_t dispatch_decode_d128(int g, const ns::DecodeParams &P, int ctas, cudaStream_t s)
+{
+    switch (g) {
+    case 1: return ns::launch_paged_decode<T, 16, 1, false, 128>(P, ctas, s);
+    case 2: return ns::launch_paged_decode<T, 16, 2, false, 128>(P, ctas, s);
+    case 3: return ns::launch_paged_decode<T, 16, 3, false, 128>(P, ctas, s);
+    case 4: return ns::launch_paged_decode<T, 16, 4, false, 128>(P, ctas, s);
+    case 5: return ns::launch_paged_decode<T, 16, 5, false, 128>(P, ctas, s);
+    case 6: return ns::launch_paged_decode<T, 16, 6, false, 128>(P, ctas, s);
+    case 7: return ns::launch_paged_decode<T, 16, 7, false, 128>(P, ctas, s);
+    default: return ns::launch_paged_decode<T, 16, 8, false, 128>(P, ctas, s);
+    }
+}
+
+template <typename T>
+int ctas_per_sm_d128(int g)
+{
+    switch (g) {
+    case 1: return ns::decode_ctas_per_sm<T, 16, 1, false, 128>();
+    case 2: return ns::decode_ctas_per_sm<T, 16, 2, false, 128>();
+    case 3: return ns::decode_ctas_per_sm<T, 16, 3, false, 128>();
+    case 4: return ns::decode_ctas_per_sm<T, 16, 4, false, 128>();
+    case 5: return ns::decode_ctas_per_sm<T, 16, 5, false, 128>();
+    case 6: return ns::decode_ctas_per_sm<T, 16, 6, false, 128>();
+    case 7: return ns::decode_ctas_per_sm<T, 16, 7, false, 128>();
+    default: return ns::decode_ctas_per_sm<T, 16, 8, false, 128>();
+    }
+}
+
 // q8_0 pools: block size 16 only.
 template <typename T>
 cudaError_t dispatch_decode_q8(int g, const ns::DecodeParams &P, int ctas, cudaStream_t s)
@@ -149,14 +181,18 @@ int dispatch_ctas_per_sm(int bs, int g)
     }
 }
 
-int resident_ctas(int dev, ns_dtype dt, int bs, int g, bool q8)
+int resident_ctas(int dev, ns_dtype dt, int bs, int g, bool q8, int head_dim)
 {
-    std::atomic<int> &slot = q8 ? g_ctas_per_sm_q8[dev][dt == NS_BF16 ? 1 : 0][g - 1]
-                                : g_ctas_per_sm[dev][dt == NS_BF16 ? 1 : 0][bs_index(bs)][g - 1];
+    const int t = dt == NS_BF16 ? 1 : 0;
+    std::atomic<int> &slot = q8 ? g_ctas_per_sm_q8[dev][t][g - 1]
+                             : head_dim == 128 ? g_ctas_per_sm_d128[dev][t][g - 1]
+                                               : g_ctas_per_sm[dev][t][bs_index(bs)][g - 1];
     int n = slot.load(std::memory_order_relaxed);
     if (n <= 0) {
         if (q8)
             n = dt == NS_BF16 ? ctas_per_sm_q8<ns::BF16>(g) : ctas_per_sm_q8<ns::F16>(g);
+        else if (head_dim == 128)
+            n = dt == NS_BF16 ? ctas_per_sm_d128<ns::BF16>(g) : ctas_per_sm_d128<ns::F16>(g);
         else
             n = dt == NS_BF16 ? dispatch_ctas_per_sm<ns::BF16>(bs, g) : dispatch_ctas_per_sm<ns::F16>(bs, g);
         slot.store(n, std::memory_order_relaxed);
@@ -170,13 +206,13 @@ struct WsLayout {
     size_t plan, counters, partials, row_seq, row_len, total;
 };
 
-WsLayout ws_layout(long long rows, int num_kv_heads)
+WsLayout ws_layout(long long rows, int num_kv_heads, int head_dim)
 {
     WsLayout L;
     L.plan = 0;
     L.counters = 256;
     L.partials = L.counters + align256((size_t)rows * num_kv_heads * sizeof(int32_t));
-    L.row_seq = L.partials + align256((size_t)ns::kMaxWorkers * 2 * ns::kSlotFloats * sizeof(float));
+    L.row_seq = L.partials + align256((size_t)ns::kMaxWorkers * 2 * ns::slot_floats(head_dim) * sizeof(float));
     L.row_len = L.row_seq + align256((size_t)rows * sizeof(int32_t));
     L.total = L.row_len + align256((size_t)rows * sizeof(int32_t));
     return L;
@@ -189,7 +225,9 @@ ns_status check_shapes(int num_q_heads, int num_kv_heads, int head_dim, int bloc
         return NS_ERR_INVALID_ARG;
     if (dtype != NS_F16 && dtype != NS_BF16)
         return NS_ERR_UNSUPPORTED;
-    if (head_dim != ns::kHeadDim || bs_index(block_size) < 0)
+    if ((head_dim != 64 && head_dim != 128) || bs_index(block_size) < 0)
+        return NS_ERR_UNSUPPORTED;
+    if (head_dim == 128 && block_size != 16)
         return NS_ERR_UNSUPPORTED;
     if (num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > ns::kMaxGroup)
         return NS_ERR_UNSUPPORTED;
@@ -219,6 +257,7 @@ struct DecodeCall {
     // q8_0 pools (k_pool and v_pool unused then)
     bool q8 = false;
     const void *k_codes = nullptr, *k_scales = nullptr, *v_codes = nullptr, *v_scales = nullptr;
+    int head_dim = 64;
 };
 
 ns_status run_decode(const DecodeCall &c, int dev)
@@ -226,7 +265,7 @@ ns_status run_decode(const DecodeCall &c, int dev)
     unsigned *status = status_word(dev);
     if (status == nullptr)
         return NS_ERR_CUDA;
-    const WsLayout L = ws_layout(c.rows, c.num_kv_heads);
+    const WsLayout L = ws_layout(c.rows, c.num_kv_heads, c.head_dim);
     char *ws = static_cast<char *>(c.workspace);
 
     ns::DecodeParams P;
@@ -270,7 +309,8 @@ ns_status run_decode(const DecodeCall &c, int dev)
                         ? 1
                         : 0;
 
-    return ns::launch_decode(P, c.dtype, c.block_size, c.cfg ? c.cfg->num_ctas : 0, c.stream, dev, c.q8);
+    return ns::launch_decode(P, c.dtype, c.block_size, c.cfg ? c.cfg->num_ctas : 0, c.stream, dev, c.q8,
+                             c.head_dim);
 }
 
 ns_status check_decode_args(const void *q, const void *k_pool, const void *v_pool,
@@ -307,14 +347,17 @@ ns_status check_decode_args(const void *q, const void *k_pool, const void *v_poo
 namespace ns {
 
 ns_status launch_decode(const DecodeParams &P, ns_dtype dtype, int block_size, int num_ctas,
-                        cudaStream_t stream, int dev, bool q8)
+                        cudaStream_t stream, int dev, bool q8, int head_dim)
 {
     const int g = P.group;
-    int ctas = num_ctas > 0 ? num_ctas : resident_ctas(dev, dtype, block_size, g, q8);
+    int ctas = num_ctas > 0 ? num_ctas : resident_ctas(dev, dtype, block_size, g, q8, head_dim);
     if (ctas > NS_MAX_CTAS)
         ctas = NS_MAX_CTAS;
     cudaError_t e;
-    if (q8)
+    if (head_dim == 128)
+        e = dtype == NS_BF16 ? dispatch_decode_d128<BF16>(g, P, ctas, stream)
+                             : dispatch_decode_d128<F16>(g, P, ctas, stream);
+    else if (q8)
         e = dtype == NS_BF16 ? dispatch_decode_q8<BF16>(g, P, ctas, stream) : dispatch_decode_q8<F16>(g, P, ctas, stream);
     else
         e = dtype == NS_BF16 ? dispatch_decode<BF16>(block_size, g, P, ctas, stream)
@@ -345,7 +388,7 @@ ns_status decode_q8_0(const void *q, const void *k_new, const void *v_new, const
                                           num_blocks, dtype, workspace, workspace_bytes, cfg);
     if (s != NS_OK)
         return s;
-    if (block_size != 16)
+    if (block_size != 16 || head_dim != 64)
         return NS_ERR_UNSUPPORTED;
     if (!aligned16(k_scales) || !aligned16(v_scales))
         return NS_ERR_INVALID_ARG;
@@ -360,6 +403,7 @@ ns_status decode_q8_0(const void *q, const void *k_new, const void *v_new, const
                  block_size, scale, out, reinterpret_cast<cudaStream_t>(stream), max_blocks_per_seq, num_blocks,
                  dtype, workspace, cfg, k_new, v_new, k_new ? slot_mapping : nullptr};
     c.q8 = true;
+    c.head_dim = head_dim;
     c.k_codes = k_codes;
     c.k_scales = k_scales;
     c.v_codes = v_codes;
@@ -393,7 +437,9 @@ ns_status ns_kv_append(const void *k, const void *v, const int64_t *slot_mapping
         return NS_ERR_INVALID_ARG;
     if (dtype != NS_F16 && dtype != NS_BF16)
         return NS_ERR_UNSUPPORTED;
-    if (head_dim != ns::kHeadDim || bs_index(block_size) < 0)
+    if ((head_dim != 64 && head_dim != 128) || bs_index(block_size) < 0)
+        return NS_ERR_UNSUPPORTED;
+    if (head_dim == 128 && block_size != 16)
         return NS_ERR_UNSUPPORTED;
     if (num_tokens == 0)
         return NS_OK;
@@ -408,7 +454,7 @@ ns_status ns_kv_append(const void *k, const void *v, const int64_t *slot_mapping
     if (status == nullptr)
         return NS_ERR_CUDA;
     const cudaError_t e = ns::launch_kv_append(k, v, slot_mapping, k_pool, v_pool, num_tokens,
-                                               num_kv_heads, block_size, num_blocks, status,
+                                               num_kv_heads, head_dim, block_size, num_blocks, status,
                                                reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? NS_OK : NS_ERR_CUDA;
 }
@@ -416,10 +462,9 @@ ns_status ns_kv_append(const void *k, const void *v, const int64_t *slot_mapping
 size_t ns_paged_attn_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim)
 {
     (void)num_q_heads;
-    (void)head_dim;
     if (num_seqs < 0 || num_kv_heads <= 0)
         return 0;
-    return ws_layout(num_seqs, num_kv_heads).total;
+    return ws_layout(num_seqs, num_kv_heads, head_dim == 128 ? 128 : 64).total;
 }
 
 ns_status ns_paged_attn_workspace_init(void *workspace, size_t workspace_bytes, ns_stream_t stream)
@@ -454,6 +499,7 @@ ns_status ns_paged_attn_decode_ex(const void *q, const void *k_pool, const void 
     DecodeCall c{q, k_pool, v_pool, block_tables, context_lens, nullptr, num_seqs, num_q_heads,
                  num_kv_heads, block_size, scale, out, reinterpret_cast<cudaStream_t>(stream),
                  max_blocks_per_seq, num_blocks, dtype, workspace, cfg, nullptr, nullptr, nullptr};
+    c.head_dim = head_dim;
     return run_decode(c, dev);
 }
 
@@ -514,6 +560,7 @@ ns_status ns_kv_append_paged_attn_decode_ex(const void *q, const void *k_new, co
                  num_kv_heads, block_size, scale, out, reinterpret_cast<cudaStream_t>(stream),
                  max_blocks_per_seq, num_blocks, dtype, workspace, cfg, k_new, v_new,
                  slot_mapping};
+    c.head_dim = head_dim;
     return run_decode(c, dev);
 }
 
@@ -554,13 +601,13 @@ ns_status ns_paged_attn_prefill_ex(const void *q, const int32_t *query_start_loc
     unsigned *status = status_word(dev);
     if (status == nullptr)
         return NS_ERR_CUDA;
-    const WsLayout L = ws_layout(total_q_tokens, num_kv_heads);
+    const WsLayout L = ws_layout(total_q_tokens, num_kv_heads, head_dim);
     char *ws = static_cast<char *>(workspace);
     int32_t *row_seq = reinterpret_cast<int32_t *>(ws + L.row_seq);
     int32_t *row_len = reinterpret_cast<int32_t *>(ws + L.row_len);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     int tc_min = cfg && cfg->tensor_core_min_span != 0 ? cfg->tensor_core_min_span : 2;
-    if (tc_min < 0 || !ns::tc_prefill_supported(block_size, num_q_heads / num_kv_heads) ||
+    if (tc_min < 0 || head_dim != 64 || !ns::tc_prefill_supported(block_size, num_q_heads / num_kv_heads) ||
         (long long)num_blocks * num_kv_heads * block_size > 0x7fffffffLL)
         tc_min = 0;
     const int phases = cfg && cfg->phases != 0 ? cfg->phases : (NS_PREFILL_WALK | NS_PREFILL_TENSOR_CORE);
@@ -571,6 +618,7 @@ ns_status ns_paged_attn_prefill_ex(const void *q, const int32_t *query_start_loc
         DecodeCall c{q, k_pool, v_pool, block_tables, row_len, row_seq, total_q_tokens, num_q_heads,
                      num_kv_heads, block_size, scale, out, st, max_blocks_per_seq, num_blocks, dtype,
                      workspace, nullptr, nullptr, nullptr, nullptr};
+        c.head_dim = head_dim;
         // the tensor-core kernel after it takes the SMs its idle CTAs leave
         c.pack = tc_min != 0 && (phases & NS_PREFILL_TENSOR_CORE) != 0;
         const ns_status r = run_decode(c, dev);

@@ -9,7 +9,7 @@
 namespace ns {
 
 cudaError_t launch_kv_append(const void *k, const void *v, const int64_t *slot_mapping, void *k_pool,
-                             void *v_pool, int num_tokens, int num_kv_heads, int block_size,
+                             void *v_pool, int num_tokens, int num_kv_heads, int head_dim, int block_size,
                              long long num_blocks, unsigned *status, cudaStream_t stream);
 
 // q8_0 append: quantise each new token's K/V rows and scatter codes and scales.
@@ -33,7 +33,7 @@ struct DecodeParams;
 // Launch the split-KV decode kernel with num_ctas CTAs, or with the resident
 // CTAs of device `dev` when num_ctas is 0.
 ns_status launch_decode(const DecodeParams &P, ns_dtype dtype, int block_size, int num_ctas,
-                        cudaStream_t stream, int dev, bool q8 = false);
+                        cudaStream_t stream, int dev, bool q8 = false, int head_dim = 64);
 
 // Chunked prefill of every span of two or more tokens on the tcgen05 tensor cores.
 // after_walk: the kernel just before it on the stream is this call's span walk

@@ -47,7 +47,23 @@ namespace ns {
 
 // Partial record of one piece of a (sequence, kv head): M[8] (running max,
 // log2 units), L[8] (sum of 2^(z-M)), acc[8][64] (unnormalised output).
-constexpr int kSlotFloats = 2 * kMaxGroup + kMaxGroup * kHeadDim;
+// Geometry of the decode for head dim D: a token row of one head spans COLS
+// lanes of 8 elements; a warp holds ROWS rows at once (a row group); a ring
+// step is 8 row groups, TOK tokens.  D 64: 8 lanes, 4 rows, 32 tokens; D 128:
+// 16 lanes, 2 rows, 16 tokens, so that registers and ring bytes per step stay
+// the same.  A partial record is M[8], L[8], acc[8][D].
+template <int D>
+struct Geo {
+    static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+    static constexpr int COLS = D / 8;
+    static constexpr int LOGC = D == 64 ? 3 : 4;
+    static constexpr int ROWS = 32 / COLS;
+    static constexpr int TOK = 8 * ROWS;
+    static constexpr int ROW_BYTES = 2 * D;
+    static constexpr int SLOT_FLOATS = 2 * kMaxGroup + kMaxGroup * D;
+};
+// Floats of a partial record for a runtime head dim (host side).
+__host__ __device__ constexpr int slot_floats(int head_dim) { return 2 * kMaxGroup + kMaxGroup * head_dim; }
 constexpr float kRescaleSlack = 8.0f;
 // One CTA per SM: two consumer warpgroups (8 warps, one worker each) and a
 // producer warpgroup.  (Measured alternative: 12 consumers, two per ring
@@ -56,7 +72,7 @@ constexpr int kConsumerWarps = 8;
 // Row groups (4 tokens each) whose scores are computed together: 2 measured
 // 1.3% faster than 1 and 4 on the batch-256 decode.
 constexpr int kQkRows = 2;
-constexpr int kStepTokens = 32;        // tokens per ring slot (one per lane for the vote)
+constexpr int kZeroElems = 2048;       // 16-bit zeros: the largest step of K or V rows
 constexpr int kMaxWorkers = 2048;      // split workers (each has two record slots)
 constexpr int kDefaultMinBlocksPerCta = 64;  // spread over a CTA's workers
 constexpr int kLensCache = 256;        // context lengths kept in shared memory
@@ -105,7 +121,7 @@ struct DecodeParams {
     long long num_blocks;
     float scale_log2;  // scale * log2(e)
     int *counters;     // [num_seqs * num_kv_heads], zero between calls
-    float *partials;   // [kMaxWorkers][2][kSlotFloats]
+    float *partials;   // [kMaxWorkers][2][Geo<D>::SLOT_FLOATS]
     ns_decode_plan *plan;
     unsigned *status;
     int min_blocks_per_cta;
@@ -117,7 +133,7 @@ struct DecodeParams {
 };
 
 // Source of the zero-filled rows of a step (32 rows of 64 elements).
-static __device__ __align__(128) uint16_t g_zero_rows[kStepTokens * kHeadDim];
+static __device__ __align__(128) uint16_t g_zero_rows[kZeroElems];
 
 // Merges queued by consumers and run by the consumers whose rings are done.
 // A ring holds at most two partial pieces (the first and last of its range),
@@ -157,7 +173,6 @@ template <int G>
 struct HeadSlots {
     static constexpr int N = G <= 1 ? 1 : (G <= 2 ? 2 : (G <= 4 ? 4 : 8));
     static constexpr int LOG = N == 1 ? 0 : (N == 2 ? 1 : (N == 4 ? 2 : 3));
-    static constexpr int SHIFT = 3 - LOG;  // lane c holds head c >> SHIFT
     static constexpr int PSTRIDE = N < 4 ? 4 : N;
 };
 
@@ -221,11 +236,11 @@ struct PieceRef {
 // One ring slot: K and V rows of one 32-token step and the q rows that ride
 // with a piece's first step.  With a fused append the new token's K/V are
 // copied straight into their row of the step.
-template <int G, bool Q8>
+template <int G, bool Q8, int D>
 struct DecodeSlot {
-    uint16_t k[kStepTokens * kHeadDim];
-    uint16_t v[kStepTokens * kHeadDim];
-    uint16_t q[G * kHeadDim];
+    uint16_t k[Geo<D>::TOK * D];
+    uint16_t v[Geo<D>::TOK * D];
+    uint16_t q[G * D];
 };
 
 // q8_0 pools: a step holds each row's 64 int8 codes and 2 fp16 scales, and the
@@ -235,21 +250,21 @@ constexpr int kQ8Scales = kHeadDim / kQ8Block;      // scales per row
 constexpr int kQ8CodeRow = kHeadDim;                // bytes of a row's codes
 constexpr int kQ8ScaleRow = kQ8Scales * 2;          // bytes of a row's scales
 template <int G>
-struct DecodeSlot<G, true> {
-    int8_t k[kStepTokens * kHeadDim];
-    int8_t v[kStepTokens * kHeadDim];
-    uint16_t ks[kStepTokens * kQ8Scales];
-    uint16_t vs[kStepTokens * kQ8Scales];
+struct DecodeSlot<G, true, 64> {
+    int8_t k[Geo<64>::TOK * kHeadDim];
+    int8_t v[Geo<64>::TOK * kHeadDim];
+    uint16_t ks[Geo<64>::TOK * kQ8Scales];
+    uint16_t vs[Geo<64>::TOK * kQ8Scales];
     uint16_t q[G * kHeadDim];
     uint16_t knew[kHeadDim];
     uint16_t vnew[kHeadDim];
 };
 
-template <int BS, int G, int S, bool Q8 = false>
+template <int BS, int G, int S, bool Q8 = false, int D = 64>
 struct DecodeSmem {
     static constexpr int NG = DecodeShape<G>::NG;
-    DecodeSlot<G, Q8> ring[NG][S];
-    float p[kConsumerWarps][kStepTokens][DecodeShape<G>::PSTRIDE];  // p per consumer warp [token][head]
+    DecodeSlot<G, Q8, D> ring[NG][S];
+    float p[kConsumerWarps][Geo<D>::TOK][DecodeShape<G>::PSTRIDE];  // p per consumer warp [token][head]
     SlotMeta meta[NG][S];
     uint64_t full[NG][S];                    // producer -> consumers: the step has landed
     uint64_t empty[NG][S];                   // consumers -> producer: the slot may be refilled
@@ -269,12 +284,12 @@ struct DecodeSmem {
 
 // Slots per ring: as many (up to four) as fit in a CTA's shared memory.
 constexpr size_t kMaxDynSmem = 227 * 1024;
-template <int BS, int G, bool Q8 = false>
+template <int BS, int G, bool Q8 = false, int D = 64>
 constexpr int decode_stages()
 {
-    return sizeof(DecodeSmem<BS, G, 4, Q8>) <= kMaxDynSmem   ? 4
-           : sizeof(DecodeSmem<BS, G, 3, Q8>) <= kMaxDynSmem ? 3
-                                                              : 2;
+    return sizeof(DecodeSmem<BS, G, 4, Q8, D>) <= kMaxDynSmem   ? 4
+           : sizeof(DecodeSmem<BS, G, 3, Q8, D>) <= kMaxDynSmem ? 3
+                                                                 : 2;
 }
 
 __device__ __forceinline__ int nblocks_of(int L, int BS) { return (L + BS - 1) / BS; }
@@ -482,19 +497,19 @@ __device__ __forceinline__ int piece_end_token(const PieceWalk &w)
     return min(w.hi * BS, w.pL);
 }
 
-// Steps (32-token ring slots) of a piece: step i covers keys
-// lo*bs + 32i .. lo*bs + 32i + 31 of the pair, i.e. 32/bs whole blocks.
-template <int BS>
+// Steps (TOK-token ring slots) of a piece: step i covers keys
+// lo*bs + TOK*i .. lo*bs + TOK*i + TOK-1 of the pair, i.e. TOK/bs whole blocks.
+template <int BS, int TOK>
 __device__ __forceinline__ int steps_of(const PieceWalk &w)
 {
-    return max(0, (piece_end_token<BS>(w) - w.lo * BS + kStepTokens - 1) / kStepTokens);
+    return max(0, (piece_end_token<BS>(w) - w.lo * BS + TOK - 1) / TOK);
 }
 
 // First token (inside the pair) of step i of the piece.
-template <int BS>
+template <int BS, int TOK>
 __device__ __forceinline__ int step_token0(const PieceWalk &w, int i)
 {
-    return w.lo * BS + i * kStepTokens;
+    return w.lo * BS + i * TOK;
 }
 
 // ---------------------------------------------------------------------------
@@ -507,23 +522,23 @@ __device__ __forceinline__ int step_token0(const PieceWalk &w, int i)
 // elements themselves, scale 1.  q8_0: the codes, converted exactly (a code
 // byte, offset by 128, is placed in the mantissa of 2^23 and 2^23 + 128 is
 // subtracted), and the fp16 scale of the 32-element block.
-template <typename T, int G, bool Q8>
+template <typename T, int G, bool Q8, int D>
 struct RowLoad;
 
-template <typename T, int G>
-struct RowLoad<T, G, false> {
-    static __device__ __forceinline__ void k(const DecodeSlot<G, false> &sl, int row, int c, float2 (&x)[4], float &d)
+template <typename T, int G, int D>
+struct RowLoad<T, G, false, D> {
+    static __device__ __forceinline__ void k(const DecodeSlot<G, false, D> &sl, int row, int c, float2 (&x)[4], float &d)
     {
-        const uint4 w = lds128(sl.k + row * kHeadDim + c * 8);
+        const uint4 w = lds128(sl.k + row * D + c * 8);
         x[0] = unpack2<T>(w.x);
         x[1] = unpack2<T>(w.y);
         x[2] = unpack2<T>(w.z);
         x[3] = unpack2<T>(w.w);
         d = 1.f;
     }
-    static __device__ __forceinline__ void v(const DecodeSlot<G, false> &sl, int row, int c, float2 (&x)[4], float &d)
+    static __device__ __forceinline__ void v(const DecodeSlot<G, false, D> &sl, int row, int c, float2 (&x)[4], float &d)
     {
-        const uint4 w = lds128(sl.v + row * kHeadDim + c * 8);
+        const uint4 w = lds128(sl.v + row * D + c * 8);
         x[0] = unpack2<T>(w.x);
         x[1] = unpack2<T>(w.y);
         x[2] = unpack2<T>(w.z);
@@ -540,7 +555,7 @@ __device__ __forceinline__ float2 q8_code_pair(uint32_t biased, int k)
 }
 
 template <typename T, int G>
-struct RowLoad<T, G, true> {
+struct RowLoad<T, G, true, 64> {
     static __device__ __forceinline__ void load(const int8_t *codes, const uint16_t *scales, int row, int c,
                                                 float2 (&x)[4], float &d)
     {
@@ -552,27 +567,28 @@ struct RowLoad<T, G, true> {
         x[3] = q8_code_pair(hi, 2);
         d = __half2float(__ushort_as_half(scales[row * kQ8Scales + (c >> 2)]));
     }
-    static __device__ __forceinline__ void k(const DecodeSlot<G, true> &sl, int row, int c, float2 (&x)[4], float &d)
+    static __device__ __forceinline__ void k(const DecodeSlot<G, true, 64> &sl, int row, int c, float2 (&x)[4], float &d)
     {
         load(sl.k, sl.ks, row, c, x, d);
     }
-    static __device__ __forceinline__ void v(const DecodeSlot<G, true> &sl, int row, int c, float2 (&x)[4], float &d)
+    static __device__ __forceinline__ void v(const DecodeSlot<G, true, 64> &sl, int row, int c, float2 (&x)[4], float &d)
     {
         load(sl.v, sl.vs, row, c, x, d);
     }
 };
 
-template <typename T, int G, bool Q8>
-__device__ __forceinline__ void process_step(const DecodeSlot<G, Q8> &sl, uint32_t vmask,
+template <typename T, int G, bool Q8, int D>
+__device__ __forceinline__ void process_step(const DecodeSlot<G, Q8, D> &sl, uint32_t vmask,
                                              const float2 (&q2)[QRegs<G>::N],
                                              float2 (&acc)[G][4], float &m_run, float &l_run,
                                              float *pbuf, int lane)
 {
+    using GD = Geo<D>;
     constexpr int NS = HeadSlots<G>::N;
-    constexpr int SHIFT = HeadSlots<G>::SHIFT;
-    constexpr int STEPS = kStepTokens / 4;
-    const int c = lane & 7;
-    const int r = lane >> 3;
+    constexpr int SHIFT = GD::LOGC - HeadSlots<G>::LOG;  // lane c holds head c >> SHIFT
+    constexpr int STEPS = GD::TOK / GD::ROWS;            // row groups of a step
+    const int c = lane & (GD::COLS - 1);
+    const int r = lane >> GD::LOGC;
 
     // ---- scores of all token rows of the step, kQkRows row groups at a
     // time (their FMA chains and shuffle levels interleave)
@@ -591,7 +607,7 @@ __device__ __forceinline__ void process_step(const DecodeSlot<G, Q8> &sl, uint32
             for (int u = 0; u < kQkRows; ++u) {
                 float2 kx[4];  // dims 2e, 2e+1 of the lane's 8
                 float kd;
-                RowLoad<T, G, Q8>::k(sl, (st + u) * 4 + r, c, kx, kd);
+                RowLoad<T, G, Q8, D>::k(sl, (st + u) * GD::ROWS + r, c, kx, kd);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float2 k0 = make_float2(kx[e].x, kx[e].x), k1 = make_float2(kx[e].y, kx[e].y);
@@ -607,11 +623,11 @@ __device__ __forceinline__ void process_step(const DecodeSlot<G, Q8> &sl, uint32
                         a[u][m] = fmul2(a[u][m], make_float2(kd, kd));
                 }
             }
-            // Reduce-scatter over the row's 8 lanes: whole pairs are halved
-            // (lane masks 4, 2, ...) while more than one is left, the last
-            // pair is split at the next mask, and lanes that still share a
-            // head (fewer than 8 slots) sum what is left.
-            int msk = 4;
+            // Reduce-scatter over the row's COLS lanes: whole pairs are halved
+            // (lane masks COLS/2, COLS/4, ...) while more than one is left,
+            // the last pair is split at the next mask, and lanes that still
+            // share a head (fewer slots than lanes) sum what is left.
+            int msk = GD::COLS / 2;
 #pragma unroll
             for (int n = NP; n > 1; n >>= 1, msk >>= 1)
 #pragma unroll
@@ -631,12 +647,12 @@ __device__ __forceinline__ void process_step(const DecodeSlot<G, Q8> &sl, uint32
                 for (int u = 0; u < kQkRows; ++u)
                     zz[u] += __shfl_xor_sync(0xffffffffu, zz[u], m);
         } else {
-            // One head: dim pairs, then a sum over the row's 8 lanes.
+            // One head: dim pairs, then a sum over the row's COLS lanes.
 #pragma unroll
             for (int u = 0; u < kQkRows; ++u) {
                 float2 kx[4];
                 float kd;
-                RowLoad<T, G, Q8>::k(sl, (st + u) * 4 + r, c, kx, kd);
+                RowLoad<T, G, Q8, D>::k(sl, (st + u) * GD::ROWS + r, c, kx, kd);
                 float2 a = fmul2(q2[0], kx[0]);
                 a = ffma2(q2[1], kx[1], a);
                 a = ffma2(q2[2], kx[2], a);
@@ -646,14 +662,14 @@ __device__ __forceinline__ void process_step(const DecodeSlot<G, Q8> &sl, uint32
                     zz[u] *= kd;
             }
 #pragma unroll
-            for (int m = 4; m >= 1; m >>= 1)
+            for (int m = GD::COLS / 2; m >= 1; m >>= 1)
 #pragma unroll
                 for (int u = 0; u < kQkRows; ++u)
                     zz[u] += __shfl_xor_sync(0xffffffffu, zz[u], m);
         }
 #pragma unroll
         for (int u = 0; u < kQkRows; ++u) {
-            const int t = (st + u) * 4 + r;
+            const int t = (st + u) * GD::ROWS + r;
             z[st + u] = !((vmask >> t) & 1u) ? -INFINITY : zz[u];
         }
     }
@@ -672,7 +688,7 @@ __device__ __forceinline__ void process_step(const DecodeSlot<G, Q8> &sl, uint32
         l_run *= alpha;
 #pragma unroll
         for (int j = 0; j < G; ++j) {
-            const float aj = __shfl_sync(0xffffffffu, alpha, (lane & ~7) | (j << SHIFT));
+            const float aj = __shfl_sync(0xffffffffu, alpha, (lane & ~(GD::COLS - 1)) | (j << SHIFT));
             const float2 a2 = make_float2(aj, aj);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
@@ -692,16 +708,16 @@ __device__ __forceinline__ void process_step(const DecodeSlot<G, Q8> &sl, uint32
     // write the same value; a padding head lands in an unused slot)
 #pragma unroll
     for (int st = 0; st < STEPS; ++st)
-        pbuf[(st * 4 + r) * HeadSlots<G>::PSTRIDE + (c >> SHIFT)] = p[st];
+        pbuf[(st * GD::ROWS + r) * HeadSlots<G>::PSTRIDE + (c >> SHIFT)] = p[st];
     __syncwarp();
 
     // ---- values
 #pragma unroll
     for (int st = 0; st < STEPS; ++st) {
-        const int t = st * 4 + r;
+        const int t = st * GD::ROWS + r;
         float2 vx[4];
         float vd;
-        RowLoad<T, G, Q8>::v(sl, t, c, vx, vd);
+        RowLoad<T, G, Q8, D>::v(sl, t, c, vx, vd);
         if constexpr (Q8) {
             // a row that holds no key has p = 0 and zero codes, but its pool
             // scale may be anything: use 0
@@ -733,56 +749,66 @@ __device__ __forceinline__ void process_step(const DecodeSlot<G, Q8> &sl, uint32
 // ---------------------------------------------------------------------------
 // Log-sum-exp merge of the partial records of one (sequence, kv head) pair by
 // one warp: pieces c0..c1 (the first in its worker's second slot when
-// c0_second), written to out[out_row + j*64 + d] for the G heads.  Pieces
-// go in chunks of kMergeChunk: lane k loads piece k's maxima and sums, and
-// lane l loads its outputs (head 2i + l/16, dims 4(l%16)..+3, i = 0..3) of
-// every piece of the chunk, all before any is used, so a chunk costs one
+// c0_second), written to out[out_row + j*D + d] for the G heads.  Pieces go
+// in chunks: lane k loads piece k's maxima and sums, and every lane loads its
+// F4 float4s of each piece's outputs (float4 i of lane l is element
+// 4(l + 32i) of acc[8][D]), all before any is used, so a chunk costs one
 // round trip to L2.  Chunks are merged online: a chunk with a larger maximum
 // rescales what came before.
 // ---------------------------------------------------------------------------
-constexpr int kMergeChunk = 8;
+template <int D>
+struct MergeGeo {
+    static constexpr int F4 = 8 * D / 128;                // float4s of acc per lane and piece
+    static constexpr int HSTEP = 128 / D;                 // heads between a lane's float4s
+    static constexpr int CHUNK = D == 64 ? 8 : 4;         // pieces in flight
+};
 
+template <int D>
 __device__ __forceinline__ const float *piece_record(const DecodeParams &P, int c0, int k, bool c0_second)
 {
     const int wh = (k == 0 && c0_second) ? 1 : 0;
-    return P.partials + ((long long)(c0 + k) * 2 + wh) * kSlotFloats;
+    return P.partials + ((long long)(c0 + k) * 2 + wh) * Geo<D>::SLOT_FLOATS;
 }
 
-template <typename T>
+template <typename T, int D>
 __device__ void merge_pieces(const DecodeParams &P, int c0, int c1, bool c0_second, long long out_row, int G,
                              int lane)
 {
+    using MG = MergeGeo<D>;
     const int npieces = c1 - c0 + 1;
-    const int hsel = lane >> 4;  // this lane's heads are 2i + hsel
+    // float4 i of this lane holds head i * HSTEP + hsel, dims dd..dd+3
+    const int hsel = D == 64 ? (lane >> 4) : 0;
+    const int dd = D == 64 ? 4 * (lane & 15) : 4 * lane;
     float mr[kMaxGroup], lr[kMaxGroup];
 #pragma unroll
     for (int j = 0; j < kMaxGroup; ++j) {
         mr[j] = -INFINITY;
         lr[j] = 0.f;
     }
-    float4 o[4];
+    float4 o[MG::F4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < MG::F4; ++i)
         o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k0 = 0; k0 < npieces; k0 += kMergeChunk) {
-        const int nk = min(kMergeChunk, npieces - k0);
+    for (int k0 = 0; k0 < npieces; k0 += MG::CHUNK) {
+        const int nk = min(MG::CHUNK, npieces - k0);
         float4 ma = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), mb = ma;
         float4 la = make_float4(0.f, 0.f, 0.f, 0.f), lb = la;
         if (lane < nk) {
-            const float4 *r = reinterpret_cast<const float4 *>(piece_record(P, c0, k0 + lane, c0_second));
+            const float4 *r = reinterpret_cast<const float4 *>(piece_record<D>(P, c0, k0 + lane, c0_second));
             ma = __ldcg(r);
             mb = __ldcg(r + 1);
             la = __ldcg(r + 2);
             lb = __ldcg(r + 3);
         }
-        float4 a[kMergeChunk][4];
+        float4 a[MG::CHUNK][MG::F4];
 #pragma unroll
-        for (int k = 0; k < kMergeChunk; ++k) {
-            const float4 *r = reinterpret_cast<const float4 *>(piece_record(P, c0, k0 + (k < nk ? k : 0), c0_second) +
-                                                               2 * kMaxGroup) + lane;
+        for (int k = 0; k < MG::CHUNK; ++k) {
+            const float4 *r = reinterpret_cast<const float4 *>(
+                                  piece_record<D>(P, c0, k0 + (k < nk ? k : 0), c0_second) + 2 * kMaxGroup) +
+                              lane;
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                a[k][i] = (k < nk && 2 * i + hsel < G) ? __ldcg(r + 32 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int i = 0; i < MG::F4; ++i)
+                a[k][i] = (k < nk && i * MG::HSTEP + hsel < G) ? __ldcg(r + 32 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         const float mk[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
         const float lk[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
@@ -805,19 +831,19 @@ __device__ void merge_pieces(const DecodeParams &P, int c0, int c1, bool c0_seco
             mr[j] = n;
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float s = hsel ? sc[2 * i + 1] : sc[2 * i];
+        for (int i = 0; i < MG::F4; ++i) {
+            const float s = hsel ? sc[i * MG::HSTEP + (MG::HSTEP > 1)] : sc[i * MG::HSTEP];
             o[i].x *= s;
             o[i].y *= s;
             o[i].z *= s;
             o[i].w *= s;
         }
 #pragma unroll
-        for (int k = 0; k < kMergeChunk; ++k) {
+        for (int k = 0; k < MG::CHUNK; ++k) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float fe = __shfl_sync(0xffffffffu, f[2 * i], k);
-                const float fo = __shfl_sync(0xffffffffu, f[2 * i + 1], k);
+            for (int i = 0; i < MG::F4; ++i) {
+                const float fe = __shfl_sync(0xffffffffu, f[i * MG::HSTEP], k);
+                const float fo = MG::HSTEP > 1 ? __shfl_sync(0xffffffffu, f[i * MG::HSTEP + (MG::HSTEP > 1)], k) : fe;
                 const float fk = hsel ? fo : fe;
                 o[i].x = fmaf(fk, a[k][i].x, o[i].x);
                 o[i].y = fmaf(fk, a[k][i].y, o[i].y);
@@ -827,14 +853,14 @@ __device__ void merge_pieces(const DecodeParams &P, int c0, int c1, bool c0_seco
         }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int h = 2 * i + hsel;
+    for (int i = 0; i < MG::F4; ++i) {
+        const int h = i * MG::HSTEP + hsel;
         if (h < G) {
-            const float inv = 1.f / (hsel ? lr[2 * i + 1] : lr[2 * i]);
+            const float inv = 1.f / (hsel ? lr[i * MG::HSTEP + (MG::HSTEP > 1)] : lr[i * MG::HSTEP]);
             uint2 w;
             w.x = pack2<T>(o[i].x * inv, o[i].y * inv);
             w.y = pack2<T>(o[i].z * inv, o[i].w * inv);
-            *reinterpret_cast<uint2 *>(P.out + out_row + h * kHeadDim + 4 * (lane & 15)) = w;
+            *reinterpret_cast<uint2 *>(P.out + out_row + h * D + dd) = w;
         }
     }
 }
@@ -848,7 +874,7 @@ struct PendingMerge {
     int pstart;
 };
 
-template <typename T>
+template <typename T, int D>
 __device__ __forceinline__ void resolve_merge(const DecodeParams &P, PendingMerge &pm, int q, int r, int G,
                                               MergeQueue &mq, int lane)
 {
@@ -864,7 +890,7 @@ __device__ __forceinline__ void resolve_merge(const DecodeParams &P, PendingMerg
         // ordered before the hand-off to whichever warp runs the merge
         __threadfence();
         const int s = pair / P.num_kv_heads, h = pair % P.num_kv_heads;
-        const long long out_row = ((long long)s * P.num_q_heads + (long long)h * G) * kHeadDim;
+        const long long out_row = ((long long)s * P.num_q_heads + (long long)h * G) * D;
         const bool c0_second = range_begin(c0, q, r) != pm.pstart;
         int idx = kMergeQueue;
         if (lane == 0)
@@ -911,7 +937,7 @@ __device__ __forceinline__ int merge_pop(MergeQueue &mq, int lane)
 
 // Run queued merge `idx` (its entry may still be being written: wait,
 // bounded, for its ready flag).
-template <typename T>
+template <typename T, int D>
 __device__ __forceinline__ bool merge_run(const DecodeParams &P, MergeQueue &mq, int idx, int G, int lane)
 {
     int ok = 1;
@@ -929,7 +955,7 @@ __device__ __forceinline__ bool merge_run(const DecodeParams &P, MergeQueue &mq,
     }
     const MergeJob j = mq.job[idx];
     __threadfence();
-    merge_pieces<T>(P, (int)j.c0, (int)j.c1, j.c0_second != 0, j.out_row, G, lane);
+    merge_pieces<T, D>(P, (int)j.c0, (int)j.c1, j.c0_second != 0, j.out_row, G, lane);
     if (lane == 0)
         P.counters[j.pair] = 0;
     return true;
@@ -941,49 +967,56 @@ __device__ __forceinline__ bool merge_run(const DecodeParams &P, MergeQueue &mq,
 // the result of the count is looked at later (resolve_merge), so the warp
 // does not wait for the atomic here.
 // ---------------------------------------------------------------------------
-template <typename T, int BS, int G>
+template <typename T, int BS, int G, int D>
 __device__ void piece_end(const DecodeParams &P, const PieceRef &pc, int worker, int q, int r,
                           float2 (&acc)[G][4], float m_run, float l_run, int lane, PendingMerge &pm,
                           MergeQueue &mq)
 {
-    constexpr int SHIFT = HeadSlots<G>::SHIFT;
-    const int c = lane & 7;
-    // lane (r, c) with (c & ((1 << SHIFT) - 1)) == 0 owns (row group r, head c >> SHIFT)
-    float M = fmaxf(m_run, __shfl_xor_sync(0xffffffffu, m_run, 8));
-    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 16));
+    using GD = Geo<D>;
+    constexpr int SHIFT = GD::LOGC - HeadSlots<G>::LOG;
+    const int c = lane & (GD::COLS - 1);
+    // lane (r, c) with (c & ((1 << SHIFT) - 1)) == 0 owns (row group r, head c >> SHIFT);
+    // the row groups' lanes are lane ^ COLS, lane ^ 2 COLS, ...
+    float M = m_run;
+#pragma unroll
+    for (int m = GD::COLS; m < 32; m <<= 1)
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
     const float f = (m_run > -INFINITY) ? fast_exp2(m_run - M) : 0.f;
     float Ls = f * l_run;
-    Ls += __shfl_xor_sync(0xffffffffu, Ls, 8);
-    Ls += __shfl_xor_sync(0xffffffffu, Ls, 16);
+#pragma unroll
+    for (int m = GD::COLS; m < 32; m <<= 1)
+        Ls += __shfl_xor_sync(0xffffffffu, Ls, m);
 #pragma unroll
     for (int j = 0; j < G; ++j) {
-        const float fj = __shfl_sync(0xffffffffu, f, (lane & ~7) | (j << SHIFT));
+        const float fj = __shfl_sync(0xffffffffu, f, (lane & ~(GD::COLS - 1)) | (j << SHIFT));
         const float2 f2 = make_float2(fj, fj);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             float2 a = fmul2(acc[j][k], f2);
-            a.x += __shfl_xor_sync(0xffffffffu, a.x, 8);
-            a.y += __shfl_xor_sync(0xffffffffu, a.y, 8);
-            a.x += __shfl_xor_sync(0xffffffffu, a.x, 16);
-            a.y += __shfl_xor_sync(0xffffffffu, a.y, 16);
+#pragma unroll
+            for (int m = GD::COLS; m < 32; m <<= 1) {
+                a.x += __shfl_xor_sync(0xffffffffu, a.x, m);
+                a.y += __shfl_xor_sync(0xffffffffu, a.y, m);
+            }
             acc[j][k] = a;
         }
     }
     // every lane now holds, for dims 8c..8c+7: the merged acc of this warp's
     // heads; head j's max and sum are in lane (j << SHIFT)
     const int s = pc.ps, h = pc.ph;
-    const long long out_row = ((long long)s * P.num_q_heads + (long long)h * G) * kHeadDim;
+    const long long out_row = ((long long)s * P.num_q_heads + (long long)h * G) * D;
+    constexpr unsigned kRowLanes = GD::COLS == 32 ? 0xffffffffu : ((1u << GD::COLS) - 1u);
     if (pc.flags & kFlagWhole) {
-        if (lane < 8) {
+        if (lane < GD::COLS) {
 #pragma unroll
             for (int j = 0; j < G; ++j) {
-                const float inv = 1.f / __shfl_sync(0xffu, Ls, j << SHIFT);
+                const float inv = 1.f / __shfl_sync(kRowLanes, Ls, j << SHIFT);
                 uint4 w;
                 w.x = pack2<T>(acc[j][0].x * inv, acc[j][0].y * inv);
                 w.y = pack2<T>(acc[j][1].x * inv, acc[j][1].y * inv);
                 w.z = pack2<T>(acc[j][2].x * inv, acc[j][2].y * inv);
                 w.w = pack2<T>(acc[j][3].x * inv, acc[j][3].y * inv);
-                *reinterpret_cast<uint4 *>(P.out + out_row + j * kHeadDim + c * 8) = w;
+                *reinterpret_cast<uint4 *>(P.out + out_row + j * D + c * 8) = w;
             }
         }
         return;
@@ -991,11 +1024,11 @@ __device__ void piece_end(const DecodeParams &P, const PieceRef &pc, int worker,
 
     // ---- partial piece: store the record, count arrivals, merge if last.
     const int which = (pc.flags & kFlagWhich1) ? 1 : 0;
-    float *rec = P.partials + ((long long)worker * 2 + which) * kSlotFloats;
-    if (lane < 8) {
+    float *rec = P.partials + ((long long)worker * 2 + which) * GD::SLOT_FLOATS;
+    if (lane < GD::COLS) {
 #pragma unroll
         for (int j = 0; j < G; ++j) {
-            float *a = rec + 2 * kMaxGroup + j * kHeadDim + c * 8;
+            float *a = rec + 2 * kMaxGroup + j * D + c * 8;
             __stcg(reinterpret_cast<float4 *>(a), make_float4(acc[j][0].x, acc[j][0].y, acc[j][1].x, acc[j][1].y));
             __stcg(reinterpret_cast<float4 *>(a + 4), make_float4(acc[j][2].x, acc[j][2].y, acc[j][3].x, acc[j][3].y));
         }
@@ -1006,7 +1039,7 @@ __device__ void piece_end(const DecodeParams &P, const PieceRef &pc, int worker,
     }
     __threadfence();
     __syncwarp();
-    resolve_merge<T>(P, pm, q, r, G, mq, lane);  // at most one count is left open
+    resolve_merge<T, D>(P, pm, q, r, G, mq, lane);  // at most one count is left open
     const int pair = s * P.num_kv_heads + h;
     pm.prev = 0;
     if (lane == 0)
@@ -1037,11 +1070,13 @@ __device__ __forceinline__ void piece_prefetch(const DecodeParams &P, const Piec
 // SlotMeta.  Consumers then hold no walk or issue state: their registers go
 // to the scores and accumulators.
 // ---------------------------------------------------------------------------
-template <typename T, int BS, int G, int S, bool Q8>
-__device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8> &sm, const Split &sp, int pwarp,
-                                int lane)
+template <typename T, int BS, int G, int S, bool Q8, int D>
+__device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8, D> &sm, const Split &sp,
+                                int pwarp, int lane)
 {
-    constexpr int KB = kStepTokens / BS;  // blocks per step
+    constexpr int TOK = Geo<D>::TOK;       // tokens per step
+    constexpr int KB = TOK / BS;           // blocks per step
+    constexpr uint32_t kRowB16 = Geo<D>::ROW_BYTES;  // a 16-bit row
     constexpr int SERVED = DecodeShape<G>::SERVED;
     const int w = pwarp * SERVED + (lane < SERVED ? lane : 0);
     const uint64_t pol = l2_evict_first_policy();
@@ -1091,7 +1126,7 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8> 
         if (P.overlap && issued == 0)
             grid_dependency_wait();
         SlotMeta &mt = sm.meta[w][slot];
-        DecodeSlot<G, Q8> &sl = sm.ring[w][slot];
+        DecodeSlot<G, Q8, D> &sl = sm.ring[w][slot];
         uint64_t *bar = &sm.full[w][slot];
         if (!has || step >= nsteps) {
             if (!ahead) {
@@ -1104,7 +1139,7 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8> 
             cur = walk;
             has = true;
             step = 0;
-            nsteps = steps_of<BS>(cur);
+            nsteps = steps_of<BS, TOK>(cur);
             trow = a_trow;
             slot_v = a_slot;
 #pragma unroll
@@ -1144,8 +1179,8 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8> 
                                ? __ldg(P.block_tables + trow * P.max_blocks_per_seq + first + KB + u)
                                : -1;
         }
-        const int tok0 = step_token0<BS>(cur, step);
-        const int nval = min(kStepTokens, piece_end_token<BS>(cur) - tok0);  // >= 1
+        const int tok0 = step_token0<BS, TOK>(cur, step);
+        const int nval = min(TOK, piece_end_token<BS>(cur) - tok0);  // >= 1
         uint32_t vm = nval >= 32 ? 0xffffffffu : ((1u << nval) - 1u);
         if (KB > 1) {
             uint32_t bm = 0;
@@ -1191,9 +1226,9 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8> 
         // without a key; the new token's rows land in the slot's staging rows
         // and the consumer quantises them into row r_new.)
         const int pend_tok = piece_end_token<BS>(cur);
-        constexpr uint32_t kRowB = Q8 ? (uint32_t)kQ8CodeRow : (uint32_t)kRowBytes;
+        constexpr uint32_t kRowB = Q8 ? (uint32_t)kQ8CodeRow : kRowB16;
         int rows[KB], za[KB], zb[KB];
-        uint32_t bytes = (first_step ? (uint32_t)G * kRowBytes : 0u) + (new_tok ? 2u * kRowBytes : 0u);
+        uint32_t bytes = (first_step ? (uint32_t)G * kRowB16 : 0u) + (new_tok ? 2u * kRowB16 : 0u);
 #pragma unroll
         for (int u = 0; u < KB; ++u) {
             const int keys = min(max(pend_tok - (tok0 + u * BS), 0), BS);
@@ -1213,13 +1248,13 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8> 
             const long long row0 = ((long long)phys[u] * P.num_kv_heads + cur.ph) * BS;  // pool row of the block
             if constexpr (!Q8) {
                 if (rows[u] > 0) {
-                    bulk_load(sl.k + u * BS * kHeadDim, P.k_pool + row0 * kHeadDim, rows[u] * kRowBytes, bar, pol);
-                    bulk_load(sl.v + u * BS * kHeadDim, P.v_pool + row0 * kHeadDim, rows[u] * kRowBytes, bar, pol);
+                    bulk_load(sl.k + u * BS * D, P.k_pool + row0 * D, rows[u] * kRowB16, bar, pol);
+                    bulk_load(sl.v + u * BS * D, P.v_pool + row0 * D, rows[u] * kRowB16, bar, pol);
                 }
             } else {
                 if (rows[u] > 0) {
-                    bulk_load(sl.k + u * BS * kHeadDim, P.k_codes + row0 * kQ8CodeRow, rows[u] * kQ8CodeRow, bar, pol);
-                    bulk_load(sl.v + u * BS * kHeadDim, P.v_codes + row0 * kQ8CodeRow, rows[u] * kQ8CodeRow, bar, pol);
+                    bulk_load(sl.k + u * BS * D, P.k_codes + row0 * kQ8CodeRow, rows[u] * kQ8CodeRow, bar, pol);
+                    bulk_load(sl.v + u * BS * D, P.v_codes + row0 * kQ8CodeRow, rows[u] * kQ8CodeRow, bar, pol);
                 }
                 if (phys[u] >= 0) {
                     bulk_load(sl.ks + u * BS * kQ8Scales, P.k_scales + row0 * kQ8Scales, BS * kQ8ScaleRow, bar, pol);
@@ -1231,28 +1266,28 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8> 
             }
             if (za[u] > rows[u]) {
                 const uint32_t n = (uint32_t)(za[u] - rows[u]) * kRowB;
-                bulk_load(sl.k + (u * BS + rows[u]) * kHeadDim, g_zero_rows, n, bar);
-                bulk_load(sl.v + (u * BS + rows[u]) * kHeadDim, g_zero_rows, n, bar);
+                bulk_load(sl.k + (u * BS + rows[u]) * D, g_zero_rows, n, bar);
+                bulk_load(sl.v + (u * BS + rows[u]) * D, g_zero_rows, n, bar);
             }
             if (zb[u] < BS) {
                 const uint32_t n = (uint32_t)(BS - zb[u]) * kRowB;
-                bulk_load(sl.k + (u * BS + zb[u]) * kHeadDim, g_zero_rows, n, bar);
-                bulk_load(sl.v + (u * BS + zb[u]) * kHeadDim, g_zero_rows, n, bar);
+                bulk_load(sl.k + (u * BS + zb[u]) * D, g_zero_rows, n, bar);
+                bulk_load(sl.v + (u * BS + zb[u]) * D, g_zero_rows, n, bar);
             }
         }
         if (first_step) {
-            const long long qoff = ((long long)cur.ps * P.num_q_heads + (long long)cur.ph * G) * kHeadDim;
-            bulk_load(sl.q, P.q + qoff, G * kRowBytes, bar);
+            const long long qoff = ((long long)cur.ps * P.num_q_heads + (long long)cur.ph * G) * D;
+            bulk_load(sl.q, P.q + qoff, G * kRowB16, bar);
         }
         if (new_tok) {
-            const long long noff = ((long long)cur.ps * P.num_kv_heads + cur.ph) * kHeadDim;
+            const long long noff = ((long long)cur.ps * P.num_kv_heads + cur.ph) * D;
             if constexpr (!Q8) {
                 const int t_new = (cur.pL - 1) - tok0;
-                bulk_load(sl.k + t_new * kHeadDim, P.k_new + noff, kRowBytes, bar);
-                bulk_load(sl.v + t_new * kHeadDim, P.v_new + noff, kRowBytes, bar);
+                bulk_load(sl.k + t_new * D, P.k_new + noff, kRowB16, bar);
+                bulk_load(sl.v + t_new * D, P.v_new + noff, kRowB16, bar);
             } else {
-                bulk_load(sl.knew, P.k_new + noff, kRowBytes, bar);
-                bulk_load(sl.vnew, P.v_new + noff, kRowBytes, bar);
+                bulk_load(sl.knew, P.k_new + noff, kRowB16, bar);
+                bulk_load(sl.vnew, P.v_new + noff, kRowB16, bar);
             }
         }
         ++issued;
@@ -1285,7 +1320,7 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8> 
 // clamped to +-127) are rounded to fp32 at each step, and d is stored as
 // fp16 (nearest even, saturating), the decisions the CPU oracle takes.
 template <typename T, int BS, int G>
-__device__ __forceinline__ void quantize_new_row(const DecodeParams &P, DecodeSlot<G, true> &sl, int t,
+__device__ __forceinline__ void quantize_new_row(const DecodeParams &P, DecodeSlot<G, true, 64> &sl, int t,
                                                  long long new_slot, int ph, int lane)
 {
     const int cc = lane & 7;
@@ -1325,13 +1360,14 @@ __device__ __forceinline__ void quantize_new_row(const DecodeParams &P, DecodeSl
     __syncwarp();
 }
 
-template <typename T, int BS, int G, int S, bool Q8>
-__device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8> &sm, const Split &sp, int ring,
-                                int warp, int lane)
+template <typename T, int BS, int G, int S, bool Q8, int D>
+__device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8, D> &sm, const Split &sp,
+                                int ring, int warp, int lane)
 {
+    using GD = Geo<D>;
     constexpr int NS = HeadSlots<G>::N;
-    constexpr int SHIFT = HeadSlots<G>::SHIFT;
-    const int c = lane & 7;
+    constexpr int SHIFT = GD::LOGC - HeadSlots<G>::LOG;
+    const int c = lane & (GD::COLS - 1);
     const int worker = worker_id(ring, sp.wmajor, DecodeShape<G>::NG);
     const int q = sp.q, r = sp.r;
     float2 q2[QRegs<G>::N];
@@ -1379,7 +1415,7 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8> 
                 const int head = i ^ (c >> SHIFT);
                 uint4 w = make_uint4(0u, 0u, 0u, 0u);
                 if (head < G)
-                    w = lds128(qs + head * kHeadDim + c * 8);
+                    w = lds128(qs + head * D + c * 8);
                 wq[i][0] = w.x;
                 wq[i][1] = w.y;
                 wq[i][2] = w.z;
@@ -1404,19 +1440,19 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8> 
         for (int step = 0;;) {
             if (nsteps > 0) {
                 const SlotMeta &mt = sm.meta[ring][slot];
-                DecodeSlot<G, Q8> &sl = sm.ring[ring][slot];
+                DecodeSlot<G, Q8, D> &sl = sm.ring[ring][slot];
                 // fused append (the piece's last step): the new token's K/V
                 // landed in the slot; this warp also writes them to the pool
                 // slot the producer checked (q8_0: quantised first)
                 if (step == nsteps - 1 && (mt.flags & kFlagNewTok)) {
                     if constexpr (!Q8) {
-                        if (lane < 16 && mt.new_slot >= 0) {
-                            const int cc = lane & 7;
-                            const uint4 val = lds128((lane < 8 ? sl.k : sl.v) + mt.t_new * kHeadDim + cc * 8);
+                        if (lane < 2 * GD::COLS && mt.new_slot >= 0) {
+                            const bool isv = lane >= GD::COLS;
+                            const int cc = lane & (GD::COLS - 1);
+                            const uint4 val = lds128((isv ? sl.v : sl.k) + mt.t_new * D + cc * 8);
                             const long long ns = mt.new_slot;
-                            const long long dst =
-                                (((ns / BS) * P.num_kv_heads + mt.ph) * BS + ns % BS) * kHeadDim + cc * 8;
-                            *reinterpret_cast<uint4 *>((lane < 8 ? P.k_pool_w : P.v_pool_w) + dst) = val;
+                            const long long dst = (((ns / BS) * P.num_kv_heads + mt.ph) * BS + ns % BS) * D + cc * 8;
+                            *reinterpret_cast<uint4 *>((isv ? P.v_pool_w : P.k_pool_w) + dst) = val;
                         }
                     } else {
                         quantize_new_row<T, BS, G>(P, sl, mt.t_new, mt.new_slot, mt.ph, lane);
@@ -1424,7 +1460,7 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8> 
                 }
                 // one step path for full and partial steps: a second, unmasked
                 // copy measured 4% slower (instruction-fetch stalls)
-                process_step<T, G, Q8>(sl, mt.vmask, q2, acc, m_run, l_run, pbuf, lane);
+                process_step<T, G, Q8, D>(sl, mt.vmask, q2, acc, m_run, l_run, pbuf, lane);
             }
             // The slot is only read (the async proxy alone writes it), so the
             // barrier's release/acquire orders these reads before the refill.
@@ -1443,18 +1479,18 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8> 
             }
         }
         if (ok)
-            piece_end<T, BS, G>(P, pr, worker, q, r, acc, m_run, l_run, lane, pm, sm.mq);
+            piece_end<T, BS, G, D>(P, pr, worker, q, r, acc, m_run, l_run, lane, pm, sm.mq);
     }
     if (!ok) {
         *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
         raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
     }
     if (ok) {
-        resolve_merge<T>(P, pm, q, r, G, sm.mq, lane);
+        resolve_merge<T, D>(P, pm, q, r, G, sm.mq, lane);
         // help drain the merge queue: most merges fall due at the end
         while (true) {
             const int idx = merge_pop(sm.mq, lane);
-            if (idx < 0 || !merge_run<T>(P, sm.mq, idx, G, lane))
+            if (idx < 0 || !merge_run<T, D>(P, sm.mq, idx, G, lane))
                 break;
         }
     }
@@ -1568,7 +1604,7 @@ __device__ __forceinline__ Split read_split(const DecodeParams &P, const Smem &s
 // Side work of the consumer warps while the first steps are in flight: rows
 // of sequences with no key get zeros (CTA s mod grid writes row s), and CTA 0
 // records the plan (workers, pairs cut across workers, most pieces of one pair).
-template <class Smem, int BS>
+template <class Smem, int BS, int D>
 __device__ void decode_side_work(const DecodeParams &P, Smem &sm, const Split &sp)
 {
     constexpr int NT = kDecodeThreads;
@@ -1591,8 +1627,8 @@ __device__ void decode_side_work(const DecodeParams &P, Smem &sm, const Split &s
             const int L = s < kLensCache ? sm.lens[s] : clamped_len(P, s, BS, false);
             if (L == 0 && (s % (int)gridDim.x) == (int)blockIdx.x &&
                 (P.table_row == nullptr || __ldg(P.table_row + s) >= 0)) {
-                uint16_t *o = P.out + (long long)s * P.num_q_heads * kHeadDim;
-                for (int i = 0; i < P.num_q_heads * kHeadDim; ++i)
+                uint16_t *o = P.out + (long long)s * P.num_q_heads * D;
+                for (int i = 0; i < P.num_q_heads * D; ++i)
                     o[i] = 0;
             }
             const int nb = nblocks_of(L, BS);
@@ -1631,10 +1667,10 @@ __device__ void decode_side_work(const DecodeParams &P, Smem &sm, const Split &s
     }
 }
 
-template <typename T, int BS, int G, int S, bool Q8>
+template <typename T, int BS, int G, int S, bool Q8, int D>
 __global__ void __launch_bounds__(kDecodeThreads, 1) paged_decode_kernel(const DecodeParams P)
 {
-    using Smem = DecodeSmem<BS, G, S, Q8>;
+    using Smem = DecodeSmem<BS, G, S, Q8, D>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     auto &sm = *reinterpret_cast<Smem *>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1652,21 +1688,21 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) paged_decode_kernel(const D
         // output and the plan, which the previous grid may still be using
         if (P.overlap)
             grid_dependency_wait();
-        decode_side_work<Smem, BS>(P, sm, sp);
-        decode_consumer<T, BS, G, S, Q8>(P, sm, sp, warp, warp, lane);
+        decode_side_work<Smem, BS, D>(P, sm, sp);
+        decode_consumer<T, BS, G, S, Q8, D>(P, sm, sp, warp, warp, lane);
     } else {
         regs_shrink<kProducerRegs>();
         if (warp - kConsumerWarps < Shape::PW)
-            decode_producer<T, BS, G, S, Q8>(P, sm, sp, warp - kConsumerWarps, lane);
+            decode_producer<T, BS, G, S, Q8, D>(P, sm, sp, warp - kConsumerWarps, lane);
     }
 }
 
 // Host-side launch helpers (defined in the per-type instantiation files).
-// Q8: the pools are q8_0 codes and scales (DecodeParams.k_codes ...).
-template <typename T, int BS, int G, bool Q8 = false>
+// Q8: the pools are q8_0 codes and scales (DecodeParams.k_codes ...); D: head dim.
+template <typename T, int BS, int G, bool Q8 = false, int D = 64>
 cudaError_t launch_paged_decode(const DecodeParams &P, int num_ctas, cudaStream_t stream);
 
-template <typename T, int BS, int G, bool Q8 = false>
+template <typename T, int BS, int G, bool Q8 = false, int D = 64>
 int decode_ctas_per_sm();
 
 }  // namespace ns

@@ -6,13 +6,13 @@
 
 namespace ns {
 
-template <typename T, int BS, int G, bool Q8>
+template <typename T, int BS, int G, bool Q8, int D>
 struct DecodeKernel {
-    static constexpr int S = decode_stages<BS, G, Q8>();
-    static_assert(sizeof(DecodeSmem<BS, G, S, Q8>) <= kMaxDynSmem, "decode shared memory");
+    static constexpr int S = decode_stages<BS, G, Q8, D>();
+    static_assert(sizeof(DecodeSmem<BS, G, S, Q8, D>) <= kMaxDynSmem, "decode shared memory");
     static constexpr int THREADS = kDecodeThreads;  // consumers + producer warpgroup
-    static constexpr size_t SMEM = sizeof(DecodeSmem<BS, G, S, Q8>);
-    static void (*fn())(const DecodeParams) { return paged_decode_kernel<T, BS, G, S, Q8>; }
+    static constexpr size_t SMEM = sizeof(DecodeSmem<BS, G, S, Q8, D>);
+    static void (*fn())(const DecodeParams) { return paged_decode_kernel<T, BS, G, S, Q8, D>; }
 
     static cudaError_t prepare()
     {
@@ -39,10 +39,10 @@ struct DecodeKernel {
     }
 };
 
-template <typename T, int BS, int G, bool Q8>
+template <typename T, int BS, int G, bool Q8, int D>
 cudaError_t launch_paged_decode(const DecodeParams &P, int num_ctas, cudaStream_t stream)
 {
-    using K = DecodeKernel<T, BS, G, Q8>;
+    using K = DecodeKernel<T, BS, G, Q8, D>;
     cudaError_t e = K::prepare();
     if (e != cudaSuccess)
         return e;
@@ -64,10 +64,10 @@ cudaError_t launch_paged_decode(const DecodeParams &P, int num_ctas, cudaStream_
     return cudaLaunchKernelEx(&cfg, K::fn(), P);
 }
 
-template <typename T, int BS, int G, bool Q8>
+template <typename T, int BS, int G, bool Q8, int D>
 int decode_ctas_per_sm()
 {
-    using K = DecodeKernel<T, BS, G, Q8>;
+    using K = DecodeKernel<T, BS, G, Q8, D>;
     if (K::prepare() != cudaSuccess)
         return 1;
     int n = 0;
@@ -76,20 +76,21 @@ int decode_ctas_per_sm()
     return n;
 }
 
-#define NS_INSTANTIATE_DECODE_G(T, BS, G, Q8)                                                       \
-    template cudaError_t launch_paged_decode<T, BS, G, Q8>(const DecodeParams &, int, cudaStream_t);   \
-    template int decode_ctas_per_sm<T, BS, G, Q8>();
+#define NS_INSTANTIATE_DECODE_G(T, BS, G, Q8, D)                                                    \
+    template cudaError_t launch_paged_decode<T, BS, G, Q8, D>(const DecodeParams &, int, cudaStream_t); \
+    template int decode_ctas_per_sm<T, BS, G, Q8, D>();
 
-#define NS_INSTANTIATE_DECODE_Q(T, BS, Q8)                                                         \
-    NS_INSTANTIATE_DECODE_G(T, BS, 1, Q8)                                                          \
-    NS_INSTANTIATE_DECODE_G(T, BS, 2, Q8)                                                          \
-    NS_INSTANTIATE_DECODE_G(T, BS, 3, Q8)                                                          \
-    NS_INSTANTIATE_DECODE_G(T, BS, 4, Q8)                                                          \
-    NS_INSTANTIATE_DECODE_G(T, BS, 5, Q8)                                                          \
-    NS_INSTANTIATE_DECODE_G(T, BS, 6, Q8)                                                          \
-    NS_INSTANTIATE_DECODE_G(T, BS, 7, Q8)                                                          \
-    NS_INSTANTIATE_DECODE_G(T, BS, 8, Q8)
+#define NS_INSTANTIATE_DECODE_QD(T, BS, Q8, D)                                                     \
+    NS_INSTANTIATE_DECODE_G(T, BS, 1, Q8, D)                                                       \
+    NS_INSTANTIATE_DECODE_G(T, BS, 2, Q8, D)                                                       \
+    NS_INSTANTIATE_DECODE_G(T, BS, 3, Q8, D)                                                       \
+    NS_INSTANTIATE_DECODE_G(T, BS, 4, Q8, D)                                                       \
+    NS_INSTANTIATE_DECODE_G(T, BS, 5, Q8, D)                                                       \
+    NS_INSTANTIATE_DECODE_G(T, BS, 6, Q8, D)                                                       \
+    NS_INSTANTIATE_DECODE_G(T, BS, 7, Q8, D)                                                       \
+    NS_INSTANTIATE_DECODE_G(T, BS, 8, Q8, D)
 
-#define NS_INSTANTIATE_DECODE(T, BS) NS_INSTANTIATE_DECODE_Q(T, BS, false)
+#define NS_INSTANTIATE_DECODE(T, BS) NS_INSTANTIATE_DECODE_QD(T, BS, false, 64)
+#define NS_INSTANTIATE_DECODE_Q(T, BS, Q8) NS_INSTANTIATE_DECODE_QD(T, BS, Q8, 64)
 
 }  // namespace ns

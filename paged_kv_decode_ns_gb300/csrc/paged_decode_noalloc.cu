@@ -31,7 +31,7 @@ namespace {
 
 constexpr size_t kPlanBytes = 256;
 constexpr size_t kCounterBytes = (size_t)NS_NOALLOC_MAX_PAIRS * sizeof(int32_t);
-constexpr size_t kPartialBytes = (size_t)ns::kMaxWorkers * 2 * ns::kSlotFloats * sizeof(float);
+constexpr size_t kPartialBytes = (size_t)ns::kMaxWorkers * 2 * ns::slot_floats(64) * sizeof(float);
 constexpr size_t kScratchBytes = kPlanBytes + kCounterBytes + kPartialBytes;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];

@@ -57,7 +57,10 @@ def test_host_checks_need_no_gpu(lib):
     # null pointers
     assert f(None, None, None, None, None, 4, 2, 64, 16, 10, 0, None) == -1
     # unsupported head_dim / block_size / dtype
-    assert f(None, None, None, None, None, 4, 2, 128, 16, 10, 0, None) == -2
+    assert f(None, None, None, None, None, 4, 2, 96, 16, 10, 0, None) == -2
+    assert f(None, None, None, None, None, 4, 2, 128, 8, 10, 0, None) == -2
+    # head_dim 128 with block_size 16 passes the shape checks
+    assert f(None, None, None, None, None, 4, 2, 128, 16, 10, 0, None) == -1
     assert f(None, None, None, None, None, 4, 2, 64, 12, 10, 0, None) == -2
     assert f(None, None, None, None, None, 4, 2, 64, 16, 10, 7, None) == -2
     # zero tokens is a no-op

@@ -171,12 +171,21 @@ def test_host_side_validation():
         nb.ns_paged_attn_decode(d.q, d.k_pool, d.v_pool, d.block_tables, d.context_lens,
                                 st.scale, d.out, d.ws[:16])
     assert e.value.status == -1
+    q96 = torch.zeros(2, 14, 96, dtype=torch.float16, device="cuda")
+    kp96 = torch.zeros(4, 2, 16, 96, dtype=torch.float16, device="cuda")
+    with pytest.raises(nb.NsError) as e:
+        nb.ns_paged_attn_decode(q96, kp96, kp96, d.block_tables, d.context_lens, st.scale,
+                                torch.empty_like(q96), d.ws)
+    assert e.value.status == -2
+    # head_dim 128 needs a larger workspace than the one sized for 64
     q128 = torch.zeros(2, 14, 128, dtype=torch.float16, device="cuda")
     kp128 = torch.zeros(4, 2, 16, 128, dtype=torch.float16, device="cuda")
+    small = nb.ns_paged_attn_workspace_bytes(2, 14, 2, 64)
+    assert nb.ns_paged_attn_workspace_bytes(2, 14, 2, 128) > small
     with pytest.raises(nb.NsError) as e:
         nb.ns_paged_attn_decode(q128, kp128, kp128, d.block_tables, d.context_lens, st.scale,
-                                torch.empty_like(q128), d.ws)
-    assert e.value.status == -2
+                                torch.empty_like(q128), d.ws[:small])
+    assert e.value.status == -1
     # a misaligned (2-byte offset) q
     flat = torch.zeros(2 * 14 * 64 + 1, dtype=torch.float16, device="cuda")
     qmis = flat[1:].view(2, 14, 64)
