@@ -137,17 +137,21 @@ static __device__ __align__(128) uint16_t g_zero_rows[kZeroElems];
 
 // Merges queued by consumers and run by the consumers whose rings are done.
 // A ring holds at most two partial pieces (the first and last of its range),
-// so at most 2 x 8 merges fall to one CTA.
+// so at most 2 x 8 merges fall to one CTA.  A merge is cut into parts of hpp
+// query heads each, so that several warps can share a long one; a part is
+// taken by advancing the cursor head = job * kMergeParts + part.
 constexpr int kMergeQueue = 32;
+constexpr int kMergeParts = 16;
 struct MergeJob {
     long long c0, c1, out_row;
     int pair, c0_second;
+    int hpp, nparts;  // query heads per part, parts
 };
 struct MergeQueue {
     MergeJob job[kMergeQueue];
     int ready[kMergeQueue];
     int tail;  // entries taken by producers of jobs
-    int head;  // entries taken to run
+    int head;  // cursor of the next part to run
     int done;  // consumer warps finished
 };
 
@@ -186,15 +190,16 @@ struct QRegs {
     static constexpr int N = HeadSlots<G>::N * 4;
 };
 
-// Rings (workers) of a CTA and how producer lanes serve them: producer warp
-// p serves rings p * SERVED .. p * SERVED + SERVED - 1, one lane each.
+// Rings (workers) of a CTA and how producer lanes serve them: lane i of
+// producer warp p serves ring i * PW + p, so that rings 0..PW-1 (the only
+// ones with work when few workers are active) each have a warp of their own.
 template <int G>
 struct DecodeShape {
     static constexpr int NG = kConsumerWarps;  // rings = workers per CTA
     static constexpr int SERVED = (NG + 3) / 4;  // two rings per producer warp: three measured slower
     static constexpr int PW = (NG + SERVED - 1) / SERVED;  // producer warps
     static constexpr int PSTRIDE = HeadSlots<G>::PSTRIDE;  // p buffer row of a warp
-    static_assert(PW <= 4, "producer lanes");
+    static_assert(PW <= 4 && PW * SERVED == NG, "producer lanes");
 };
 
 enum : int {
@@ -747,21 +752,32 @@ __device__ __forceinline__ void process_step(const DecodeSlot<G, Q8, D> &sl, uin
 }
 
 // ---------------------------------------------------------------------------
-// Log-sum-exp merge of the partial records of one (sequence, kv head) pair by
-// one warp: pieces c0..c1 (the first in its worker's second slot when
-// c0_second), written to out[out_row + j*D + d] for the G heads.  Pieces go
-// in chunks: lane k loads piece k's maxima and sums, and every lane loads its
-// F4 float4s of each piece's outputs (float4 i of lane l is element
-// 4(l + 32i) of acc[8][D]), all before any is used, so a chunk costs one
-// round trip to L2.  Chunks are merged online: a chunk with a larger maximum
-// rescales what came before.
+// Log-sum-exp merge of the partial records of one (sequence, kv head) pair:
+// pieces c0..c1 (the first in its worker's second record slot when
+// c0_second).  One warp merges one part, query heads h0..h0+HPP-1 of the
+// group, and writes out[out_row + j*D + d] for those heads.  A head's row of
+// one piece is D/4 float4s, one per lane, so a warp reads PPR = 128/D rows
+// at once (lane l: row l / (D/4), dims 4(l mod D/4)..+3).  A chunk of CH
+// pieces is loaded at once -- lane k also loads piece k's maxima and sums --
+// so that a chunk costs one round trip to L2; chunks are merged online (a
+// chunk with a larger maximum rescales what came before).
 // ---------------------------------------------------------------------------
+constexpr int kMergeLoads = 24;  // float4 loads in flight per lane (16 and 32 measured slower)
 template <int D>
 struct MergeGeo {
-    static constexpr int F4 = 8 * D / 128;                // float4s of acc per lane and piece
-    static constexpr int HSTEP = 128 / D;                 // heads between a lane's float4s
-    static constexpr int CHUNK = D == 64 ? 8 : 4;         // pieces in flight
+    static constexpr int LPP = D / 4;                 // lanes of one (head, piece) row
+    static constexpr int PPR = 32 / LPP;              // rows a warp reads at once
+    static constexpr int BUDGET = kMergeLoads * PPR;  // (head, piece) rows in flight
 };
+
+// Query heads per part for a merge of n pieces: the most heads whose rows of
+// all n pieces fit in one chunk (1 when even one head's do not).
+template <int D>
+__device__ __forceinline__ int merge_heads_per_part(int n)
+{
+    constexpr int B = MergeGeo<D>::BUDGET;
+    return n <= B / 8 ? 8 : n <= B / 4 ? 4 : n <= B / 2 ? 2 : 1;
+}
 
 template <int D>
 __device__ __forceinline__ const float *piece_record(const DecodeParams &P, int c0, int k, bool c0_second)
@@ -770,202 +786,238 @@ __device__ __forceinline__ const float *piece_record(const DecodeParams &P, int 
     return P.partials + ((long long)(c0 + k) * 2 + wh) * Geo<D>::SLOT_FLOATS;
 }
 
-template <typename T, int D>
-__device__ void merge_pieces(const DecodeParams &P, int c0, int c1, bool c0_second, long long out_row, int G,
-                             int lane)
+template <typename T, int D, int HPP>
+__device__ void merge_part(const DecodeParams &P, int c0, int c1, bool c0_second, long long out_row, int h0, int G,
+                           int lane)
 {
     using MG = MergeGeo<D>;
+    constexpr int CH = MG::BUDGET / HPP < 64 ? MG::BUDGET / HPP : 64;  // pieces per chunk
+    constexpr int NJ = CH / MG::PPR;                                     // loads per head and lane
+    constexpr int U = (CH + 31) / 32;                                    // pieces per lane (maxima, sums)
+    const int sub = lane / MG::LPP, dd = 4 * (lane % MG::LPP);
     const int npieces = c1 - c0 + 1;
-    // float4 i of this lane holds head i * HSTEP + hsel, dims dd..dd+3
-    const int hsel = D == 64 ? (lane >> 4) : 0;
-    const int dd = D == 64 ? 4 * (lane & 15) : 4 * lane;
-    float mr[kMaxGroup], lr[kMaxGroup];
+    float mr[HPP], lr[HPP];
+    float4 o[HPP];
 #pragma unroll
-    for (int j = 0; j < kMaxGroup; ++j) {
-        mr[j] = -INFINITY;
-        lr[j] = 0.f;
-    }
-    float4 o[MG::F4];
-#pragma unroll
-    for (int i = 0; i < MG::F4; ++i)
+    for (int i = 0; i < HPP; ++i) {
+        mr[i] = -INFINITY;
+        lr[i] = 0.f;
         o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k0 = 0; k0 < npieces; k0 += MG::CHUNK) {
-        const int nk = min(MG::CHUNK, npieces - k0);
-        float4 ma = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), mb = ma;
-        float4 la = make_float4(0.f, 0.f, 0.f, 0.f), lb = la;
-        if (lane < nk) {
-            const float4 *r = reinterpret_cast<const float4 *>(piece_record<D>(P, c0, k0 + lane, c0_second));
-            ma = __ldcg(r);
-            mb = __ldcg(r + 1);
-            la = __ldcg(r + 2);
-            lb = __ldcg(r + 3);
+    }
+    for (int k0 = 0; k0 < npieces; k0 += CH) {
+        const int nk = min(CH, npieces - k0);
+        // lane l holds the maxima and sums of pieces l, l + 32, ...
+        float mk[U][HPP], lk[U][HPP];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int i = 0; i < HPP; ++i) {
+                mk[u][i] = -INFINITY;
+                lk[u][i] = 0.f;
+                if (lane + 32 * u < nk && h0 + i < G) {
+                    const float *r = piece_record<D>(P, c0, k0 + lane + 32 * u, c0_second);
+                    mk[u][i] = __ldcg(r + h0 + i);
+                    lk[u][i] = __ldcg(r + kMaxGroup + h0 + i);
+                }
+            }
+        float4 a[HPP][NJ];
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            const int k = j * MG::PPR + sub;
+            const float *r = piece_record<D>(P, c0, k0 + (k < nk ? k : 0), c0_second) + 2 * kMaxGroup + dd;
+#pragma unroll
+            for (int i = 0; i < HPP; ++i)
+                a[i][j] = (k < nk && h0 + i < G) ? __ldcg(reinterpret_cast<const float4 *>(r + (h0 + i) * D))
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        float4 a[MG::CHUNK][MG::F4];
 #pragma unroll
-        for (int k = 0; k < MG::CHUNK; ++k) {
-            const float4 *r = reinterpret_cast<const float4 *>(
-                                  piece_record<D>(P, c0, k0 + (k < nk ? k : 0), c0_second) + 2 * kMaxGroup) +
-                              lane;
+        for (int i = 0; i < HPP; ++i) {
+            float n = mk[0][i];
 #pragma unroll
-            for (int i = 0; i < MG::F4; ++i)
-                a[k][i] = (k < nk && i * MG::HSTEP + hsel < G) ? __ldcg(r + 32 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        const float mk[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
-        const float lk[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
-        float f[kMaxGroup], sc[kMaxGroup];
-#pragma unroll
-        for (int j = 0; j < kMaxGroup; ++j) {
-            float n = mk[j];
+            for (int u = 1; u < U; ++u)
+                n = fmaxf(n, mk[u][i]);
 #pragma unroll
             for (int o2 = 16; o2 >= 1; o2 >>= 1)
                 n = fmaxf(n, __shfl_xor_sync(0xffffffffu, n, o2));
-            n = fmaxf(n, mr[j]);
-            // weights of what came before and of lane k's piece (0 for an empty one)
-            sc[j] = mr[j] > -INFINITY ? fast_exp2(mr[j] - n) : 0.f;
-            f[j] = (j < G && mk[j] > -INFINITY) ? fast_exp2(mk[j] - n) : 0.f;
-            float w = f[j] * lk[j];
+            n = fmaxf(n, mr[i]);
+            // weights of what came before and of this lane's pieces (0 for an empty one)
+            const float sc = mr[i] > -INFINITY ? fast_exp2(mr[i] - n) : 0.f;
+            float f[U], w = 0.f;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                f[u] = mk[u][i] > -INFINITY ? fast_exp2(mk[u][i] - n) : 0.f;
+                w += f[u] * lk[u][i];
+            }
 #pragma unroll
             for (int o2 = 16; o2 >= 1; o2 >>= 1)
                 w += __shfl_xor_sync(0xffffffffu, w, o2);
-            lr[j] = lr[j] * sc[j] + w;
-            mr[j] = n;
-        }
+            lr[i] = lr[i] * sc + w;
+            mr[i] = n;
+            o[i].x *= sc;
+            o[i].y *= sc;
+            o[i].z *= sc;
+            o[i].w *= sc;
 #pragma unroll
-        for (int i = 0; i < MG::F4; ++i) {
-            const float s = hsel ? sc[i * MG::HSTEP + (MG::HSTEP > 1)] : sc[i * MG::HSTEP];
-            o[i].x *= s;
-            o[i].y *= s;
-            o[i].z *= s;
-            o[i].w *= s;
-        }
-#pragma unroll
-        for (int k = 0; k < MG::CHUNK; ++k) {
-#pragma unroll
-            for (int i = 0; i < MG::F4; ++i) {
-                const float fe = __shfl_sync(0xffffffffu, f[i * MG::HSTEP], k);
-                const float fo = MG::HSTEP > 1 ? __shfl_sync(0xffffffffu, f[i * MG::HSTEP + (MG::HSTEP > 1)], k) : fe;
-                const float fk = hsel ? fo : fe;
-                o[i].x = fmaf(fk, a[k][i].x, o[i].x);
-                o[i].y = fmaf(fk, a[k][i].y, o[i].y);
-                o[i].z = fmaf(fk, a[k][i].z, o[i].z);
-                o[i].w = fmaf(fk, a[k][i].w, o[i].w);
+            for (int j = 0; j < NJ; ++j) {
+                // piece j * PPR + sub: lane (j * PPR) % 32 + sub, copy (j * PPR) / 32
+                const float fk = __shfl_sync(0xffffffffu, f[(j * MG::PPR) / 32], (j * MG::PPR) % 32 + sub);
+                o[i].x = fmaf(fk, a[i][j].x, o[i].x);
+                o[i].y = fmaf(fk, a[i][j].y, o[i].y);
+                o[i].z = fmaf(fk, a[i][j].z, o[i].z);
+                o[i].w = fmaf(fk, a[i][j].w, o[i].w);
             }
         }
     }
 #pragma unroll
-    for (int i = 0; i < MG::F4; ++i) {
-        const int h = i * MG::HSTEP + hsel;
-        if (h < G) {
-            const float inv = 1.f / (hsel ? lr[i * MG::HSTEP + (MG::HSTEP > 1)] : lr[i * MG::HSTEP]);
+    for (int i = 0; i < HPP; ++i) {
+        // the PPR rows of a lane column hold different pieces: add them
+#pragma unroll
+        for (int m = MG::LPP; m < 32; m <<= 1) {
+            o[i].x += __shfl_xor_sync(0xffffffffu, o[i].x, m);
+            o[i].y += __shfl_xor_sync(0xffffffffu, o[i].y, m);
+            o[i].z += __shfl_xor_sync(0xffffffffu, o[i].z, m);
+            o[i].w += __shfl_xor_sync(0xffffffffu, o[i].w, m);
+        }
+        if (lane < MG::LPP && h0 + i < G) {
+            const float inv = 1.f / lr[i];
             uint2 w;
             w.x = pack2<T>(o[i].x * inv, o[i].y * inv);
             w.y = pack2<T>(o[i].z * inv, o[i].w * inv);
-            *reinterpret_cast<uint2 *>(P.out + out_row + h * D + dd) = w;
+            *reinterpret_cast<uint2 *>(P.out + out_row + (h0 + i) * D + dd) = w;
         }
     }
 }
 
-// An arrival count whose result this warp has not looked at yet: the warp
-// that brings a pair's count to its number of pieces queues the pair's merge.
+// The partial records a warp has stored but not yet counted (at most two: the
+// first and the last piece of its range).  Their arrivals are counted at the
+// end of the ring, behind one fence: a pair's merge cannot start before the
+// last piece of its other workers' ranges anyway.
 struct PendingMerge {
-    int prev;  // lane 0: the count before this warp's arrival
-    int pair;  // -1: nothing pending
-    int pspan;
-    int pstart;
+    int n;
+    int pair0, pspan0, pstart0;
+    int pair1, pspan1, pstart1;
 };
 
+// Queue the merge of `pair` when this warp's arrival was the last (prev =
+// the count before it).
 template <typename T, int D>
-__device__ __forceinline__ void resolve_merge(const DecodeParams &P, PendingMerge &pm, int q, int r, int G,
-                                              MergeQueue &mq, int lane)
+__device__ __forceinline__ void queue_if_last(const DecodeParams &P, int pair, int pspan, int pstart, int prev,
+                                              int q, int r, int G, MergeQueue &mq, int lane)
 {
-    if (pm.pair < 0)
+    const int c0 = worker_of(pstart, q, r);
+    const int c1 = worker_of(pstart + pspan - 1, q, r);
+    if (prev != c1 - c0)
         return;
-    const int pair = pm.pair;
-    pm.pair = -1;
-    const int c0 = worker_of(pm.pstart, q, r);
-    const int c1 = worker_of(pm.pstart + pm.pspan - 1, q, r);
-    const int prev = __shfl_sync(0xffffffffu, pm.prev, 0);
-    if (prev == (int)(c1 - c0)) {  // every piece has arrived
-        // the other pieces' records (published before their counts) are
-        // ordered before the hand-off to whichever warp runs the merge
-        __threadfence();
-        const int s = pair / P.num_kv_heads, h = pair % P.num_kv_heads;
-        const long long out_row = ((long long)s * P.num_q_heads + (long long)h * G) * D;
-        const bool c0_second = range_begin(c0, q, r) != pm.pstart;
-        int idx = kMergeQueue;
-        if (lane == 0)
-            idx = atomicAdd(&mq.tail, 1);
-        idx = __shfl_sync(0xffffffffu, idx, 0);
-        // A ring holds at most two partial pieces, so a CTA queues at most
-        // 2 x 8 merges and the queue cannot fill; the check guards the bound.
-        if (idx >= kMergeQueue) {
-            if (lane == 0)
-                raise_status(P.status, NS_DEV_MERGE_QUEUE);
-        } else {
-            if (lane == 0) {
-                MergeJob &j = mq.job[idx];
-                j.c0 = c0;
-                j.c1 = c1;
-                j.out_row = out_row;
-                j.pair = pair;
-                j.c0_second = c0_second ? 1 : 0;
-                st_release_cta(&mq.ready[idx], 1);
-            }
-        }
-    }
-}
-
-// Take the next queued merge (lane 0's result, broadcast), or -1 when every
-// queued entry is taken.
-__device__ __forceinline__ int merge_pop(MergeQueue &mq, int lane)
-{
-    int idx = -1;
-    if (lane == 0) {
-        while (true) {
-            const int h = ld_acquire_cta(&mq.head);
-            const int t = min(ld_acquire_cta(&mq.tail), kMergeQueue);
-            if (h >= t)
-                break;
-            if (atomicCAS(&mq.head, h, h + 1) == h) {
-                idx = h;
-                break;
-            }
-        }
-    }
-    return __shfl_sync(0xffffffffu, idx, 0);
-}
-
-// Run queued merge `idx` (its entry may still be being written: wait,
-// bounded, for its ready flag).
-template <typename T, int D>
-__device__ __forceinline__ bool merge_run(const DecodeParams &P, MergeQueue &mq, int idx, int G, int lane)
-{
-    int ok = 1;
-    if (lane == 0) {
-        const unsigned long long t0 = global_timer_ns();
-        while (ld_acquire_cta(&mq.ready[idx]) == 0)
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
-                ok = 0;
-                break;
-            }
-    }
-    if (!__shfl_sync(0xffffffffu, ok, 0)) {
-        raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
-        return false;
-    }
-    const MergeJob j = mq.job[idx];
+    // every piece has arrived: the other pieces' records (published before
+    // their counts) are ordered before the hand-off to whichever warp runs
+    // the merge
     __threadfence();
-    merge_pieces<T, D>(P, (int)j.c0, (int)j.c1, j.c0_second != 0, j.out_row, G, lane);
+    const int s = pair / P.num_kv_heads, h = pair % P.num_kv_heads;
+    const long long out_row = ((long long)s * P.num_q_heads + (long long)h * G) * D;
+    const bool c0_second = range_begin(c0, q, r) != pstart;
+    int idx = kMergeQueue;
     if (lane == 0)
-        P.counters[j.pair] = 0;
+        idx = atomicAdd(&mq.tail, 1);
+    idx = __shfl_sync(0xffffffffu, idx, 0);
+    // A ring holds at most two partial pieces, so a CTA queues at most
+    // 2 x 8 merges and the queue cannot fill; the check guards the bound.
+    if (idx >= kMergeQueue) {
+        if (lane == 0)
+            raise_status(P.status, NS_DEV_MERGE_QUEUE);
+    } else if (lane == 0) {
+        MergeJob &j = mq.job[idx];
+        j.c0 = c0;
+        j.c1 = c1;
+        j.out_row = out_row;
+        j.pair = pair;
+        j.c0_second = c0_second ? 1 : 0;
+        j.hpp = merge_heads_per_part<D>(c1 - c0 + 1);
+        j.nparts = (G + j.hpp - 1) / j.hpp;
+        st_release_cta(&mq.ready[idx], 1);
+    }
+}
+
+// Count this warp's stored records and queue the merges it completes.
+template <typename T, int D>
+__device__ __forceinline__ void count_arrivals(const DecodeParams &P, PendingMerge &pm, int q, int r, int G,
+                                               MergeQueue &mq, int lane)
+{
+    if (pm.n == 0)
+        return;
+    __threadfence();  // the records before their counts
+    int prev0 = 0, prev1 = 0;
+    if (lane == 0) {
+        prev0 = atomicAdd(P.counters + pm.pair0, 1);
+        if (pm.n > 1)
+            prev1 = atomicAdd(P.counters + pm.pair1, 1);
+    }
+    prev0 = __shfl_sync(0xffffffffu, prev0, 0);
+    prev1 = __shfl_sync(0xffffffffu, prev1, 0);
+    queue_if_last<T, D>(P, pm.pair0, pm.pspan0, pm.pstart0, prev0, q, r, G, mq, lane);
+    if (pm.n > 1)
+        queue_if_last<T, D>(P, pm.pair1, pm.pspan1, pm.pstart1, prev1, q, r, G, mq, lane);
+    pm.n = 0;
+}
+
+// Take the next part of a queued merge: lane 0's cursor value (broadcast),
+// -1 when every queued part is taken, -2 when a reserved entry was not
+// filled in time.
+__device__ __forceinline__ bool merge_ready_wait(MergeQueue &mq, int job)
+{
+    const unsigned long long t0 = global_timer_ns();
+    while (ld_acquire_cta(&mq.ready[job]) == 0)
+        if (global_timer_ns() - t0 > kWaitLimitNs)
+            return false;
     return true;
 }
 
+__device__ __forceinline__ int merge_pop(MergeQueue &mq, int lane)
+{
+    int got = -1;
+    if (lane == 0) {
+        while (true) {
+            const int c = ld_acquire_cta(&mq.head);
+            const int job = c / kMergeParts, part = c % kMergeParts;
+            if (job >= min(ld_acquire_cta(&mq.tail), kMergeQueue))
+                break;
+            if (!merge_ready_wait(mq, job)) {  // its parts are known once it is filled
+                got = -2;
+                break;
+            }
+            const int next = part + 1 < mq.job[job].nparts ? c + 1 : (job + 1) * kMergeParts;
+            if (atomicCAS(&mq.head, c, next) == c) {
+                got = c;
+                break;
+            }
+        }
+    }
+    return __shfl_sync(0xffffffffu, got, 0);
+}
+
+// Run part `c % kMergeParts` of queued merge `c / kMergeParts` (filled: the
+// pop waited for it).
+template <typename T, int D>
+__device__ __forceinline__ void merge_run(const DecodeParams &P, MergeQueue &mq, int c, int G, int lane)
+{
+    const int job = c / kMergeParts, part = c % kMergeParts;
+    const MergeJob j = mq.job[job];
+    const int c0 = (int)j.c0, c1 = (int)j.c1, h0 = part * j.hpp;
+    const bool second = j.c0_second != 0;
+    switch (j.hpp) {
+    case 8: merge_part<T, D, 8>(P, c0, c1, second, j.out_row, h0, G, lane); break;
+    case 4: merge_part<T, D, 4>(P, c0, c1, second, j.out_row, h0, G, lane); break;
+    case 2: merge_part<T, D, 2>(P, c0, c1, second, j.out_row, h0, G, lane); break;
+    default: merge_part<T, D, 1>(P, c0, c1, second, j.out_row, h0, G, lane); break;
+    }
+    if (lane == 0 && part == 0)
+        P.counters[j.pair] = 0;
+}
+
 // ---------------------------------------------------------------------------
-// End of a piece for one warp: combine the 4 row groups (shuffles), then
-// write the output (whole pair) or the partial record and count its arrival;
-// the result of the count is looked at later (resolve_merge), so the warp
-// does not wait for the atomic here.
+// End of a piece for one warp: combine the row groups (shuffles), then
+// write the output (whole pair) or the partial record, whose arrival is
+// counted at the end of the ring (count_arrivals), so that the warp waits
+// neither for a fence nor for an atomic here.
 // ---------------------------------------------------------------------------
 template <typename T, int BS, int G, int D>
 __device__ void piece_end(const DecodeParams &P, const PieceRef &pc, int worker, int q, int r,
@@ -1037,16 +1089,17 @@ __device__ void piece_end(const DecodeParams &P, const PieceRef &pc, int worker,
             __stcg(rec + kMaxGroup + (c >> SHIFT), Ls);
         }
     }
-    __threadfence();
-    __syncwarp();
-    resolve_merge<T, D>(P, pm, q, r, G, mq, lane);  // at most one count is left open
     const int pair = s * P.num_kv_heads + h;
-    pm.prev = 0;
-    if (lane == 0)
-        pm.prev = atomicAdd(P.counters + pair, 1);
-    pm.pair = pair;
-    pm.pspan = pc.pspan;
-    pm.pstart = pc.pstart;
+    if (pm.n == 0) {
+        pm.pair0 = pair;
+        pm.pspan0 = pc.pspan;
+        pm.pstart0 = pc.pstart;
+    } else {
+        pm.pair1 = pair;
+        pm.pspan1 = pc.pspan;
+        pm.pstart1 = pc.pstart;
+    }
+    ++pm.n;
 }
 
 // Table row, first-step table entries and slot_mapping entry of a piece.
@@ -1063,7 +1116,7 @@ __device__ __forceinline__ void piece_prefetch(const DecodeParams &P, const Piec
 
 // ---------------------------------------------------------------------------
 // Producer warps: lane i of producer warp p serves ring (worker)
-// w = p * SERVED + i.  It walks w's pieces one piece ahead, reads the
+// w = i * PW + p.  It walks w's pieces one piece ahead, reads the
 // block-table entries of each step one step ahead, and issues the TMA copies
 // of the next step into w's ring as soon as its consumers free a slot, with
 // the step's description (piece, valid keys, fused slot) in the slot's
@@ -1078,7 +1131,7 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8, 
     constexpr int KB = TOK / BS;           // blocks per step
     constexpr uint32_t kRowB16 = Geo<D>::ROW_BYTES;  // a 16-bit row
     constexpr int SERVED = DecodeShape<G>::SERVED;
-    const int w = pwarp * SERVED + (lane < SERVED ? lane : 0);
+    const int w = (lane < SERVED ? lane : 0) * DecodeShape<G>::PW + pwarp;
     const uint64_t pol = l2_evict_first_policy();
     bool done = lane >= SERVED;
     // `walk` runs one piece ahead of `cur`: the table entries of the next
@@ -1378,7 +1431,7 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8, 
         q2[i] = make_float2(0.f, 0.f);
     float *pbuf = &sm.p[warp][0][0];
     PendingMerge pm;
-    pm.pair = -1;
+    pm.n = 0;
     int slot = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -1485,19 +1538,40 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8, 
         *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
         raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
     }
-    if (ok) {
-        resolve_merge<T, D>(P, pm, q, r, G, sm.mq, lane);
-        // help drain the merge queue: most merges fall due at the end
-        while (true) {
-            const int idx = merge_pop(sm.mq, lane);
-            if (idx < 0 || !merge_run<T, D>(P, sm.mq, idx, G, lane))
-                break;
-        }
-    }
+    if (ok)
+        count_arrivals<T, D>(P, pm, q, r, G, sm.mq, lane);
     __syncwarp();
     if (lane == 0) {
         __threadfence_block();  // this warp's queued jobs before its count
         atomicAdd(&sm.mq.done, 1);
+    }
+    if (!ok)
+        return;
+    // Run merge parts until every ring of the CTA has ended (no job can
+    // come after that) and the queue is empty: the parts of a long merge
+    // spread over the warps that are idle by then.
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        int all = 0, late = 0;
+        if (lane == 0) {
+            all = ld_acquire_cta(&sm.mq.done) >= DecodeShape<G>::NG;
+            late = global_timer_ns() - t0 > kWaitLimitNs;
+        }
+        all = __shfl_sync(0xffffffffu, all, 0);
+        late = __shfl_sync(0xffffffffu, late, 0);
+        const int c = merge_pop(sm.mq, lane);
+        if (c >= 0) {
+            merge_run<T, D>(P, sm.mq, c, G, lane);
+            continue;
+        }
+        if (c == -2 || late) {
+            if (lane == 0)
+                raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
+            break;
+        }
+        if (all)
+            break;
+        __nanosleep(200);
     }
 }
 
