@@ -12,12 +12,16 @@
 //
 //   warp 9   producer: TMA 3D load of the Q tile; per 128-key tile, one TMA 2D
 //            load per pool block for K and for V (128-byte swizzle), into a
-//            2-stage ring;
-//   warp 8   allocates 512 TMEM columns; lane 0 issues tcgen05.mma:
+//            4-stage ring, the next tile's block-table entries read ahead;
+//   warp 8   allocates 512 TMEM columns; lane 0 issues the score products
 //              S[128x128] = Q K^T   (4 steps of K=16, A and B K-major)
+//            as soon as the softmax has read the previous S;
+//   warp 10  lane 0 issues the value products
 //              O_h[128x64] += P_h V_h (4 steps of K=16 per key half h,
 //                                    P read from TMEM, V MN-major)
-//            and commits each group to an mbarrier;
+//            from one of two P buffers, so that neither kind of product
+//            waits behind the other's issue (a tile's 8 value products take
+//            ~0.7 us to issue, against ~0.15 us for its 4 score products);
 //   warps 0-7 softmax: thread t owns row t % 128 (TMEM lane) and key columns
 //            64 h .. 64 h + 63 of each tile, h = t / 128.  Each key half has
 //            its own running max (moving lazily, by more than 8 in log2 units),
@@ -42,17 +46,19 @@ namespace {
 
 constexpr int kKT = 128;         // keys per K/V tile
 constexpr int kRows = 128;       // MMA M
-// TMEM columns: S [0,128); O of key half h [128 + 64h, 192 + 64h); P part p,
-// key half h [256 + 64p + 32h, 288 + 64p + 32h) (two 16-bit values a column)
+// TMEM columns: S [0,128); O of key half h [128 + 64h, 192 + 64h); P of
+// tile j in buffer b = j mod 2, part p, key half h: [256 + NP*64 b + 64p + 32h,
+// + 32) (two 16-bit values a column; NP parts, at most 512 columns in all)
 constexpr int kTmemCols = 512;
 constexpr int kTmemO = 128;
 constexpr int kTmemP = 256;
-constexpr int kStages = 3;       // K/V tiles in flight: a tile's copies take ~2 us under load
+constexpr int kStages = 4;       // K/V tiles in flight (3 measured 4% slower, 5 alike)
 constexpr int kSoftmaxThreads = 256;  // two warpgroups: key columns 0..63 and 64..127 of each row
 constexpr int kHalf = kKT / 2;         // key columns per softmax thread
-constexpr int kMmaWarp = 8;
+constexpr int kMmaWarp = 8;            // score products; TMEM allocation
 constexpr int kProducerWarp = 9;
-constexpr int kThreads = 320;          // warps 0-7 softmax, 8 MMA, 9 producer
+constexpr int kPvWarp = 10;            // value products
+constexpr int kThreads = 352;          // warps 0-7 softmax, 8 and 10 MMA, 9 producer
 constexpr float kSlack = 8.0f;   // lazy rescale: the max moves by more than this (log2 units)
 // Every exponential runs on the MUFU pipe: an FMA-pipe polynomial for half of
 // them measured 12% slower (its instructions cost more than MUFU).
@@ -93,7 +99,7 @@ struct alignas(1024) PrefillSmem {
     uint64_t s_full;
     uint64_t s_free;
     uint64_t p_full;
-    uint64_t o_done;
+    uint64_t o_done[2];  // value products of the tiles that used P buffer b done
     // the two softmax halves of a row exchange their maxima and sums once,
     // at the end, through these
     uint64_t xbar;
@@ -186,6 +192,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_v, const PrefillParams P)
 {
     constexpr int NP = PParts<T>::N;
+    static_assert(kTmemP + 2 * NP * (kKT / 2) <= kTmemCols, "two P buffers fit in TMEM");
     extern __shared__ unsigned char smem_raw[];
     PrefillSmem<NP> &sm = smem_of<NP>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -226,7 +233,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_init(&sm.s_full, 1);
         mbar_init(&sm.s_free, kSoftmaxThreads);
         mbar_init(&sm.p_full, kSoftmaxThreads);
-        mbar_init(&sm.o_done, 1);
+        mbar_init(&sm.o_done[0], 1);
+        mbar_init(&sm.o_done[1], 1);
         mbar_init(&sm.xbar, kSoftmaxThreads);
         mbar_init(&sm.rem_bar, kSoftmaxThreads);
         mbar_init_fence();
@@ -269,19 +277,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         constexpr int kBlocksPerTile = kKT / BS;
         const int nb_seq = (L + BS - 1) / BS;
+        // lane i < kBlocksPerTile: the table entry of block i of key tile j
+        // (-1 past the sequence); tile j+1's entry loads while tile j's
+        // slot is awaited, so no copy waits on a table read
+        auto table_entry = [&](int j) {
+            const int blk = (j0 + j) * kBlocksPerTile + lane;
+            return (lane < kBlocksPerTile && j < tiles && blk < nb_seq)
+                       ? __ldg(P.block_tables + (long long)s * P.max_blocks_per_seq + blk)
+                       : -1;
+        };
         bool ok = true;
         int issued = 0;
+        int next_phys = table_entry(0);
         for (int j = 0; ok && j < tiles; ++j) {
             const int stage = j % kStages;
             const uint32_t par = ((uint32_t)(j / kStages) & 1u) ^ 1u;
-            int phys = -1;
+            int phys = next_phys;
+            next_phys = table_entry(j + 1);
             const int blk = (j0 + j) * kBlocksPerTile + lane;
-            if (lane < kBlocksPerTile && blk < nb_seq) {
-                phys = __ldg(P.block_tables + (long long)s * P.max_blocks_per_seq + blk);
-                if (phys < 0 || (long long)phys >= P.num_blocks) {
-                    raise_status(P.status, NS_DEV_BAD_BLOCK_ID);
-                    phys = -1;
-                }
+            if (lane < kBlocksPerTile && blk < nb_seq && (phys < 0 || (long long)phys >= P.num_blocks)) {
+                raise_status(P.status, NS_DEV_BAD_BLOCK_ID);
+                phys = -1;
             }
             const unsigned mask = __ballot_sync(0xffffffffu, phys >= 0);
             if (lane == 0) {
@@ -315,53 +331,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issue
+        // ------------------------------------------------------------ score products
         if (lane == 0 && tiles > 0) {
             const uint32_t idesc_s = tc::idesc_f16(kRows, kKT, ab_fmt, false);
-            const uint32_t idesc_o = tc::idesc_f16(kRows, kHeadDim, ab_fmt, true);
             const uint32_t q_addr = smem_addr(sm.q);
-            // S_j = Q K_j^T into TMEM columns [0, 128)
-            auto issue_s = [&](int j) {
+            // S_j = Q K_j^T into TMEM columns [0, 128), once K_j has landed
+            // and the softmax has read S_{j-1}
+            bool ok = mbar_wait(&sm.q_full, 0);
+            for (int j = 0; ok && j < tiles; ++j) {
+                ok = mbar_wait(&sm.kv_full[j % kStages], (uint32_t)(j / kStages) & 1u) &&
+                     (j == 0 || mbar_wait(&sm.s_free, (uint32_t)(j - 1) & 1u));
+                if (!ok)
+                    break;
+                tc::fence_after_sync();
                 const uint32_t k_addr = smem_addr(sm.k[j % kStages]);
 #pragma unroll
                 for (int kk = 0; kk < kHeadDim / 16; ++kk)
                     tc::mma_ss(tmem, tc::desc_sw128(q_addr + kk * 32), tc::desc_sw128(k_addr + kk * 32),
                                idesc_s, kk > 0 ? 1u : 0u);
                 tc::mma_commit(&sm.s_full);
-            };
-            // Order: S_0, then per tile j: S_{j+1} as soon as the softmax has
-            // read S_j, then PV_j once P_j is in TMEM -- the softmax of tile j
-            // overlaps S_{j+1} and PV_{j-1} on the tensor core.
-            bool ok = mbar_wait(&sm.q_full, 0) && mbar_wait(&sm.kv_full[0], 0);
-            if (ok) {
-                tc::fence_after_sync();
-                issue_s(0);
             }
+            if (!ok)
+                raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
+        }
+        __syncwarp();
+    } else if (warp == kPvWarp) {
+        // ------------------------------------------------------------ value products
+        if (lane == 0 && tiles > 0) {
+            const uint32_t idesc_o = tc::idesc_f16(kRows, kHeadDim, ab_fmt, true);
+            bool ok = true;
             for (int j = 0; ok && j < tiles; ++j) {
-                if (j + 1 < tiles) {
-                    ok = mbar_wait(&sm.kv_full[(j + 1) % kStages], (uint32_t)((j + 1) / kStages) & 1u) &&
-                         mbar_wait(&sm.s_free, (uint32_t)j & 1u);
-                    if (!ok)
-                        break;
-                    tc::fence_after_sync();
-                    issue_s(j + 1);
-                }
+                // P_j is in TMEM buffer j mod 2 (and V_j landed before S_j was computed)
                 ok = mbar_wait(&sm.p_full, (uint32_t)j & 1u);
                 if (!ok)
                     break;
                 tc::fence_after_sync();
                 const uint32_t v_addr = smem_addr(sm.v[j % kStages]);
+                const uint32_t p_buf = kTmemP + (uint32_t)(j & 1) * (NP * kKT / 2);
 #pragma unroll
                 for (int part = 0; part < NP; ++part)
 #pragma unroll
                     for (int kk = 0; kk < kKT / 16; ++kk) {
                         // keys 16 kk ..: key half kk / 4 accumulates into its own O
-                        const uint32_t p_cols = kTmemP + part * (kKT / 2) + (kk >> 2) * (kHalf / 2) + (kk & 3) * 8;
+                        const uint32_t p_cols = p_buf + part * (kKT / 2) + (kk >> 2) * (kHalf / 2) + (kk & 3) * 8;
                         tc::mma_ts(tmem + kTmemO + (kk >> 2) * kHeadDim, tmem + p_cols,
                                    tc::desc_sw128(v_addr + kk * 16 * kRowBytes), idesc_o,
                                    (j > 0 || part > 0 || (kk & 3) > 0) ? 1u : 0u);
                     }
-                tc::mma_commit(&sm.o_done);
+                tc::mma_commit(&sm.o_done[j & 1]);
                 tc::mma_commit(&sm.kv_empty[j % kStages]);
             }
             if (!ok)
@@ -447,13 +464,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             l += (ls2[0].x + ls2[0].y) + (ls2[1].x + ls2[1].y);
 
-            // PV of the previous tile must be done before P and O are touched.
-            if (j > 0 && !mbar_wait(&sm.o_done, (uint32_t)(j - 1) & 1u)) {
+            // P buffer j mod 2 is free once the value products of tile j-2
+            // are done; O may be rescaled once those of tile j-1 are (a
+            // commit covers every product issued before it)
+            const bool any_rescale = __any_sync(0xffffffffu, rescale);
+            if (any_rescale ? (j > 0 && !mbar_wait(&sm.o_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u))
+                            : (j > 1 && !mbar_wait(&sm.o_done[j & 1], (uint32_t)((j - 2) >> 1) & 1u))) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
-            if (__any_sync(0xffffffffu, rescale)) {
+            if (any_rescale) {
                 // this key half's O row
                 const float a = rescale ? alpha : 1.f;
 #pragma unroll
@@ -470,13 +491,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             // P row r, this half's keys c0 .. c0 + 63: column c holds keys
             // c0 + 2c (low half) and c0 + 2c + 1
-            tc::tmem_st32(lane_addr + kTmemP + hf * (kHalf / 2), pk);
+            const uint32_t p_buf = kTmemP + (uint32_t)(j & 1) * (NP * kKT / 2);
+            tc::tmem_st32(lane_addr + p_buf + hf * (kHalf / 2), pk);
             if (NP == 2) {
                 uint32_t pl[kHalf / 2];
 #pragma unroll
                 for (int c = 0; c < kHalf / 2; ++c)
                     pl[c] = pack2<T>(sv[2 * c], sv[2 * c + 1]);
-                tc::tmem_st32(lane_addr + kTmemP + (NP - 1) * (kKT / 2) + hf * (kHalf / 2), pl);
+                tc::tmem_st32(lane_addr + p_buf + (NP - 1) * (kKT / 2) + hf * (kHalf / 2), pl);
             }
             // Values of keys past the context, or of blocks that were not
             // loaded, must be zero: P is zero there but 0 * NaN is not.  This
@@ -518,7 +540,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = false;
         }
         if (ok && tiles > 0) {
-            ok = mbar_wait(&sm.o_done, (uint32_t)(tiles - 1) & 1u);
+            ok = mbar_wait(&sm.o_done[(tiles - 1) & 1], (uint32_t)((tiles - 1) >> 1) & 1u);
             if (ok) {
                 tc::fence_after_sync();
                 float ob[32];
