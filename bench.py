@@ -226,7 +226,19 @@ def make_workload(name: str):
     return wl.WORKLOADS[name]()
 
 
-def workload_config(st, name, pools, layers=1, kv="native"):
+def decode_policy(args):
+    """The forced decode policy the command line asks for, or None (automatic)."""
+    p = {}
+    if getattr(args, "whole_sequences", False):
+        p["whole_sequences"] = 1
+    if getattr(args, "min_blocks_per_cta", 0):
+        p["min_blocks_per_cta"] = args.min_blocks_per_cta
+    if getattr(args, "num_ctas", 0):
+        p["num_ctas"] = args.num_ctas
+    return p or None
+
+
+def workload_config(st, name, pools, layers=1, kv="native", policy=None):
     step = ("fused kv_append + split-KV paged decode" if st.is_decode
             else "kv_append + chunked prefill (tensor-core spans, decode-walk rows)")
     if layers > 1:
@@ -246,6 +258,7 @@ def workload_config(st, name, pools, layers=1, kv="native"):
             "head_dim": st.head_dim, "block_size": st.block_size,
             "num_blocks": st.num_blocks, "step": step, "query_tokens": st.num_tokens,
             "kv_cache": "q8_0 (int8 codes, fp16 scale per 32 elements)" if kv == "q8_0" else st.dtype,
+            "decode_policy": dict(policy) if policy else "auto",
             "l2": l2}
 
 
@@ -297,7 +310,7 @@ class Step:
     generator); block tables, lengths and slots are shared.
     """
 
-    def __init__(self, st, dev, npools, layers=1, overlap=False, kv="native"):
+    def __init__(self, st, dev, npools, layers=1, overlap=False, kv="native", policy=None):
         import torch
         from paged_kv_decode_ns_gb300 import binding as nb
         self.nb, self.torch, self.st, self.dev = nb, torch, st, dev
@@ -330,9 +343,12 @@ class Step:
         self.launches = 1 if self.decode else 4
         self.layers = layers
         self.config = None
-        if overlap:  # programmatic dependent launches (see ns_decode_config.overlap_prologue)
+        if overlap or policy:
             self.config = nb.DecodeConfig()
+        if overlap:  # programmatic dependent launches (see ns_decode_config.overlap_prologue)
             self.config.overlap_prologue = 1
+        for k, v in (policy or {}).items():  # a forced split policy (decode workloads)
+            setattr(self.config, k, v)
         self.layer_io = []
         self.q8pools = []
         if kv == "q8_0":
@@ -479,7 +495,7 @@ def bench_ours(args):
     npools = max(1, args.pools if args.pools else math.ceil(2 * L2_BYTES / max(pool_bytes, 1)))
     if args.layers > 1:
         npools = 1  # the layers' pools are the rotation
-    step = Step(st, dev, npools, layers=args.layers, overlap=args.overlap, kv=args.kv)
+    step = Step(st, dev, npools, layers=args.layers, overlap=args.overlap, kv=args.kv, policy=decode_policy(args))
     stream = torch.cuda.current_stream(dev)
 
     sampler = ClockSampler(local) if rank == 0 else None
@@ -647,7 +663,7 @@ def bench_ours(args):
                      if args.layers > 1 else None),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": st.dtype, "data": "synthetic (seeded; no dataset or weights involved)",
-        "config": dict(workload_config(st, args.workload, npools, args.layers, args.kv),
+        "config": dict(workload_config(st, args.workload, npools, args.layers, args.kv, decode_policy(args)),
                        overlap_prologue=bool(args.overlap)),
         "roofline": roofline,
         "cpu_baseline": cpu,
@@ -656,6 +672,8 @@ def bench_ours(args):
                 "us_per_step": 1e3 * te2e_max / n_e2e, "steps": n_e2e},
         "gpu_launches": args.steps * step.launches,
         "clocks": clocks,
+        # the device's record of the last call's split (decode workloads)
+        "plan": nb.ns_read_decode_plan(step.ws) if st.is_decode and args.layers == 1 else None,
     }
 
 
@@ -712,6 +730,11 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=1,
                     help="attention layers per step (decode workloads; 24 = the Qwen2.5-0.5B stack)")
     ap.add_argument("--pools", type=int, default=0, help="rotating pool copies (0 = enough to exceed 2x L2)")
+    ap.add_argument("--whole-sequences", action="store_true",
+                    help="force whole (sequence, kv head) pairs per worker (no split, no merge)")
+    ap.add_argument("--min-blocks-per-cta", type=int, default=0,
+                    help="force the split's minimum KV blocks per CTA (0 = automatic)")
+    ap.add_argument("--num-ctas", type=int, default=0, help="force the decode grid (0 = one CTA per SM)")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--soak-s", type=float, default=1.0)
     ap.add_argument("--traffic", type=float, default=None,
