@@ -629,7 +629,7 @@ ns_status ns_paged_attn_prefill_ex(const void *q, const int32_t *query_start_loc
         return NS_OK;
     return ns::launch_tc_prefill(q, query_start_loc, k_pool, v_pool, block_tables, context_lens,
                                  num_seqs, total_q_tokens, num_q_heads, num_kv_heads, block_size,
-                                 scale, out, max_blocks_per_seq, num_blocks, dtype, status,
+                                 scale, out, max_blocks_per_seq, num_blocks, dtype, tc_min, status,
                                  (phases & NS_PREFILL_WALK) != 0, st) == cudaSuccess
                ? NS_OK
                : NS_ERR_CUDA;

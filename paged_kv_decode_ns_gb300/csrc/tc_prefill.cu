@@ -34,6 +34,7 @@
 //            warpgroup for all 128 columns took ~1.5 us of ~1.9 us per tile.)
 // Values of keys past the context are zeroed in shared memory before the PV
 // product, so undefined (even NaN) pool slots never reach the accumulator.
+#include <algorithm>
 #include <cstddef>
 #include <cudaTypedefs.h>
 
@@ -73,6 +74,7 @@ struct PrefillParams {
     int num_kv_heads;
     int group;
     int qt;  // tokens per query tile
+    int min_span;  // spans of at least this many query tokens run here
     int max_blocks_per_seq;
     long long num_blocks;
     float scale_log2;
@@ -150,7 +152,7 @@ __device__ void find_unit(const PrefillParams &P, PrefillSmem<NP> &sm, int lane)
         int tiles = 0;
         if (s >= 0) {
             const int n = __ldg(P.qsl + s + 1) - __ldg(P.qsl + s);
-            tiles = n >= 2 ? (n + P.qt - 1) / P.qt : 0;
+            tiles = n >= P.min_span ? (n + P.qt - 1) / P.qt : 0;
         }
         long long w = (long long)tiles * P.num_kv_heads;
         long long incl = w;
@@ -689,10 +691,12 @@ cudaError_t launch_tc_prefill(const void *q, const int32_t *query_start_loc, con
                               const int32_t *context_lens, int num_seqs, int total_q_tokens,
                               int num_q_heads, int num_kv_heads, int block_size, float scale,
                               void *out, int max_blocks_per_seq, long long num_blocks, ns_dtype dtype,
-                              unsigned *status, bool after_walk, cudaStream_t stream)
+                              int min_span, unsigned *status, bool after_walk, cudaStream_t stream)
 {
     const int G = num_q_heads / num_kv_heads;
     const int qt = kRows / G;
+    if (min_span < 1)
+        return cudaErrorInvalidValue;
     CUtensorMap tq, tk, tv;
     {
         const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)num_q_heads, (cuuint64_t)total_q_tokens};
@@ -720,12 +724,16 @@ cudaError_t launch_tc_prefill(const void *q, const int32_t *query_start_loc, con
     P.num_kv_heads = num_kv_heads;
     P.group = G;
     P.qt = qt;
+    P.min_span = min_span;
     P.max_blocks_per_seq = max_blocks_per_seq;
     P.num_blocks = num_blocks;
     P.scale_log2 = scale * 1.4426950408889634f;
     P.status = status;
-    // an upper bound on the units (2 CTAs each); CTA pairs without one exit at once
-    const long long units = (long long)num_kv_heads * ((total_q_tokens + qt - 1) / qt + num_seqs);
+    // an upper bound on the units (2 CTAs each): a span of n >= min_span
+    // tokens has ceil(n / qt) query tiles, and there are at most
+    // min(num_seqs, T / min_span) such spans; CTA pairs without a unit exit at once
+    const long long spans = std::min<long long>(num_seqs, total_q_tokens / min_span);
+    const long long units = (long long)num_kv_heads * ((total_q_tokens + qt - 1) / qt + spans);
     const int grid = (int)(2 * units > 0x7ffffffe ? 0x7ffffffe : 2 * units);
     if (grid == 0)
         return cudaSuccess;

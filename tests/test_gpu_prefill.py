@@ -134,3 +134,33 @@ def test_tensor_core_and_cuda_core_paths_agree(orc):
     compare(cuda_core, ref, st.dtype, "cuda-core path")
     compare(d.out, ref, st.dtype, "tensor-core path")
     _gpu.assert_no_device_status()
+
+
+@pytest.mark.parametrize("min_span", [5, 40])
+def test_raised_tensor_core_threshold_partitions_the_rows(min_span, orc):
+    """With tensor_core_min_span raised, spans below it are the walk's alone and
+    spans at or above it the tensor-core kernel's alone: each phase run by
+    itself leaves the other's rows untouched (still NaN), and both together
+    match the oracle."""
+    rng = np.random.default_rng(700 + min_span)
+    lens = np.array([1, 3, 60, 5, 300, 45, 4], np.int32)
+    qlens = np.array([1, 3, 40, 5, 100, 39, 2], np.int32)
+    st = wl.make_step(rng, lens, qlens, dtype=wl.F16, poison_unused=True)
+    ref, kp, vp = orc.step(st)
+    d = DevStep(st, k_pool=kp, v_pool=vp)
+    span_of_row = np.repeat(np.arange(len(qlens)), qlens)
+    tc_rows = torch.from_numpy(qlens[span_of_row] >= min_span).to(d.out.device)
+    for phase, mine in ((nb.NS_PREFILL_TENSOR_CORE, tc_rows), (nb.NS_PREFILL_WALK, ~tc_rows)):
+        d.out.fill_(float("nan"))
+        cfg = _prefill_cfg(min_span)
+        cfg.phases = phase
+        nb.ns_paged_attn_prefill(d.q, d.query_start_loc, d.k_pool, d.v_pool, d.block_tables,
+                                 d.context_lens, st.scale, d.out, d.ws, config=cfg)
+        torch.cuda.synchronize()
+        written = ~torch.isnan(d.out.float()).flatten(1).any(dim=1)
+        assert torch.equal(written, mine), f"phase {phase}: rows written {written.tolist()}"
+    nb.ns_paged_attn_prefill(d.q, d.query_start_loc, d.k_pool, d.v_pool, d.block_tables,
+                             d.context_lens, st.scale, d.out, d.ws, config=_prefill_cfg(min_span))
+    torch.cuda.synchronize()
+    compare(d.out, ref, st.dtype, f"min_span {min_span}")
+    _gpu.assert_no_device_status()
