@@ -83,8 +83,9 @@ constexpr int kLensCache = 256;        // context lengths kept in shared memory
 // (2, 3 and 4 measured alike on the batch-256 decode; 1 and 6 slower.)
 constexpr int kPieceCost = 4;
 // Pieces the automatic split aims at for the longest pair when the batch is
-// small (measured: the 4-sequence step 16.4 -> 12.5 us and the batch-32
-// step 20.5 -> ~20.2 us against 8 blocks a worker).
+// small, and the pairs per warp below which every warp takes a range
+// (measured against 8 blocks a worker: the 4-sequence step 16.4 -> 13.3 us,
+// batch 32 20.5 -> 20.2 us, 8 x 4096 tokens 23.2 -> 21.5 us).
 constexpr int kAutoPieces = 32;
 
 // Length of a pair in the split's coordinates (0 for a pair with no block).
@@ -1666,9 +1667,13 @@ __device__ __forceinline__ Split read_split(const DecodeParams &P, const Smem &s
     unsigned per_worker = (unsigned)max(1, (P.min_blocks_per_cta + NG - 1) / NG);
     // Automatic policy: no more blocks a worker than keep the longest pair
     // in about kAutoPieces pieces, so that short steps use more workers
-    // (cut finer: more pieces, but each merge part still loads in one round trip)
-    if (P.auto_policy)
+    // (cut finer: more pieces, but each merge part still loads in one round
+    // trip); with at most W / kAutoPieces live pairs, every warp.
+    if (P.auto_policy) {
         per_worker = min(per_worker, (unsigned)max(1, (maxnb + kPieceCost + kAutoPieces - 1) / kAutoPieces));
+        if (live * kAutoPieces <= W)
+            per_worker = 1;
+    }
     int gw = (int)(((unsigned)total + per_worker - 1u) / per_worker);
     gw = min(gw, min(W, kMaxWorkers));
     gw = max(1, min(gw, total));  // no empty ranges: every worker between a pair's first and last holds a piece
