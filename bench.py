@@ -56,14 +56,15 @@ KERNEL_SOURCES = {
                           "paged_kv_decode_ns_gb300/csrc/tcgen05.cuh", "include/ns_paged.h"],
 }
 PROFILED_TRAFFIC = {
-    # ncu capture of the committed kernel: 238.98 MB read + 3.62 MB written
+    # ncu capture of the committed kernel (dram__bytes_read.sum + dram__bytes_write.sum
+    # of one launch of the default command): 239.03 MB read + 3.33 MB written
     ("decode_b256", "paged_decode_kernel"): {
-        "sources_sha256": "3c26dd70990d2b3c7545686f5ba11b9bb7efb23dbda11ec47bee18f1042ad834",
-        "bytes": 242606336},
+        "sources_sha256": "4739802e7053aa7e6b38c054c1c759dee82b68a8f3bd7f9adaf1c68c0fa00353",
+        "bytes": 242360064},
     # ncu capture of the committed kernel: 4.73 MB read, 0 written
     ("mixed_chunked_prefill", "tc_prefill_kernel"): {
-        "sources_sha256": "3552f5a02d6dee42418d7d962677d7dc296afe0c5bd6f54467f02d85eeaf77ee",
-        "bytes": 4728576},
+        "sources_sha256": "007c4465a7f009addeaf16729db53fd6af56abb8e42d2ef2b7ffb1c179e38fe6",
+        "bytes": 4728832},
 }
 
 
@@ -101,6 +102,16 @@ def kernel_sources_sha(kernel: str) -> str:
             h.update(rel.encode())
             h.update(strip_comments(f.read()).encode())
     return h.hexdigest()
+
+
+def traffic_source(args, traffic):
+    """Where the roofline's traffic figure comes from (it is not measured in this run)."""
+    if args.traffic is not None:
+        return "--traffic on the command line"
+    if traffic is None:
+        return None
+    return ("ncu capture (dram__bytes_read.sum + dram__bytes_write.sum, one launch) of the same "
+            "kernel sources, matched by their sha256 in bench.py")
 
 
 def profiled_traffic(workload: str, kernel: str):
@@ -623,6 +634,7 @@ def bench_ours(args):
             profiled_traffic(args.workload, "paged_decode_kernel") if args.kv == "native" else None)
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                     "frac": achieved / peak, "traffic": traffic,
+                    "traffic_source": traffic_source(args, traffic),
                     "kernel": "paged_decode_kernel (fused kv_append + split-KV decode"
                               + (", q8_0 pools)" if args.kv == "q8_0" else ")"),
                     "bytes_per_launch": alg_bytes, "launch_us": launch_ms * 1e3,
@@ -636,6 +648,7 @@ def bench_ours(args):
                                                                                   "tc_prefill_kernel")
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": traffic,
+                    "traffic_source": traffic_source(args, traffic),
                     "kernel": "tc_prefill_kernel (tcgen05, spans of 2+ rows)",
                     "flops_per_launch": flops, "launch_us": launch_ms * 1e3,
                     "peak_source": f"{peak_src} bf16_tflops (burst) x nominal fp16/bf16 ratio 1.0"}
