@@ -342,10 +342,9 @@ ns_status ns_paged_attn_prefill_ex(const void *q, const int32_t *query_start_loc
  * cannot allocate device memory.
  *
  * The pages describe no such entry point; it serves callers that may not
- * call cudaMalloc or a caching allocator at all: code that runs while a CUDA
- * graph is being captured (an allocation cannot be captured), plugins inside
- * a host runtime that owns every device allocation, and serving loops that
- * must not allocate once they run.  It takes the same inputs and output as
+ * call cudaMalloc or a caching allocator at all: plugins inside a host
+ * runtime that owns every device allocation, and serving loops that must not
+ * allocate once they run.  It takes the same inputs and output as
  * ns_paged_attn_decode (same checks, same result) but no workspace: the split
  * partial records, arrival counters and plan record live in a scratch array
  * compiled into the library (about 8.7 MB, held by every GPU that loads the
@@ -353,8 +352,7 @@ ns_status ns_paged_attn_prefill_ex(const void *q, const int32_t *query_start_loc
  *   - num_seqs * num_kv_heads must not exceed NS_NOALLOC_MAX_PAIRS; larger
  *     calls return NS_ERR_UNSUPPORTED and launch nothing.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current.
  *   - Every call clears the arrival counters it needs (cudaMemsetAsync on
  *     `stream`) before its kernel; it allocates and frees nothing.
  *   - All calls share the one array: calls that overlap on the GPU (two

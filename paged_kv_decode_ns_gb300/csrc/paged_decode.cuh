@@ -10,33 +10,40 @@
 //
 // How (GB300-first design, not the pages' Triton kernel):
 //  * Workers are warps.  The KV blocks of all (sequence, kv head) pairs are
-//    laid end to end and worker w of Gw takes blocks [w*B/Gw, (w+1)*B/Gw),
-//    so every warp gets the same number of blocks whatever the length mix,
-//    and no warp ever waits on another: a pair cut by a worker boundary
-//    yields a partial (max, sum, unnormalised output) record written by the
-//    warp alone, and the warp that finishes a pair's last piece merges the
-//    records (log-sum-exp) and writes the output.  Gw is chosen on the
-//    device from the real lengths; when no pair is long, whole pairs are
-//    dealt round-robin and nothing is merged.
-//  * Per-warp TMA rings.  Each warp streams its range through its own ring
-//    of S slots of 16 tokens: TMA bulk copies (cp.async.bulk) of the K and V
-//    rows of 16/bs whole blocks (half a block at block size 32), issued S
-//    steps ahead of use, L2 evict-first, completed on the slot's mbarrier.
-//    The first step of a piece also brings the group's q rows, and with a
-//    fused append the step that holds the new token brings its K/V rows.
-//    Block-table entries are read 32 at a time, the next 32 prefetched.
-//  * Lane layout.  Lane (r, c) = (lane>>3, lane&7) owns dims 8c..8c+7 of
-//    token rows r, r+4, r+8, r+12 of a step, for all G query heads of the
-//    GQA group, so one 16-byte shared load feeds every head.  Dot products
-//    run on packed fp32 FMA (two per instruction).  The partial sums of a
-//    token are combined by a shuffle reduce-scatter over the row's 8 lanes;
-//    the heads are padded to a power of two N and slot i of lane c holds
-//    head i ^ (c >> (3 - log2 N)), so the halving steps need no
-//    lane-dependent selects and lane c ends with head c >> (3 - log2 N).
+//    laid end to end (each pair counted kPieceCost blocks longer) and worker
+//    c of Gw takes an equal run of them, so every warp gets the same share
+//    whatever the length mix, and no warp ever waits on another: a pair cut
+//    by a worker boundary yields a partial (max, sum, unnormalised output)
+//    record written by the warp alone; at the end of its ring the warp
+//    counts its records, and the warp whose count completes a pair queues
+//    its log-sum-exp merge, which the CTA's idle warps run in parts of 1-8
+//    query heads.  Gw is chosen on the device from the real lengths and the
+//    batch (read_split); when no pair is long, whole pairs are dealt
+//    round-robin and nothing is merged.
+//  * Per-warp TMA rings, fed by a producer warpgroup.  Each consumer warp
+//    streams its range through its own ring of S slots of TOK tokens (32 at
+//    head_dim 64, 16 at 128): TMA bulk copies (cp.async.bulk) of the K and V
+//    rows of TOK/bs whole blocks, issued S steps ahead of use, L2
+//    evict-first, completed on the slot's mbarrier.  The first step of a
+//    piece also brings the group's q rows, and with a fused append the step
+//    that holds the new token brings its K/V rows.  Block-table entries are
+//    read one step ahead.
+//  * Lane layout (head_dim 64).  Lane (r, c) = (lane>>3, lane&7) owns dims
+//    8c..8c+7 of token rows r, r+4, ..., r+28 of a step, for all G query
+//    heads of the GQA group, so one 16-byte shared load feeds every head.
+//    Scores run on packed fp32 FMA with two heads per instruction (q held as
+//    head pairs); the partial sums of a token are combined by a shuffle
+//    reduce-scatter over the row's lanes; the heads are padded to a power
+//    of two N and slot i of lane c holds head i ^ (c >> (3 - log2 N)), so
+//    the halving steps need no lane-dependent selects and lane c ends with
+//    head c >> (3 - log2 N).  At head_dim 128 a row spans 16 lanes.
 //  * Online softmax per (row group, head) in log2 units with lazy
 //    rescaling: the running max moves only when a score exceeds it by more
 //    than kRescaleSlack, and the result is exact because sum and accumulator
 //    share the stale max.
+//  * q8_0 pools (Q8): a step carries each row's int8 codes and fp16 block
+//    scales; codes convert exactly to fp32 and the scales apply per
+//    32-element block; the fused append quantises the new token.
 //  * Every wait is bounded; a timeout sets NS_DEV_WAIT_TIMEOUT and the warp
 //    stops, waiting -- again bounded -- for its own copies in flight.
 #pragma once

@@ -3,8 +3,7 @@
 //
 // ns_paged_attn_decode needs a caller-provided workspace (split-KV partial
 // records, one arrival counter per (sequence, kv head) and a plan record).
-// Some callers cannot call cudaMalloc or a caching allocator: code that runs
-// while a CUDA graph is being captured (allocation is not capturable), plugins
+// Some callers cannot call cudaMalloc or a caching allocator: plugins
 // embedded in a host runtime that owns every device allocation, and serving
 // loops that forbid allocation after start-up.  This file gives them
 // ns_paged_attn_decode_noalloc, which runs the same kernel (and grid) over a
@@ -14,8 +13,8 @@
 // library holds it (about 8.7 MB) until the process exits.  Host code cannot
 // use the array's name as a device address, so the first call on each device
 // asks the runtime for that device's address (cudaGetSymbolAddress) with the
-// device current, checks the result and caches it; that first call should come
-// before any stream capture.  Every call shares the one array: calls that
+// device current, checks the result and caches it.  Every call shares the one
+// array: calls that
 // overlap on the GPU (two streams, two threads) race and give wrong results.
 // The arrival counters must start at zero, so each call clears them with
 // cudaMemsetAsync on its own stream before the kernel; the partial records need

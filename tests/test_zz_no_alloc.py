@@ -1,9 +1,8 @@
 """The allocation-free decode entry point, ns_paged_attn_decode_noalloc.
 
-Some callers cannot allocate device memory: code that runs while a CUDA graph
-is being captured (an allocation cannot be captured), plugins that live inside
-a host runtime which owns every device allocation, and serving loops that must
-not allocate once they are running.  For them the library runs the split-KV
+Some callers cannot allocate device memory: plugins that live inside a host
+runtime which owns every device allocation, and serving loops that must not
+allocate once they are running.  For them the library runs the split-KV
 decode over scratch memory that is part of the library image instead of a
 caller-provided workspace.  This file checks, through the C ABI, that two
 calls in a row give the same bits as ns_paged_attn_decode with a workspace
