@@ -30,10 +30,14 @@
  *               decode, its fused append and the prefill, whose spans then
  *               all take the split-KV walk; the tensor-core prefill, the
  *               q8_0 pools and the allocation-free entry point take 64).
- *               num_q_heads must be a multiple of num_kv_heads with at most
- *               8 query heads per KV head; query head j reads KV head
- *               j / (num_q_heads / num_kv_heads).  block_size must be 4, 8,
- *               16 or 32.
+ *               num_q_heads must be a multiple of num_kv_heads; query head
+ *               j reads KV head j / G, G = num_q_heads / num_kv_heads.  G is
+ *               at most 8, or up to 64 when it is a multiple of
+ *               n = ceil(G / 8): such a group runs as n groups of G / n heads
+ *               over the same KV head (the tensor-core prefill and the
+ *               allocation-free entry point take G <= 8; larger groups'
+ *               spans take the split-KV walk).  block_size must be 4, 8, 16
+ *               or 32.
  *  Pool layout  k_pool and v_pool are [num_blocks][num_kv_heads][block_size]
  *               [head_dim]: one (block, kv head) is block_size*head_dim
  *               contiguous elements.  Token slot s lives in block

@@ -14,6 +14,7 @@ namespace {
 __device__ unsigned int g_device_status;
 
 constexpr int kMaxDevices = 64;
+constexpr int kMaxLargeGroup = 64;  // query heads per kv head (above ns::kMaxGroup: virtual kv heads)
 std::atomic<unsigned *> g_status_ptr[kMaxDevices];
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_ctas_per_sm[kMaxDevices][2][4][ns::kMaxGroup];
@@ -206,6 +207,18 @@ struct WsLayout {
     size_t plan, counters, partials, row_seq, row_len, total;
 };
 
+// Groups of more than kMaxGroup query heads run as kv_sub groups of G / kv_sub
+// heads each (virtual kv heads over the same pool head); 0 when G cannot be
+// cut so (G not a multiple of ceil(G / kMaxGroup)), 1 for G <= kMaxGroup.
+int kv_sub(int num_q_heads, int num_kv_heads)
+{
+    if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
+        return 1;
+    const int g = num_q_heads / num_kv_heads;
+    const int sub = (g + ns::kMaxGroup - 1) / ns::kMaxGroup;
+    return g % sub == 0 ? sub : 0;
+}
+
 WsLayout ws_layout(long long rows, int num_kv_heads, int head_dim)
 {
     WsLayout L;
@@ -229,7 +242,8 @@ ns_status check_shapes(int num_q_heads, int num_kv_heads, int head_dim, int bloc
         return NS_ERR_UNSUPPORTED;
     if (head_dim == 128 && block_size != 16)
         return NS_ERR_UNSUPPORTED;
-    if (num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > ns::kMaxGroup)
+    if (num_q_heads % num_kv_heads != 0 || num_q_heads / num_kv_heads > kMaxLargeGroup ||
+        kv_sub(num_q_heads, num_kv_heads) == 0)
         return NS_ERR_UNSUPPORTED;
     return NS_OK;
 }
@@ -265,7 +279,8 @@ ns_status run_decode(const DecodeCall &c, int dev)
     unsigned *status = status_word(dev);
     if (status == nullptr)
         return NS_ERR_CUDA;
-    const WsLayout L = ws_layout(c.rows, c.num_kv_heads, c.head_dim);
+    const int sub = kv_sub(c.num_q_heads, c.num_kv_heads);
+    const WsLayout L = ws_layout(c.rows, c.num_kv_heads * sub, c.head_dim);
     char *ws = static_cast<char *>(c.workspace);
 
     ns::DecodeParams P;
@@ -284,8 +299,9 @@ ns_status run_decode(const DecodeCall &c, int dev)
     P.v_pool_w = const_cast<uint16_t *>(static_cast<const uint16_t *>(c.v_pool));
     P.num_seqs = c.rows;
     P.num_q_heads = c.num_q_heads;
-    P.num_kv_heads = c.num_kv_heads;
-    P.group = c.num_q_heads / c.num_kv_heads;
+    P.num_kv_heads = c.num_kv_heads * sub;  // virtual kv heads
+    P.group = c.num_q_heads / P.num_kv_heads;
+    P.kv_sub = sub;
     P.max_blocks_per_seq = c.max_blocks_per_seq;
     P.num_blocks = c.num_blocks;
     P.scale_log2 = c.scale * 1.4426950408889634f;
@@ -332,7 +348,7 @@ ns_status check_decode_args(const void *q, const void *k_pool, const void *v_poo
         return NS_ERR_INVALID_ARG;
     if (max_blocks_per_seq < 1 || num_blocks < 1 || !std::isfinite(scale))
         return NS_ERR_INVALID_ARG;
-    if (!ns::split_fits(rows, num_kv_heads, max_blocks_per_seq))
+    if (!ns::split_fits(rows, (long long)num_kv_heads * kv_sub(num_q_heads, num_kv_heads), max_blocks_per_seq))
         return NS_ERR_UNSUPPORTED;
     if (workspace_bytes < ns_paged_attn_workspace_bytes(rows, num_q_heads, num_kv_heads, head_dim))
         return NS_ERR_INVALID_ARG;
@@ -464,7 +480,8 @@ size_t ns_paged_attn_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_h
     (void)num_q_heads;
     if (num_seqs < 0 || num_kv_heads <= 0)
         return 0;
-    return ws_layout(num_seqs, num_kv_heads, head_dim == 128 ? 128 : 64).total;
+    const int sub = kv_sub(num_q_heads, num_kv_heads);
+    return ws_layout(num_seqs, num_kv_heads * (sub > 0 ? sub : 1), head_dim == 128 ? 128 : 64).total;
 }
 
 ns_status ns_paged_attn_workspace_init(void *workspace, size_t workspace_bytes, ns_stream_t stream)
@@ -601,7 +618,7 @@ ns_status ns_paged_attn_prefill_ex(const void *q, const int32_t *query_start_loc
     unsigned *status = status_word(dev);
     if (status == nullptr)
         return NS_ERR_CUDA;
-    const WsLayout L = ws_layout(total_q_tokens, num_kv_heads, head_dim);
+    const WsLayout L = ws_layout(total_q_tokens, num_kv_heads * kv_sub(num_q_heads, num_kv_heads), head_dim);
     char *ws = static_cast<char *>(workspace);
     int32_t *row_seq = reinterpret_cast<int32_t *>(ws + L.row_seq);
     int32_t *row_len = reinterpret_cast<int32_t *>(ws + L.row_len);

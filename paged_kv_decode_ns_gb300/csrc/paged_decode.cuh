@@ -142,7 +142,18 @@ struct DecodeParams {
     int overlap;      // launched as a programmatic dependent: wait for the previous grid (see the prologue)
     int pack;         // number workers CTA-major even when only some have work
     unsigned long long wait_limit_ns;  // consumers' waits for a ring step (the producer's own drain keeps kWaitLimitNs)
+    // A group of more than 8 query heads runs as kv_sub groups of group / kv_sub
+    // heads: num_kv_heads and group above count these virtual kv heads, and
+    // virtual head h reads the pools' (and the new K/V's) head h / kv_sub.
+    int kv_sub;
 };
+
+// The pools' kv heads, and the pools' head of virtual kv head h.
+__device__ __forceinline__ int pool_heads(const DecodeParams &P) { return P.num_kv_heads / max(P.kv_sub, 1); }
+__device__ __forceinline__ int pool_head(const DecodeParams &P, int h) { return h / max(P.kv_sub, 1); }
+// Whether virtual kv head h stores the new token into the pools (one of each
+// pool head's virtual heads does).
+__device__ __forceinline__ bool stores_new_token(const DecodeParams &P, int h) { return h % max(P.kv_sub, 1) == 0; }
 
 // Source of the zero-filled rows of a step (32 rows of 64 elements).
 static __device__ __align__(128) uint16_t g_zero_rows[kZeroElems];
@@ -1308,9 +1319,10 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8, 
             mbar_arrive(bar);
         else
             mbar_arrive_expect_tx(bar, bytes);
+        const int pool_h = pool_head(P, cur.ph), pool_hkv = pool_heads(P);
 #pragma unroll
         for (int u = 0; u < KB; ++u) {
-            const long long row0 = ((long long)phys[u] * P.num_kv_heads + cur.ph) * BS;  // pool row of the block
+            const long long row0 = ((long long)phys[u] * pool_hkv + pool_h) * BS;  // pool row of the block
             if constexpr (!Q8) {
                 if (rows[u] > 0) {
                     bulk_load(sl.k + u * BS * D, P.k_pool + row0 * D, rows[u] * kRowB16, bar, pol);
@@ -1345,7 +1357,7 @@ __device__ void decode_producer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8, 
             bulk_load(sl.q, P.q + qoff, G * kRowB16, bar);
         }
         if (new_tok) {
-            const long long noff = ((long long)cur.ps * P.num_kv_heads + cur.ph) * D;
+            const long long noff = ((long long)cur.ps * pool_hkv + pool_h) * D;
             if constexpr (!Q8) {
                 const int t_new = (cur.pL - 1) - tok0;
                 bulk_load(sl.k + t_new * D, P.k_new + noff, kRowB16, bar);
@@ -1413,8 +1425,8 @@ __device__ __forceinline__ void quantize_new_row(const DecodeParams &P, DecodeSl
         *reinterpret_cast<uint2 *>(row) = make_uint2(packed[0], packed[1]);
         if ((cc & 3) == 0)
             (isv ? sl.vs : sl.ks)[t * kQ8Scales + (cc >> 2)] = d16;
-        if (new_slot >= 0) {
-            const long long prow = ((new_slot / BS) * P.num_kv_heads + ph) * BS + new_slot % BS;
+        if (new_slot >= 0 && stores_new_token(P, ph)) {
+            const long long prow = ((new_slot / BS) * pool_heads(P) + pool_head(P, ph)) * BS + new_slot % BS;
             int8_t *codes = const_cast<int8_t *>(isv ? P.v_codes : P.k_codes);
             uint16_t *scales = const_cast<uint16_t *>(isv ? P.v_scales : P.k_scales);
             *reinterpret_cast<uint2 *>(codes + prow * kQ8CodeRow + cc * 8) = make_uint2(packed[0], packed[1]);
@@ -1511,12 +1523,13 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8, 
                 // slot the producer checked (q8_0: quantised first)
                 if (step == nsteps - 1 && (mt.flags & kFlagNewTok)) {
                     if constexpr (!Q8) {
-                        if (lane < 2 * GD::COLS && mt.new_slot >= 0) {
+                        if (lane < 2 * GD::COLS && mt.new_slot >= 0 && stores_new_token(P, mt.ph)) {
                             const bool isv = lane >= GD::COLS;
                             const int cc = lane & (GD::COLS - 1);
                             const uint4 val = lds128((isv ? sl.v : sl.k) + mt.t_new * D + cc * 8);
                             const long long ns = mt.new_slot;
-                            const long long dst = (((ns / BS) * P.num_kv_heads + mt.ph) * BS + ns % BS) * D + cc * 8;
+                            const long long dst =
+                                (((ns / BS) * pool_heads(P) + pool_head(P, mt.ph)) * BS + ns % BS) * D + cc * 8;
                             *reinterpret_cast<uint4 *>((isv ? P.v_pool_w : P.k_pool_w) + dst) = val;
                         }
                     } else {

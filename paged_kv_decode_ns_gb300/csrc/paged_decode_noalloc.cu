@@ -121,6 +121,7 @@ extern "C" ns_status ns_paged_attn_decode_noalloc(const void *q, const void *k_p
     P.whole_sequences = 0;
     P.auto_policy = 1;
     P.wait_limit_ns = ns::kWaitLimitNs;
+    P.kv_sub = 1;  // groups of at most ns::kMaxGroup heads only
 
     return ns::launch_decode(P, dtype, block_size, 0, st, dev);
 }

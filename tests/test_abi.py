@@ -72,8 +72,12 @@ def test_host_checks_need_no_gpu(lib):
                   P, ctypes.c_size_t]
     # 14 q heads over 4 kv heads is not a grouping
     assert d(None, None, None, None, None, 4, 14, 4, 64, 16, 0.125, None, None, 8, 10, 0, None, 0) == -2
-    # more than 8 q heads per kv head
+    # 9 q heads per kv head: more than 8, and not cut evenly into groups of at most 8
     assert d(None, None, None, None, None, 4, 18, 2, 64, 16, 0.125, None, None, 8, 10, 0, None, 0) == -2
+    # more than 64 q heads per kv head
+    assert d(None, None, None, None, None, 4, 72, 1, 64, 16, 0.125, None, None, 8, 10, 0, None, 0) == -2
+    # 16 q heads per kv head (two groups of 8) passes the shape checks
+    assert d(None, None, None, None, None, 4, 32, 2, 64, 16, 0.125, None, None, 8, 10, 0, None, 0) == -1
     # null pointers
     assert d(None, None, None, None, None, 4, 14, 2, 64, 16, 0.125, None, None, 8, 10, 0, None, 0) == -1
 
