@@ -624,7 +624,8 @@ ns_status ns_paged_attn_prefill_ex(const void *q, const int32_t *query_start_loc
     int32_t *row_len = reinterpret_cast<int32_t *>(ws + L.row_len);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     int tc_min = cfg && cfg->tensor_core_min_span != 0 ? cfg->tensor_core_min_span : 2;
-    if (tc_min < 0 || head_dim != 64 || !ns::tc_prefill_supported(block_size, num_q_heads / num_kv_heads) ||
+    if (tc_min < 0 || (head_dim == 128 && block_size != 16) ||
+        !ns::tc_prefill_supported(block_size, num_q_heads / num_kv_heads) ||
         (long long)num_blocks * num_kv_heads * block_size > 0x7fffffffLL)
         tc_min = 0;
     const int phases = cfg && cfg->phases != 0 ? cfg->phases : (NS_PREFILL_WALK | NS_PREFILL_TENSOR_CORE);
@@ -646,7 +647,7 @@ ns_status ns_paged_attn_prefill_ex(const void *q, const int32_t *query_start_loc
         return NS_OK;
     return ns::launch_tc_prefill(q, query_start_loc, k_pool, v_pool, block_tables, context_lens,
                                  num_seqs, total_q_tokens, num_q_heads, num_kv_heads, block_size,
-                                 scale, out, max_blocks_per_seq, num_blocks, dtype, tc_min, status,
+                                 scale, out, max_blocks_per_seq, num_blocks, dtype, tc_min, head_dim, status,
                                  (phases & NS_PREFILL_WALK) != 0, st) == cudaSuccess
                ? NS_OK
                : NS_ERR_CUDA;

@@ -44,6 +44,7 @@ cudaError_t launch_tc_prefill(const void *q, const int32_t *query_start_loc, con
                               const int32_t *context_lens, int num_seqs, int total_q_tokens,
                               int num_q_heads, int num_kv_heads, int block_size, float scale,
                               void *out, int max_blocks_per_seq, long long num_blocks, ns_dtype dtype,
-                              int min_span, unsigned *status, bool after_walk, cudaStream_t stream);
+                              int min_span, int head_dim, unsigned *status, bool after_walk,
+                              cudaStream_t stream);
 
 }  // namespace ns

@@ -45,17 +45,29 @@ namespace ns {
 
 namespace {
 
-constexpr int kKT = 128;         // keys per K/V tile
 constexpr int kRows = 128;       // MMA M
-// TMEM columns: S [0,128); O of key half h [128 + 64h, 192 + 64h); P of
-// tile j in buffer b = j mod 2, part p, key half h: [256 + NP*64 b + 64p + 32h,
-// + 32) (two 16-bit values a column; NP parts, at most 512 columns in all)
 constexpr int kTmemCols = 512;
-constexpr int kTmemO = 128;
-constexpr int kTmemP = 256;
-constexpr int kStages = 4;       // K/V tiles in flight (3 measured 4% slower, 5 alike)
-constexpr int kSoftmaxThreads = 256;  // two warpgroups: key columns 0..63 and 64..127 of each row
-constexpr int kHalf = kKT / 2;         // key columns per softmax thread
+constexpr int kRegionBytes = 128;     // 64 elements of a row: one 128-byte swizzle span
+constexpr int kSoftmaxThreads = 256;  // two warpgroups: the two key halves of each tile
+
+// Geometry by head dim D.  A row of D elements is D/64 regions of 64; each
+// region of a Q, K or V tile is its own 128-byte-swizzled panel in shared
+// memory, loaded by its own TMA box.  D 64: 128-key tiles, 4 stages; D 128:
+// 64-key tiles and 3 stages, so that shared memory and TMEM fit.
+// TMEM columns: S [0, KT); O of key half h [KT + D h, KT + D (h+1)); P of
+// tile j in buffer b = j mod 2, part p, key half h: [KT + 2D + NP KT/2 b +
+// KT/2 p + KT/4 h, + KT/4) (two 16-bit values a column; NP parts).
+template <int D>
+struct TcGeo {
+    static constexpr int KT = D == 64 ? 128 : 64;  // keys per K/V tile
+    static constexpr int REG = D / 64;             // regions of a row
+    static constexpr int HALF = KT / 2;            // key columns per softmax thread
+    static constexpr int STAGES = D == 64 ? 4 : 3; // K/V tiles in flight (D 64: 3 measured 4% slower, 5 alike)
+    static constexpr int TMEM_O = KT;
+    static constexpr int TMEM_P = KT + 2 * D;
+    static constexpr int ROW_BYTES = 2 * D;
+    static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+};
 constexpr int kMmaWarp = 8;            // score products; TMEM allocation
 constexpr int kProducerWarp = 9;
 constexpr int kPvWarp = 10;            // value products
@@ -90,14 +102,15 @@ struct PParts {
 };
 
 // NP (the P parts, 1 or 2) sizes no member: P lives in TMEM.
-template <int NP>
+template <int NP, int D>
 struct alignas(1024) PrefillSmem {
-    uint8_t q[kRows * 128];
-    uint8_t k[kStages][kKT * 128];
-    uint8_t v[kStages][kKT * 128];
+    using GG = TcGeo<D>;
+    uint8_t q[GG::REG][kRows * kRegionBytes];
+    uint8_t k[GG::STAGES][GG::REG][GG::KT * kRegionBytes];
+    uint8_t v[GG::STAGES][GG::REG][GG::KT * kRegionBytes];
     uint64_t q_full;
-    uint64_t kv_full[kStages];
-    uint64_t kv_empty[kStages];
+    uint64_t kv_full[GG::STAGES];
+    uint64_t kv_empty[GG::STAGES];
     uint64_t s_full;
     uint64_t s_free;
     uint64_t p_full;
@@ -108,41 +121,54 @@ struct alignas(1024) PrefillSmem {
     float xm[2][kRows];  // [half][row]
     float xl[2][kRows];
     // rank 1's unnormalised rows, written remotely into rank 0 with 16-byte stores
-    alignas(16) float rem_o[kRows][kHeadDim];
+    alignas(16) float rem_o[kRows][D];
     float rem_m[kRows];
     float rem_l[kRows];
     uint64_t rem_bar;
     uint32_t tmem_base;
-    uint32_t loaded[kStages];  // bit i: block i of the tile was loaded
+    uint32_t loaded[GG::STAGES];  // bit i: block i of the tile was loaded
     int u_s, u_h, u_i0, u_n, u_L, u_tiles, u_ok;
     int u_j0, u_nt;  // this CTA's key tiles: [u_j0, u_j0 + u_nt)
 };
 
 // Vector (16-byte) and mbarrier (8-byte) accesses need these alignments.
-static_assert(offsetof(PrefillSmem<1>, rem_o) % 16 == 0 && offsetof(PrefillSmem<2>, rem_o) % 16 == 0,
+using Smem164 = PrefillSmem<1, 64>;
+using Smem264 = PrefillSmem<2, 64>;
+using Smem1128 = PrefillSmem<1, 128>;
+using Smem2128 = PrefillSmem<2, 128>;
+static_assert(offsetof(Smem164, rem_o) % 16 == 0 && offsetof(Smem264, rem_o) % 16 == 0 &&
+                  offsetof(Smem1128, rem_o) % 16 == 0 && offsetof(Smem2128, rem_o) % 16 == 0,
               "remote 16-byte stores into rem_o");
-static_assert(offsetof(PrefillSmem<1>, q_full) % 8 == 0 && offsetof(PrefillSmem<2>, rem_bar) % 8 == 0,
+static_assert(offsetof(Smem164, q_full) % 8 == 0 && offsetof(Smem264, rem_bar) % 8 == 0 &&
+                  offsetof(Smem1128, q_full) % 8 == 0 && offsetof(Smem2128, rem_bar) % 8 == 0,
               "mbarriers are 8-byte aligned");
+// every swizzled panel starts on a 1024-byte boundary
+static_assert(offsetof(Smem1128, k) % 1024 == 0 && offsetof(Smem1128, v) % 1024 == 0 &&
+                  offsetof(Smem164, k) % 1024 == 0 && offsetof(Smem164, v) % 1024 == 0 &&
+                  (TcGeo<128>::KT * kRegionBytes) % 1024 == 0,
+              "128-byte swizzle panels are 1024-byte aligned");
 
-template <int NP>
+template <int NP, int D>
 constexpr size_t smem_bytes()
 {
-    return sizeof(PrefillSmem<NP>) + 1024;  // + alignment slack
+    return sizeof(PrefillSmem<NP, D>) + 1024;  // + alignment slack
 }
 
-static_assert(smem_bytes<1>() <= 227 * 1024 && smem_bytes<2>() <= 227 * 1024, "prefill shared memory");
+static_assert(smem_bytes<1, 64>() <= 227 * 1024 && smem_bytes<2, 64>() <= 227 * 1024 &&
+                  smem_bytes<1, 128>() <= 227 * 1024 && smem_bytes<2, 128>() <= 227 * 1024,
+              "prefill shared memory");
 
-template <int NP>
-__device__ __forceinline__ PrefillSmem<NP> &smem_of(unsigned char *raw)
+template <int NP, int D>
+__device__ __forceinline__ PrefillSmem<NP, D> &smem_of(unsigned char *raw)
 {
     const uintptr_t a = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023);
-    return *reinterpret_cast<PrefillSmem<NP> *>(a);
+    return *reinterpret_cast<PrefillSmem<NP, D> *>(a);
 }
 
 // Find this CTA's unit.  Units are enumerated spans last-to-first (later
 // chunks sit on longer prefixes), query tiles last-to-first, then kv heads.
-template <int NP>
-__device__ void find_unit(const PrefillParams &P, PrefillSmem<NP> &sm, int lane)
+template <class Smem>
+__device__ void find_unit(const PrefillParams &P, Smem &sm, int lane)
 {
     const long long u = blockIdx.x >> 1;  // one unit per 2-CTA cluster
     long long base = 0;
@@ -188,15 +214,23 @@ __device__ void find_unit(const PrefillParams &P, PrefillSmem<NP> &sm, int lane)
         sm.u_ok = -1;  // no unit for this CTA
 }
 
-template <typename T, int BS>
+// P of a softmax thread's key half into TMEM: 32 columns (D 64) or 16 (D 128).
+__device__ __forceinline__ void store_p(uint32_t addr, const uint32_t (&v)[32]) { tc::tmem_st32(addr, v); }
+__device__ __forceinline__ void store_p(uint32_t addr, const uint32_t (&v)[16]) { tc::tmem_st16(addr, v); }
+
+template <typename T, int BS, int D>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const PrefillParams P)
 {
     constexpr int NP = PParts<T>::N;
+    using GG = TcGeo<D>;
+    constexpr int kKT = GG::KT, kHalf = GG::HALF, kStages = GG::STAGES, kRowBytes = GG::ROW_BYTES;
+    constexpr int kTmemO = GG::TMEM_O, kTmemP = GG::TMEM_P, REG = GG::REG;
+    constexpr int OC = D / 2;  // output columns of a softmax thread
     static_assert(kTmemP + 2 * NP * (kKT / 2) <= kTmemCols, "two P buffers fit in TMEM");
     extern __shared__ unsigned char smem_raw[];
-    PrefillSmem<NP> &sm = smem_of<NP>(smem_raw);
+    PrefillSmem<NP, D> &sm = smem_of<NP, D>(smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = P.group;
 
@@ -249,8 +283,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // Rows of the Q tile the TMA box does not cover are zeroed once.
     if (warp < 4 && (int)threadIdx.x >= P.qt * G) {
 #pragma unroll
-        for (int b = 0; b < kRowBytes; b += 16)
-            *reinterpret_cast<uint4 *>(sm.q + threadIdx.x * kRowBytes + b) = make_uint4(0, 0, 0, 0);
+        for (int g = 0; g < REG; ++g)
+#pragma unroll
+            for (int b = 0; b < kRegionBytes; b += 16)
+                *reinterpret_cast<uint4 *>(sm.q[g] + threadIdx.x * kRegionBytes + b) = make_uint4(0, 0, 0, 0);
         tc::fence_async_smem();
     }
     if (warp == kMmaWarp) {
@@ -275,7 +311,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc::prefetch_tensormap(&tm_k);
             tc::prefetch_tensormap(&tm_v);
             mbar_arrive_expect_tx(&sm.q_full, (uint32_t)(P.qt * G * kRowBytes));
-            tc::tma_load_3d(sm.q, &tm_q, 0, h * G, __ldg(P.qsl + s) + i0, &sm.q_full);
+#pragma unroll
+            for (int g = 0; g < REG; ++g)
+                tc::tma_load_3d(sm.q[g], &tm_q, g * 64, h * G, __ldg(P.qsl + s) + i0, &sm.q_full);
         }
         constexpr int kBlocksPerTile = kKT / BS;
         const int nb_seq = (L + BS - 1) / BS;
@@ -315,8 +353,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (ok && phys >= 0) {
                 const int row = (int)(((long long)phys * P.num_kv_heads + h) * BS);
-                tc::tma_load_2d(sm.k[stage] + lane * BS * kRowBytes, &tm_k, 0, row, &sm.kv_full[stage]);
-                tc::tma_load_2d(sm.v[stage] + lane * BS * kRowBytes, &tm_v, 0, row, &sm.kv_full[stage]);
+#pragma unroll
+                for (int g = 0; g < REG; ++g) {
+                    tc::tma_load_2d(sm.k[stage][g] + lane * BS * kRegionBytes, &tm_k, g * 64, row, &sm.kv_full[stage]);
+                    tc::tma_load_2d(sm.v[stage][g] + lane * BS * kRegionBytes, &tm_v, g * 64, row, &sm.kv_full[stage]);
+                }
             }
             if (ok)
                 issued = j + 1;
@@ -336,7 +377,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ score products
         if (lane == 0 && tiles > 0) {
             const uint32_t idesc_s = tc::idesc_f16(kRows, kKT, ab_fmt, false);
-            const uint32_t q_addr = smem_addr(sm.q);
+            const uint32_t q_addr = smem_addr(sm.q[0]);  // region g at + g * kRows * kRegionBytes
             // S_j = Q K_j^T into TMEM columns [0, 128), once K_j has landed
             // and the softmax has read S_{j-1}
             bool ok = mbar_wait(&sm.q_full, 0);
@@ -346,11 +387,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (!ok)
                     break;
                 tc::fence_after_sync();
-                const uint32_t k_addr = smem_addr(sm.k[j % kStages]);
+                const uint32_t k_addr = smem_addr(sm.k[j % kStages][0]);  // region g at + g * kKT * kRegionBytes
 #pragma unroll
-                for (int kk = 0; kk < kHeadDim / 16; ++kk)
-                    tc::mma_ss(tmem, tc::desc_sw128(q_addr + kk * 32), tc::desc_sw128(k_addr + kk * 32),
-                               idesc_s, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    // dims 16 kk ..: region kk / 4, 32 bytes a step inside it
+                    const int g = kk >> 2;
+                    tc::mma_ss(tmem, tc::desc_sw128(q_addr + g * kRows * kRegionBytes + (kk & 3) * 32),
+                               tc::desc_sw128(k_addr + g * kKT * kRegionBytes + (kk & 3) * 32), idesc_s,
+                               kk > 0 ? 1u : 0u);
+                }
                 tc::mma_commit(&sm.s_full);
             }
             if (!ok)
@@ -360,7 +405,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (warp == kPvWarp) {
         // ------------------------------------------------------------ value products
         if (lane == 0 && tiles > 0) {
-            const uint32_t idesc_o = tc::idesc_f16(kRows, kHeadDim, ab_fmt, true);
+            const uint32_t idesc_o = tc::idesc_f16(kRows, 64, ab_fmt, true);  // one region of O per product
             bool ok = true;
             for (int j = 0; ok && j < tiles; ++j) {
                 // P_j is in TMEM buffer j mod 2 (and V_j landed before S_j was computed)
@@ -368,17 +413,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (!ok)
                     break;
                 tc::fence_after_sync();
-                const uint32_t v_addr = smem_addr(sm.v[j % kStages]);
+                const uint32_t v_addr = smem_addr(sm.v[j % kStages][0]);  // region g at + g * kKT * kRegionBytes
                 const uint32_t p_buf = kTmemP + (uint32_t)(j & 1) * (NP * kKT / 2);
 #pragma unroll
                 for (int part = 0; part < NP; ++part)
 #pragma unroll
                     for (int kk = 0; kk < kKT / 16; ++kk) {
-                        // keys 16 kk ..: key half kk / 4 accumulates into its own O
-                        const uint32_t p_cols = p_buf + part * (kKT / 2) + (kk >> 2) * (kHalf / 2) + (kk & 3) * 8;
-                        tc::mma_ts(tmem + kTmemO + (kk >> 2) * kHeadDim, tmem + p_cols,
-                                   tc::desc_sw128(v_addr + kk * 16 * kRowBytes), idesc_o,
-                                   (j > 0 || part > 0 || (kk & 3) > 0) ? 1u : 0u);
+                        // keys 16 kk ..: key half kk / KH accumulates into its own O,
+                        // one product per 64-dim region of V
+                        constexpr int KH = kHalf / 16;
+                        const int hh = kk / KH, ki = kk % KH;
+                        const uint32_t p_cols = p_buf + part * (kKT / 2) + hh * (kHalf / 2) + ki * 8;
+#pragma unroll
+                        for (int g = 0; g < REG; ++g)
+                            tc::mma_ts(tmem + kTmemO + hh * D + g * 64, tmem + p_cols,
+                                       tc::desc_sw128(v_addr + g * kKT * kRegionBytes + kk * 16 * kRegionBytes),
+                                       idesc_o, (j > 0 || part > 0 || ki > 0) ? 1u : 0u);
                     }
                 tc::mma_commit(&sm.o_done[j & 1]);
                 tc::mma_commit(&sm.kv_empty[j % kStages]);
@@ -480,27 +530,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 // this key half's O row
                 const float a = rescale ? alpha : 1.f;
 #pragma unroll
-                for (int c = 0; c < kHeadDim / 32; ++c) {
+                for (int c = 0; c < D / 32; ++c) {
                     float ov[32];
-                    tc::tmem_ld32(lane_addr + kTmemO + hf * kHeadDim + c * 32, ov);
+                    tc::tmem_ld32(lane_addr + kTmemO + hf * D + c * 32, ov);
                     tc::tmem_ld_wait();
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
                         ov[e] *= a;
-                    tc::tmem_st32(lane_addr + kTmemO + hf * kHeadDim + c * 32, ov);
+                    tc::tmem_st32(lane_addr + kTmemO + hf * D + c * 32, ov);
                 }
                 tc::tmem_st_wait();
             }
             // P row r, this half's keys c0 .. c0 + 63: column c holds keys
             // c0 + 2c (low half) and c0 + 2c + 1
             const uint32_t p_buf = kTmemP + (uint32_t)(j & 1) * (NP * kKT / 2);
-            tc::tmem_st32(lane_addr + p_buf + hf * (kHalf / 2), pk);
+            store_p(lane_addr + p_buf + hf * (kHalf / 2), pk);
             if (NP == 2) {
                 uint32_t pl[kHalf / 2];
 #pragma unroll
                 for (int c = 0; c < kHalf / 2; ++c)
                     pl[c] = pack2<T>(sv[2 * c], sv[2 * c + 1]);
-                tc::tmem_st32(lane_addr + p_buf + (NP - 1) * (kKT / 2) + hf * (kHalf / 2), pl);
+                store_p(lane_addr + p_buf + (NP - 1) * (kKT / 2) + hf * (kHalf / 2), pl);
             }
             // Values of keys past the context, or of blocks that were not
             // loaded, must be zero: P is zero there but 0 * NaN is not.  This
@@ -511,12 +561,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const int key = tbase + r;
-                const bool blk_loaded = (sm.loaded[stage] >> (r / BS)) & 1u;
-                if (key >= L || !blk_loaded) {
+                const bool blk_loaded = r < kKT && ((sm.loaded[stage] >> (r / BS)) & 1u);
+                if (r < kKT && (key >= L || !blk_loaded)) {
+                    // this half's share of the row: bytes 64 hf.. of its one
+                    // region (D 64), or region hf (D 128)
+                    uint8_t *row = REG == 1 ? sm.v[stage][0] + r * kRegionBytes + hf * (kRegionBytes / 2)
+                                            : sm.v[stage][hf] + r * kRegionBytes;
 #pragma unroll
                     for (int b = 0; b < kRowBytes / 2; b += 16)
-                        *reinterpret_cast<uint4 *>(sm.v[stage] + r * kRowBytes + hf * (kRowBytes / 2) + b) =
-                            make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(row + b) = make_uint4(0, 0, 0, 0);
                 }
             }
             tc::tmem_st_wait();
@@ -529,7 +582,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         sm.xm[hf][r] = m;
         sm.xl[hf][r] = l;
         mbar_arrive(&sm.xbar);
-        float ov[32];
+        float ov[OC];
         float fa = 0.f, fb = 0.f;  // factors of key halves 0 and 1
         if (ok && mbar_wait(&sm.xbar, 0)) {
             const float ma = sm.xm[0][r], mb = sm.xm[1][r];
@@ -545,27 +598,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ok = mbar_wait(&sm.o_done[(tiles - 1) & 1], (uint32_t)((tiles - 1) >> 1) & 1u);
             if (ok) {
                 tc::fence_after_sync();
-                float ob[32];
-                tc::tmem_ld32(lane_addr + kTmemO + hf * 32, ov);
-                tc::tmem_ld32(lane_addr + kTmemO + kHeadDim + hf * 32, ob);
-                tc::tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    ov[c] = fmaf(fa, ov[c], fb * ob[c]);
+                for (int ch = 0; ch < OC / 32; ++ch) {
+                    float oa[32], ob[32];
+                    tc::tmem_ld32(lane_addr + kTmemO + hf * OC + ch * 32, oa);
+                    tc::tmem_ld32(lane_addr + kTmemO + D + hf * OC + ch * 32, ob);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        ov[ch * 32 + c] = fmaf(fa, oa[c], fb * ob[c]);
+                }
             }
         }
         if (!ok || tiles == 0) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
+            for (int c = 0; c < OC; ++c)
                 ov[c] = 0.f;
         }
         if (!ok)
             raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
         if (rank != 0) {
             // rank 1: hand (max, sum, half rows) to rank 0 through distributed shared memory
-            const uint32_t dst = tc::map_to_rank(&sm.rem_o[r][hf * 32], 0);
+            const uint32_t dst = tc::map_to_rank(&sm.rem_o[r][hf * OC], 0);
 #pragma unroll
-            for (int c = 0; c < 32; c += 4)
+            for (int c = 0; c < OC; c += 4)
                 tc::st_cluster_v4(dst + c * 4, ov[c], ov[c + 1], ov[c + 2], ov[c + 3]);
             if (hf == 0) {
                 tc::st_cluster_f32(tc::map_to_rank(&sm.rem_m[r], 0), m);
@@ -582,10 +638,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const float inv = 1.f / (f0 * l + f1 * l1);
                 const float a0 = f0 * inv, a1 = f1 * inv;
                 const long long tok_g = __ldg(P.qsl + s) + i0 + tok;
-                uint16_t *o = P.out + (tok_g * P.num_q_heads + (long long)h * G + (r % G)) * kHeadDim + hf * 32;
-                const float *o1 = &sm.rem_o[r][hf * 32];
+                uint16_t *o = P.out + (tok_g * P.num_q_heads + (long long)h * G + (r % G)) * D + hf * OC;
+                const float *o1 = &sm.rem_o[r][hf * OC];
 #pragma unroll
-                for (int c = 0; c < 32; c += 8) {
+                for (int c = 0; c < OC; c += 8) {
                     uint4 w;
                     w.x = pack2<T>(fmaf(ov[c], a0, o1[c] * a1), fmaf(ov[c + 1], a0, o1[c + 1] * a1));
                     w.y = pack2<T>(fmaf(ov[c + 2], a0, o1[c + 2] * a1), fmaf(ov[c + 3], a0, o1[c + 3] * a1));
@@ -649,7 +705,7 @@ bool tc_prefill_supported(int block_size, int group)
     return (block_size == 16 || block_size == 32) && group >= 1 && group <= kMaxGroup;
 }
 
-template <typename T, int BS>
+template <typename T, int BS, int D>
 static cudaError_t launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
                              const PrefillParams &P, int grid, bool overlap, cudaStream_t stream)
 {
@@ -659,15 +715,15 @@ static cudaError_t launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const
     if (e != cudaSuccess)
         return e;
     if (!(dev < 31 && ((done_mask >> dev) & 1))) {
-        e = cudaFuncSetAttribute(tc_prefill_kernel<T, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem_bytes<PParts<T>::N>());
+        e = cudaFuncSetAttribute(tc_prefill_kernel<T, BS, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem_bytes<PParts<T>::N, D>());
         if (e != cudaSuccess)
             return e;
         if (dev < 31)
             __atomic_fetch_or(&done_mask, 1 << dev, __ATOMIC_RELAXED);
     }
     if (!overlap) {
-        tc_prefill_kernel<T, BS><<<grid, kThreads, smem_bytes<PParts<T>::N>(), stream>>>(tq, tk, tv, P);
+        tc_prefill_kernel<T, BS, D><<<grid, kThreads, smem_bytes<PParts<T>::N, D>(), stream>>>(tq, tk, tv, P);
         return cudaGetLastError();
     }
     // programmatic dependent of the kernel before it (the span walk of the same
@@ -676,14 +732,14 @@ static cudaError_t launch_tc(const CUtensorMap &tq, const CUtensorMap &tk, const
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem_bytes<PParts<T>::N>();
+    cfg.dynamicSmemBytes = smem_bytes<PParts<T>::N, D>();
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_prefill_kernel<T, BS>, tq, tk, tv, P);
+    return cudaLaunchKernelEx(&cfg, tc_prefill_kernel<T, BS, D>, tq, tk, tv, P);
 }
 
 cudaError_t launch_tc_prefill(const void *q, const int32_t *query_start_loc, const void *k_pool,
@@ -691,25 +747,28 @@ cudaError_t launch_tc_prefill(const void *q, const int32_t *query_start_loc, con
                               const int32_t *context_lens, int num_seqs, int total_q_tokens,
                               int num_q_heads, int num_kv_heads, int block_size, float scale,
                               void *out, int max_blocks_per_seq, long long num_blocks, ns_dtype dtype,
-                              int min_span, unsigned *status, bool after_walk, cudaStream_t stream)
+                              int min_span, int head_dim, unsigned *status, bool after_walk,
+                              cudaStream_t stream)
 {
     const int G = num_q_heads / num_kv_heads;
     const int qt = kRows / G;
-    if (min_span < 1)
+    if (min_span < 1 || (head_dim != 64 && head_dim != 128))
         return cudaErrorInvalidValue;
+    const int row_bytes = 2 * head_dim;
     CUtensorMap tq, tk, tv;
     {
-        const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)num_q_heads, (cuuint64_t)total_q_tokens};
-        const cuuint64_t strides[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)num_q_heads * kRowBytes};
-        const cuuint32_t box[3] = {(cuuint32_t)kHeadDim, (cuuint32_t)G, (cuuint32_t)qt};
+        // boxes of 64 elements (one 128-byte swizzle span); a 128-element row is two
+        const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_q_heads, (cuuint64_t)total_q_tokens};
+        const cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)num_q_heads * row_bytes};
+        const cuuint32_t box[3] = {64u, (cuuint32_t)G, (cuuint32_t)qt};
         if (!encode(&tq, dtype, 3, q, dims, strides, box))
             return cudaErrorInvalidValue;
     }
     {
         const cuuint64_t rows = (cuuint64_t)num_blocks * num_kv_heads * block_size;
-        const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, rows};
-        const cuuint64_t strides[1] = {(cuuint64_t)kRowBytes};
-        const cuuint32_t box[2] = {(cuuint32_t)kHeadDim, (cuuint32_t)block_size};
+        const cuuint64_t dims[2] = {(cuuint64_t)head_dim, rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+        const cuuint32_t box[2] = {64u, (cuuint32_t)block_size};
         if (!encode(&tk, dtype, 2, k_pool, dims, strides, box) ||
             !encode(&tv, dtype, 2, v_pool, dims, strides, box))
             return cudaErrorInvalidValue;
@@ -737,11 +796,14 @@ cudaError_t launch_tc_prefill(const void *q, const int32_t *query_start_loc, con
     const int grid = (int)(2 * units > 0x7ffffffe ? 0x7ffffffe : 2 * units);
     if (grid == 0)
         return cudaSuccess;
+    if (head_dim == 128)  // block size 16 only
+        return dtype == NS_BF16 ? launch_tc<BF16, 16, 128>(tq, tk, tv, P, grid, after_walk, stream)
+                                : launch_tc<F16, 16, 128>(tq, tk, tv, P, grid, after_walk, stream);
     if (dtype == NS_BF16)
-        return block_size == 16 ? launch_tc<BF16, 16>(tq, tk, tv, P, grid, after_walk, stream)
-                                : launch_tc<BF16, 32>(tq, tk, tv, P, grid, after_walk, stream);
-    return block_size == 16 ? launch_tc<F16, 16>(tq, tk, tv, P, grid, after_walk, stream)
-                            : launch_tc<F16, 32>(tq, tk, tv, P, grid, after_walk, stream);
+        return block_size == 16 ? launch_tc<BF16, 16, 64>(tq, tk, tv, P, grid, after_walk, stream)
+                                : launch_tc<BF16, 32, 64>(tq, tk, tv, P, grid, after_walk, stream);
+    return block_size == 16 ? launch_tc<F16, 16, 64>(tq, tk, tv, P, grid, after_walk, stream)
+                            : launch_tc<F16, 32, 64>(tq, tk, tv, P, grid, after_walk, stream);
 }
 
 }  // namespace ns

@@ -79,3 +79,44 @@ def test_d128_rejects_other_block_sizes():
     with pytest.raises(nb.NsError) as e:
         d.decode()
     assert e.value.status == -2
+
+
+@pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (8, 1), (4, 1)])
+def test_d128_tensor_core_spans(dtype, hq, hkv, orc):
+    """Spans of 2+ rows on the tcgen05 kernel at head_dim 128 (64-key tiles,
+    two 64-element regions a row): ragged prefixes, query tiles cut mid-span,
+    key tiles cut mid-block, NaN in unused pool slots."""
+    rng = np.random.default_rng(5500 + hq + hkv)
+    lens = np.array([2, 30, 150, 129, 400, 700], np.int32)
+    qlens = np.array([2, 30, 19, 128, 37, 300], np.int32)
+    st = wl.make_step(rng, lens, qlens, dtype=dtype, num_q_heads=hq, num_kv_heads=hkv, head_dim=128,
+                      poison_unused=True, name="d128_tc")
+    ref, kp, vp = orc.step(st, num_threads=max(1, orc.max_threads()))
+    d = _gpu.DevStep(st)
+    d.append()
+    out = d.prefill()
+    torch.cuda.synchronize()
+    _gpu.assert_no_device_status()
+    _gpu.compare(out, ref, st.dtype, f"d128 tc Hq={hq} Hkv={hkv}")
+
+
+def test_d128_tensor_core_and_walk_agree(orc):
+    rng = np.random.default_rng(5600)
+    lens = np.array([1, 512 + 1500, 17, 512 + 900], np.int32)
+    qlens = np.array([1, 512, 1, 512], np.int32)
+    st = wl.make_step(rng, lens, qlens, dtype=wl.BF16, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                      name="d128_mixed")
+    ref, kp, vp = orc.step(st, num_threads=max(1, orc.max_threads()))
+    d = _gpu.DevStep(st, k_pool=kp, v_pool=vp)
+    outs = []
+    for min_span in (-1, 2):
+        cfg = nb.PrefillConfig()
+        cfg.tensor_core_min_span = min_span
+        nb.ns_paged_attn_prefill(d.q, d.query_start_loc, d.k_pool, d.v_pool, d.block_tables,
+                                 d.context_lens, st.scale, d.out, d.ws, config=cfg)
+        torch.cuda.synchronize()
+        outs.append(d.out.clone())
+    _gpu.compare(outs[0], ref, st.dtype, "d128 walk")
+    _gpu.compare(outs[1], ref, st.dtype, "d128 tensor cores")
+    _gpu.assert_no_device_status()
