@@ -57,14 +57,14 @@ KERNEL_SOURCES = {
 }
 PROFILED_TRAFFIC = {
     # ncu capture of the committed kernel (dram__bytes_read.sum + dram__bytes_write.sum
-    # of one launch of the default command): 239.03 MB read + 3.33 MB written
+    # of one launch of the default command): 238.99 MB read + 3.43 MB written
     ("decode_b256", "paged_decode_kernel"): {
-        "sources_sha256": "4739802e7053aa7e6b38c054c1c759dee82b68a8f3bd7f9adaf1c68c0fa00353",
-        "bytes": 242360064},
+        "sources_sha256": "b71eea5f48220dfc0a5f6970c9dc889ae3df360cc5ffd51db7803d3c982b2d14",
+        "bytes": 242425856},
     # ncu capture of the committed kernel: 4.73 MB read, 0 written
     ("mixed_chunked_prefill", "tc_prefill_kernel"): {
-        "sources_sha256": "007c4465a7f009addeaf16729db53fd6af56abb8e42d2ef2b7ffb1c179e38fe6",
-        "bytes": 4728832},
+        "sources_sha256": "1c38659a2c17008cf617a9648c5de5523e66db5ab2b571864923f45d99693816",
+        "bytes": 4729344},
 }
 
 
