@@ -26,10 +26,8 @@
  *               stream) and the call returns without synchronising.  Inputs
  *               must stay valid until the work completes.
  *  Elements     K, V, q and out are fp16 or bf16 (`ns_dtype`), all of one type.
- *  Shapes       head_dim is 64, or 128 with block_size 16 (the split-KV
- *               decode, its fused append and the prefill, whose spans then
- *               all take the split-KV walk; the tensor-core prefill, the
- *               q8_0 pools and the allocation-free entry point take 64).
+ *  Shapes       head_dim is 64, or 128 with block_size 16 (the q8_0 pools
+ *               and the allocation-free entry point take 64).
  *               num_q_heads must be a multiple of num_kv_heads; query head
  *               j reads KV head j / G, G = num_q_heads / num_kv_heads.  G is
  *               at most 8, or up to 64 when it is a multiple of
