@@ -778,12 +778,14 @@ __device__ __forceinline__ void process_step(const DecodeSlot<G, Q8, D> &sl, uin
 // Log-sum-exp merge of the partial records of one (sequence, kv head) pair:
 // pieces c0..c1 (the first in its worker's second record slot when
 // c0_second).  One warp merges one part, query heads h0..h0+HPP-1 of the
-// group, and writes out[out_row + j*D + d] for those heads.  A head's row of
-// one piece is D/4 float4s, one per lane, so a warp reads PPR = 128/D rows
-// at once (lane l: row l / (D/4), dims 4(l mod D/4)..+3).  A chunk of CH
-// pieces is loaded at once -- lane k also loads piece k's maxima and sums --
-// so that a chunk costs one round trip to L2; chunks are merged online (a
-// chunk with a larger maximum rescales what came before).
+// group, and writes out[out_row + j*D + d] for those heads.  Parts of 1 or 2
+// heads (many pieces): a head's row of one piece is D/4 float4s, one per
+// lane, so a warp reads PPR = 128/D rows at once (lane l: row l / (D/4),
+// dims 4(l mod D/4)..+3).  A chunk of CH pieces is loaded at once -- lane k
+// also loads piece k's maxima and sums -- so that a chunk costs one round
+// trip to L2; chunks are merged online (a chunk with a larger maximum
+// rescales what came before).  Parts of 4 or 8 heads (few pieces) take
+// merge_part_lanes, where no value crosses lanes.
 // ---------------------------------------------------------------------------
 constexpr int kMergeLoads = 24;  // float4 loads in flight per lane (16 and 32 measured slower)
 template <int D>
@@ -911,6 +913,94 @@ __device__ void merge_part(const DecodeParams &P, int c0, int c1, bool c0_second
     }
 }
 
+// A part of HPP >= 4 heads: lane l merges head h0 + l / (32 / HPP), DPL
+// consecutive dims, over all pieces itself -- it loads each piece's maximum
+// and sum of its head and its dims' rows (a chunk of CH pieces per round
+// trip), so that no value crosses lanes.
+template <typename T, int D, int HPP>
+__device__ void merge_part_lanes(const DecodeParams &P, int c0, int c1, bool c0_second, long long out_row, int h0,
+                                 int G, int lane)
+{
+    constexpr int LPH = 32 / HPP;             // lanes per head
+    constexpr int DPL = D / LPH;              // dims per lane
+    constexpr int NV = DPL / 4;               // float4 of a piece's row per lane
+    constexpr int CH = kMergeLoads * 4 / DPL;  // pieces per chunk
+    static_assert(NV >= 1 && CH >= 1, "merge geometry");
+    const int head = h0 + lane / LPH;
+    const bool live = head < G;
+    const int d0 = (lane % LPH) * DPL;
+    const int npieces = c1 - c0 + 1;
+    float m = -INFINITY, w = 0.f;
+    float4 o[NV];
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+        o[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k0 = 0; k0 < npieces; k0 += CH) {
+        const int nk = min(CH, npieces - k0);
+        float mk[CH], lk[CH];
+        float4 a[CH][NV];
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            mk[k] = -INFINITY;
+            lk[k] = 0.f;
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+                a[k][v] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (k < nk && live) {
+                const float *r = piece_record<D>(P, c0, k0 + k, c0_second);
+                mk[k] = __ldcg(r + head);
+                lk[k] = __ldcg(r + kMaxGroup + head);
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+                    a[k][v] = __ldcg(reinterpret_cast<const float4 *>(r + 2 * kMaxGroup + head * D + d0 + 4 * v));
+            }
+        }
+        float mn = m;
+#pragma unroll
+        for (int k = 0; k < CH; ++k)
+            mn = fmaxf(mn, mk[k]);
+        const float sc = m > -INFINITY ? fast_exp2(m - mn) : 0.f;
+        w *= sc;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            o[v].x *= sc;
+            o[v].y *= sc;
+            o[v].z *= sc;
+            o[v].w *= sc;
+        }
+#pragma unroll
+        for (int k = 0; k < CH; ++k) {
+            const float f = mk[k] > -INFINITY ? fast_exp2(mk[k] - mn) : 0.f;
+            w = fmaf(f, lk[k], w);
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                o[v].x = fmaf(f, a[k][v].x, o[v].x);
+                o[v].y = fmaf(f, a[k][v].y, o[v].y);
+                o[v].z = fmaf(f, a[k][v].z, o[v].z);
+                o[v].w = fmaf(f, a[k][v].w, o[v].w);
+            }
+        }
+        m = mn;
+    }
+    if (live) {
+        const float inv = 1.f / w;
+        uint16_t *dst = P.out + out_row + (long long)head * D + d0;
+#pragma unroll
+        for (int v = 0; v < NV; v += 2) {
+            uint4 u;
+            u.x = pack2<T>(o[v].x * inv, o[v].y * inv);
+            u.y = pack2<T>(o[v].z * inv, o[v].w * inv);
+            if (v + 1 < NV) {
+                u.z = pack2<T>(o[v + 1].x * inv, o[v + 1].y * inv);
+                u.w = pack2<T>(o[v + 1].z * inv, o[v + 1].w * inv);
+                *reinterpret_cast<uint4 *>(dst + 4 * v) = u;
+            } else {
+                *reinterpret_cast<uint2 *>(dst + 4 * v) = make_uint2(u.x, u.y);
+            }
+        }
+    }
+}
+
 // The partial records a warp has stored but not yet counted (at most two: the
 // first and the last piece of its range).  Their arrivals are counted at the
 // end of the ring, behind one fence: a pair's merge cannot start before the
@@ -1027,8 +1117,8 @@ __device__ __forceinline__ void merge_run(const DecodeParams &P, MergeQueue &mq,
     const int c0 = (int)j.c0, c1 = (int)j.c1, h0 = part * j.hpp;
     const bool second = j.c0_second != 0;
     switch (j.hpp) {
-    case 8: merge_part<T, D, 8>(P, c0, c1, second, j.out_row, h0, G, lane); break;
-    case 4: merge_part<T, D, 4>(P, c0, c1, second, j.out_row, h0, G, lane); break;
+    case 8: merge_part_lanes<T, D, 8>(P, c0, c1, second, j.out_row, h0, G, lane); break;
+    case 4: merge_part_lanes<T, D, 4>(P, c0, c1, second, j.out_row, h0, G, lane); break;
     case 2: merge_part<T, D, 2>(P, c0, c1, second, j.out_row, h0, G, lane); break;
     default: merge_part<T, D, 1>(P, c0, c1, second, j.out_row, h0, G, lane); break;
     }
