@@ -196,6 +196,15 @@ ns_status ns_paged_attn_decode(const void *q, const void *k_pool, const void *v_
  *                       (ns_paged_attn_workspace_init) before its next use.  For
  *                       testing the failure path: a limit shorter than a copy's
  *                       latency makes every call time out.
+ *   merge_levels        0 = automatic; 1 = every cut pair merges its pieces'
+ *                       records in one step; 2 = a pair cut into 16 or more
+ *                       pieces first combines its pieces inside each CTA
+ *                       (block size 16, head_dim 64, 16-bit pools; elsewhere
+ *                       ignored).  Automatic takes 2 there when the pairs are
+ *                       few for the CTAs' warps (32 or more warps a pair) and
+ *                       no table_row indirection is used.  The result is the
+ *                       same up to rounding order.
+ *   reserved            must be 0.
  */
 #define NS_MAX_CTAS 1024
 typedef struct ns_decode_config {
@@ -204,7 +213,8 @@ typedef struct ns_decode_config {
     int whole_sequences;
     int overlap_prologue;
     int wait_limit_ns;
-    int reserved[3];
+    int merge_levels;
+    int reserved[2];
 } ns_decode_config;
 
 /* ns_paged_attn_decode with policy overrides (cfg may be NULL = auto). */
@@ -272,7 +282,8 @@ typedef struct ns_decode_plan {
     int32_t max_pieces;
     int32_t whole_sequences;
     int32_t workers_active;
-    int32_t reserved[8];
+    int32_t merge_levels;  /* 1 or 2: the merge the kernel was built for (see merge_levels above) */
+    int32_t reserved[7];
 } ns_decode_plan;
 
 /* Copy the plan record out of `workspace` (synchronises `stream`). */

@@ -43,7 +43,7 @@ class NsError(RuntimeError):
 class DecodeConfig(ctypes.Structure):
     _fields_ = [("num_ctas", ctypes.c_int), ("min_blocks_per_cta", ctypes.c_int),
                 ("whole_sequences", ctypes.c_int), ("overlap_prologue", ctypes.c_int),
-                ("wait_limit_ns", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
+                ("wait_limit_ns", ctypes.c_int), ("merge_levels", ctypes.c_int), ("reserved", ctypes.c_int * 2)]
 
 
 class PrefillConfig(ctypes.Structure):
@@ -55,7 +55,8 @@ class DecodePlan(ctypes.Structure):
     _fields_ = [("ctas_launched", ctypes.c_int32), ("ctas_active", ctypes.c_int32),
                 ("total_blocks", ctypes.c_int64), ("split_pairs", ctypes.c_int32),
                 ("max_pieces", ctypes.c_int32), ("whole_sequences", ctypes.c_int32),
-                ("workers_active", ctypes.c_int32), ("reserved", ctypes.c_int32 * 8)]
+                ("workers_active", ctypes.c_int32), ("merge_levels", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 7)]
 
 
 _LIB = None

@@ -83,6 +83,22 @@ cudaError_t dispatch_decode_g(int g, const ns::DecodeParams &P, int ctas, cudaSt
     }
 }
 
+// Two-level merge kernels: block size 16, head_dim 64, 16-bit pools.
+template <typename T>
+cudaError_t dispatch_decode_two(int g, const ns::DecodeParams &P, int ctas, cudaStream_t s)
+{
+    switch (g) {
+    case 1: return ns::launch_paged_decode<T, 16, 1, false, 64, true>(P, ctas, s);
+    case 2: return ns::launch_paged_decode<T, 16, 2, false, 64, true>(P, ctas, s);
+    case 3: return ns::launch_paged_decode<T, 16, 3, false, 64, true>(P, ctas, s);
+    case 4: return ns::launch_paged_decode<T, 16, 4, false, 64, true>(P, ctas, s);
+    case 5: return ns::launch_paged_decode<T, 16, 5, false, 64, true>(P, ctas, s);
+    case 6: return ns::launch_paged_decode<T, 16, 6, false, 64, true>(P, ctas, s);
+    case 7: return ns::launch_paged_decode<T, 16, 7, false, 64, true>(P, ctas, s);
+    default: return ns::launch_paged_decode<T, 16, 8, false, 64, true>(P, ctas, s);
+    }
+}
+
 template <typename T>
 cudaError_t dispatch_decode(int bs, int g, const ns::DecodeParams &P, int ctas, cudaStream_t s)
 {
@@ -316,6 +332,7 @@ ns_status run_decode(const DecodeCall &c, int dev)
     P.pack = c.pack ? 1 : 0;
     P.wait_limit_ns = (c.cfg && c.cfg->wait_limit_ns > 0) ? (unsigned long long)c.cfg->wait_limit_ns
                                                            : ns::kWaitLimitNs;
+    P.merge_levels = c.cfg ? c.cfg->merge_levels : 0;
     P.k_codes = static_cast<const int8_t *>(c.k_codes);
     P.v_codes = static_cast<const int8_t *>(c.v_codes);
     P.k_scales = static_cast<const uint16_t *>(c.k_scales);
@@ -353,7 +370,7 @@ ns_status check_decode_args(const void *q, const void *k_pool, const void *v_poo
     if (workspace_bytes < ns_paged_attn_workspace_bytes(rows, num_q_heads, num_kv_heads, head_dim))
         return NS_ERR_INVALID_ARG;
     if (cfg && (cfg->num_ctas < 0 || cfg->num_ctas > NS_MAX_CTAS || cfg->min_blocks_per_cta < 0 ||
-                cfg->wait_limit_ns < 0))
+                cfg->wait_limit_ns < 0 || cfg->merge_levels < 0 || cfg->merge_levels > 2))
         return NS_ERR_INVALID_ARG;
     return NS_OK;
 }
@@ -369,8 +386,20 @@ ns_status launch_decode(const DecodeParams &P, ns_dtype dtype, int block_size, i
     int ctas = num_ctas > 0 ? num_ctas : resident_ctas(dev, dtype, block_size, g, q8, head_dim);
     if (ctas > NS_MAX_CTAS)
         ctas = NS_MAX_CTAS;
+    // Two-level merges where a cut pair has many pieces in each CTA: few
+    // pairs for the CTAs' warps (at least 32 warps a pair) that could fill
+    // them (the pairs' table rows span at least a block a warp).
+    bool two = false;
+    if (head_dim == 64 && !q8 && block_size == 16) {
+        const long long pairs = (long long)P.num_seqs * P.num_kv_heads, warps = (long long)ctas * kConsumerWarps;
+        two = P.merge_levels == 2 ||
+              (P.merge_levels == 0 && P.table_row == nullptr && pairs * 32 <= warps &&
+               pairs * P.max_blocks_per_seq >= warps);
+    }
     cudaError_t e;
-    if (head_dim == 128)
+    if (two)
+        e = dtype == NS_BF16 ? dispatch_decode_two<BF16>(g, P, ctas, stream) : dispatch_decode_two<F16>(g, P, ctas, stream);
+    else if (head_dim == 128)
         e = dtype == NS_BF16 ? dispatch_decode_d128<BF16>(g, P, ctas, stream)
                              : dispatch_decode_d128<F16>(g, P, ctas, stream);
     else if (q8)

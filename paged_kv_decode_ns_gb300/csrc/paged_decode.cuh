@@ -146,6 +146,7 @@ struct DecodeParams {
     // heads: num_kv_heads and group above count these virtual kv heads, and
     // virtual head h reads the pools' (and the new K/V's) head h / kv_sub.
     int kv_sub;
+    int merge_levels;  // host: 0 automatic, 1 or 2 forced (the kernel instantiation follows it)
 };
 
 // The pools' kv heads, and the pools' head of virtual kv head h.
@@ -167,9 +168,10 @@ constexpr int kMergeQueue = 32;
 constexpr int kMergeParts = 16;
 struct MergeJob {
     long long c0, c1, out_row;
-    int pair, c0_second;
-    int hpp, nparts;  // query heads per part, parts
+    int pair, c0_second;  // c0_second: bit 0 the first record is in c0's second slot; kJobPerCta
+    int hpp, nparts;      // query heads per part, parts
 };
+constexpr int kJobPerCta = 2;  // a two-level merge over one record per CTA
 struct MergeQueue {
     MergeJob job[kMergeQueue];
     int ready[kMergeQueue];
@@ -308,6 +310,9 @@ struct DecodeSmem {
     int lens[kLensCache];                    // clamped context lengths of rows 0..kLensCache-1
     int abort_flag;  // set by a warp that gave up waiting
     int plan_split, plan_maxp;
+    // two-level merges: pieces of a cut pair in this CTA that have arrived,
+    // by the pair's first worker in the CTA
+    int cta_count[kConsumerWarps];
 };
 
 // Slots per ring: as many (up to four) as fit in a CTA's shared memory.
@@ -811,7 +816,28 @@ __device__ __forceinline__ const float *piece_record(const DecodeParams &P, int 
     return P.partials + ((long long)(c0 + k) * 2 + wh) * Geo<D>::SLOT_FLOATS;
 }
 
-template <typename T, int D, int HPP>
+// Records of a two-level merge: record 0 is worker c0's; record k >= 1 is in
+// the first slot of the first worker of the k-th CTA after c0's, where the
+// CTA's pieces of the pair were combined (c1 - c0 + 1 counts the records).
+template <int D>
+__device__ __forceinline__ const float *cta_record(const DecodeParams &P, int c0, int k, bool c0_second)
+{
+    constexpr int NG = kConsumerWarps;
+    const int wk = k == 0 ? c0 : (c0 / NG + k) * NG;
+    const int wh = (k == 0 && c0_second) ? 1 : 0;
+    return P.partials + ((long long)wk * 2 + wh) * Geo<D>::SLOT_FLOATS;
+}
+
+template <int D, bool PER_CTA>
+__device__ __forceinline__ const float *record_at(const DecodeParams &P, int c0, int k, bool c0_second)
+{
+    if constexpr (PER_CTA)
+        return cta_record<D>(P, c0, k, c0_second);
+    else
+        return piece_record<D>(P, c0, k, c0_second);
+}
+
+template <typename T, int D, int HPP, bool PER_CTA = false>
 __device__ void merge_part(const DecodeParams &P, int c0, int c1, bool c0_second, long long out_row, int h0, int G,
                            int lane)
 {
@@ -840,7 +866,7 @@ __device__ void merge_part(const DecodeParams &P, int c0, int c1, bool c0_second
                 mk[u][i] = -INFINITY;
                 lk[u][i] = 0.f;
                 if (lane + 32 * u < nk && h0 + i < G) {
-                    const float *r = piece_record<D>(P, c0, k0 + lane + 32 * u, c0_second);
+                    const float *r = record_at<D, PER_CTA>(P, c0, k0 + lane + 32 * u, c0_second);
                     mk[u][i] = __ldcg(r + h0 + i);
                     lk[u][i] = __ldcg(r + kMaxGroup + h0 + i);
                 }
@@ -849,7 +875,7 @@ __device__ void merge_part(const DecodeParams &P, int c0, int c1, bool c0_second
 #pragma unroll
         for (int j = 0; j < NJ; ++j) {
             const int k = j * MG::PPR + sub;
-            const float *r = piece_record<D>(P, c0, k0 + (k < nk ? k : 0), c0_second) + 2 * kMaxGroup + dd;
+            const float *r = record_at<D, PER_CTA>(P, c0, k0 + (k < nk ? k : 0), c0_second) + 2 * kMaxGroup + dd;
 #pragma unroll
             for (int i = 0; i < HPP; ++i)
                 a[i][j] = (k < nk && h0 + i < G) ? __ldcg(reinterpret_cast<const float4 *>(r + (h0 + i) * D))
@@ -916,10 +942,12 @@ __device__ void merge_part(const DecodeParams &P, int c0, int c1, bool c0_second
 // A part of HPP >= 4 heads: lane l merges head h0 + l / (32 / HPP), DPL
 // consecutive dims, over all pieces itself -- it loads each piece's maximum
 // and sum of its head and its dims' rows (a chunk of CH pieces per round
-// trip), so that no value crosses lanes.
-template <typename T, int D, int HPP>
+// trip), so that no value crosses lanes.  REC: the result is a partial
+// record (maxima, sums, unnormalised rows) at rec, which may be one of the
+// records read, rather than the output.
+template <typename T, int D, int HPP, bool PER_CTA = false, bool REC = false>
 __device__ void merge_part_lanes(const DecodeParams &P, int c0, int c1, bool c0_second, long long out_row, int h0,
-                                 int G, int lane)
+                                 int G, int lane, float *rec = nullptr)
 {
     constexpr int LPH = 32 / HPP;             // lanes per head
     constexpr int DPL = D / LPH;              // dims per lane
@@ -947,7 +975,7 @@ __device__ void merge_part_lanes(const DecodeParams &P, int c0, int c1, bool c0_
             for (int v = 0; v < NV; ++v)
                 a[k][v] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (k < nk && live) {
-                const float *r = piece_record<D>(P, c0, k0 + k, c0_second);
+                const float *r = record_at<D, PER_CTA>(P, c0, k0 + k, c0_second);
                 mk[k] = __ldcg(r + head);
                 lk[k] = __ldcg(r + kMaxGroup + head);
 #pragma unroll
@@ -981,6 +1009,19 @@ __device__ void merge_part_lanes(const DecodeParams &P, int c0, int c1, bool c0_
             }
         }
         m = mn;
+    }
+    if constexpr (REC) {
+        __syncwarp();  // every lane has read its rows before any is overwritten
+        if (live) {
+            if (lane % LPH == 0) {
+                __stcg(rec + head, m);
+                __stcg(rec + kMaxGroup + head, w);
+            }
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+                __stcg(reinterpret_cast<float4 *>(rec + 2 * kMaxGroup + head * D + d0 + 4 * v), o[v]);
+        }
+        return;
     }
     if (live) {
         const float inv = 1.f / w;
@@ -1072,6 +1113,135 @@ __device__ __forceinline__ void count_arrivals(const DecodeParams &P, PendingMer
     pm.n = 0;
 }
 
+// ---------------------------------------------------------------------------
+// Two-level merges (kernels instantiated with TWO, chosen by the host when
+// few pairs are cut over many workers numbered CTA-major, so that each pair
+// has many pieces in each CTA).  A pair cut into at least kTwoLevelPieces
+// pieces is merged in two levels: its pieces inside one CTA are counted in
+// shared memory and combined by the last of them into one record (into the
+// output when the CTA holds every piece); the CTA records are then counted
+// in global memory and merged as one-level pairs are.  Other pairs merge in
+// one level.
+// ---------------------------------------------------------------------------
+constexpr int kTwoLevelPieces = 16;
+
+// Queue the merge of `pair` over records c0..c1 (flags: kJob* bits); the
+// caller's fence orders every record before the hand-off.
+template <typename T, int D>
+__device__ __forceinline__ void queue_job(const DecodeParams &P, int pair, int c0, int c1, int flags, int G,
+                                          MergeQueue &mq, int lane)
+{
+    const int s = pair / P.num_kv_heads, h = pair % P.num_kv_heads;
+    const long long out_row = ((long long)s * P.num_q_heads + (long long)h * G) * D;
+    int idx = kMergeQueue;
+    if (lane == 0)
+        idx = atomicAdd(&mq.tail, 1);
+    idx = __shfl_sync(0xffffffffu, idx, 0);
+    if (idx >= kMergeQueue) {
+        if (lane == 0)
+            raise_status(P.status, NS_DEV_MERGE_QUEUE);
+    } else if (lane == 0) {
+        MergeJob &j = mq.job[idx];
+        j.c0 = c0;
+        j.c1 = c1;
+        j.out_row = out_row;
+        j.pair = pair;
+        j.c0_second = flags;
+        j.hpp = merge_heads_per_part<D>(c1 - c0 + 1);
+        j.nparts = (G + j.hpp - 1) / j.hpp;
+        st_release_cta(&mq.ready[idx], 1);
+    }
+}
+
+// One pending record: the pair, its workers c0..c1, lo..hi of them in this
+// CTA, and whether it merges in two levels.
+struct Arrival {
+    int pair, c0, c1, lo, hi;
+    bool sec, two;
+};
+
+__device__ __forceinline__ Arrival arrival_of(int pair, int pspan, int pstart, const Split &sp)
+{
+    constexpr int NG = kConsumerWarps;
+    Arrival a;
+    a.pair = pair;
+    a.c0 = worker_of(pstart, sp.q, sp.r);
+    a.c1 = worker_of(pstart + pspan - 1, sp.q, sp.r);
+    a.sec = range_begin(a.c0, sp.q, sp.r) != pstart;
+    const int wlo = (int)blockIdx.x * NG;
+    a.lo = max(a.c0, wlo);
+    a.hi = min(a.c1, wlo + NG - 1);
+    a.two = !sp.wmajor && a.c1 - a.c0 + 1 >= kTwoLevelPieces && a.hi > a.lo;
+    return a;
+}
+
+// After the count (prev: the count before this arrival): queue the merge
+// when this was the last arrival, or, in two levels, combine this CTA's
+// pieces when this was the last of them.
+template <typename T, int D>
+__device__ __forceinline__ void arrive_two(const DecodeParams &P, const Arrival &a, int prev, int G,
+                                           MergeQueue &mq, int lane)
+{
+    constexpr int NG = kConsumerWarps;
+    int n = a.c1 - a.c0 + 1, flags = a.sec ? 1 : 0;
+    if (a.two) {
+        if (prev != a.hi - a.lo)
+            return;  // another warp of this CTA combines
+        __threadfence_block();  // the other warps' records, counted before this one
+        const bool lsec = a.lo == a.c0 && a.sec;
+        const int nc = a.c1 / NG - a.c0 / NG + 1;
+        if (nc == 1) {
+            const int s = a.pair / P.num_kv_heads, h = a.pair % P.num_kv_heads;
+            merge_part_lanes<T, D, 8>(P, a.lo, a.hi, lsec, ((long long)s * P.num_q_heads + (long long)h * G) * D, 0,
+                                      G, lane);
+            return;
+        }
+        // the CTA record replaces the record of the pair's first worker here
+        float *rec = const_cast<float *>(piece_record<D>(P, a.lo, 0, lsec));
+        merge_part_lanes<T, D, 8, false, true>(P, a.lo, a.hi, lsec, 0, 0, G, lane, rec);
+        __threadfence();  // the CTA record before its count
+        prev = 0;
+        if (lane == 0)
+            prev = atomicAdd(P.counters + a.pair, 1);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        n = nc;
+        flags |= kJobPerCta;
+    }
+    if (prev != n - 1)
+        return;
+    __threadfence();  // every record before the hand-off to whichever warp runs the merge
+    queue_job<T, D>(P, a.pair, a.c0, a.c0 + n - 1, flags, G, mq, lane);
+}
+
+template <typename T, int D>
+__device__ __forceinline__ void count_arrivals_two(const DecodeParams &P, PendingMerge &pm, const Split &sp, int G,
+                                                   MergeQueue &mq, int *cta_count, int lane)
+{
+    if (pm.n == 0)
+        return;
+    constexpr int NG = kConsumerWarps;
+    const Arrival a0 = arrival_of(pm.pair0, pm.pspan0, pm.pstart0, sp);
+    const Arrival a1 = pm.n > 1 ? arrival_of(pm.pair1, pm.pspan1, pm.pstart1, sp) : a0;
+    // the records before their counts (a count in this CTA needs CTA scope only)
+    if (!a0.two || (pm.n > 1 && !a1.two))
+        __threadfence();
+    else
+        __threadfence_block();
+    const int wlo = (int)blockIdx.x * NG;
+    int prev0 = 0, prev1 = 0;
+    if (lane == 0) {
+        prev0 = a0.two ? atomicAdd(cta_count + (a0.lo - wlo), 1) : atomicAdd(P.counters + a0.pair, 1);
+        if (pm.n > 1)
+            prev1 = a1.two ? atomicAdd(cta_count + (a1.lo - wlo), 1) : atomicAdd(P.counters + a1.pair, 1);
+    }
+    prev0 = __shfl_sync(0xffffffffu, prev0, 0);
+    prev1 = __shfl_sync(0xffffffffu, prev1, 0);
+    arrive_two<T, D>(P, a0, prev0, G, mq, lane);
+    if (pm.n > 1)
+        arrive_two<T, D>(P, a1, prev1, G, mq, lane);
+    pm.n = 0;
+}
+
 // Take the next part of a queued merge: lane 0's cursor value (broadcast),
 // -1 when every queued part is taken, -2 when a reserved entry was not
 // filled in time.
@@ -1109,12 +1279,33 @@ __device__ __forceinline__ int merge_pop(MergeQueue &mq, int lane)
 
 // Run part `c % kMergeParts` of queued merge `c / kMergeParts` (filled: the
 // pop waited for it).
-template <typename T, int D>
+template <typename T, int D, bool TWO = false>
 __device__ __forceinline__ void merge_run(const DecodeParams &P, MergeQueue &mq, int c, int G, int lane)
 {
     const int job = c / kMergeParts, part = c % kMergeParts;
     const MergeJob j = mq.job[job];
     const int c0 = (int)j.c0, c1 = (int)j.c1, h0 = part * j.hpp;
+    if constexpr (TWO) {
+        const bool second = (j.c0_second & 1) != 0;
+        if (j.c0_second & kJobPerCta) {
+            switch (j.hpp) {
+            case 8: merge_part_lanes<T, D, 8, true>(P, c0, c1, second, j.out_row, h0, G, lane); break;
+            case 4: merge_part_lanes<T, D, 4, true>(P, c0, c1, second, j.out_row, h0, G, lane); break;
+            case 2: merge_part<T, D, 2, true>(P, c0, c1, second, j.out_row, h0, G, lane); break;
+            default: merge_part<T, D, 1, true>(P, c0, c1, second, j.out_row, h0, G, lane); break;
+            }
+        } else {
+            switch (j.hpp) {
+            case 8: merge_part_lanes<T, D, 8>(P, c0, c1, second, j.out_row, h0, G, lane); break;
+            case 4: merge_part_lanes<T, D, 4>(P, c0, c1, second, j.out_row, h0, G, lane); break;
+            case 2: merge_part<T, D, 2>(P, c0, c1, second, j.out_row, h0, G, lane); break;
+            default: merge_part<T, D, 1>(P, c0, c1, second, j.out_row, h0, G, lane); break;
+            }
+        }
+        if (lane == 0 && part == 0)
+            P.counters[j.pair] = 0;
+        return;
+    }
     const bool second = j.c0_second != 0;
     switch (j.hpp) {
     case 8: merge_part_lanes<T, D, 8>(P, c0, c1, second, j.out_row, h0, G, lane); break;
@@ -1527,7 +1718,7 @@ __device__ __forceinline__ void quantize_new_row(const DecodeParams &P, DecodeSl
     __syncwarp();
 }
 
-template <typename T, int BS, int G, int S, bool Q8, int D>
+template <typename T, int BS, int G, int S, bool Q8, int D, bool TWO>
 __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8, D> &sm, const Split &sp,
                                 int ring, int warp, int lane)
 {
@@ -1653,8 +1844,12 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8, 
         *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
         raise_status(P.status, NS_DEV_WAIT_TIMEOUT);
     }
-    if (ok)
-        count_arrivals<T, D>(P, pm, q, r, G, sm.mq, lane);
+    if (ok) {
+        if constexpr (TWO)
+            count_arrivals_two<T, D>(P, pm, sp, G, sm.mq, sm.cta_count, lane);
+        else
+            count_arrivals<T, D>(P, pm, q, r, G, sm.mq, lane);
+    }
     __syncwarp();
     if (lane == 0) {
         __threadfence_block();  // this warp's queued jobs before its count
@@ -1676,7 +1871,7 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8, 
         late = __shfl_sync(0xffffffffu, late, 0);
         const int c = merge_pop(sm.mq, lane);
         if (c >= 0) {
-            merge_run<T, D>(P, sm.mq, c, G, lane);
+            merge_run<T, D, TWO>(P, sm.mq, c, G, lane);
             continue;
         }
         if (c == -2 || late) {
@@ -1745,6 +1940,8 @@ __device__ void decode_prologue(const DecodeParams &P, Smem &sm)
     }
     if (tid < kMergeQueue)
         sm.mq.ready[tid] = 0;
+    if (tid < kConsumerWarps)
+        sm.cta_count[tid] = 0;
     if (tid == 0) {
         sm.mq.tail = 0;
         sm.mq.head = 0;
@@ -1803,7 +2000,7 @@ __device__ __forceinline__ Split read_split(const DecodeParams &P, const Smem &s
 // of sequences with no key get zeros (CTA s mod grid writes row s), and CTA 0
 // records the plan (workers, pairs cut across workers, most pieces of one pair).
 template <class Smem, int BS, int D>
-__device__ void decode_side_work(const DecodeParams &P, Smem &sm, const Split &sp)
+__device__ void decode_side_work(const DecodeParams &P, Smem &sm, const Split &sp, int levels)
 {
     constexpr int NT = kDecodeThreads;
     constexpr int NC = kConsumerWarps * 32;
@@ -1859,13 +2056,14 @@ __device__ void decode_side_work(const DecodeParams &P, Smem &sm, const Split &s
         pl.max_pieces = sp.whole ? 1 : sm.plan_maxp;
         pl.whole_sequences = sp.whole ? 1 : 0;
         pl.workers_active = wact;
-        for (int i = 0; i < 8; ++i)
+        pl.merge_levels = levels;
+        for (int i = 0; i < 7; ++i)
             pl.reserved[i] = 0;
         *P.plan = pl;
     }
 }
 
-template <typename T, int BS, int G, int S, bool Q8, int D>
+template <typename T, int BS, int G, int S, bool Q8, int D, bool TWO = false>
 __global__ void __launch_bounds__(kDecodeThreads, 1) paged_decode_kernel(const DecodeParams P)
 {
     using Smem = DecodeSmem<BS, G, S, Q8, D>;
@@ -1886,8 +2084,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) paged_decode_kernel(const D
         // output and the plan, which the previous grid may still be using
         if (P.overlap)
             grid_dependency_wait();
-        decode_side_work<Smem, BS, D>(P, sm, sp);
-        decode_consumer<T, BS, G, S, Q8, D>(P, sm, sp, warp, warp, lane);
+        decode_side_work<Smem, BS, D>(P, sm, sp, TWO ? 2 : 1);
+        decode_consumer<T, BS, G, S, Q8, D, TWO>(P, sm, sp, warp, warp, lane);
     } else {
         regs_shrink<kProducerRegs>();
         if (warp - kConsumerWarps < Shape::PW)
@@ -1897,7 +2095,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) paged_decode_kernel(const D
 
 // Host-side launch helpers (defined in the per-type instantiation files).
 // Q8: the pools are q8_0 codes and scales (DecodeParams.k_codes ...); D: head dim.
-template <typename T, int BS, int G, bool Q8 = false, int D = 64>
+template <typename T, int BS, int G, bool Q8 = false, int D = 64, bool TWO = false>
 cudaError_t launch_paged_decode(const DecodeParams &P, int num_ctas, cudaStream_t stream);
 
 template <typename T, int BS, int G, bool Q8 = false, int D = 64>
