@@ -57,14 +57,14 @@ KERNEL_SOURCES = {
 }
 PROFILED_TRAFFIC = {
     # ncu capture of the committed kernel (dram__bytes_read.sum + dram__bytes_write.sum
-    # of one launch of the default command): 238.99 MB read + 3.43 MB written
+    # of one launch of the default command): 238.98 MB read + 3.38 MB written
     ("decode_b256", "paged_decode_kernel"): {
-        "sources_sha256": "b71eea5f48220dfc0a5f6970c9dc889ae3df360cc5ffd51db7803d3c982b2d14",
-        "bytes": 242425856},
+        "sources_sha256": "c797090fa8e2689dcb1413d51b125c4885231269ed8fe0b4fd81f8b44de00f83",
+        "bytes": 242362624},
     # ncu capture of the committed kernel: 4.73 MB read, 0 written
     ("mixed_chunked_prefill", "tc_prefill_kernel"): {
-        "sources_sha256": "1c38659a2c17008cf617a9648c5de5523e66db5ab2b571864923f45d99693816",
-        "bytes": 4729344},
+        "sources_sha256": "a4e34f993685ddb0cd1276982b530ecc310ec1829fdf04089afed5a489c60f25",
+        "bytes": 4728832},
 }
 
 
@@ -246,6 +246,8 @@ def decode_policy(args):
         p["min_blocks_per_cta"] = args.min_blocks_per_cta
     if getattr(args, "num_ctas", 0):
         p["num_ctas"] = args.num_ctas
+    if getattr(args, "merge_levels", 0):
+        p["merge_levels"] = args.merge_levels
     return p or None
 
 
@@ -748,6 +750,8 @@ def main(argv=None):
     ap.add_argument("--min-blocks-per-cta", type=int, default=0,
                     help="force the split's minimum KV blocks per CTA (0 = automatic)")
     ap.add_argument("--num-ctas", type=int, default=0, help="force the decode grid (0 = one CTA per SM)")
+    ap.add_argument("--merge-levels", type=int, default=0, choices=[0, 1, 2],
+                    help="force one- or two-level merges of cut pairs (0 = automatic)")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--soak-s", type=float, default=1.0)
     ap.add_argument("--traffic", type=float, default=None,
