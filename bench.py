@@ -63,8 +63,8 @@ PROFILED_TRAFFIC = {
         "bytes": 242362624},
     # ncu capture of the committed kernel: 4.73 MB read, 0 written
     ("mixed_chunked_prefill", "tc_prefill_kernel"): {
-        "sources_sha256": "a4e34f993685ddb0cd1276982b530ecc310ec1829fdf04089afed5a489c60f25",
-        "bytes": 4728832},
+        "sources_sha256": "dc7e7767b5ed32791155281aabc498f1bf5ef60ab74f169a39dd48bfaaf84944",
+        "bytes": 4729088},
 }
 
 
