@@ -337,8 +337,14 @@ ns_status run_decode(const DecodeCall &c, int dev)
     P.v_codes = static_cast<const int8_t *>(c.v_codes);
     P.k_scales = static_cast<const uint16_t *>(c.k_scales);
     P.v_scales = static_cast<const uint16_t *>(c.v_scales);
-    P.auto_policy = (c.cfg == nullptr || (c.cfg->num_ctas == 0 && c.cfg->min_blocks_per_cta == 0 &&
-                                          c.cfg->whole_sequences == 0))
+    // The span walk of a mixed prefill call (pack) shares the SMs with the
+    // tensor-core kernel after it, so it keeps the default blocks per worker:
+    // the automatic finer cut spreads a few live rows over every warp of the
+    // grid, which holds all SMs and cuts a long row into so many pieces that
+    // its one-level merge is the walk's tail (16 decode rows of 103-4096
+    // tokens beside two 512-token chunks: the call 55.3 -> 49.2 us).
+    P.auto_policy = (!c.pack && (c.cfg == nullptr || (c.cfg->num_ctas == 0 && c.cfg->min_blocks_per_cta == 0 &&
+                                                      c.cfg->whole_sequences == 0)))
                         ? 1
                         : 0;
 

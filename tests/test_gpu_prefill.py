@@ -24,6 +24,29 @@ def test_mixed_chunked_prefill_step(orc):
     _gpu.assert_no_device_status()
 
 
+def test_mixed_step_walk_keeps_default_blocks_per_worker(orc):
+    """Beside tensor-core spans, the single-token rows' walk keeps the default
+    8 blocks a worker (no finer automatic cut). Its workers fill the fewest
+    CTAs, and the 4096-token row is cut into at most 34 pieces. The output
+    still matches the oracle."""
+    st = wl.mixed_chunked_prefill()
+    ref, kp, vp = orc.step(st, num_threads=max(1, orc.max_threads()))
+    d = DevStep(st, k_pool=kp, v_pool=vp)
+    out = d.prefill()
+    torch.cuda.synchronize()
+    compare(out, ref, st.dtype, "mixed step")
+    _gpu.assert_no_device_status()
+    plan = nb.ns_read_decode_plan(d.ws)
+    dec = st.query_lens == 1
+    nblocks = -(-st.context_lens[dec].astype(np.int64) // st.block_size)
+    assert plan["total_blocks"] == st.num_kv_heads * nblocks.sum()
+    virtual = st.num_kv_heads * (nblocks + 4).sum()  # 4 virtual blocks of split cost a pair
+    workers = -(-virtual // 8)
+    assert plan["whole_sequences"] == 0 and plan["workers_active"] == workers
+    assert plan["ctas_active"] == -(-workers // 8)
+    assert 2 <= plan["max_pieces"] <= -(-(nblocks.max() + 4) // 8) + 1
+
+
 @pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
 @pytest.mark.parametrize("bs", [4, 16])
 def test_spans_with_ragged_prefixes(dtype, bs, orc):
