@@ -202,8 +202,9 @@ ns_status ns_paged_attn_decode(const void *q, const void *k_pool, const void *v_
  *                       (block size 16, head_dim 64, 16-bit pools; elsewhere
  *                       ignored).  Automatic takes 2 there when the pairs are
  *                       few for the CTAs' warps (32 or more warps a pair) and
- *                       no table_row indirection is used.  The result is the
- *                       same up to rounding order.
+ *                       their table rows span the warps; the single-token
+ *                       rows of a prefill call choose the same way.  The
+ *                       result is the same up to rounding order.
  *   reserved            must be 0.
  */
 #define NS_MAX_CTAS 1024

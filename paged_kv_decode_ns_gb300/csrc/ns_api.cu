@@ -284,6 +284,7 @@ struct DecodeCall {
     const void *k_new, *v_new;
     const int64_t *slot_mapping;
     bool pack = false;  // keep the workers on the fewest CTAs (another kernel waits for the SMs)
+    bool fixed_split = false;  // default blocks per worker, no automatic finer cut
     // q8_0 pools (k_pool and v_pool unused then)
     bool q8 = false;
     const void *k_codes = nullptr, *k_scales = nullptr, *v_codes = nullptr, *v_scales = nullptr;
@@ -337,14 +338,8 @@ ns_status run_decode(const DecodeCall &c, int dev)
     P.v_codes = static_cast<const int8_t *>(c.v_codes);
     P.k_scales = static_cast<const uint16_t *>(c.k_scales);
     P.v_scales = static_cast<const uint16_t *>(c.v_scales);
-    // The span walk of a mixed prefill call (pack) shares the SMs with the
-    // tensor-core kernel after it, so it keeps the default blocks per worker:
-    // the automatic finer cut spreads a few live rows over every warp of the
-    // grid, which holds all SMs and cuts a long row into so many pieces that
-    // its one-level merge is the walk's tail (16 decode rows of 103-4096
-    // tokens beside two 512-token chunks: the call 55.3 -> 49.2 us).
-    P.auto_policy = (!c.pack && (c.cfg == nullptr || (c.cfg->num_ctas == 0 && c.cfg->min_blocks_per_cta == 0 &&
-                                                      c.cfg->whole_sequences == 0)))
+    P.auto_policy = (!c.fixed_split && (c.cfg == nullptr || (c.cfg->num_ctas == 0 && c.cfg->min_blocks_per_cta == 0 &&
+                                                             c.cfg->whole_sequences == 0)))
                         ? 1
                         : 0;
 
@@ -399,8 +394,7 @@ ns_status launch_decode(const DecodeParams &P, ns_dtype dtype, int block_size, i
     if (head_dim == 64 && !q8 && block_size == 16) {
         const long long pairs = (long long)P.num_seqs * P.num_kv_heads, warps = (long long)ctas * kConsumerWarps;
         two = P.merge_levels == 2 ||
-              (P.merge_levels == 0 && P.table_row == nullptr && pairs * 32 <= warps &&
-               pairs * P.max_blocks_per_seq >= warps);
+              (P.merge_levels == 0 && pairs * 32 <= warps && pairs * P.max_blocks_per_seq >= warps);
     }
     cudaError_t e;
     if (two)
@@ -674,6 +668,15 @@ ns_status ns_paged_attn_prefill_ex(const void *q, const int32_t *query_start_loc
         c.head_dim = head_dim;
         // the tensor-core kernel after it takes the SMs its idle CTAs leave
         c.pack = tc_min != 0 && (phases & NS_PREFILL_TENSOR_CORE) != 0;
+        // With more query tokens than spans, some span has two or more and the
+        // tensor-core kernel has work beside the walk: the walk then keeps the
+        // default blocks per worker. The automatic finer cut spreads a few live
+        // rows over every warp of the grid, which holds all SMs and cuts a long
+        // row into so many pieces that its merge is the walk's tail (16 decode
+        // rows of 103-4096 tokens beside two 512-token chunks: the call 55.3 ->
+        // 49.2 us). Calls of single-token spans keep the automatic split, which
+        // measured faster for them (4 sequences 19.5 -> 16.5 us).
+        c.fixed_split = c.pack && total_q_tokens > num_seqs;
         const ns_status r = run_decode(c, dev);
         if (r != NS_OK)
             return r;

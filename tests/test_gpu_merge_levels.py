@@ -93,3 +93,18 @@ def test_merge_levels_out_of_range_refused():
     c.merge_levels = 3
     with pytest.raises(nb.NsError):
         d.decode(c)
+
+
+def test_long_context_through_prefill_two_level(long_ctx):
+    """The same rows as single-token spans of a prefill call: the span walk
+    takes the automatic split and the two-level merge, and matches the
+    oracle."""
+    st, ref, kp, vp = long_ctx
+    d = DevStep(st, k_pool=kp, v_pool=vp)
+    out = d.prefill()
+    torch.cuda.synchronize()
+    compare(out, ref, st.dtype, "prefill rows")
+    plan = nb.ns_read_decode_plan(d.ws)
+    assert plan["merge_levels"] == 2 and plan["max_pieces"] >= 16
+    assert plan["workers_active"] == plan["ctas_launched"] * 8
+    _gpu.assert_no_device_status()
