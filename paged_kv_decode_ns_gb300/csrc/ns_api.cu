@@ -666,17 +666,18 @@ ns_status ns_paged_attn_prefill_ex(const void *q, const int32_t *query_start_loc
                      num_kv_heads, block_size, scale, out, st, max_blocks_per_seq, num_blocks, dtype,
                      workspace, nullptr, nullptr, nullptr, nullptr};
         c.head_dim = head_dim;
-        // the tensor-core kernel after it takes the SMs its idle CTAs leave
-        c.pack = tc_min != 0 && (phases & NS_PREFILL_TENSOR_CORE) != 0;
         // With more query tokens than spans, some span has two or more and the
-        // tensor-core kernel has work beside the walk: the walk then keeps the
-        // default blocks per worker. The automatic finer cut spreads a few live
-        // rows over every warp of the grid, which holds all SMs and cuts a long
-        // row into so many pieces that its merge is the walk's tail (16 decode
-        // rows of 103-4096 tokens beside two 512-token chunks: the call 55.3 ->
-        // 49.2 us). Calls of single-token spans keep the automatic split, which
-        // measured faster for them (4 sequences 19.5 -> 16.5 us).
-        c.fixed_split = c.pack && total_q_tokens > num_seqs;
+        // tensor-core kernel after the walk has work: the walk then packs its
+        // workers on the fewest CTAs (the tensor-core kernel takes the SMs its
+        // idle CTAs leave) and keeps the default blocks per worker. The
+        // automatic finer cut spreads a few live rows over every warp of the
+        // grid, which holds all SMs and cuts a long row into so many pieces that
+        // its merge is the walk's tail (16 decode rows of 103-4096 tokens beside
+        // two 512-token chunks: the call 55.3 -> 49.2 us). Otherwise every span
+        // has one token (or some are empty) and the walk is split as a decode
+        // step is.
+        c.pack = total_q_tokens > num_seqs && tc_min != 0 && (phases & NS_PREFILL_TENSOR_CORE) != 0;
+        c.fixed_split = c.pack;
         const ns_status r = run_decode(c, dev);
         if (r != NS_OK)
             return r;
