@@ -26,9 +26,9 @@ def test_mixed_chunked_prefill_step(orc):
 
 def test_mixed_step_walk_keeps_default_blocks_per_worker(orc):
     """Beside tensor-core spans, the single-token rows' walk keeps the default
-    8 blocks a worker (no finer automatic cut). Its workers fill the fewest
-    CTAs, and the 4096-token row is cut into at most 34 pieces. The output
-    still matches the oracle."""
+    8 blocks a worker (no finer automatic cut) on a grid of one CTA per
+    (span, kv head) pair. Its workers fill the fewest CTAs, and the 4096-token
+    row is cut into at most 34 pieces. The output still matches the oracle."""
     st = wl.mixed_chunked_prefill()
     ref, kp, vp = orc.step(st, num_threads=max(1, orc.max_threads()))
     d = DevStep(st, k_pool=kp, v_pool=vp)
@@ -45,6 +45,9 @@ def test_mixed_step_walk_keeps_default_blocks_per_worker(orc):
     assert plan["whole_sequences"] == 0 and plan["workers_active"] == workers
     assert plan["ctas_active"] == -(-workers // 8)
     assert 2 <= plan["max_pieces"] <= -(-(nblocks.max() + 4) // 8) + 1
+    # its grid: one CTA per (span, kv head) pair at most
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert plan["ctas_launched"] == min(sms, st.num_seqs * st.num_kv_heads)
 
 
 @pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
