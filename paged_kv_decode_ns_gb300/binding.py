@@ -10,6 +10,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import threading
 
 import torch
 
@@ -135,11 +136,76 @@ def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
 
 
 def _stream(stream) -> int:
+    if getattr(_capture, "on", False):
+        return _STREAM_SLOT
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
     return int(stream)
+
+
+# While a call is prepared, the entry points record their marshalled arguments
+# instead of calling the library, and the stream argument is a slot filled in
+# at each run.
+_capture = threading.local()
+_STREAM_SLOT = object()
+
+
+def _invoke(name: str, *args) -> int:
+    if getattr(_capture, "on", False):
+        _capture.record = (name, args)
+        return NS_OK
+    return getattr(lib(), name)(*args)
+
+
+class PreparedCall:
+    """One launching entry point with its arguments checked and marshalled once.
+
+    Calling it runs the same C entry point again on the same buffers (with
+    whatever they hold then) on ``stream`` (default: the current stream); only
+    the stream is looked up per call.  The object references every tensor and
+    config it was prepared with, so their memory stays allocated while it
+    lives.  One object must not be called from two threads at once.
+    """
+
+    __slots__ = ("name", "_fn", "_args", "_slot", "_keep")
+
+    def __init__(self, name: str, args: tuple, keep: list):
+        self.name = name
+        self._fn = getattr(lib(), name)
+        self._args = list(args)
+        slots = [i for i, a in enumerate(self._args) if a is _STREAM_SLOT]
+        if len(slots) != 1:
+            raise RuntimeError(f"{name}: expected one stream argument")
+        self._slot = slots[0]
+        self._keep = keep
+
+    def __call__(self, stream=None):
+        self._args[self._slot] = _stream(stream)
+        _check(self._fn(*self._args), self.name)
+
+
+def prepare(fn, *args, **kwargs) -> PreparedCall:
+    """``fn`` (a launching entry point of this module: ns_kv_append,
+    ns_paged_attn_decode, ns_kv_append_paged_attn_decode, ns_paged_attn_prefill
+    or a q8_0 one) with these arguments, checked now and run by calling the
+    returned object.  It is what a serving loop that calls the same step on the
+    same buffers every iteration uses, so that a call costs the host one
+    foreign call."""
+    if kwargs.get("stream") is not None:
+        raise ValueError("the stream is given to each run of a prepared call")
+    _capture.on, _capture.record = True, None
+    try:
+        fn(*args, **kwargs)
+    finally:
+        _capture.on = False
+    if _capture.record is None:
+        raise TypeError(f"{getattr(fn, '__name__', fn)} cannot be prepared")
+    name, marshalled = _capture.record
+    _capture.record = None
+    keep = [a for a in list(args) + list(kwargs.values()) if a is not None]
+    return PreparedCall(name, marshalled, keep)
 
 
 def ns_version() -> int:
@@ -167,10 +233,10 @@ def ns_kv_append(k, v, slot_mapping, k_pool, v_pool, stream=None):
     if slot_mapping.shape != (T,):
         raise ValueError("slot_mapping must be [num_tokens]")
     dt = _dtype_code(k)
-    st = lib().ns_kv_append(_dev(k, "k"), _dev(v, "v", k.dtype),
-                            _dev(slot_mapping, "slot_mapping", torch.int64),
-                            _dev(k_pool, "k_pool", k.dtype), _dev(v_pool, "v_pool", k.dtype),
-                            T, hkv, d, bs, nb, dt, _stream(stream))
+    st = _invoke("ns_kv_append", _dev(k, "k"), _dev(v, "v", k.dtype),
+                 _dev(slot_mapping, "slot_mapping", torch.int64),
+                 _dev(k_pool, "k_pool", k.dtype), _dev(v_pool, "v_pool", k.dtype),
+                 T, hkv, d, bs, nb, dt, _stream(stream))
     _check(st, "ns_kv_append")
 
 
@@ -201,9 +267,9 @@ def ns_paged_attn_decode(q, k_pool, v_pool, block_tables, context_lens, scale, o
     args = (p["q"], p["k"], p["v"], p["bt"], p["cl"], S, hq, hkv, d, bs, float(scale), p["out"],
             _stream(stream), block_tables.shape[1], nb, dt, p["ws"], workspace.numel())
     if config is None:
-        _check(lib().ns_paged_attn_decode(*args), "ns_paged_attn_decode")
+        _check(_invoke("ns_paged_attn_decode", *args), "ns_paged_attn_decode")
     else:
-        _check(lib().ns_paged_attn_decode_ex(*args, ctypes.byref(config)), "ns_paged_attn_decode_ex")
+        _check(_invoke("ns_paged_attn_decode_ex", *args, ctypes.byref(config)), "ns_paged_attn_decode_ex")
 
 
 def ns_paged_attn_decode_noalloc(q, k_pool, v_pool, block_tables, context_lens, scale, out,
@@ -237,7 +303,8 @@ def ns_kv_append_paged_attn_decode(q, k_new, v_new, slot_mapping, k_pool, v_pool
                                                 out, workspace)
     if k_new.shape != (S, hkv, d) or v_new.shape != (S, hkv, d) or slot_mapping.shape != (S,):
         raise ValueError("k_new/v_new must be [num_seqs, Hkv, D], slot_mapping [num_seqs]")
-    st = lib().ns_kv_append_paged_attn_decode_ex(
+    st = _invoke(
+        "ns_kv_append_paged_attn_decode_ex",
         p["q"], _dev(k_new, "k_new", q.dtype), _dev(v_new, "v_new", q.dtype),
         _dev(slot_mapping, "slot_mapping", torch.int64), p["k"], p["v"], p["bt"], p["cl"], S, hq,
         hkv, d, bs, float(scale), p["out"], _stream(stream), block_tables.shape[1], nb, dt,
@@ -257,9 +324,9 @@ def ns_paged_attn_prefill(q, query_start_loc, k_pool, v_pool, block_tables, cont
             p["cl"], S, T, hq, hkv, d, bs, float(scale), p["out"], _stream(stream),
             block_tables.shape[1], nb, dt, p["ws"], workspace.numel())
     if config is None:
-        _check(lib().ns_paged_attn_prefill(*args), "ns_paged_attn_prefill")
+        _check(_invoke("ns_paged_attn_prefill", *args), "ns_paged_attn_prefill")
     else:
-        _check(lib().ns_paged_attn_prefill_ex(*args, ctypes.byref(config)),
+        _check(_invoke("ns_paged_attn_prefill_ex", *args, ctypes.byref(config)),
                "ns_paged_attn_prefill_ex")
 
 
@@ -278,9 +345,9 @@ def ns_kv_append_q8_0(k, v, slot_mapping, k_codes, k_scales, v_codes, v_scales, 
     nb, hkv2, bs, d2, kc, ks, vc, vs = _q8_pools(k_codes, k_scales, v_codes, v_scales)
     if v.shape != k.shape or hkv2 != hkv or d2 != d or slot_mapping.shape != (T,):
         raise ValueError("shape mismatch")
-    st = lib().ns_kv_append_q8_0(_dev(k, "k"), _dev(v, "v", k.dtype),
-                                 _dev(slot_mapping, "slot_mapping", torch.int64), kc, ks, vc, vs, T, hkv, d,
-                                 bs, nb, _dtype_code(k), _stream(stream))
+    st = _invoke("ns_kv_append_q8_0", _dev(k, "k"), _dev(v, "v", k.dtype),
+                 _dev(slot_mapping, "slot_mapping", torch.int64), kc, ks, vc, vs, T, hkv, d,
+                 bs, nb, _dtype_code(k), _stream(stream))
     _check(st, "ns_kv_append_q8_0")
 
 
@@ -291,7 +358,8 @@ def ns_paged_attn_decode_q8_0(q, k_codes, k_scales, v_codes, v_scales, block_tab
     nb, hkv, bs, d2, kc, ks, vc, vs = _q8_pools(k_codes, k_scales, v_codes, v_scales)
     if d2 != d or out.shape != q.shape or context_lens.shape != (S,) or block_tables.shape[0] != S:
         raise ValueError("shape mismatch")
-    st = lib().ns_paged_attn_decode_q8_0(
+    st = _invoke(
+        "ns_paged_attn_decode_q8_0",
         _dev(q, "q"), kc, ks, vc, vs, _dev(block_tables, "block_tables", torch.int32),
         _dev(context_lens, "context_lens", torch.int32), S, hq, hkv, d, bs, float(scale),
         _dev(out, "out", q.dtype), _stream(stream), block_tables.shape[1], nb, _dtype_code(q),
@@ -308,7 +376,7 @@ def ns_kv_append_paged_attn_decode_q8_0(q, k_new, v_new, slot_mapping, k_codes, 
         raise ValueError("k_new/v_new must be [num_seqs, Hkv, D], slot_mapping [num_seqs]")
     if d2 != d or out.shape != q.shape or context_lens.shape != (S,) or block_tables.shape[0] != S:
         raise ValueError("shape mismatch")
-    st = lib().ns_kv_append_paged_attn_decode_q8_0(
+    st = _invoke("ns_kv_append_paged_attn_decode_q8_0", 
         _dev(q, "q"), _dev(k_new, "k_new", q.dtype), _dev(v_new, "v_new", q.dtype),
         _dev(slot_mapping, "slot_mapping", torch.int64), kc, ks, vc, vs,
         _dev(block_tables, "block_tables", torch.int32), _dev(context_lens, "context_lens", torch.int32), S, hq,
