@@ -325,7 +325,9 @@ ns_status ns_paged_attn_prefill(const void *q, const int32_t *query_start_loc,
 /*
  * Policy overrides for the chunked prefill (tests and measurements).
  *   tensor_core_min_span  0 = auto: spans of 2 or more query tokens run on the
- *                         tensor cores when block_size is 16 or 32; a positive
+ *                         tensor cores when block_size is 16 or 32, unless the
+ *                         call has no more query tokens than spans (then every
+ *                         row takes the split-KV walk); a positive
  *                         value raises that threshold; -1 = never (every row
  *                         takes the split-KV decode walk)
  *   phases                0 = everything; else a mask of the parts to run

@@ -658,6 +658,12 @@ ns_status ns_paged_attn_prefill_ex(const void *q, const int32_t *query_start_loc
     int32_t *row_len = reinterpret_cast<int32_t *>(ws + L.row_len);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     int tc_min = cfg && cfg->tensor_core_min_span != 0 ? cfg->tensor_core_min_span : 2;
+    // Automatic: with no more query tokens than spans, every span has one token
+    // unless some are empty, so all rows take the split-KV walk (a longer span
+    // beside empty ones as well) and no tensor-core kernel is launched (4
+    // single-token spans: 18.4 -> 17.6 us a call, batch 32 24.4 -> 23.2).
+    if (!(cfg && cfg->tensor_core_min_span != 0) && total_q_tokens <= num_seqs)
+        tc_min = 0;
     if (tc_min < 0 || (head_dim == 128 && block_size != 16) ||
         !ns::tc_prefill_supported(block_size, num_q_heads / num_kv_heads) ||
         (long long)num_blocks * num_kv_heads * block_size > 0x7fffffffLL)

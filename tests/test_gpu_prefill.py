@@ -190,3 +190,19 @@ def test_raised_tensor_core_threshold_partitions_the_rows(min_span, orc):
     torch.cuda.synchronize()
     compare(d.out, ref, st.dtype, f"min_span {min_span}")
     _gpu.assert_no_device_status()
+
+
+def test_no_more_tokens_than_spans_all_on_the_walk(orc):
+    """With as many query tokens as spans (one empty span, one of two tokens)
+    every row takes the split-KV walk, the two-token span too: the output
+    matches the oracle."""
+    rng = np.random.default_rng(77)
+    lens = np.array([7, 40, 20, 130, 3], np.int32)
+    qlens = np.array([0, 2, 1, 1, 1], np.int32)
+    st = wl.make_step(rng, lens, qlens, dtype=wl.F16, poison_unused=True)
+    ref, kp, vp = orc.step(st)
+    d = DevStep(st, k_pool=kp, v_pool=vp)
+    out = d.prefill()
+    torch.cuda.synchronize()
+    compare(out, ref, st.dtype, "tokens <= spans")
+    _gpu.assert_no_device_status()
