@@ -89,3 +89,26 @@ def test_second_stage_gives_each_layer_its_own_output_twin():
     assert outs[1] is step.layer_io[-1][-1]         # the read-back is the last layer's
     use(0)
     assert step.layer_io == io0
+
+
+def test_prepared_calls_follow_the_buffer_set():
+    """The bench's steps are prepared calls cached per buffer set: the second
+    staging gets calls prepared on its own buffers, and switching back reuses
+    the first set's calls."""
+    torch = __import__("torch")
+    d_all, step = _staged_step(torch, layers=False)
+    step.stage, step.calls = 0, {}
+    made = []
+
+    def make():
+        made.append((step.q.data_ptr(), step.out))
+        return len(made)
+    first = bench.Step.prepared(step, ("decode", 0), make)
+    assert bench.Step.prepared(step, ("decode", 0), make) == first and len(made) == 1
+    d_all2, use, outs = bench.second_stage(step, d_all, torch)
+    use(1)
+    second = bench.Step.prepared(step, ("decode", 0), make)
+    assert second != first and made[1] == (step.q.data_ptr(), outs[1])
+    assert made[1][0] != made[0][0]
+    use(0)
+    assert bench.Step.prepared(step, ("decode", 0), make) == first and len(made) == 2
