@@ -2,8 +2,8 @@
 
 Every wait inside the kernels has a time limit; when it runs out the kernel
 sets NS_DEV_WAIT_TIMEOUT, stops issuing copies, waits for its own copies in
-flight and returns, so that the context stays usable (SURVEY failure
-detection: a GPU wait that gives up and reports, never a trap or a hang).  The
+flight and returns, so that the context stays usable (failure detection: a
+GPU wait that gives up and reports, never a trap or a hang).  The
 test shortens the limit of the computing warps' waits for their next K/V
 step (ns_decode_config.wait_limit_ns) below a copy's latency, so the wait
 runs out on a real workload with nothing faulting, and checks that the call
