@@ -198,6 +198,8 @@ def prepare(fn, *args, **kwargs) -> PreparedCall:
     _capture.on, _capture.record = True, None
     try:
         fn(*args, **kwargs)
+    except ctypes.ArgumentError as e:  # an entry point that calls the library directly
+        raise TypeError(f"{getattr(fn, '__name__', fn)} cannot be prepared") from e
     finally:
         _capture.on = False
     if _capture.record is None:
