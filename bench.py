@@ -57,10 +57,10 @@ KERNEL_SOURCES = {
 }
 PROFILED_TRAFFIC = {
     # ncu capture of the committed kernel (dram__bytes_read.sum + dram__bytes_write.sum
-    # of one launch of the default command): 238.99 MB read + 3.60 MB written
+    # of one launch of the default command): 238.97 MB read + 3.02 MB written
     ("decode_b256", "paged_decode_kernel"): {
-        "sources_sha256": "dfb5074766f2bdb2c7e7b203e81891a2da1f0ca6a467cf71584df57fff3e19e2",
-        "bytes": 242586624},
+        "sources_sha256": "2b58c7c4cb7198c03f7ca272085777c9b661caccb0b7a272b9f5b5c754fc564d",
+        "bytes": 241993216},
     # ncu capture of the committed kernel: 4.73 MB read, 0 written
     ("mixed_chunked_prefill", "tc_prefill_kernel"): {
         "sources_sha256": "dc7e7767b5ed32791155281aabc498f1bf5ef60ab74f169a39dd48bfaaf84944",

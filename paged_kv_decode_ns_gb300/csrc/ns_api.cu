@@ -100,6 +100,23 @@ cudaError_t dispatch_decode_two(int g, const ns::DecodeParams &P, int ctas, cuda
     }
 }
 
+// Short-walk kernels: block size 16, head_dim 64, 16-bit pools.
+template <typename T>
+cudaError_t dispatch_decode_short(int g, const ns::DecodeParams &P, int ctas, cudaStream_t s)
+{
+    constexpr int VU = ns::kShortWalkValuesUnroll;
+    switch (g) {
+    case 1: return ns::launch_paged_decode<T, 16, 1, false, 64, false, VU>(P, ctas, s);
+    case 2: return ns::launch_paged_decode<T, 16, 2, false, 64, false, VU>(P, ctas, s);
+    case 3: return ns::launch_paged_decode<T, 16, 3, false, 64, false, VU>(P, ctas, s);
+    case 4: return ns::launch_paged_decode<T, 16, 4, false, 64, false, VU>(P, ctas, s);
+    case 5: return ns::launch_paged_decode<T, 16, 5, false, 64, false, VU>(P, ctas, s);
+    case 6: return ns::launch_paged_decode<T, 16, 6, false, 64, false, VU>(P, ctas, s);
+    case 7: return ns::launch_paged_decode<T, 16, 7, false, 64, false, VU>(P, ctas, s);
+    default: return ns::launch_paged_decode<T, 16, 8, false, 64, false, VU>(P, ctas, s);
+    }
+}
+
 template <typename T>
 cudaError_t dispatch_decode(int bs, int g, const ns::DecodeParams &P, int ctas, cudaStream_t s)
 {
@@ -395,11 +412,14 @@ ns_status launch_decode(const DecodeParams &P, ns_dtype dtype, int block_size, i
     // Two-level merges where a cut pair has many pieces in each CTA: few
     // pairs for the CTAs' warps (at least 32 warps a pair) that could fill
     // them (the pairs' table rows span at least a block a warp).
-    bool two = false;
+    bool two = false, shortw = false;
     if (head_dim == 64 && !q8 && block_size == 16) {
         const long long pairs = (long long)P.num_seqs * P.num_kv_heads, warps = (long long)ctas * kConsumerWarps;
         two = P.merge_levels == 2 ||
               (P.merge_levels == 0 && pairs * 32 <= warps && pairs * P.max_blocks_per_seq >= warps);
+        // Short walks: when the pairs' table rows bound every worker's share at
+        // 16 blocks (8 steps), the kernel with the values pass looped.
+        shortw = !two && pairs * (P.max_blocks_per_seq + kPieceCost) <= 16 * warps;
     }
     cudaError_t e;
     if (two)
@@ -409,6 +429,9 @@ ns_status launch_decode(const DecodeParams &P, ns_dtype dtype, int block_size, i
                              : dispatch_decode_d128<F16>(g, P, ctas, stream);
     else if (q8)
         e = dtype == NS_BF16 ? dispatch_decode_q8<BF16>(g, P, ctas, stream) : dispatch_decode_q8<F16>(g, P, ctas, stream);
+    else if (shortw)
+        e = dtype == NS_BF16 ? dispatch_decode_short<BF16>(g, P, ctas, stream)
+                             : dispatch_decode_short<F16>(g, P, ctas, stream);
     else
         e = dtype == NS_BF16 ? dispatch_decode<BF16>(block_size, g, P, ctas, stream)
                              : dispatch_decode<F16>(block_size, g, P, ctas, stream);

@@ -79,6 +79,11 @@ constexpr int kConsumerWarps = 8;
 // Row groups (4 tokens each) whose scores are computed together: 2 measured
 // 1.3% faster than 1 and 4 on the batch-256 decode.
 constexpr int kQkRows = 2;
+// Row groups of the values pass a trip in the short-walk kernels, which the
+// host takes when no worker can have more than a few steps: less code to
+// fetch (batch 32 19.56 -> 18.98 us, 4 sequences 13.41 -> 13.10), where batch
+// 256 ran slower with it (57.6 -> 59.3 us) and keeps the whole unroll.
+constexpr int kShortWalkValuesUnroll = 4;
 constexpr int kZeroElems = 2048;       // 16-bit zeros: the largest step of K or V rows
 constexpr int kMaxWorkers = 2048;      // split workers (each has two record slots)
 constexpr int kDefaultMinBlocksPerCta = 64;  // spread over a CTA's workers
@@ -610,7 +615,8 @@ struct RowLoad<T, G, true, 64> {
     }
 };
 
-template <typename T, int G, bool Q8, int D>
+// VU: row groups of the values pass unrolled per trip (0: all of them).
+template <typename T, int G, bool Q8, int D, int VU = 0>
 __device__ __forceinline__ void process_step(const DecodeSlot<G, Q8, D> &sl, uint32_t vmask,
                                              const float2 (&q2)[QRegs<G>::N],
                                              float2 (&acc)[G][4], float &m_run, float &l_run,
@@ -745,7 +751,7 @@ __device__ __forceinline__ void process_step(const DecodeSlot<G, Q8, D> &sl, uin
     __syncwarp();
 
     // ---- values
-#pragma unroll
+#pragma unroll (VU == 0 ? STEPS : VU)
     for (int st = 0; st < STEPS; ++st) {
         const int t = st * GD::ROWS + r;
         float2 vx[4];
@@ -1720,7 +1726,7 @@ __device__ __forceinline__ void quantize_new_row(const DecodeParams &P, DecodeSl
     __syncwarp();
 }
 
-template <typename T, int BS, int G, int S, bool Q8, int D, bool TWO>
+template <typename T, int BS, int G, int S, bool Q8, int D, bool TWO, int VU>
 __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8, D> &sm, const Split &sp,
                                 int ring, int warp, int lane)
 {
@@ -1821,7 +1827,7 @@ __device__ void decode_consumer(const DecodeParams &P, DecodeSmem<BS, G, S, Q8, 
                 }
                 // one step path for full and partial steps: a second, unmasked
                 // copy measured 4% slower (instruction-fetch stalls)
-                process_step<T, G, Q8, D>(sl, mt.vmask, q2, acc, m_run, l_run, pbuf, lane);
+                process_step<T, G, Q8, D, VU>(sl, mt.vmask, q2, acc, m_run, l_run, pbuf, lane);
             }
             // The slot is only read (the async proxy alone writes it), so the
             // barrier's release/acquire orders these reads before the refill.
@@ -2065,7 +2071,7 @@ __device__ void decode_side_work(const DecodeParams &P, Smem &sm, const Split &s
     }
 }
 
-template <typename T, int BS, int G, int S, bool Q8, int D, bool TWO = false>
+template <typename T, int BS, int G, int S, bool Q8, int D, bool TWO = false, int VU = 0>
 __global__ void __launch_bounds__(kDecodeThreads, 1) paged_decode_kernel(const DecodeParams P)
 {
     using Smem = DecodeSmem<BS, G, S, Q8, D>;
@@ -2087,7 +2093,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) paged_decode_kernel(const D
         if (P.overlap)
             grid_dependency_wait();
         decode_side_work<Smem, BS, D>(P, sm, sp, TWO ? 2 : 1);
-        decode_consumer<T, BS, G, S, Q8, D, TWO>(P, sm, sp, warp, warp, lane);
+        decode_consumer<T, BS, G, S, Q8, D, TWO, VU>(P, sm, sp, warp, warp, lane);
     } else {
         regs_shrink<kProducerRegs>();
         if (warp - kConsumerWarps < Shape::PW)
@@ -2096,8 +2102,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) paged_decode_kernel(const D
 }
 
 // Host-side launch helpers (defined in the per-type instantiation files).
-// Q8: the pools are q8_0 codes and scales (DecodeParams.k_codes ...); D: head dim.
-template <typename T, int BS, int G, bool Q8 = false, int D = 64, bool TWO = false>
+// Q8: the pools are q8_0 codes and scales (DecodeParams.k_codes ...); D: head dim;
+// TWO: two-level merges; VU: the values pass's unroll (0: whole).
+template <typename T, int BS, int G, bool Q8 = false, int D = 64, bool TWO = false, int VU = 0>
 cudaError_t launch_paged_decode(const DecodeParams &P, int num_ctas, cudaStream_t stream);
 
 template <typename T, int BS, int G, bool Q8 = false, int D = 64>

@@ -6,13 +6,13 @@
 
 namespace ns {
 
-template <typename T, int BS, int G, bool Q8, int D, bool TWO = false>
+template <typename T, int BS, int G, bool Q8, int D, bool TWO = false, int VU = 0>
 struct DecodeKernel {
     static constexpr int S = decode_stages<BS, G, Q8, D>();
     static_assert(sizeof(DecodeSmem<BS, G, S, Q8, D>) <= kMaxDynSmem, "decode shared memory");
     static constexpr int THREADS = kDecodeThreads;  // consumers + producer warpgroup
     static constexpr size_t SMEM = sizeof(DecodeSmem<BS, G, S, Q8, D>);
-    static void (*fn())(const DecodeParams) { return paged_decode_kernel<T, BS, G, S, Q8, D, TWO>; }
+    static void (*fn())(const DecodeParams) { return paged_decode_kernel<T, BS, G, S, Q8, D, TWO, VU>; }
 
     static cudaError_t prepare()
     {
@@ -39,10 +39,10 @@ struct DecodeKernel {
     }
 };
 
-template <typename T, int BS, int G, bool Q8, int D, bool TWO>
+template <typename T, int BS, int G, bool Q8, int D, bool TWO, int VU>
 cudaError_t launch_paged_decode(const DecodeParams &P, int num_ctas, cudaStream_t stream)
 {
-    using K = DecodeKernel<T, BS, G, Q8, D, TWO>;
+    using K = DecodeKernel<T, BS, G, Q8, D, TWO, VU>;
     cudaError_t e = K::prepare();
     if (e != cudaSuccess)
         return e;
@@ -105,5 +105,21 @@ int decode_ctas_per_sm()
     NS_INSTANTIATE_DECODE_TWO_G(T, BS, 7) \
     NS_INSTANTIATE_DECODE_TWO_G(T, BS, 8)
 #define NS_INSTANTIATE_DECODE_Q(T, BS, Q8) NS_INSTANTIATE_DECODE_QD(T, BS, Q8, 64)
+
+// Short-walk kernels (16-bit pools, head_dim 64): the values pass unrolled
+// kShortWalkValuesUnroll row groups a trip, for less code to fetch when each
+// worker runs few steps.
+#define NS_INSTANTIATE_DECODE_SHORT_G(T, BS, G)                                                    \
+    template cudaError_t launch_paged_decode<T, BS, G, false, 64, false, kShortWalkValuesUnroll>( \
+        const DecodeParams &, int, cudaStream_t);
+#define NS_INSTANTIATE_DECODE_SHORT(T, BS)  \
+    NS_INSTANTIATE_DECODE_SHORT_G(T, BS, 1) \
+    NS_INSTANTIATE_DECODE_SHORT_G(T, BS, 2) \
+    NS_INSTANTIATE_DECODE_SHORT_G(T, BS, 3) \
+    NS_INSTANTIATE_DECODE_SHORT_G(T, BS, 4) \
+    NS_INSTANTIATE_DECODE_SHORT_G(T, BS, 5) \
+    NS_INSTANTIATE_DECODE_SHORT_G(T, BS, 6) \
+    NS_INSTANTIATE_DECODE_SHORT_G(T, BS, 7) \
+    NS_INSTANTIATE_DECODE_SHORT_G(T, BS, 8)
 
 }  // namespace ns
