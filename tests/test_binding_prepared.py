@@ -115,3 +115,20 @@ def test_prepare_checks_like_the_call_and_takes_no_stream(fake):
     # a failed prepare leaves the binding calling the library again
     nb.ns_kv_append_paged_attn_decode(**a, stream=3)
     assert fake.calls[-1][0] == "ns_kv_append_paged_attn_decode_ex"
+
+
+def test_prepared_q8_0_fused_decode(fake):
+    S, hq, hkv, d, nbk, bs = 2, 14, 2, 64, 6, 16
+    h = torch.float16
+    q, out = torch.zeros(S, hq, d, dtype=h), torch.zeros(S, hq, d, dtype=h)
+    kn, vn = torch.zeros(S, hkv, d, dtype=h), torch.zeros(S, hkv, d, dtype=h)
+    slots = torch.zeros(S, dtype=torch.int64)
+    kc, vc = (torch.zeros(nbk, hkv, bs, d, dtype=torch.int8) for _ in range(2))
+    ks, vs = (torch.zeros(nbk, hkv, bs, d // 32, dtype=h) for _ in range(2))
+    bt, cl = torch.zeros(S, 3, dtype=torch.int32), torch.ones(S, dtype=torch.int32)
+    ws = torch.zeros(4096, dtype=torch.uint8)
+    args = (q, kn, vn, slots, kc, ks, vc, vs, bt, cl, 0.125, out, ws)
+    nb.ns_kv_append_paged_attn_decode_q8_0(*args, stream=11)
+    nb.prepare(nb.ns_kv_append_paged_attn_decode_q8_0, *args)(stream=11)
+    assert fake.calls[0] == fake.calls[1]
+    assert fake.calls[0][0] == "ns_kv_append_paged_attn_decode_q8_0"
